@@ -1,0 +1,239 @@
+"""Python access to the double-precision CPU oracle in ``vpd_oracle.c``.
+
+TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's
+CPU-baseline leg are the only callers allowed. The product path never imports
+this module, and this module imports nothing from the product package.
+
+The C source is compiled with the host compiler (``gcc -O2``, no fast-math) into
+``oracle/_build/``; :func:`build` does it explicitly, and the first call to any
+function does it on demand. Inputs are any array-likes convertible exactly to
+float64 (fp32/bf16/fp16 values upcast exactly); outputs are float64 numpy
+arrays. Every function runs one token row at a time over the full vocabulary;
+``threads > 1`` only splits the rows over host threads (the C calls release
+the interpreter lock).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "vpd_oracle.c")
+LIBRARY = os.path.join(_HERE, "_build", "libvpd_oracle.so")
+
+_lock = threading.Lock()
+_lib = None
+
+_f64p = ctypes.POINTER(ctypes.c_double)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+
+
+def compile_command(source: str = SOURCE, output: str = LIBRARY) -> list[str]:
+    """The host-compiler command that builds the oracle library."""
+    return ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", output, source, "-lm"]
+
+
+def build(force: bool = False, source: str = SOURCE, output: str = LIBRARY) -> str:
+    """Compile the oracle if the library is missing or older than its source."""
+    os.makedirs(os.path.dirname(output), exist_ok=True)
+    stale = (not os.path.exists(output)) or os.path.getmtime(output) < os.path.getmtime(source)
+    if force or stale:
+        tmp = output + f".tmp{os.getpid()}"
+        subprocess.run(compile_command(source, tmp), check=True)
+        os.replace(tmp, output)
+    return output
+
+
+def load(path: str | None = None):
+    """Load (building first if needed) and return the ctypes handle."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _declare(ctypes.CDLL(build()))
+    return _lib
+
+
+def _declare(lib):
+    lib.vpd_oracle_row_stats.argtypes = [ctypes.c_int64, _f64p, _f64p, _f64p]
+    lib.vpd_oracle_row_stats.restype = ctypes.c_int
+    lib.vpd_oracle_segment_stats.argtypes = [ctypes.c_int64, _f64p, ctypes.c_int, _i64p, _f64p, _f64p]
+    lib.vpd_oracle_segment_stats.restype = ctypes.c_int
+    lib.vpd_oracle_jsd.argtypes = [ctypes.c_int64, ctypes.c_int64, _f64p, _f64p, ctypes.c_double,
+                                   _f64p, _f64p, _f64p, _f64p, _f64p, _f64p]
+    lib.vpd_oracle_jsd.restype = None
+    lib.vpd_oracle_kl.argtypes = [ctypes.c_int64, ctypes.c_int64, _f64p, _f64p, ctypes.c_int,
+                                  _f64p, _f64p, _f64p, _f64p]
+    lib.vpd_oracle_kl.restype = None
+    lib.vpd_oracle_entropy.argtypes = [ctypes.c_int64, ctypes.c_int64, _f64p, _f64p, _f64p, _f64p]
+    lib.vpd_oracle_entropy.restype = None
+    lib.vpd_oracle_logprobs.argtypes = [ctypes.c_int64, ctypes.c_int64, _f64p, ctypes.c_int64, _i64p,
+                                        ctypes.c_int64, _f64p, _f64p, _f64p]
+    lib.vpd_oracle_logprobs.restype = ctypes.c_int64
+    return lib
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    if a.dtype == np.int64:
+        return a.ctypes.data_as(_i64p)
+    return a.ctypes.data_as(_f64p)
+
+
+def _rows2d(x) -> np.ndarray:
+    x = _f64(x)
+    if x.ndim == 1:
+        x = x[None, :]
+    if x.ndim != 2:
+        raise ValueError("oracle inputs are [N, V]")
+    return x
+
+
+def _split(n: int, threads: int):
+    threads = max(1, min(threads, n))
+    step = (n + threads - 1) // threads if n else 0
+    return [(a, min(a + step, n)) for a in range(0, n, step)] if n else []
+
+
+def _run(n: int, threads: int, fn):
+    parts = _split(n, threads)
+    if len(parts) <= 1:
+        for a, b in parts:
+            fn(a, b)
+        return
+    with ThreadPoolExecutor(max_workers=len(parts)) as ex:
+        list(ex.map(lambda ab: fn(*ab), parts))
+
+
+def row_stats(x):
+    """(m, lse, code) per row: max over the finite support, log of the sum-exp
+    relative to it, and 0 / 1 (NaN or +inf present) / 2 (fully -inf)."""
+    lib = load()
+    x = _rows2d(x)
+    n, v = x.shape
+    m = np.empty(n)
+    lse = np.empty(n)
+    code = np.empty(n, dtype=np.int64)
+    for r in range(n):
+        mr = ctypes.c_double()
+        lr = ctypes.c_double()
+        code[r] = lib.vpd_oracle_row_stats(v, _ptr(x[r]), ctypes.byref(mr), ctypes.byref(lr))
+        m[r], lse[r] = mr.value, lr.value
+    return m, lse, code
+
+
+def segment_stats(x, widths):
+    """Statistics (m, Z) of one row merged over ordered segments."""
+    lib = load()
+    x = _f64(x).reshape(-1)
+    w = np.ascontiguousarray(np.asarray(widths, dtype=np.int64))
+    m = ctypes.c_double()
+    z = ctypes.c_double()
+    rc = lib.vpd_oracle_segment_stats(x.size, _ptr(x), int(w.size), _ptr(w), ctypes.byref(m), ctypes.byref(z))
+    if rc:
+        raise ValueError("segment widths must be >= 0 and sum to the vocabulary size")
+    return m.value, z.value
+
+
+def jsd(s, t, beta: float, g=None, grad: bool = True, threads: int = 1):
+    """Generalized JSD per row. Returns (loss, kl_tm, kl_sm, ds, dt); kl_tm and
+    kl_sm are KL(P_t||M) and KL(P_s||M) (NaN on the beta = 0 / 1 branches);
+    ds, dt are None when grad is False."""
+    lib = load()
+    s = _rows2d(s)
+    t = _rows2d(t)
+    if s.shape != t.shape:
+        raise ValueError("student and teacher must have the same [N, V] shape")
+    n, v = s.shape
+    g = None if g is None else _f64(g).reshape(n)
+    loss, a, b = np.empty(n), np.empty(n), np.empty(n)
+    ds = np.empty((n, v)) if grad else None
+    dt = np.empty((n, v)) if grad else None
+
+    def part(r0, r1):
+        sl = slice(r0, r1)
+        lib.vpd_oracle_jsd(r1 - r0, v, _ptr(s[sl]), _ptr(t[sl]), float(beta),
+                           None if g is None else _ptr(g[sl]), _ptr(loss[sl]), _ptr(a[sl]),
+                           _ptr(b[sl]), None if ds is None else _ptr(ds[sl]),
+                           None if dt is None else _ptr(dt[sl]))
+
+    _run(n, threads, part)
+    return loss, a, b, ds, dt
+
+
+def kl(s, t, reverse: bool, g=None, grad: bool = True, threads: int = 1):
+    """KL(P_t||P_s) (reverse False) or KL(P_s||P_t) (reverse True) per row.
+    Returns (loss, ds, dt)."""
+    lib = load()
+    s = _rows2d(s)
+    t = _rows2d(t)
+    if s.shape != t.shape:
+        raise ValueError("student and teacher must have the same [N, V] shape")
+    n, v = s.shape
+    g = None if g is None else _f64(g).reshape(n)
+    loss = np.empty(n)
+    ds = np.empty((n, v)) if grad else None
+    dt = np.empty((n, v)) if grad else None
+
+    def part(r0, r1):
+        sl = slice(r0, r1)
+        lib.vpd_oracle_kl(r1 - r0, v, _ptr(s[sl]), _ptr(t[sl]), int(bool(reverse)),
+                          None if g is None else _ptr(g[sl]), _ptr(loss[sl]),
+                          None if ds is None else _ptr(ds[sl]), None if dt is None else _ptr(dt[sl]))
+
+    _run(n, threads, part)
+    return loss, ds, dt
+
+
+def entropy(x, g=None, grad: bool = True, threads: int = 1):
+    """Entropy per row. Returns (out, dx)."""
+    lib = load()
+    x = _rows2d(x)
+    n, v = x.shape
+    g = None if g is None else _f64(g).reshape(n)
+    out = np.empty(n)
+    dx = np.empty((n, v)) if grad else None
+
+    def part(r0, r1):
+        sl = slice(r0, r1)
+        lib.vpd_oracle_entropy(r1 - r0, v, _ptr(x[sl]), None if g is None else _ptr(g[sl]),
+                               _ptr(out[sl]), None if dx is None else _ptr(dx[sl]))
+
+    _run(n, threads, part)
+    return out, dx
+
+
+def logprobs(x, index, ignore_index: int = -100, g=None, grad: bool = True, threads: int = 1):
+    """Selected log-probs. index is [N] or [N, K]; returns (out [N, K], dx, errors)."""
+    lib = load()
+    x = _rows2d(x)
+    n, v = x.shape
+    idx = np.ascontiguousarray(np.asarray(index, dtype=np.int64)).reshape(n, -1)
+    k = idx.shape[1]
+    g = None if g is None else _f64(g).reshape(n, k)
+    out = np.empty((n, k))
+    dx = np.empty((n, v)) if grad else None
+    errors = [0]
+    err_lock = threading.Lock()
+
+    def part(r0, r1):
+        sl = slice(r0, r1)
+        e = lib.vpd_oracle_logprobs(r1 - r0, v, _ptr(x[sl]), k, _ptr(idx[sl]), int(ignore_index),
+                                    None if g is None else _ptr(g[sl]), _ptr(out[sl]),
+                                    None if dx is None else _ptr(dx[sl]))
+        with err_lock:
+            errors[0] += int(e)
+
+    _run(n, threads, part)
+    return out, dx, errors[0]

@@ -1,0 +1,54 @@
+"""Each planted mistake in a copy of the oracle must fail at least one pin.
+
+The mistakes are the plausible ones: a transposed mixture weight, a dropped
+term, a wrong sign, a swapped operand, the wrong reduction in a gradient, a
+missing max subtraction, a swapped endpoint branch. The copy is compiled into
+a temporary directory on the CPU; the committed oracle is never modified.
+"""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle_pins
+from oracle import oracle as O
+
+MUTANTS = {
+    "mixture weights transposed": ("const double lw_s = log(1.0 - beta);", "const double lw_s = log(beta);"),
+    "dropped (1-beta) in the loss": ("double value = beta * a + (1.0 - beta) * b;", "double value = beta * a + b;"),
+    "wrong sign of B in dS": ("(lp - lm - b)", "(lp - lm + b)"),
+    "A used in place of B in dS": ("(lp - lm - b)", "(lp - lm - a)"),
+    "operands swapped in KL": ("csum_add(&kl, exp(la) * (la - lb));", "csum_add(&kl, exp(la) * (lb - la));"),
+    "forward/reverse branches swapped": ("return kl_row(V, t, s, g, dt, ds);", "return kl_row(V, s, t, g, ds, dt);"),
+    "entropy gradient sign": ("(lp + value)", "(lp - value)"),
+    "log-prob gradient sign": ("dxr[j] -= exp(log_prob(&st, xr[j])) * gs;", "dxr[j] += exp(log_prob(&st, xr[j])) * gs;"),
+    "max not subtracted": ("csum_add(&z, exp(v - r.m));", "csum_add(&z, exp(v));"),
+    "min instead of max": ("if (v > r.m)", "if (v < r.m && r.m != -INFINITY || r.m == -INFINITY)"),
+    "KL gradient target index": ("db[j] = g * (b - a);", "db[j] = g * (a - b);"),
+    "teacher weight in dT": ("g * beta * exp(lq)", "g * (1.0 - beta) * exp(lq)"),
+    "support violation ignored": ("if (xa[j] != -INFINITY && xb[j] == -INFINITY) {",
+                                  "if (0 && xa[j] != -INFINITY && xb[j] == -INFINITY) {"),
+    "empty segment not skipped": ("if (!r.empty)\n            csum_add(&z, r.z * exp(r.m - m));",
+                                  "csum_add(&z, r.z * exp(r.m - m));"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, tmp_path, monkeypatch):
+    old, new = MUTANTS[name]
+    with open(O.SOURCE) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation site for '{name}' must be unique"
+    mutant_c = tmp_path / "mutant.c"
+    mutant_c.write_text(src.replace(old, new))
+    lib_path = str(tmp_path / "libmutant.so")
+    subprocess.run(O.compile_command(str(mutant_c), lib_path), check=True)
+    monkeypatch.setattr(O, "_lib", O.load(lib_path))
+    failed = []
+    for pin in oracle_pins.PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, FloatingPointError):
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught the planted mistake '{name}'"
