@@ -1,0 +1,399 @@
+#!/usr/bin/env python
+"""Benchmark of the fused JSD forward+backward at the Qwen2.5 vocabulary.
+
+Workload (one step): generalized JSD (beta = 0.5) forward and backward to both
+inputs, gradients in bf16, on the causal-shift rows 0..N-2 of [N = 4 x 2048,
+V = 151936] bf16 student and teacher logits (seeded synthetic logits with the
+shape of the pages' Qwen2.5 runs; see softmax_divergence_lm_gb300/synth.py),
+through the C-ABI call ``vpd_jsd_fwdbwd``.
+
+Prints ONE JSON line (rank 0): tokens/s over all ranks, the roofline of the
+dominant kernel (algorithmic bytes: read s and t once, write dS and dT once,
+8 V bytes per token), the same metric end to end with host buffers, the CPU
+oracle timed on a bounded sample, SM clocks sampled during the timed region,
+and the library's kernel-launch count.
+
+Multi-GPU (torchrun, one process per GPU): every rank runs the full workload
+on its own GPU (rows are independent, so the op shards by token rows with no
+data exchange); a barrier brackets the timed region and the time is the max
+over ranks. ``--impl reference`` times the CPU oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "JSD fwd+bwd tokens/s at V=151936 bf16; achieved HBM GB/s vs GB300 peak"
+UNIT = "tokens/s"
+BATCH, SEQ, VOCAB, BETA = 4, 2048, 151936, 0.5
+ROWS = BATCH * SEQ - 1  # causal-shift rows 0..N-2 of the [N, V] buffer
+BYTES_PER_TOKEN = 8 * VOCAB  # read s, t (bf16) once + write dS, dT (bf16) once
+WORKLOAD = (f"qwen_vocab: JSD beta={BETA} fwd+bwd (both grads, bf16) on rows 0..N-2 of "
+            f"[N={BATCH}x{SEQ}, V={VOCAB}] bf16 logits; vocab ids 151646..151935 = -inf")
+FUSED_SOURCE = os.path.join(ROOT, "softmax_divergence_lm_gb300", "csrc", "vpd_fused.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--e2e-steps", type=int, default=8)
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="target wall time of the CPU-oracle sample")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (barrier and max over ranks only; no data exchange)
+# ---------------------------------------------------------------------------
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"]
+        except Exception:  # noqa: BLE001
+            sel = ["-i", str(device_index)]
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", *sel], stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        self.t0 = self.t1 = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def finish(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[5:10]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 1 <= r[0] <= self.t1 + 1] or rows
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in inside for n, v in zip(names, r[3][1:]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def fused_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("vpd_fused.cu", "vpd_device.cuh"):
+        with open(os.path.join(ROOT, "softmax_divergence_lm_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_hash: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    this exact kernel source; None otherwise."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_sha") != kernel_hash:
+        return None
+    return rec.get("bytes_per_launch_full_workload")
+
+
+def cpu_oracle_rate(s_rows, t_rows, seconds_target: float, threads: int):
+    """Time the CPU oracle (fwd+bwd, beta = 0.5) on a bounded sample of rows."""
+    from oracle import oracle as O
+    import numpy as np
+
+    O.build()
+    n_all = s_rows.shape[0]
+    probe = min(n_all, max(threads, 16))
+    s64 = s_rows[:probe].float().cpu().double().numpy()
+    t64 = t_rows[:probe].float().cpu().double().numpy()
+    t0 = time.perf_counter()
+    O.jsd(s64, t64, BETA, threads=threads)
+    per_row = (time.perf_counter() - t0) / probe
+    n = int(min(n_all, max(probe, seconds_target / max(per_row, 1e-9))))
+    idx = torch.linspace(0, n_all - 1, n).round().long().to(s_rows.device)
+    s64 = s_rows[idx].float().cpu().double().numpy()
+    t64 = t_rows[idx].float().cpu().double().numpy()
+    t0 = time.perf_counter()
+    O.jsd(s64, t64, BETA, threads=threads)
+    dt = time.perf_counter() - t0
+    del np
+    return n / dt, n, dt
+
+
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+def run_ours(args, world, rank, local):
+    from softmax_divergence_lm_gb300 import binding as B
+    from softmax_divergence_lm_gb300 import build as cuda_build
+    from softmax_divergence_lm_gb300 import synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        cuda_build.build()
+    barrier(world)
+    B.load()
+    s3, t3 = synth.qwen_vocab(device=dev)
+    s = s3.view(BATCH * SEQ, VOCAB)[:-1]
+    t = t3.view(BATCH * SEQ, VOCAB)[:-1]
+    g = torch.full((ROWS,), 1.0 / ROWS, device=dev)
+    loss = torch.empty(ROWS, device=dev)
+    saved = torch.empty(ROWS, B.SAVED_PAIR, device=dev)
+    ds = torch.empty(ROWS, VOCAB, dtype=torch.bfloat16, device=dev)
+    dt = torch.empty(ROWS, VOCAB, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        B.vpd_jsd_fwdbwd(s, t, BETA, None, g, loss, saved, ds, dt, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    launches_per_step = None
+    c0 = B.vpd_launch_count()
+    step()
+    torch.cuda.synchronize(dev)
+    launches_per_step = B.vpd_launch_count() - c0
+
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.mark_start()
+    c0 = B.vpd_launch_count()
+    start.record(stream)
+    for i in range(args.steps):
+        events[i][0].record(stream)
+        step()
+        events[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = B.vpd_launch_count() - c0
+    clocks.mark_end()
+    barrier(world)
+    clock_info = clocks.finish()
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), world)
+    per_launch_ms = statistics.mean(a.elapsed_time(b) for a, b in events)
+    ms_per_step = elapsed_ms / args.steps
+    tokens_per_step = ROWS * world
+    value = tokens_per_step / (ms_per_step / 1e3)
+
+    peak, peak_kind = measured_peak()
+    alg_bytes = BYTES_PER_TOKEN * ROWS
+    achieved = alg_bytes / (per_launch_ms / 1e3) / 1e9
+    kernel_hash = fused_source_hash()
+    fused = launches_per_step == 1
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(kernel_hash) if fused else None,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+                "kernel": "k_jsd_fused (one launch per step)" if fused else f"{launches_per_step} streaming launches per step",
+                "algorithmic_bytes_per_launch": alg_bytes, "launch_ms": round(per_launch_ms, 4),
+                "frac_of_8TBps_nameplate": round(achieved / 8000.0, 4)}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, B, s, t, g, dev, stream, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = host_threads()
+        rate, n, secs = cpu_oracle_rate(s, t, args.cpu_seconds, threads)
+        cpu = {"value": round(rate, 2), "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{n} of the {ROWS} workload rows (evenly spaced), fp64 oracle fwd+bwd, {secs:.1f} s wall"}
+
+    if rank == 0:
+        out = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+               "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+               "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+               "config": {"workload": WORKLOAD, "tokens_per_step_per_gpu": ROWS, "vocab": VOCAB, "beta": BETA,
+                          "grads": "dS and dT, bf16", "l2": "inputs (4.98 GB per step) larger than the 129 MB L2",
+                          "parallelism": f"rows sharded: {world} independent replica(s), no collective"},
+               "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clock_info,
+               "gpu_launches": launches, "impl": "ours"}
+        print(json.dumps(out), flush=True)
+
+
+def run_e2e(args, B, s, t, g, dev, stream, world):
+    """The same step through the C-ABI call with host buffers: every step copies
+    the inputs from pinned host memory and the loss and gradients back."""
+    n, v = s.shape
+    s_h = torch.empty(n, v, dtype=s.dtype, pin_memory=True)
+    t_h = torch.empty(n, v, dtype=t.dtype, pin_memory=True)
+    s_h.copy_(s)
+    t_h.copy_(t)
+    s_d = torch.empty_like(s)
+    t_d = torch.empty_like(t)
+    loss = torch.empty(n, device=dev)
+    saved = torch.empty(n, 6, device=dev)
+    ds = torch.empty(n, v, dtype=torch.bfloat16, device=dev)
+    dt = torch.empty(n, v, dtype=torch.bfloat16, device=dev)
+    loss_h = torch.empty(n, pin_memory=True)
+    ds_h = torch.empty(n, v, dtype=torch.bfloat16, pin_memory=True)
+    dt_h = torch.empty(n, v, dtype=torch.bfloat16, pin_memory=True)
+
+    def step():
+        s_d.copy_(s_h, non_blocking=True)
+        t_d.copy_(t_h, non_blocking=True)
+        B.vpd_jsd_fwdbwd(s_d, t_d, BETA, None, g, loss, saved, ds, dt, stream)
+        loss_h.copy_(loss, non_blocking=True)
+        ds_h.copy_(ds, non_blocking=True)
+        dt_h.copy_(dt, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for _ in range(args.e2e_steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(start.elapsed_time(end), world) / args.e2e_steps
+    h2d = 2 * n * v * s.element_size()
+    d2h = n * 4 + 2 * n * v * 2
+    return {"value": round(n * world / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
+            "path": "pinned host -> device copies, vpd_jsd_fwdbwd, device -> pinned host copies (loss, dS, dT)"}
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args, world, rank):
+    """The CPU oracle, as it stands, on a bounded sample of the same workload."""
+    if rank != 0:
+        return
+    from oracle import oracle as O
+    from softmax_divergence_lm_gb300 import synth
+
+    O.build()
+    threads = host_threads()
+    rows = 256
+    s3, t3 = synth.qwen_vocab(device="cpu", batch=1, seq=rows + 1)
+    s64 = s3.view(rows + 1, VOCAB)[:-1].float().double().numpy()
+    t64 = t3.view(rows + 1, VOCAB)[:-1].float().double().numpy()
+    for _ in range(max(1, min(args.warmup, 2))):
+        O.jsd(s64, t64, BETA, threads=threads)
+    steps = max(1, min(args.steps, 20))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        O.jsd(s64, t64, BETA, threads=threads)
+    secs = time.perf_counter() - t0
+    value = rows * steps / secs
+    sample = f"{rows} rows of the same recipe per step (CPU-generated), fp64 oracle fwd+bwd, {steps} steps"
+    out = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": steps,
+           "warmup": max(1, min(args.warmup, 2)), "ms_per_step": round(secs / steps * 1e3, 2),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": WORKLOAD, "tokens_per_step_per_gpu": rows, "vocab": VOCAB, "beta": BETA},
+           "impl": "reference",
+           "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": threads, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
+        return
+    world, rank, local = dist_setup()
+    try:
+        run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

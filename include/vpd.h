@@ -1,0 +1,230 @@
+/*
+ * vpd.h -- C ABI of the GB300 (sm_103a) per-token vocabulary softmax
+ * divergence library (libvpd): generalized Jensen-Shannon divergence JSD_beta,
+ * forward/reverse KL, entropy and selected (top-k) log-probabilities between
+ * language-model logits, each with its closed-form backward.
+ *
+ * Sources (web pages), cited below by short name:
+ *   [JSD page]  DeepSpeed pull request #8958, "[VocabTP] Add vocabulary-parallel
+ *               generalized JSD with Triton kernels".
+ *   [ops page]  DeepSpeed pull request #8791, "Add vocabulary-parallel logprobs,
+ *               entropy and KL ops".
+ *
+ * Notation for one token row r of logits s (student) and t (teacher), or x:
+ *   S_x = { j : x_j > -inf },  m_x = max_{S_x} x_j,  Z_x = sum_{S_x} e^{x_j - m_x},
+ *   L_x = ln Z_x,  ln p_j = (s_j - m_s) - L_s,  ln q_j = (t_j - m_t) - L_t,
+ *   M_j = (1 - beta) p_j + beta q_j.
+ * The max and the log-sum-exp are kept separate ([ops page], "How"). Natural
+ * logarithms throughout; every output is float32.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Ownership: the caller owns every buffer. The library allocates no device or
+ *   host memory and keeps no state between calls (besides one device error
+ *   word per GPU, see vpd_device_status). Pointers documented as "device" must
+ *   be device-accessible addresses on the current CUDA device.
+ * Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
+ *   default stream) and the call returns without waiting, except where stated.
+ * Errors: argument, dtype and shape problems are detected on the host before
+ *   anything is launched, and the call returns the matching code with nothing
+ *   written. A launch failure returns VPD_ERR_CUDA. vpd_last_error() gives a
+ *   one-line description of the last failure on the calling thread.
+ * Rows: N = 0 is a no-op. V = 0 gives NaN rows (no distribution).
+ * Special rows ([ops page], "How" and the review thread "Prevent NaN gradients
+ *   from fully masked padding rows"): a row that is fully -inf in any input of
+ *   the op has no distribution; its output is NaN and its gradient exactly 0,
+ *   so masking the output afterwards is safe. A row whose KL is +inf (the
+ *   target has mass on a token the other side masks, decided by logit
+ *   finiteness, [ops page], "Tests") also gets a zero gradient. A row holding
+ *   NaN or +inf is outside the contract; it is given a NaN output and a zero
+ *   gradient.
+ * Temperature, T^2 scaling, masking and reduction over tokens stay with the
+ *   caller ([JSD page], "Changes"; [ops page], "Limitations").
+ */
+#ifndef VPD_H
+#define VPD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define VPD_ABI_VERSION 1
+/* Most vocabulary segments one call accepts. */
+#define VPD_MAX_SEGMENTS 256
+
+typedef enum {
+    VPD_OK = 0,
+    VPD_ERR_ARG = 1,     /* NULL pointer, beta outside [0, 1], k < 1, misaligned pointer ... */
+    VPD_ERR_DTYPE = 2,   /* unknown dtype, or student and teacher dtypes differ */
+    VPD_ERR_SHAPE = 3,   /* rows/vocab mismatch, stride < vocab, segment widths not summing to vocab */
+    VPD_ERR_INDEX = 4,   /* reported by the host-side index helpers only */
+    VPD_ERR_CUDA = 5,    /* a CUDA call or launch failed */
+    VPD_ERR_TIMEOUT = 6, /* a bounded device-side wait gave up (see vpd_device_status) */
+    VPD_ERR_UNSUPPORTED = 7
+} vpd_status;
+
+typedef enum { VPD_F32 = 0, VPD_BF16 = 1, VPD_F16 = 2 } vpd_dtype;
+
+/* A read-only [N, V] logits view. Row r starts at element
+ *     (r / rows_per_batch) * batch_stride + (r % rows_per_batch) * row_stride
+ * when rows_per_batch > 0, else at r * row_stride (strides in elements).
+ * rows_per_batch / batch_stride describe a non-contiguous causal-shift view such
+ * as logits[:, :-1, :] of a [B, T, V] tensor ([JSD page], "Changes": non-contiguous
+ * causal-shift views). `data` must be aligned to the element size. */
+typedef struct {
+    const void *data;       /* device pointer to element (0, 0) */
+    int32_t dtype;          /* vpd_dtype */
+    int64_t rows;           /* N >= 0 */
+    int64_t vocab;          /* V >= 0 */
+    int64_t row_stride;     /* elements between consecutive rows of a batch, >= V */
+    int64_t rows_per_batch; /* 0: plain 2-D view */
+    int64_t batch_stride;   /* elements between batches when rows_per_batch > 0 */
+} vpd_view;
+
+/* An ordered split of the vocabulary into segments, the single-GPU stand-in for
+ * vocabulary shards ([JSD page], "Changes": uneven vocabulary shards and empty
+ * local shards). Widths are host memory, each >= 0, summing to V; count <=
+ * VPD_MAX_SEGMENTS. Per-segment statistics are merged as the shards' MAX and SUM
+ * all-reduces would merge them, an empty or fully -inf segment contributing
+ * (-inf, 0) ([ops page], "How" and the review thread "Reject unsupported empty
+ * shards consistently across TP ranks"). A NULL pointer or count 0 means one
+ * segment spanning the vocabulary. */
+typedef struct {
+    int32_t count;
+    const int64_t *widths;
+} vpd_segments;
+
+/* A gradient output: dense [N, V] rows, `row_stride` elements apart, in `dtype`
+ * (float32, or bf16/fp16 rounded to nearest even). A NULL vpd_grad pointer or
+ * NULL `data` means that gradient is not wanted (e.g. a detached teacher,
+ * [JSD page], "Changes"). */
+typedef struct {
+    void *data;
+    int32_t dtype;
+    int64_t row_stride;
+} vpd_grad;
+
+/* Per-row state saved by a forward for its backward ([ops page], "How": only the
+ * inputs and [N] statistics are saved). Float32, row-major, device memory:
+ *   JSD and KL:  [N, 6] = (m_s, L_s, m_t, L_t, A, B), A = KL(P_t || M) and
+ *                B = KL(P_s || M) with M taken at beta (so at beta = 0, A is the
+ *                forward KL and B = 0; at beta = 1, A = 0 and B is the reverse KL).
+ *   entropy:     [N, 3] = (m, L, H)
+ *   log-probs:   [N, 2] = (m, L)
+ * A row with NaN or +inf input stores m = NaN; a fully -inf row stores m = -inf. */
+#define VPD_SAVED_PAIR 6
+#define VPD_SAVED_ENTROPY 3
+#define VPD_SAVED_LOGPROBS 2
+
+/* ---------------------------------------------------------------------------
+ * Generalized JSD ([JSD page], "Motivation", "Changes", "Scope and limitations").
+ *   JSD_beta = beta * KL(P_t || M) + (1 - beta) * KL(P_s || M),  0 < beta < 1;
+ *   beta = 0 is the explicit forward-KL branch KL(P_t || P_s) and beta = 1 the
+ *   explicit reverse-KL branch KL(P_s || P_t): branches, not limits.
+ * s, t: student and teacher views with the same N, V and dtype; they share the
+ *   segment table. beta in [0, 1].
+ * ------------------------------------------------------------------------- */
+
+/* Forward in two input passes, the pages' design ([JSD page], "Scope and
+ * limitations": statistics, then divergence): a paired-statistics kernel merges
+ * per-segment (max, sum-exp) of both inputs, then a divergence kernel reduces the
+ * two KL-to-mixture expectations together ([JSD page], "Changes").
+ * loss:  device float[N], the per-token divergence.
+ * saved: device float[N, 6] (see above), required: it also carries the
+ *        statistics from the first kernel to the second. */
+vpd_status vpd_jsd_fwd(const vpd_view *s, const vpd_view *t, double beta, const vpd_segments *seg,
+                       float *loss, float *saved, void *stream);
+
+/* Backward: recomputes P_s, P_t and M from the inputs and the saved statistics,
+ * with no saved probability tensors ([JSD page], "Changes"; [ops page], "How").
+ *   0 < beta < 1: dS_j = g (1 - beta) p_j (ln p_j - ln M_j - B),
+ *                 dT_j = g beta q_j (ln q_j - ln M_j - A);
+ *   beta = 0:     dS = g (p - q),  dT_j = g q_j (ln q_j - ln p_j - KL);
+ *   beta = 1:     dS_j = g p_j (ln p_j - ln q_j - KL),  dT = g (q - p).
+ * Tokens outside the support and rows with a non-finite loss get exactly 0.
+ * grad_loss: device float[N], the upstream gradient g (NULL means 1).
+ * saved: device float[N, 6] written by vpd_jsd_fwd or vpd_jsd_fwdbwd with the
+ *   same inputs and beta.
+ * ds, dt: gradient outputs; either may be absent (NULL or NULL data). */
+vpd_status vpd_jsd_bwd(const vpd_view *s, const vpd_view *t, double beta, const vpd_segments *seg,
+                       const float *grad_loss, const float *saved, const vpd_grad *ds,
+                       const vpd_grad *dt, void *stream);
+
+/* Forward and backward in one call, with the upstream gradient given up front.
+ * When a row pair fits on chip across one thread-block cluster, each row pair is
+ * read from HBM once: statistics, divergence and gradients come from the
+ * on-chip copy. Otherwise the call runs the two forward kernels and the backward
+ * kernel in turn. Outputs as vpd_jsd_fwd (loss, and saved, which is required)
+ * plus the gradients as vpd_jsd_bwd. */
+vpd_status vpd_jsd_fwdbwd(const vpd_view *s, const vpd_view *t, double beta,
+                          const vpd_segments *seg, const float *grad_loss, float *loss,
+                          float *saved, const vpd_grad *ds, const vpd_grad *dt, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Forward / reverse KL ([ops page], "What"): reverse = 0 gives KL(P_t || P_s)
+ * (the teacher is the target), reverse = 1 gives KL(P_s || P_t). The forward is
+ * one online pass over the inputs (running maxima with rescaled sums). Saved
+ * layout and backward are those of the JSD beta = 0 / 1 branches.
+ * ------------------------------------------------------------------------- */
+vpd_status vpd_kl_fwd(const vpd_view *s, const vpd_view *t, int32_t reverse,
+                      const vpd_segments *seg, float *loss, float *saved, void *stream);
+vpd_status vpd_kl_bwd(const vpd_view *s, const vpd_view *t, int32_t reverse,
+                      const vpd_segments *seg, const float *grad_loss, const float *saved,
+                      const vpd_grad *ds, const vpd_grad *dt, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Entropy ([ops page], "What"): H = -sum_{S} p_j ln p_j, one online pass;
+ * backward dX_j = -g p_j (ln p_j + H).
+ * out: device float[N]; saved: device float[N, 3] or NULL.
+ * ------------------------------------------------------------------------- */
+vpd_status vpd_entropy_fwd(const vpd_view *x, const vpd_segments *seg, float *out, float *saved,
+                           void *stream);
+vpd_status vpd_entropy_bwd(const vpd_view *x, const vpd_segments *seg, const float *grad_out,
+                           const float *saved, const vpd_grad *dx, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Selected / top-k log-probabilities ([ops page], "What"):
+ *   out[r, k] = ln p_{index[r, k]}; a position equal to ignore_index returns 0
+ *   and takes no gradient; a selected token with a -inf logit returns -inf and
+ *   takes no gradient.
+ * index: device int64[N, k] (row-major, k >= 1).
+ * out: device float[N, k]; saved: device float[N, 2] or NULL.
+ * err_flag: device int32[1], required. The call sets it to 0, and to 1 if any
+ *   index outside [0, V) (other than ignore_index) is found; such positions
+ *   output NaN. Reading the flag is the caller's synchronisation point (the
+ *   pages' wrapper syncs on this check, [ops page], review thread "Provide a path
+ *   for reusing validated shard metadata").
+ * Backward: dX_j = sum_k g_rk [j == index_rk] - p_j sum_k g_rk over the positions
+ *   with a finite output. grad_out: device float[N, k] (NULL means 1).
+ * ------------------------------------------------------------------------- */
+vpd_status vpd_logprobs_fwd(const vpd_view *x, const vpd_segments *seg, const int64_t *index,
+                            int32_t k, int64_t ignore_index, float *out, float *saved,
+                            int32_t *err_flag, void *stream);
+vpd_status vpd_logprobs_bwd(const vpd_view *x, const vpd_segments *seg, const int64_t *index,
+                            int32_t k, int64_t ignore_index, const float *grad_out,
+                            const float *saved, const vpd_grad *dx, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Utilities.
+ * ------------------------------------------------------------------------- */
+/* Name of a status code (static string). */
+const char *vpd_status_string(vpd_status status);
+/* Description of the last failure on the calling thread ("" if none). */
+const char *vpd_last_error(void);
+/* VPD_ABI_VERSION of the loaded library. */
+int32_t vpd_abi_version(void);
+/* Number of kernel launches this library has issued since it was loaded
+ * (all threads, all devices); lets a caller count the device work of a call. */
+uint64_t vpd_launch_count(void);
+/* Synchronises `stream`, then reads and clears the device error word that the
+ * library's kernels set when a bounded wait gives up. Returns VPD_OK, or
+ * VPD_ERR_TIMEOUT with the failure described in vpd_last_error(). */
+vpd_status vpd_device_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VPD_H */

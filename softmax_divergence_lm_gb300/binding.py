@@ -1,0 +1,271 @@
+"""Thin ctypes binding of libvpd (``include/vpd.h``), with the C names.
+
+Every function here only marshals arguments: torch tensors become ``vpd_view``
+/ ``vpd_grad`` descriptors holding device pointers, shapes and strides, and
+the call runs on the current CUDA stream. All computation happens in the CUDA
+kernels of ``libvpd.so``; there is no fallback. Loading fails loudly when the
+library is missing (build it with ``python -m softmax_divergence_lm_gb300.build``).
+
+Logits tensors may be 2-D ``[N, V]`` with unit stride along V (any row stride)
+or 3-D ``[B, T, V]`` with unit stride along V (any batch and row strides, e.g.
+the causal-shift view ``logits[:, :-1, :]``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+VPD_OK, VPD_ERR_ARG, VPD_ERR_DTYPE, VPD_ERR_SHAPE, VPD_ERR_INDEX, VPD_ERR_CUDA, VPD_ERR_TIMEOUT, \
+    VPD_ERR_UNSUPPORTED = range(8)
+VPD_F32, VPD_BF16, VPD_F16 = 0, 1, 2
+VPD_MAX_SEGMENTS = 256
+SAVED_PAIR, SAVED_ENTROPY, SAVED_LOGPROBS = 6, 3, 2
+
+_DTYPES = {torch.float32: VPD_F32, torch.bfloat16: VPD_BF16, torch.float16: VPD_F16}
+
+# every symbol declared in include/vpd.h
+SYMBOLS = ("vpd_jsd_fwd", "vpd_jsd_bwd", "vpd_jsd_fwdbwd", "vpd_kl_fwd", "vpd_kl_bwd",
+           "vpd_entropy_fwd", "vpd_entropy_bwd", "vpd_logprobs_fwd", "vpd_logprobs_bwd",
+           "vpd_status_string", "vpd_last_error", "vpd_abi_version", "vpd_device_status",
+           "vpd_launch_count")
+
+
+class VpdError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_status_name(status)}: {message}")
+        self.status = status
+
+
+class vpd_view(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("rows", ctypes.c_int64),
+                ("vocab", ctypes.c_int64), ("row_stride", ctypes.c_int64),
+                ("rows_per_batch", ctypes.c_int64), ("batch_stride", ctypes.c_int64)]
+
+
+class vpd_segments(ctypes.Structure):
+    _fields_ = [("count", ctypes.c_int32), ("widths", ctypes.POINTER(ctypes.c_int64))]
+
+
+class vpd_grad(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("row_stride", ctypes.c_int64)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIBRARY
+
+
+def load():
+    """Load libvpd.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise ImportError(f"libvpd.so is not built ({path}); run "
+                                  "`python -m softmax_divergence_lm_gb300.build`")
+            _lib = _declare(ctypes.CDLL(path))
+    return _lib
+
+
+def _declare(lib):
+    P = ctypes.POINTER
+    V, S, G = P(vpd_view), P(vpd_segments), P(vpd_grad)
+    f, vp, i32, i64, dbl = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+    sig = {
+        "vpd_jsd_fwd": [V, V, dbl, S, f, f, vp],
+        "vpd_jsd_bwd": [V, V, dbl, S, f, f, G, G, vp],
+        "vpd_jsd_fwdbwd": [V, V, dbl, S, f, f, f, G, G, vp],
+        "vpd_kl_fwd": [V, V, i32, S, f, f, vp],
+        "vpd_kl_bwd": [V, V, i32, S, f, f, G, G, vp],
+        "vpd_entropy_fwd": [V, S, f, f, vp],
+        "vpd_entropy_bwd": [V, S, f, f, G, vp],
+        "vpd_logprobs_fwd": [V, S, f, i32, i64, f, f, f, vp],
+        "vpd_logprobs_bwd": [V, S, f, i32, i64, f, f, G, vp],
+        "vpd_device_status": [vp],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.vpd_status_string.argtypes = [ctypes.c_int]
+    lib.vpd_status_string.restype = ctypes.c_char_p
+    lib.vpd_last_error.argtypes = []
+    lib.vpd_last_error.restype = ctypes.c_char_p
+    lib.vpd_abi_version.argtypes = []
+    lib.vpd_abi_version.restype = ctypes.c_int32
+    lib.vpd_launch_count.argtypes = []
+    lib.vpd_launch_count.restype = ctypes.c_uint64
+    return lib
+
+
+def _status_name(status: int) -> str:
+    try:
+        return load().vpd_status_string(status).decode()
+    except Exception:  # noqa: BLE001 - naming only
+        return f"status {status}"
+
+
+def _check(status: int):
+    if status != VPD_OK:
+        raise VpdError(status, load().vpd_last_error().decode())
+
+
+# ---------------------------------------------------------------------------
+# Marshalling.
+# ---------------------------------------------------------------------------
+def make_view(x: torch.Tensor) -> vpd_view:
+    if x.dtype not in _DTYPES:
+        raise TypeError(f"logits dtype {x.dtype} is not float32/bfloat16/float16")
+    if not x.is_cuda:
+        raise ValueError("logits must be CUDA tensors")
+    if x.dim() == 2:
+        n, v = x.shape
+        if v > 1 and x.stride(1) != 1:
+            raise ValueError("the vocabulary dimension must have unit stride")
+        return vpd_view(x.data_ptr(), _DTYPES[x.dtype], n, v, x.stride(0) if n > 1 else v, 0, 0)
+    if x.dim() == 3:
+        b, t, v = x.shape
+        if v > 1 and x.stride(2) != 1:
+            raise ValueError("the vocabulary dimension must have unit stride")
+        return vpd_view(x.data_ptr(), _DTYPES[x.dtype], b * t, v, x.stride(1) if t > 1 else v,
+                        t, x.stride(0))
+    raise ValueError("logits must be [N, V] or [B, T, V]")
+
+
+def make_grad(g: torch.Tensor | None) -> vpd_grad | None:
+    if g is None:
+        return None
+    if g.dtype not in _DTYPES:
+        raise TypeError(f"gradient dtype {g.dtype} is not float32/bfloat16/float16")
+    if not g.is_cuda:
+        raise ValueError("gradients must be CUDA tensors")
+    if g.dim() == 3:
+        g = g.view(-1, g.shape[-1])
+    if g.dim() != 2 or (g.shape[1] > 1 and g.stride(1) != 1):
+        raise ValueError("gradient must be a dense [N, V] (or [B, T, V]) tensor with unit vocab stride")
+    return vpd_grad(g.data_ptr(), _DTYPES[g.dtype], g.stride(0) if g.shape[0] > 1 else g.shape[1])
+
+
+def make_segments(widths) -> tuple[vpd_segments | None, object]:
+    if widths is None:
+        return None, None
+    arr = (ctypes.c_int64 * len(widths))(*[int(w) for w in widths])
+    return vpd_segments(len(widths), arr), arr  # keep arr alive alongside
+
+
+def _fptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError("float32 per-row buffers must be contiguous CUDA tensors")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def _ref(x):
+    return None if x is None else ctypes.byref(x)
+
+
+# ---------------------------------------------------------------------------
+# Entry points (same names and argument order as include/vpd.h).
+# ---------------------------------------------------------------------------
+def vpd_jsd_fwd(s, t, beta, segments, loss, saved, stream=None):
+    vs, vt = make_view(s), make_view(t)
+    seg, _keep = make_segments(segments)
+    _check(load().vpd_jsd_fwd(ctypes.byref(vs), ctypes.byref(vt), float(beta), _ref(seg),
+                              _fptr(loss), _fptr(saved), _stream(stream)))
+
+
+def vpd_jsd_bwd(s, t, beta, segments, grad_loss, saved, ds, dt, stream=None):
+    vs, vt = make_view(s), make_view(t)
+    seg, _keep = make_segments(segments)
+    gs, gt = make_grad(ds), make_grad(dt)
+    _check(load().vpd_jsd_bwd(ctypes.byref(vs), ctypes.byref(vt), float(beta), _ref(seg),
+                              _fptr(grad_loss), _fptr(saved), _ref(gs), _ref(gt), _stream(stream)))
+
+
+def vpd_jsd_fwdbwd(s, t, beta, segments, grad_loss, loss, saved, ds, dt, stream=None):
+    vs, vt = make_view(s), make_view(t)
+    seg, _keep = make_segments(segments)
+    gs, gt = make_grad(ds), make_grad(dt)
+    _check(load().vpd_jsd_fwdbwd(ctypes.byref(vs), ctypes.byref(vt), float(beta), _ref(seg),
+                                 _fptr(grad_loss), _fptr(loss), _fptr(saved), _ref(gs), _ref(gt),
+                                 _stream(stream)))
+
+
+def vpd_kl_fwd(s, t, reverse, segments, loss, saved, stream=None):
+    vs, vt = make_view(s), make_view(t)
+    seg, _keep = make_segments(segments)
+    _check(load().vpd_kl_fwd(ctypes.byref(vs), ctypes.byref(vt), int(bool(reverse)), _ref(seg),
+                             _fptr(loss), _fptr(saved), _stream(stream)))
+
+
+def vpd_kl_bwd(s, t, reverse, segments, grad_loss, saved, ds, dt, stream=None):
+    vs, vt = make_view(s), make_view(t)
+    seg, _keep = make_segments(segments)
+    gs, gt = make_grad(ds), make_grad(dt)
+    _check(load().vpd_kl_bwd(ctypes.byref(vs), ctypes.byref(vt), int(bool(reverse)), _ref(seg),
+                             _fptr(grad_loss), _fptr(saved), _ref(gs), _ref(gt), _stream(stream)))
+
+
+def vpd_entropy_fwd(x, segments, out, saved, stream=None):
+    vx = make_view(x)
+    seg, _keep = make_segments(segments)
+    _check(load().vpd_entropy_fwd(ctypes.byref(vx), _ref(seg), _fptr(out), _fptr(saved), _stream(stream)))
+
+
+def vpd_entropy_bwd(x, segments, grad_out, saved, dx, stream=None):
+    vx = make_view(x)
+    seg, _keep = make_segments(segments)
+    gx = make_grad(dx)
+    _check(load().vpd_entropy_bwd(ctypes.byref(vx), _ref(seg), _fptr(grad_out), _fptr(saved), _ref(gx),
+                                  _stream(stream)))
+
+
+def _index_ptr(index: torch.Tensor):
+    if index.dtype != torch.int64 or not index.is_cuda or not index.is_contiguous():
+        raise ValueError("index must be a contiguous int64 CUDA tensor")
+    return index.data_ptr()
+
+
+def vpd_logprobs_fwd(x, segments, index, k, ignore_index, out, saved, err_flag, stream=None):
+    vx = make_view(x)
+    seg, _keep = make_segments(segments)
+    if err_flag.dtype != torch.int32 or not err_flag.is_cuda:
+        raise ValueError("err_flag must be an int32 CUDA tensor")
+    _check(load().vpd_logprobs_fwd(ctypes.byref(vx), _ref(seg), _index_ptr(index), int(k), int(ignore_index),
+                                   _fptr(out), _fptr(saved), err_flag.data_ptr(), _stream(stream)))
+
+
+def vpd_logprobs_bwd(x, segments, index, k, ignore_index, grad_out, saved, dx, stream=None):
+    vx = make_view(x)
+    seg, _keep = make_segments(segments)
+    gx = make_grad(dx)
+    _check(load().vpd_logprobs_bwd(ctypes.byref(vx), _ref(seg), _index_ptr(index), int(k), int(ignore_index),
+                                   _fptr(grad_out), _fptr(saved), _ref(gx), _stream(stream)))
+
+
+def vpd_device_status(stream=None):
+    _check(load().vpd_device_status(_stream(stream)))
+
+
+def vpd_abi_version() -> int:
+    return int(load().vpd_abi_version())
+
+
+def vpd_launch_count() -> int:
+    return int(load().vpd_launch_count())

@@ -1,0 +1,329 @@
+// vpd_api.cu -- the extern "C" entry points of libvpd (declared in vpd.h):
+// argument validation on the host, before anything is launched, then dispatch
+// to the kernels on the caller's stream. Nothing here allocates memory.
+
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "vpd.h"
+#include "vpd_internal.h"
+
+namespace vpd {
+// Reads and clears the device error word (defined with the fused kernel).
+cudaError_t take_device_error(cudaStream_t stream, int* code);
+}  // namespace vpd
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+vpd_status fail(vpd_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+vpd_status ok() {
+  g_last_error[0] = '\0';
+  return VPD_OK;
+}
+
+vpd_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(VPD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int elem_size(int dtype) { return dtype == VPD_F32 ? 4 : 2; }
+bool dtype_ok(int dtype) { return dtype == VPD_F32 || dtype == VPD_BF16 || dtype == VPD_F16; }
+
+vpd_status check_view(const vpd_view* v, const char* name, vpd::View* out) {
+  if (!v) return fail(VPD_ERR_ARG, "%s: NULL view", name);
+  if (!dtype_ok(v->dtype)) return fail(VPD_ERR_DTYPE, "%s: unknown dtype %d", name, v->dtype);
+  if (v->rows < 0 || v->vocab < 0)
+    return fail(VPD_ERR_SHAPE, "%s: negative rows or vocab", name);
+  if (v->row_stride < v->vocab)
+    return fail(VPD_ERR_SHAPE, "%s: row_stride %lld < vocab %lld", name, (long long)v->row_stride,
+                (long long)v->vocab);
+  if (v->rows_per_batch < 0 || (v->rows_per_batch > 0 && v->batch_stride < 0))
+    return fail(VPD_ERR_SHAPE, "%s: bad batch layout", name);
+  if (v->rows > 0 && v->vocab > 0) {
+    if (!v->data) return fail(VPD_ERR_ARG, "%s: NULL data", name);
+    if (reinterpret_cast<uintptr_t>(v->data) % elem_size(v->dtype))
+      return fail(VPD_ERR_ARG, "%s: data not aligned to its element size", name);
+  }
+  out->data = static_cast<const char*>(v->data);
+  out->dtype = v->dtype;
+  out->rows = v->rows;
+  out->vocab = v->vocab;
+  out->map = {v->row_stride, v->rows_per_batch, v->batch_stride};
+  return VPD_OK;
+}
+
+vpd_status check_pair(const vpd_view* s, const vpd_view* t, vpd::View* vs, vpd::View* vt) {
+  vpd_status st = check_view(s, "student", vs);
+  if (st != VPD_OK) return st;
+  st = check_view(t, "teacher", vt);
+  if (st != VPD_OK) return st;
+  if (vs->rows != vt->rows || vs->vocab != vt->vocab)
+    return fail(VPD_ERR_SHAPE, "student [%lld, %lld] and teacher [%lld, %lld] differ",
+                (long long)vs->rows, (long long)vs->vocab, (long long)vt->rows,
+                (long long)vt->vocab);
+  if (vs->dtype != vt->dtype) return fail(VPD_ERR_DTYPE, "student and teacher dtypes differ");
+  return VPD_OK;
+}
+
+vpd_status check_segments(const vpd_segments* seg, int64_t vocab, vpd::Segs* out) {
+  if (!seg || seg->count == 0) {
+    out->count = 1;
+    out->off[0] = 0;
+    out->off[1] = vocab;
+    return VPD_OK;
+  }
+  if (seg->count < 0 || seg->count > VPD_MAX_SEGMENTS)
+    return fail(VPD_ERR_ARG, "segment count %d outside [0, %d]", seg->count, VPD_MAX_SEGMENTS);
+  if (!seg->widths) return fail(VPD_ERR_ARG, "NULL segment widths");
+  out->count = seg->count;
+  out->off[0] = 0;
+  for (int k = 0; k < seg->count; ++k) {
+    if (seg->widths[k] < 0) return fail(VPD_ERR_SHAPE, "segment %d has negative width", k);
+    out->off[k + 1] = out->off[k] + seg->widths[k];
+  }
+  if (out->off[seg->count] != vocab)
+    return fail(VPD_ERR_SHAPE, "segment widths sum to %lld, vocab is %lld",
+                (long long)out->off[seg->count], (long long)vocab);
+  return VPD_OK;
+}
+
+vpd_status check_grad(const vpd_grad* g, const char* name, int64_t vocab, int64_t rows,
+                      vpd::Grad* out) {
+  out->data = nullptr;
+  out->dtype = VPD_F32;
+  out->row_stride = 0;
+  if (!g || !g->data) return VPD_OK;
+  if (!dtype_ok(g->dtype)) return fail(VPD_ERR_DTYPE, "%s: unknown gradient dtype %d", name, g->dtype);
+  if (g->row_stride < vocab)
+    return fail(VPD_ERR_SHAPE, "%s: gradient row_stride < vocab", name);
+  if (reinterpret_cast<uintptr_t>(g->data) % elem_size(g->dtype))
+    return fail(VPD_ERR_ARG, "%s: gradient not aligned to its element size", name);
+  if (rows > 0 && vocab > 0) out->data = static_cast<char*>(g->data);
+  out->dtype = g->dtype;
+  out->row_stride = g->row_stride;
+  return VPD_OK;
+}
+
+vpd_status check_beta(double beta) {
+  if (!(beta >= 0.0 && beta <= 1.0)) return fail(VPD_ERR_ARG, "beta %g outside [0, 1]", beta);
+  return VPD_OK;
+}
+
+vpd_status check_grads_pair(const vpd_grad* ds, const vpd_grad* dt, const vpd::View& v,
+                            vpd::Grad* gs, vpd::Grad* gt) {
+  vpd_status st = check_grad(ds, "ds", v.vocab, v.rows, gs);
+  if (st != VPD_OK) return st;
+  st = check_grad(dt, "dt", v.vocab, v.rows, gt);
+  if (st != VPD_OK) return st;
+  if (gs->data && gt->data && gs->dtype != gt->dtype)
+    return fail(VPD_ERR_DTYPE, "ds and dt must share one dtype");
+  return VPD_OK;
+}
+
+#define VPD_TRY(x)                     \
+  do {                                 \
+    vpd_status _st = (x);              \
+    if (_st != VPD_OK) return _st;     \
+  } while (0)
+
+#define VPD_CUDA(x, what)                          \
+  do {                                             \
+    cudaError_t _e = (x);                          \
+    if (_e != cudaSuccess) return cuda_fail(_e, what); \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+vpd_status vpd_jsd_fwd(const vpd_view* s, const vpd_view* t, double beta, const vpd_segments* seg,
+                       float* loss, float* saved, void* stream) {
+  vpd::View vs, vt;
+  vpd::Segs sg;
+  VPD_TRY(check_pair(s, t, &vs, &vt));
+  VPD_TRY(check_beta(beta));
+  VPD_TRY(check_segments(seg, vs.vocab, &sg));
+  if (vs.rows == 0) return ok();
+  if (!loss || !saved) return fail(VPD_ERR_ARG, "vpd_jsd_fwd: loss and saved are required");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  VPD_CUDA(vpd::launch_pair_stats(vs, vt, sg, saved, st), "paired statistics kernel");
+  VPD_CUDA(vpd::launch_jsd_div(vs, vt, beta, loss, saved, st), "divergence kernel");
+  return ok();
+}
+
+vpd_status vpd_jsd_bwd(const vpd_view* s, const vpd_view* t, double beta, const vpd_segments* seg,
+                       const float* grad_loss, const float* saved, const vpd_grad* ds,
+                       const vpd_grad* dt, void* stream) {
+  vpd::View vs, vt;
+  vpd::Segs sg;
+  vpd::Grad gs, gt;
+  VPD_TRY(check_pair(s, t, &vs, &vt));
+  VPD_TRY(check_beta(beta));
+  VPD_TRY(check_segments(seg, vs.vocab, &sg));
+  VPD_TRY(check_grads_pair(ds, dt, vs, &gs, &gt));
+  if (vs.rows == 0 || (!gs.data && !gt.data)) return ok();
+  if (!saved) return fail(VPD_ERR_ARG, "vpd_jsd_bwd: saved is required");
+  VPD_CUDA(vpd::launch_pair_bwd(vs, vt, beta, grad_loss, saved, gs, gt,
+                                static_cast<cudaStream_t>(stream)),
+           "backward kernel");
+  return ok();
+}
+
+vpd_status vpd_jsd_fwdbwd(const vpd_view* s, const vpd_view* t, double beta,
+                          const vpd_segments* seg, const float* grad_loss, float* loss,
+                          float* saved, const vpd_grad* ds, const vpd_grad* dt, void* stream) {
+  vpd::View vs, vt;
+  vpd::Segs sg;
+  vpd::Grad gs, gt;
+  VPD_TRY(check_pair(s, t, &vs, &vt));
+  VPD_TRY(check_beta(beta));
+  VPD_TRY(check_segments(seg, vs.vocab, &sg));
+  VPD_TRY(check_grads_pair(ds, dt, vs, &gs, &gt));
+  if (vs.rows == 0) return ok();
+  if (!loss || !saved) return fail(VPD_ERR_ARG, "vpd_jsd_fwdbwd: loss and saved are required");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = vpd::launch_jsd_fused(vs, vt, beta, grad_loss, loss, saved, gs, gt, st);
+  if (e == cudaSuccess) return ok();
+  if (e != cudaErrorNotSupported) return cuda_fail(e, "fused single-read kernel");
+  VPD_CUDA(vpd::launch_pair_stats(vs, vt, sg, saved, st), "paired statistics kernel");
+  VPD_CUDA(vpd::launch_jsd_div(vs, vt, beta, loss, saved, st), "divergence kernel");
+  VPD_CUDA(vpd::launch_pair_bwd(vs, vt, beta, grad_loss, saved, gs, gt, st), "backward kernel");
+  return ok();
+}
+
+vpd_status vpd_kl_fwd(const vpd_view* s, const vpd_view* t, int32_t reverse,
+                      const vpd_segments* seg, float* loss, float* saved, void* stream) {
+  vpd::View vs, vt;
+  vpd::Segs sg;
+  VPD_TRY(check_pair(s, t, &vs, &vt));
+  VPD_TRY(check_segments(seg, vs.vocab, &sg));
+  if (vs.rows == 0) return ok();
+  if (!loss) return fail(VPD_ERR_ARG, "vpd_kl_fwd: loss is required");
+  VPD_CUDA(vpd::launch_kl_fwd(vs, vt, reverse ? 1 : 0, sg, loss, saved,
+                              static_cast<cudaStream_t>(stream)),
+           "single-pass KL kernel");
+  return ok();
+}
+
+vpd_status vpd_kl_bwd(const vpd_view* s, const vpd_view* t, int32_t reverse,
+                      const vpd_segments* seg, const float* grad_loss, const float* saved,
+                      const vpd_grad* ds, const vpd_grad* dt, void* stream) {
+  vpd::View vs, vt;
+  vpd::Segs sg;
+  vpd::Grad gs, gt;
+  VPD_TRY(check_pair(s, t, &vs, &vt));
+  VPD_TRY(check_segments(seg, vs.vocab, &sg));
+  VPD_TRY(check_grads_pair(ds, dt, vs, &gs, &gt));
+  if (vs.rows == 0 || (!gs.data && !gt.data)) return ok();
+  if (!saved) return fail(VPD_ERR_ARG, "vpd_kl_bwd: saved is required");
+  VPD_CUDA(vpd::launch_pair_bwd(vs, vt, reverse ? 1.0 : 0.0, grad_loss, saved, gs, gt,
+                                static_cast<cudaStream_t>(stream)),
+           "backward kernel");
+  return ok();
+}
+
+vpd_status vpd_entropy_fwd(const vpd_view* x, const vpd_segments* seg, float* out, float* saved,
+                           void* stream) {
+  vpd::View vx;
+  vpd::Segs sg;
+  VPD_TRY(check_view(x, "x", &vx));
+  VPD_TRY(check_segments(seg, vx.vocab, &sg));
+  if (vx.rows == 0) return ok();
+  if (!out) return fail(VPD_ERR_ARG, "vpd_entropy_fwd: out is required");
+  VPD_CUDA(vpd::launch_entropy_fwd(vx, sg, out, saved, static_cast<cudaStream_t>(stream)),
+           "entropy kernel");
+  return ok();
+}
+
+vpd_status vpd_entropy_bwd(const vpd_view* x, const vpd_segments* seg, const float* grad_out,
+                           const float* saved, const vpd_grad* dx, void* stream) {
+  vpd::View vx;
+  vpd::Segs sg;
+  vpd::Grad gx;
+  VPD_TRY(check_view(x, "x", &vx));
+  VPD_TRY(check_segments(seg, vx.vocab, &sg));
+  VPD_TRY(check_grad(dx, "dx", vx.vocab, vx.rows, &gx));
+  if (vx.rows == 0 || !gx.data) return ok();
+  if (!saved) return fail(VPD_ERR_ARG, "vpd_entropy_bwd: saved is required");
+  VPD_CUDA(vpd::launch_entropy_bwd(vx, grad_out, saved, gx, static_cast<cudaStream_t>(stream)),
+           "entropy backward kernel");
+  return ok();
+}
+
+vpd_status vpd_logprobs_fwd(const vpd_view* x, const vpd_segments* seg, const int64_t* index,
+                            int32_t k, int64_t ignore_index, float* out, float* saved,
+                            int32_t* err_flag, void* stream) {
+  vpd::View vx;
+  vpd::Segs sg;
+  VPD_TRY(check_view(x, "x", &vx));
+  VPD_TRY(check_segments(seg, vx.vocab, &sg));
+  if (k < 1) return fail(VPD_ERR_ARG, "vpd_logprobs_fwd: k must be >= 1");
+  if (!err_flag) return fail(VPD_ERR_ARG, "vpd_logprobs_fwd: err_flag is required");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  VPD_CUDA(cudaMemsetAsync(err_flag, 0, sizeof(int32_t), st), "clearing err_flag");
+  if (vx.rows == 0) return ok();
+  if (!index || !out) return fail(VPD_ERR_ARG, "vpd_logprobs_fwd: index and out are required");
+  VPD_CUDA(vpd::launch_logprobs_fwd(vx, sg, index, k, ignore_index, out, saved, err_flag, st),
+           "log-prob kernel");
+  return ok();
+}
+
+vpd_status vpd_logprobs_bwd(const vpd_view* x, const vpd_segments* seg, const int64_t* index,
+                            int32_t k, int64_t ignore_index, const float* grad_out,
+                            const float* saved, const vpd_grad* dx, void* stream) {
+  vpd::View vx;
+  vpd::Segs sg;
+  vpd::Grad gx;
+  VPD_TRY(check_view(x, "x", &vx));
+  VPD_TRY(check_segments(seg, vx.vocab, &sg));
+  VPD_TRY(check_grad(dx, "dx", vx.vocab, vx.rows, &gx));
+  if (k < 1) return fail(VPD_ERR_ARG, "vpd_logprobs_bwd: k must be >= 1");
+  if (vx.rows == 0 || !gx.data) return ok();
+  if (!index || !saved) return fail(VPD_ERR_ARG, "vpd_logprobs_bwd: index and saved are required");
+  VPD_CUDA(vpd::launch_logprobs_bwd(vx, index, k, ignore_index, grad_out, saved, gx,
+                                    static_cast<cudaStream_t>(stream)),
+           "log-prob backward kernel");
+  return ok();
+}
+
+const char* vpd_status_string(vpd_status status) {
+  switch (status) {
+    case VPD_OK: return "VPD_OK";
+    case VPD_ERR_ARG: return "VPD_ERR_ARG";
+    case VPD_ERR_DTYPE: return "VPD_ERR_DTYPE";
+    case VPD_ERR_SHAPE: return "VPD_ERR_SHAPE";
+    case VPD_ERR_INDEX: return "VPD_ERR_INDEX";
+    case VPD_ERR_CUDA: return "VPD_ERR_CUDA";
+    case VPD_ERR_TIMEOUT: return "VPD_ERR_TIMEOUT";
+    case VPD_ERR_UNSUPPORTED: return "VPD_ERR_UNSUPPORTED";
+  }
+  return "unknown vpd_status";
+}
+
+const char* vpd_last_error(void) { return g_last_error; }
+
+int32_t vpd_abi_version(void) { return VPD_ABI_VERSION; }
+
+uint64_t vpd_launch_count(void) { return vpd::launch_count(); }
+
+vpd_status vpd_device_status(void* stream) {
+  int code = 0;
+  VPD_CUDA(vpd::take_device_error(static_cast<cudaStream_t>(stream), &code), "reading device status");
+  if (code)
+    return fail(VPD_ERR_TIMEOUT, "a bounded device-side wait gave up (code %d)", code);
+  return ok();
+}
+
+}  // extern "C"

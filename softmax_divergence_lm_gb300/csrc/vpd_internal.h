@@ -1,0 +1,69 @@
+// vpd_internal.h -- host-side descriptions of views, gradients and segment
+// tables after validation, and the kernel launchers the C ABI dispatches to.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "vpd.h"
+#include "vpd_device.cuh"
+
+namespace vpd {
+
+// A validated logits view.
+struct View {
+  const char* data;  // element (0, 0)
+  int dtype;         // Dtype
+  int64_t rows;
+  int64_t vocab;
+  RowMap map;
+};
+
+// A validated gradient output; data == nullptr means "not wanted".
+struct Grad {
+  char* data;
+  int dtype;
+  int64_t row_stride;
+};
+
+// Segment table as offsets: segment k spans [off[k], off[k + 1]).
+struct Segs {
+  int count;
+  int64_t off[VPD_MAX_SEGMENTS + 1];
+};
+
+// Streaming kernels: one CTA per row at a time (grid-stride over rows).
+cudaError_t launch_pair_stats(const View& s, const View& t, const Segs& seg, float* saved,
+                              cudaStream_t stream);
+cudaError_t launch_jsd_div(const View& s, const View& t, double beta, float* loss, float* saved,
+                           cudaStream_t stream);
+cudaError_t launch_pair_bwd(const View& s, const View& t, double beta, const float* grad_loss,
+                            const float* saved, const Grad& ds, const Grad& dt, cudaStream_t stream);
+cudaError_t launch_kl_fwd(const View& s, const View& t, int reverse, const Segs& seg, float* loss,
+                          float* saved, cudaStream_t stream);
+cudaError_t launch_entropy_fwd(const View& x, const Segs& seg, float* out, float* saved,
+                               cudaStream_t stream);
+cudaError_t launch_entropy_bwd(const View& x, const float* grad, const float* saved, const Grad& dx,
+                               cudaStream_t stream);
+cudaError_t launch_logprobs_fwd(const View& x, const Segs& seg, const int64_t* index, int k,
+                                int64_t ignore_index, float* out, float* saved, int32_t* err_flag,
+                                cudaStream_t stream);
+cudaError_t launch_logprobs_bwd(const View& x, const int64_t* index, int k, int64_t ignore_index,
+                                const float* grad, const float* saved, const Grad& dx,
+                                cudaStream_t stream);
+
+// Single-read fused JSD forward+backward on thread-block clusters. Returns
+// cudaErrorNotSupported (without launching) when the row pair does not fit on
+// chip or the layout does not allow it; the caller then uses the streaming path.
+cudaError_t launch_jsd_fused(const View& s, const View& t, double beta, const float* grad_loss,
+                             float* loss, float* saved, const Grad& ds, const Grad& dt,
+                             cudaStream_t stream);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Counts every kernel launch the library issues (read by vpd_launch_count).
+void note_launch();
+uint64_t launch_count();
+
+}  // namespace vpd
