@@ -153,11 +153,16 @@ vpd_status vpd_jsd_bwd(const vpd_view *s, const vpd_view *t, double beta, const 
                        const vpd_grad *dt, void *stream);
 
 /* Forward and backward in one call, with the upstream gradient given up front.
- * When a row pair fits on chip across one thread-block cluster, each row pair is
- * read from HBM once: statistics, divergence and gradients come from the
- * on-chip copy. Otherwise the call runs the two forward kernels and the backward
- * kernel in turn. Outputs as vpd_jsd_fwd (loss, and saved, which is required)
- * plus the gradients as vpd_jsd_bwd. */
+ * The single-read path runs when the inputs are bf16 or fp16, V is a multiple
+ * of 8, every row of the inputs and gradients starts on a 16-byte boundary,
+ * the gradients are float32 or the input dtype, there is one segment, and the
+ * row fits on a thread-block cluster (V <= 307200). There a cluster of up to
+ * 16 CTAs holds each row pair on chip and statistics, divergence and
+ * gradients come from one HBM read; a bf16 row whose finite max exceeds 2^126
+ * is treated as out of contract (NaN, zero gradient). Otherwise the call runs
+ * the two forward kernels and the backward kernel in turn. Outputs as
+ * vpd_jsd_fwd (loss, and saved, which is required) plus the gradients as
+ * vpd_jsd_bwd. */
 vpd_status vpd_jsd_fwdbwd(const vpd_view *s, const vpd_view *t, double beta,
                           const vpd_segments *seg, const float *grad_loss, float *loss,
                           float *saved, const vpd_grad *ds, const vpd_grad *dt, void *stream);

@@ -194,9 +194,14 @@ vpd_status vpd_jsd_fwdbwd(const vpd_view* s, const vpd_view* t, double beta,
   if (vs.rows == 0) return ok();
   if (!loss || !saved) return fail(VPD_ERR_ARG, "vpd_jsd_fwdbwd: loss and saved are required");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = vpd::launch_jsd_fused(vs, vt, beta, grad_loss, loss, saved, gs, gt, st);
-  if (e == cudaSuccess) return ok();
-  if (e != cudaErrorNotSupported) return cuda_fail(e, "fused single-read kernel");
+  // The single-read kernel merges statistics over its CTA slices; a call with
+  // several vocabulary segments takes the streaming kernels, which merge them
+  // segment by segment.
+  if (sg.count == 1) {
+    cudaError_t e = vpd::launch_jsd_fused(vs, vt, beta, grad_loss, loss, saved, gs, gt, st);
+    if (e == cudaSuccess) return ok();
+    if (e != cudaErrorNotSupported) return cuda_fail(e, "fused single-read kernel");
+  }
   VPD_CUDA(vpd::launch_pair_stats(vs, vt, sg, saved, st), "paired statistics kernel");
   VPD_CUDA(vpd::launch_jsd_div(vs, vt, beta, loss, saved, st), "divergence kernel");
   VPD_CUDA(vpd::launch_pair_bwd(vs, vt, beta, grad_loss, saved, gs, gt, st), "backward kernel");
