@@ -57,6 +57,9 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="target wall time of the CPU-oracle sample")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--sweep", action="store_true",
+                   help="instead of the headline line, print one JSONL record per workload x op x phase")
+    p.add_argument("--sweep-steps", type=int, default=10)
     return p.parse_args()
 
 
@@ -420,8 +423,148 @@ def run_reference(args, world, rank):
     print(json.dumps(out), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# Sweep: every workload x op x phase (tokens/s, GB/s of minimum bytes, and
+# the fraction of the measured peak). Minimum bytes: each input row read once
+# and each gradient row written once.
+# ---------------------------------------------------------------------------
+def _time_call(fn, steps, warmup, stream):
+    for _ in range(max(3, warmup)):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def run_sweep(args):
+    from softmax_divergence_lm_gb300 import binding as B
+    from softmax_divergence_lm_gb300 import build as cuda_build
+    from softmax_divergence_lm_gb300 import synth
+
+    cuda_build.build()
+    B.load()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    peak, kind = measured_peak()
+    steps = args.sweep_steps
+
+    def emit(workload, op, phase, dtype, beta, n, v, min_bytes, ms, extra=None):
+        gbs = min_bytes / (ms / 1e3) / 1e9
+        rec = {"workload": workload, "op": op, "phase": phase, "dtype": dtype, "beta": beta, "N": n, "V": v,
+               "min_bytes": int(min_bytes), "ms": round(ms, 4), "tokens_per_s": round(n / (ms / 1e3), 1),
+               "GBps": round(gbs, 1), "frac_of_measured_peak": round(gbs / peak, 4), "peak_GBps": peak,
+               "peak_source": kind, "frac_of_8TBps": round(gbs / 8000.0, 4)}
+        if extra:
+            rec.update(extra)
+        print(json.dumps(rec), flush=True)
+
+    def pair_suite(name, s, t, betas, gdtype, segments=None, do_kl=True, fused_only=False):
+        n, v = s.shape[0] if s.dim() == 2 else s.shape[0] * s.shape[1], s.shape[-1]
+        es, eg = s.element_size(), torch.empty((), dtype=gdtype).element_size()
+        loss = torch.empty(n, device=dev)
+        saved = torch.empty(n, 6, device=dev)
+        ds = torch.empty(n, v, dtype=gdtype, device=dev)
+        dt = torch.empty(n, v, dtype=gdtype, device=dev)
+        g = torch.full((n,), 1.0 / n, device=dev)
+        rd, wr = 2 * n * v * es, 2 * n * v * eg
+        dt_name = str(s.dtype).replace("torch.", "")
+        for beta in betas:
+            if not fused_only:
+                ms = _time_call(lambda: B.vpd_jsd_fwd(s, t, beta, segments, loss, saved), steps, 3, stream)
+                emit(name, "jsd", "fwd (two-pass)", dt_name, beta, n, v, rd, ms)
+                ms = _time_call(lambda: B.vpd_jsd_bwd(s, t, beta, segments, g, saved, ds, dt), steps, 3, stream)
+                emit(name, "jsd", "bwd", dt_name, beta, n, v, rd + wr, ms)
+            c0 = B.vpd_launch_count()
+            B.vpd_jsd_fwdbwd(s, t, beta, segments, g, loss, saved, ds, dt)
+            torch.cuda.synchronize()
+            path = "fused single-read" if B.vpd_launch_count() - c0 == 1 else "streaming"
+            ms = _time_call(lambda: B.vpd_jsd_fwdbwd(s, t, beta, segments, g, loss, saved, ds, dt), steps, 3, stream)
+            emit(name, "jsd", "fwd+bwd", dt_name, beta, n, v, rd + wr, ms, {"path": path})
+        if do_kl:
+            for rev in (False, True):
+                opn = "kl_reverse" if rev else "kl_forward"
+                ms = _time_call(lambda: B.vpd_kl_fwd(s, t, rev, segments, loss, saved), steps, 3, stream)
+                emit(name, opn, "fwd (single pass)", dt_name, None, n, v, rd, ms)
+                ms = _time_call(lambda: B.vpd_kl_bwd(s, t, rev, segments, g, saved, ds, dt), steps, 3, stream)
+                emit(name, opn, "bwd", dt_name, None, n, v, rd + wr, ms)
+        del ds, dt
+
+    def single_suite(name, x, gdtype, ids=None):
+        n, v = x.shape
+        ex, eg = x.element_size(), torch.empty((), dtype=gdtype).element_size()
+        dx = torch.empty(n, v, dtype=gdtype, device=dev)
+        out = torch.empty(n, device=dev)
+        saved = torch.empty(n, 3, device=dev)
+        g = torch.full((n,), 1.0 / n, device=dev)
+        dt_name = str(x.dtype).replace("torch.", "")
+        ms = _time_call(lambda: B.vpd_entropy_fwd(x, None, out, saved), steps, 3, stream)
+        emit(name, "entropy", "fwd (single pass)", dt_name, None, n, v, n * v * ex, ms)
+        ms = _time_call(lambda: B.vpd_entropy_bwd(x, None, g, saved, dx), steps, 3, stream)
+        emit(name, "entropy", "bwd", dt_name, None, n, v, n * v * (ex + eg), ms)
+        if ids is not None:
+            k = ids.shape[1]
+            lp = torch.empty(n, k, device=dev)
+            ls = torch.empty(n, 2, device=dev)
+            err = torch.empty(1, dtype=torch.int32, device=dev)
+            gk = torch.full((n, k), 1.0 / n, device=dev)
+            ms = _time_call(lambda: B.vpd_logprobs_fwd(x, None, ids, k, -100, lp, ls, err), steps, 3, stream)
+            emit(name, f"logprobs_top{k}", "fwd", dt_name, None, n, v, n * v * ex, ms)
+            ms = _time_call(lambda: B.vpd_logprobs_bwd(x, None, ids, k, -100, gk, ls, dx), steps, 3, stream)
+            emit(name, f"logprobs_top{k}", "bwd", dt_name, None, n, v, n * v * (ex + eg), ms)
+        del dx
+
+    # page-shaped local shard, bf16
+    s, t, ids = synth.page_shard(device=dev)
+    pair_suite("page_shard 8192x16032", s, t, (0.1, 0.5, 0.9), torch.bfloat16)
+    single_suite("page_shard 8192x16032", s, torch.bfloat16, ids)
+    del s, t, ids
+    torch.cuda.empty_cache()
+    # Qwen2.5 vocabulary, rows 0..N-2 and the [4, 2047, V] causal view
+    s3, t3 = synth.qwen_vocab(device=dev)
+    n = BATCH * SEQ
+    pair_suite("qwen_vocab rows 0..N-2", s3.view(n, VOCAB)[:-1], t3.view(n, VOCAB)[:-1], (0.5,), torch.bfloat16,
+               do_kl=True)
+    pair_suite("qwen_vocab causal [4,2047,V]", s3[:, :-1], t3[:, :-1], (0.5,), torch.bfloat16, do_kl=False,
+               fused_only=True)
+    del s3, t3
+    torch.cuda.empty_cache()
+    # numerical edge cases, fp32, 8 segments
+    s, t, info = synth.edge_cases(device=dev)
+    pair_suite("edge_cases 4096x128256 fp32 8 segments", s, t, (0.0, 0.25, 0.5, 0.75, 1.0), torch.float32,
+               segments=info["segments"], do_kl=False)
+    del s, t
+    torch.cuda.empty_cache()
+    # large throughput sweep, bf16 and fp16
+    for dt_ in (torch.bfloat16, torch.float16):
+        s, t = synth.large_sweep(device=dev, dtype=dt_)
+        pair_suite(f"large_sweep 32768x262144", s, t, (0.5,), dt_, do_kl=False)
+        n, v = s.shape
+        loss = torch.empty(n, device=dev)
+        saved = torch.empty(n, 6, device=dev)
+        ds = torch.empty(n, v, dtype=dt_, device=dev)
+        dtg = torch.empty(n, v, dtype=dt_, device=dev)
+        g = torch.full((n,), 1.0 / n, device=dev)
+        nm = str(dt_).replace("torch.", "")
+        ms = _time_call(lambda: B.vpd_kl_fwd(s, t, False, None, loss, saved), steps, 3, stream)
+        emit("large_sweep 32768x262144", "kl_forward", "fwd (single pass)", nm, None, n, v, 2 * n * v * 2, ms)
+        ms = _time_call(lambda: B.vpd_kl_bwd(s, t, False, None, g, saved, ds, dtg), steps, 3, stream)
+        emit("large_sweep 32768x262144", "kl_forward", "bwd", nm, None, n, v, 4 * n * v * 2, ms)
+        del ds, dtg
+        single_suite("large_sweep 32768x262144", s, dt_)
+        del s, t
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.impl == "reference":
         run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
         return

@@ -223,6 +223,14 @@ int32_t vpd_abi_version(void);
 /* Number of kernel launches this library has issued since it was loaded
  * (all threads, all devices); lets a caller count the device work of a call. */
 uint64_t vpd_launch_count(void);
+/* Test hook for the failure path. The next single-read launch of
+ * vpd_jsd_fwdbwd made from this thread withholds the shared-memory copy of row
+ * `row` in the first CTA of the cluster that owns it, so that CTA's bounded
+ * wait expires (after about two seconds). The kernel then records the timeout,
+ * every CTA leaves its row loop, the outputs of that call are unspecified, and
+ * vpd_device_status reports VPD_ERR_TIMEOUT; the device stays usable. A
+ * negative row clears the hook. Returns VPD_OK. */
+vpd_status vpd_test_withhold_copy(int64_t row);
 /* Synchronises `stream`, then reads and clears the device error word that the
  * library's kernels set when a bounded wait gives up. Returns VPD_OK, or
  * VPD_ERR_TIMEOUT with the failure described in vpd_last_error(). */

@@ -32,7 +32,7 @@ _DTYPES = {torch.float32: VPD_F32, torch.bfloat16: VPD_BF16, torch.float16: VPD_
 SYMBOLS = ("vpd_jsd_fwd", "vpd_jsd_bwd", "vpd_jsd_fwdbwd", "vpd_kl_fwd", "vpd_kl_bwd",
            "vpd_entropy_fwd", "vpd_entropy_bwd", "vpd_logprobs_fwd", "vpd_logprobs_bwd",
            "vpd_status_string", "vpd_last_error", "vpd_abi_version", "vpd_device_status",
-           "vpd_launch_count")
+           "vpd_launch_count", "vpd_test_withhold_copy")
 
 
 class VpdError(RuntimeError):
@@ -104,6 +104,8 @@ def _declare(lib):
     lib.vpd_abi_version.restype = ctypes.c_int32
     lib.vpd_launch_count.argtypes = []
     lib.vpd_launch_count.restype = ctypes.c_uint64
+    lib.vpd_test_withhold_copy.argtypes = [ctypes.c_int64]
+    lib.vpd_test_withhold_copy.restype = ctypes.c_int
     return lib
 
 
@@ -269,3 +271,7 @@ def vpd_abi_version() -> int:
 
 def vpd_launch_count() -> int:
     return int(load().vpd_launch_count())
+
+
+def vpd_test_withhold_copy(row: int):
+    _check(load().vpd_test_withhold_copy(int(row)))

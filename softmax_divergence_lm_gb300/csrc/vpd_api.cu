@@ -20,6 +20,7 @@ cudaError_t take_device_error(cudaStream_t stream, int* code);
 namespace {
 
 thread_local char g_last_error[512] = "";
+thread_local int64_t g_withhold_row = -1;  // vpd_test_withhold_copy
 
 vpd_status fail(vpd_status st, const char* fmt, ...) {
   va_list ap;
@@ -198,7 +199,8 @@ vpd_status vpd_jsd_fwdbwd(const vpd_view* s, const vpd_view* t, double beta,
   // several vocabulary segments takes the streaming kernels, which merge them
   // segment by segment.
   if (sg.count == 1) {
-    cudaError_t e = vpd::launch_jsd_fused(vs, vt, beta, grad_loss, loss, saved, gs, gt, st);
+    cudaError_t e = vpd::launch_jsd_fused(vs, vt, beta, grad_loss, loss, saved, gs, gt, st, g_withhold_row);
+    if (e == cudaSuccess) g_withhold_row = -1;
     if (e == cudaSuccess) return ok();
     if (e != cudaErrorNotSupported) return cuda_fail(e, "fused single-read kernel");
   }
@@ -322,6 +324,11 @@ const char* vpd_last_error(void) { return g_last_error; }
 int32_t vpd_abi_version(void) { return VPD_ABI_VERSION; }
 
 uint64_t vpd_launch_count(void) { return vpd::launch_count(); }
+
+vpd_status vpd_test_withhold_copy(int64_t row) {
+  g_withhold_row = row < 0 ? -1 : row;
+  return ok();
+}
 
 vpd_status vpd_device_status(void* stream) {
   int code = 0;

@@ -203,11 +203,15 @@ __device__ __forceinline__ Stat stat_init() { return {neg_inf(), 0.f}; }
 // (so that -inf entries give 0 and NaN entries give NaN).
 __device__ __forceinline__ float stat_ref(float m) { return m == neg_inf() ? 0.f : m; }
 
+// e^x to full fp32 accuracy, for the few rescalings of partial sums (the
+// hardware approximation's error would compound over a merge tree).
+__device__ __forceinline__ float exp_acc(float x) { return expf(x); }
+
 // Merge: MAX of the maxima, SUM of the sums rescaled to it.
 __device__ __forceinline__ Stat stat_merge(Stat a, Stat b) {
   float m = fmaxf(a.m, b.m);
   float r = stat_ref(m);
-  return {m, a.z * expd(a.m - r) + b.z * expd(b.m - r)};
+  return {m, a.z * exp_acc(a.m - r) + b.z * exp_acc(b.m - r)};
 }
 
 // Add a group of N values (one 16-byte vector) to a running statistic.
@@ -217,7 +221,7 @@ __device__ __forceinline__ void stat_add(Stat& st, const float (&x)[N]) {
 #pragma unroll
   for (int i = 1; i < N; ++i) mx = fmaxf(mx, x[i]);
   if (mx > st.m) {
-    st.z *= expd(st.m - mx);
+    st.z *= exp_acc(st.m - mx);
     st.m = mx;
   }
   const float r = stat_ref(st.m);

@@ -1,680 +1,44 @@
-// vpd_fused.cu -- single-read fused JSD forward+backward on thread-block
-// clusters, and the device error word read by vpd_device_status.
-//
-// Source: DeepSpeed pull request #8958, "[VocabTP] Add vocabulary-parallel
-// generalized JSD with Triton kernels": the op (section Changes: paired softmax
-// statistics, the two KL-to-mixture expectations reduced together, a backward
-// that recomputes P_s, P_t and M in registers; beta = 0 / 1 as explicit KL
-// branches) and the reason the pages need two input passes (section Scope and
-// limitations: the mixture is nonlinear in the normalised probabilities, so the
-// statistics must be global before the divergence).
-//
-// Design. One cluster of C CTAs (C in {1, 2, 4, 8, 16}) owns one token row at a
-// time; CTA c holds columns [c W, (c + 1) W) of both inputs, every thread R
-// 16-byte vectors of each, in registers. The row pair is read from HBM once:
-//   1. TMA bulk copies (cp.async.bulk, mbarrier completion) stage the CTA's
-//      slice of the next rows in shared memory (two stages) while the current
-//      row is computed from registers;
-//   2. pass A: NaN-propagating max of the raw 16-bit pairs (a NaN or +inf row
-//      is outside the contract, and so is a finite row max above 2^126 here),
-//      then -inf is clamped to a finite floor so that no later product forms
-//      0 * inf;
-//   3. pass B: per-thread (max, sum-exp), merged over the CTA and then over the
-//      cluster through distributed shared memory: the MAX / SUM merge of
-//      per-shard statistics, with the CTA slices as shards;
-//   4. pass C: log2 p, log2 q, p, q and log2 M, M = (1 - beta) p + beta q; the
-//      two expectations A = KL(P_t || M) and B = KL(P_s || M) are reduced
-//      together over the CTA and the cluster; log2 M stays in registers;
-//   5. pass D: dS = g (1 - beta) p (ln p - ln M - B), dT = g beta q (ln q - ln M
-//      - A), stored straight from registers with 16-byte stores.
-// Arithmetic is fp32 (packed fp32x2 where it pairs up) in base-2 logarithms, so
-// that the hardware ex2 / lg2 apply without rescaling; sums are converted to
-// nats once per row.
-//
-// Every wait on an mbarrier is bounded: when it gives up, the kernel records
-// an error in g_device_error, finishes its row loop without hanging, waits
-// (bounded) for its own copies in flight, and returns.
+// vpd_fused.cu -- host dispatch of the single-read fused JSD forward+backward
+// (device code and design notes in vpd_fused.cuh): shape checks, the choice of
+// cluster size and register budget, and the device error words read by
+// vpd_device_status.
 
 #include <cuda_runtime.h>
 
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 
+#include "vpd_fused.cuh"
 #include "vpd_internal.h"
 
 namespace vpd {
-
-// Set by a kernel whose bounded wait gave up; read and cleared by
-// take_device_error (vpd_device_status).
-__device__ int g_device_error = 0;
+namespace fused {
+// Instantiated in vpd_fused_bf16.cu and vpd_fused_f16.cu.
+extern template cudaError_t launch_typed<InBF16>(const FusedArgs&, const Config&, int, bool, cudaStream_t, int*);
+extern template cudaError_t launch_typed<InF16>(const FusedArgs&, const Config&, int, bool, cudaStream_t, int*);
+cudaError_t take_error_bf16(int* code);
+cudaError_t take_error_f16(int* code);
+}  // namespace fused
 
 cudaError_t take_device_error(cudaStream_t stream, int* code) {
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return e;
-  e = cudaMemcpyFromSymbol(code, g_device_error, sizeof(int));
+  int a = 0, b = 0;
+  e = fused::take_error_bf16(&a);
   if (e != cudaSuccess) return e;
-  if (*code) {
-    const int zero = 0;
-    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
-  }
+  e = fused::take_error_f16(&b);
+  *code = a | b;
   return e;
 }
 
 namespace {
 
-constexpr int kT = 480;                 // threads per CTA (15 warps, up to 136 registers each)
-constexpr int kStages = 2;              // shared-memory stages per CTA
-constexpr int kMaxR = 5;                // 16-byte vectors per input per thread
-constexpr uint32_t kSpinLimit = 1u << 24;  // try_wait rounds before giving up
-constexpr float kTiny = 1e-37f;         // keeps M > 0 so ln M stays finite
-constexpr float kMaxLogit = 8.5070592e37f;  // 2^126: a larger finite row max is out of contract
-
-// ---------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* mb, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(mb)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* mb, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(mb)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* mb, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(mb)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait(uint64_t* mb, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
-    if (mbar_try_wait(mb, parity)) return true;
-  return false;
-}
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* mb) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(mb))
-      : "memory");
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::
-          : "memory");
-}
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_size() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_index() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_count() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-  return r;
-}
-// Load a float from the same shared-memory offset in CTA `rank` of the cluster.
-__device__ __forceinline__ float ld_cluster(const float* p, uint32_t rank) {
-  uint32_t remote;
-  float v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(p)), "r"(rank));
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
-}
-__device__ __forceinline__ uint4 ld_shared16(const void* p) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(smem_addr(p)));
-  return v;
-}
-__device__ __forceinline__ void st_global16(void* p, uint4 v) {
-  asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
-// ---------------------------------------------------------------------------
-// 16-bit input formats: pairs of values packed in one 32-bit word.
-// ---------------------------------------------------------------------------
-// -inf is clamped to a finite floor (twice, packed) so that every log2 p_j
-// computed later stays finite: (x - m) log2 e cannot overflow while the row
-// max is at most 2^126 (larger rows are out of contract in this kernel).
-struct InBF16 {
-  static constexpr uint32_t kNegInf2 = 0xff80ff80u;
-  static constexpr uint32_t kNegBig2 = 0xf180f180u;  // -2^100
-  __device__ static __forceinline__ uint32_t max_nan(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-  }
-  __device__ static __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-  }
-  // volatile: recomputed in every pass instead of kept alive across passes
-  __device__ static __forceinline__ float2 unpack(uint32_t w) {
-    uint32_t lo, hi;
-    asm volatile("shl.b32 %0, %2, 16;\n\tand.b32 %1, %2, 0xffff0000;" : "=r"(lo), "=r"(hi) : "r"(w));
-    return make_float2(__uint_as_float(lo), __uint_as_float(hi));
-  }
-};
-struct InF16 {
-  static constexpr uint32_t kNegInf2 = 0xfc00fc00u;
-  static constexpr uint32_t kNegBig2 = 0xfbfffbffu;  // -65504, the most negative finite
-  __device__ static __forceinline__ uint32_t max_nan(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("max.NaN.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-  }
-  __device__ static __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("max.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-  }
-  __device__ static __forceinline__ float2 unpack(uint32_t w) {
-    float lo, hi;
-    asm volatile("{ .reg .f16 a, b; mov.b32 {a, b}, %2; cvt.f32.f16 %0, a; cvt.f32.f16 %1, b; }"
-                 : "=f"(lo), "=f"(hi)
-                 : "r"(w));
-    return make_float2(lo, hi);
-  }
-};
-
-// Gradient formats for 8 values (one 16-byte input vector).
-template <class G>
-struct Out;
-template <>
-struct Out<GBF16> {
-  static constexpr int kSize = 2;
-  __device__ static __forceinline__ uint32_t pack(float2 v) {
-    uint32_t d;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(v.y), "f"(v.x));
-    return d;
-  }
-  __device__ static __forceinline__ void store8(char* p, const float2 (&v)[4]) {
-    st_global16(p, make_uint4(pack(v[0]), pack(v[1]), pack(v[2]), pack(v[3])));
-  }
-};
-template <>
-struct Out<GF16> {
-  static constexpr int kSize = 2;
-  __device__ static __forceinline__ uint32_t pack(float2 v) {
-    uint32_t d;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(v.y), "f"(v.x));
-    return d;
-  }
-  __device__ static __forceinline__ void store8(char* p, const float2 (&v)[4]) {
-    st_global16(p, make_uint4(pack(v[0]), pack(v[1]), pack(v[2]), pack(v[3])));
-  }
-};
-template <>
-struct Out<GF32> {
-  static constexpr int kSize = 4;
-  __device__ static __forceinline__ void store8(char* p, const float2 (&v)[4]) {
-    st_global16(p, make_uint4(__float_as_uint(v[0].x), __float_as_uint(v[0].y), __float_as_uint(v[1].x),
-                              __float_as_uint(v[1].y)));
-    st_global16(p + 16, make_uint4(__float_as_uint(v[2].x), __float_as_uint(v[2].y), __float_as_uint(v[3].x),
-                                   __float_as_uint(v[3].y)));
-  }
-};
-
-__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
-__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
-__device__ __forceinline__ float2 ex2_2(float2 a) { return make_float2(ex2(a.x), ex2(a.y)); }
-__device__ __forceinline__ float2 lg2_2(float2 a) { return make_float2(lg2(a.x), lg2(a.y)); }
-
-// ---------------------------------------------------------------------------
-// Cluster reductions by push. Each CTA reduces its partial over its warps
-// (shuffles + shared memory), then one lane per peer sends it with st.async
-// into that peer's slot for this CTA; the bytes complete on the peer's
-// mbarrier. A receiver arms its own mbarrier for C partials, waits on it and
-// merges the C slots from its own shared memory. There is no cluster-wide
-// barrier and no fence on the gradient stores in flight. Slots and mbarriers
-// are double-buffered by row parity: a CTA cannot run two rows ahead of a
-// peer, since it needs that peer's partial of every row to proceed.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t map_rank(uint32_t local, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void push16(uint32_t remote, float a, float b, float c, float d, uint32_t remote_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(remote),
-      "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
-      : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* mb, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(mb)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* mb, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
-    if (mbar_try_wait_cluster(mb, parity)) return true;
-  return false;
-}
-
-struct Pair {  // statistics of both inputs and their out-of-contract flags
-  float ms, zs, mt, zt, bad_s, bad_t;
-};
-struct PairOps {
-  using V = Pair;
-  static constexpr int kW = 8;  // floats per slot
-  __device__ static V id() { return {neg_inf(), 0.f, neg_inf(), 0.f, 0.f, 0.f}; }
-  __device__ static V merge(const V& a, const V& b) {
-    const Stat s = stat_merge({a.ms, a.zs}, {b.ms, b.zs});
-    const Stat t = stat_merge({a.mt, a.zt}, {b.mt, b.zt});
-    return {s.m, s.z, t.m, t.z, fmaxf(a.bad_s, b.bad_s), fmaxf(a.bad_t, b.bad_t)};
-  }
-  __device__ static V shfl(const V& a, int o) {
-    return {__shfl_xor_sync(0xffffffffu, a.ms, o),    __shfl_xor_sync(0xffffffffu, a.zs, o),
-            __shfl_xor_sync(0xffffffffu, a.mt, o),    __shfl_xor_sync(0xffffffffu, a.zt, o),
-            __shfl_xor_sync(0xffffffffu, a.bad_s, o), __shfl_xor_sync(0xffffffffu, a.bad_t, o)};
-  }
-  __device__ static void put(float* p, const V& v) {
-    p[0] = v.ms, p[1] = v.zs, p[2] = v.mt, p[3] = v.zt, p[4] = v.bad_s, p[5] = v.bad_t;
-  }
-  __device__ static V get(const float* p) { return {p[0], p[1], p[2], p[3], p[4], p[5]}; }
-  __device__ static void push(uint32_t dst, const V& v, uint32_t bar) {
-    push16(dst, v.ms, v.zs, v.mt, v.zt, bar);
-    push16(dst + 16, v.bad_s, v.bad_t, 0.f, 0.f, bar);
-  }
-};
-
-struct Sums {  // A, B and the support-violation flag of the KL branches
-  float a, b, viol;
-};
-struct SumOps {
-  using V = Sums;
-  static constexpr int kW = 4;
-  __device__ static V id() { return {0.f, 0.f, 0.f}; }
-  __device__ static V merge(const V& x, const V& y) { return {x.a + y.a, x.b + y.b, fmaxf(x.viol, y.viol)}; }
-  __device__ static V shfl(const V& x, int o) {
-    return {__shfl_xor_sync(0xffffffffu, x.a, o), __shfl_xor_sync(0xffffffffu, x.b, o),
-            __shfl_xor_sync(0xffffffffu, x.viol, o)};
-  }
-  __device__ static void put(float* p, const V& v) { p[0] = v.a, p[1] = v.b, p[2] = v.viol; }
-  __device__ static V get(const float* p) { return {p[0], p[1], p[2]}; }
-  __device__ static void push(uint32_t dst, const V& v, uint32_t bar) { push16(dst, v.a, v.b, v.viol, 0.f, bar); }
-};
-
-template <class Ops>
-__device__ __forceinline__ typename Ops::V warp_reduce(typename Ops::V v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = Ops::merge(v, Ops::shfl(v, o));
-  return v;
-}
-
-// Reduce v over this CTA and push the result to slot `crank` of every CTA.
-template <class Ops>
-__device__ __forceinline__ void reduce_and_push(typename Ops::V v, float* warp_slots, float* slots,
-                                                uint64_t* bar, uint32_t crank, uint32_t csize) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = warp_reduce<Ops>(v);
-  if (lane == 0) Ops::put(warp_slots + warp * Ops::kW, v);
-  __syncthreads();
-  if (warp == 0) {
-    typename Ops::V w = lane < kT / 32 ? Ops::get(warp_slots + lane * Ops::kW) : Ops::id();
-    w = warp_reduce<Ops>(w);
-    if (lane < static_cast<int>(csize))
-      Ops::push(map_rank(smem_addr(slots + crank * Ops::kW), lane), w, map_rank(smem_addr(bar), lane));
-  }
-}
-
-// Arm this CTA's mbarrier for the C partials of one row, wait (bounded) and
-// merge them. `ok` becomes false (for every thread) if the wait gave up.
-template <class Ops>
-__device__ __forceinline__ typename Ops::V collect(const float* slots, uint64_t* bar, uint32_t parity,
-                                                   uint32_t csize, bool& ok) {
-  if (threadIdx.x == 0) mbar_expect_tx(bar, csize * Ops::kW * 4u);
-  const bool mine = mbar_wait_cluster(bar, parity);
-  ok = __syncthreads_and(mine) && ok;
-  const int lane = threadIdx.x & 31;
-  typename Ops::V c = lane < static_cast<int>(csize) ? Ops::get(slots + lane * Ops::kW) : Ops::id();
-  return warp_reduce<Ops>(c);
-}
-
-enum Mode : int { kInterior = 0, kForwardKL = 1, kReverseKL = 2 };
-
-struct FusedArgs {
-  const char* s;
-  const char* t;
-  RowMap ms, mt;
-  int64_t rows;
-  int64_t vocab;
-  int W;  // slice width per CTA (elements, multiple of 8)
-  float beta;
-  const float* grad_loss;
-  float* loss;
-  float* saved;
-  Grad ds, dt;
-};
-
-// Shared memory: [kStages][2 inputs][W] 16-bit elements, then this tail.
-struct Tail {
-  uint64_t tma_bar[kStages];
-  uint64_t stat_bar[2];
-  uint64_t sum_bar[2];
-  float stat_warp[kT / 32 * PairOps::kW];
-  float sum_warp[kT / 32 * SumOps::kW];
-  __align__(16) float stat_slot[2][16 * PairOps::kW];
-  __align__(16) float sum_slot[2][16 * SumOps::kW];
-};
-
-// Statistics partial of one row read straight from its shared-memory stage:
-// NaN-propagating maxima of the raw pairs, then the sum of 2^((x - m) log2 e)
-// relative to this thread's max (a -inf entry contributes 2^-inf = 0).
-template <class In, int R>
-__device__ __forceinline__ Pair stage_stats(const unsigned char* sb, int W, int len) {
-  const int tid = threadIdx.x;
-  uint32_t mxs = In::kNegInf2, mxt = In::kNegInf2;
-#pragma unroll
-  for (int k = 0; k < R; ++k) {
-    const int e0 = (k * kT + tid) * 8;
-    if (e0 < len) {
-      const uint4 u = ld_shared16(sb + e0 * 2);
-      const uint4 v = ld_shared16(sb + static_cast<size_t>(W) * 2 + e0 * 2);
-      mxs = In::max_nan(In::max_nan(mxs, u.x), In::max_nan(u.y, In::max_nan(u.z, u.w)));
-      mxt = In::max_nan(In::max_nan(mxt, v.x), In::max_nan(v.y, In::max_nan(v.z, v.w)));
-    }
-  }
-  const float2 ms2 = In::unpack(mxs), mt2 = In::unpack(mxt);
-  const float m_s = fmaxf(ms2.x, ms2.y), m_t = fmaxf(mt2.x, mt2.y);
-  const bool bad_s = isnan(ms2.x) || isnan(ms2.y) || m_s > kMaxLogit;
-  const bool bad_t = isnan(mt2.x) || isnan(mt2.y) || m_t > kMaxLogit;
-  const float2 l2e2 = f2(kLog2e), ns2 = f2(-stat_ref(m_s) * kLog2e), nt2 = f2(-stat_ref(m_t) * kLog2e);
-  float2 zs2 = f2(0.f), zt2 = f2(0.f);
-#pragma unroll
-  for (int k = 0; k < R; ++k) {
-    const int e0 = (k * kT + tid) * 8;
-    if (e0 < len) {
-      const uint4 u = ld_shared16(sb + e0 * 2);
-      const uint4 v = ld_shared16(sb + static_cast<size_t>(W) * 2 + e0 * 2);
-      const uint32_t us[4] = {u.x, u.y, u.z, u.w}, vs[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        zs2 = add2(zs2, ex2_2(fma2(In::unpack(us[w]), l2e2, ns2)));  // -inf gives 2^-inf = 0
-        zt2 = add2(zt2, ex2_2(fma2(In::unpack(vs[w]), l2e2, nt2)));
-      }
-    }
-  }
-  return {m_s, zs2.x + zs2.y, m_t, zt2.x + zt2.y, bad_s ? 1.f : 0.f, bad_t ? 1.f : 0.f};
-}
-
-// Copy one row's stage into registers with -inf clamped to the floor; flags a
-// KL support violation (the target finite where the other side is -inf).
-template <class In, int R, int MODE>
-__device__ __forceinline__ void stage_to_regs(const unsigned char* sb, int W, int len, uint32_t (&xs)[R][4],
-                                              uint32_t (&xt)[R][4], uint32_t& viol) {
-  const int tid = threadIdx.x;
-  viol = 0;
-#pragma unroll
-  for (int k = 0; k < R; ++k) {
-    const int e0 = (k * kT + tid) * 8;
-    if (e0 < len) {
-      const uint4 u = ld_shared16(sb + e0 * 2);
-      const uint4 v = ld_shared16(sb + static_cast<size_t>(W) * 2 + e0 * 2);
-      const uint32_t us[4] = {u.x, u.y, u.z, u.w}, vs[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        if (MODE != kInterior) {
-          const uint32_t tgt = MODE == kForwardKL ? vs[w] : us[w];
-          const uint32_t oth = MODE == kForwardKL ? us[w] : vs[w];
-          viol |= __vcmpeq2(oth, In::kNegInf2) & ~__vcmpeq2(tgt, In::kNegInf2);
-        }
-        xs[k][w] = In::max2(us[w], In::kNegBig2);
-        xt[k][w] = In::max2(vs[w], In::kNegBig2);
-      }
-    } else {
-#pragma unroll
-      for (int w = 0; w < 4; ++w) xs[k][w] = xt[k][w] = In::kNegBig2;
-    }
-  }
-}
-
-template <class In, class G, int R, int MODE>
-__global__ void __launch_bounds__(kT, 1) k_jsd_fused(FusedArgs a) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  const int W = a.W;
-  unsigned char* stage_base = smem;
-  Tail* tail = reinterpret_cast<Tail*>(smem + static_cast<size_t>(kStages) * 2 * W * 2);
-  auto stage_ptr = [&](int st) { return stage_base + static_cast<size_t>(st) * 2 * W * 2; };
-
-  const uint32_t crank = cluster_rank(), csize = cluster_size();
-  const int64_t q = cluster_index(), Q = cluster_count();
-  const int tid = threadIdx.x;
-  const int64_t col0 = static_cast<int64_t>(crank) * W;
-  const int64_t rest = a.vocab - col0;
-  const int len = rest <= 0 ? 0 : (rest < W ? static_cast<int>(rest) : W);
-  const uint32_t bytes = static_cast<uint32_t>(len) * 2u;
-
-  auto issue = [&](int64_t r, int st) {  // one thread: both inputs' slices of row r into stage st
-    unsigned char* dst = stage_ptr(st);
-    mbar_expect_tx(&tail->tma_bar[st], 2 * bytes);
-    bulk_load(dst, a.s + (a.ms.offset(r) + col0) * 2, bytes, &tail->tma_bar[st]);
-    bulk_load(dst + static_cast<size_t>(W) * 2, a.t + (a.mt.offset(r) + col0) * 2, bytes, &tail->tma_bar[st]);
-  };
-
-  if (tid == 0) {
-    for (int st = 0; st < kStages; ++st) mbar_init(&tail->tma_bar[st], 1);
-    for (int p = 0; p < 2; ++p) {
-      mbar_init(&tail->stat_bar[p], 1);
-      mbar_init(&tail->sum_bar[p], 1);
-    }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-  uint32_t pending = 0;         // bit st: a copy into stage st is in flight
-  uint32_t tma_done[kStages] = {0, 0};  // completed waits per stage
-  if (tid == 0 && bytes) {
-    for (int st = 0; st < kStages; ++st)
-      if (q + st * Q < a.rows) issue(q + st * Q, st);
-  }
-  if (bytes)
-    for (int st = 0; st < kStages; ++st)
-      if (q + st * Q < a.rows) pending |= 1u << st;
-  cluster_sync();  // every CTA's mbarriers are initialised before any push
-
-  bool ok = true;
-  auto wait_stage = [&](int st) {
-    if (!bytes) return;
-    const bool mine = mbar_wait(&tail->tma_bar[st], tma_done[st] & 1u);
-    ok = __syncthreads_and(mine) && ok;
-    ++tma_done[st];
-    pending &= ~(1u << st);
-  };
-
-  const float beta = a.beta;
-  const float2 ws2 = f2(1.f - beta), wt2 = f2(beta), tiny2 = f2(kTiny), l2e2 = f2(kLog2e);
-  uint32_t xs[R][4], xt[R][4];
-  uint32_t viol = 0;
-
-  // Row 0 of this cluster: statistics partial straight from its stage, then registers.
-  if (q < a.rows) {
-    wait_stage(0);
-    reduce_and_push<PairOps>(stage_stats<In, R>(stage_ptr(0), W, len), tail->stat_warp, tail->stat_slot[0],
-                             &tail->stat_bar[0], crank, csize);
-    stage_to_regs<In, R, MODE>(stage_ptr(0), W, len, xs, xt, viol);
-    __syncthreads();
-    if (tid == 0 && bytes && q + kStages * Q < a.rows) issue(q + kStages * Q, 0);
-    if (bytes && q + kStages * Q < a.rows) pending |= 1u;
-  }
-
-  int64_t i = 0;
-  for (int64_t r = q; r < a.rows && ok; r += Q, ++i) {
-    const int par = static_cast<int>(i & 1);
-    const uint32_t ph = static_cast<uint32_t>((i >> 1) & 1);
-    const bool has_next = r + Q < a.rows;
-    const int nst = static_cast<int>((i + 1) % kStages);  // stage of the next row
-
-    // (1) global statistics of row r
-    const Pair g_st = collect<PairOps>(tail->stat_slot[par], &tail->stat_bar[par], ph, csize, ok);
-    const bool row_ok = g_st.bad_s == 0.f && g_st.bad_t == 0.f && g_st.ms != neg_inf() && g_st.mt != neg_inf();
-    const float Ks = row_ok ? log2f(g_st.zs) : qnan();  // log2 Z
-    const float Kt = row_ok ? log2f(g_st.zt) : qnan();
-    const float2 nms2 = f2(-g_st.ms), nmt2 = f2(-g_st.mt), nKs2 = f2(-Ks), nKt2 = f2(-Kt);
-
-    // (2) pass C of row r from registers: the two KL-to-mixture expectations
-    // (or the KL branch) in log2 units; log2 M stays in registers
-    float2 lam_m[R][4];
-    float2 acc_a = f2(0.f), acc_b = f2(0.f);
-    if (row_ok) {
-#pragma unroll
-      for (int k = 0; k < R; ++k)
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const float2 lp = fma2(add2(In::unpack(xs[k][w]), nms2), l2e2, nKs2);
-          const float2 lq = fma2(add2(In::unpack(xt[k][w]), nmt2), l2e2, nKt2);
-          if (MODE == kInterior) {
-            const float2 p = ex2_2(lp), qv = ex2_2(lq);
-            const float2 lm = lg2_2(fma2(ws2, p, fma2(wt2, qv, tiny2)));
-            lam_m[k][w] = lm;
-            const float2 nlm = make_float2(-lm.x, -lm.y);
-            acc_a = fma2(qv, add2(lq, nlm), acc_a);
-            acc_b = fma2(p, add2(lp, nlm), acc_b);
-          } else if (MODE == kForwardKL) {  // KL(q || p)
-            acc_a = fma2(ex2_2(lq), add2(lq, make_float2(-lp.x, -lp.y)), acc_a);
-          } else {  // KL(p || q)
-            acc_a = fma2(ex2_2(lp), add2(lp, make_float2(-lq.x, -lq.y)), acc_a);
-          }
-        }
-    }
-    reduce_and_push<SumOps>({kLn2 * (acc_a.x + acc_a.y), kLn2 * (acc_b.x + acc_b.y), viol ? 1.f : 0.f},
-                            tail->sum_warp, tail->sum_slot[par], &tail->sum_bar[par], crank, csize);
-
-    // (3) statistics partial of the next row, straight from its stage, while
-    // this row's sums travel
-    if (has_next) {
-      wait_stage(nst);
-      reduce_and_push<PairOps>(stage_stats<In, R>(stage_ptr(nst), W, len), tail->stat_warp,
-                               tail->stat_slot[par ^ 1], &tail->stat_bar[par ^ 1], crank, csize);
-    }
-
-    // (4) global sums of row r; the per-token value and saved statistics
-    const Sums g_ab = collect<SumOps>(tail->sum_slot[par], &tail->sum_bar[par], ph, csize, ok);
-    float A = g_ab.a, B = g_ab.b, value;
-    if (!row_ok) {
-      value = qnan();
-      A = B = qnan();
-    } else if (MODE == kInterior) {
-      value = beta * A + (1.f - beta) * B;
-    } else {
-      value = g_ab.viol != 0.f ? pos_inf() : A;
-      A = MODE == kForwardKL ? value : 0.f;
-      B = MODE == kForwardKL ? 0.f : value;
-    }
-    if (crank == 0 && tid == 0) {
-      a.loss[r] = value;
-      float* sv = a.saved + r * VPD_SAVED_PAIR;
-      sv[0] = g_st.bad_s != 0.f ? qnan() : g_st.ms;
-      sv[1] = g_st.bad_s != 0.f ? qnan() : (g_st.ms == neg_inf() ? neg_inf() : kLn2 * log2f(g_st.zs));
-      sv[2] = g_st.bad_t != 0.f ? qnan() : g_st.mt;
-      sv[3] = g_st.bad_t != 0.f ? qnan() : (g_st.mt == neg_inf() ? neg_inf() : kLn2 * log2f(g_st.zt));
-      sv[4] = A;
-      sv[5] = B;
-    }
-
-    // (5) pass D of row r: gradients, e.g. dS = p (g (1-beta) ln2 (lam_p - lam_M) - g (1-beta) B)
-    const float gr = a.grad_loss ? __ldg(a.grad_loss + r) : 1.f;
-    char* ds_row = a.ds.data ? a.ds.data + (r * a.ds.row_stride + col0) * Out<G>::kSize : nullptr;
-    char* dt_row = a.dt.data ? a.dt.data + (r * a.dt.row_stride + col0) * Out<G>::kSize : nullptr;
-    if (ds_row || dt_row) {
-      const bool live = row_ok && isfinite(value);
-      const float cs = MODE == kInterior ? gr * (1.f - beta) : gr;
-      const float ct = MODE == kInterior ? gr * beta : gr;
-      const float2 cs2 = f2(live ? cs * kLn2 : 0.f), ct2 = f2(live ? ct * kLn2 : 0.f);
-      const float2 ncs2 = f2(live ? -cs * (MODE == kInterior ? B : value) : 0.f);
-      const float2 nct2 = f2(live ? -ct * (MODE == kInterior ? A : value) : 0.f);
-      const float2 g2 = f2(live ? gr : 0.f);
-#pragma unroll
-      for (int k = 0; k < R; ++k) {
-        const int e0 = (k * kT + tid) * 8;
-        if (e0 >= len) continue;
-        float2 gs[4], gt[4];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          if (!live) {
-            gs[w] = gt[w] = f2(0.f);
-            continue;
-          }
-          const float2 lp = fma2(add2(In::unpack(xs[k][w]), nms2), l2e2, nKs2);
-          const float2 lq = fma2(add2(In::unpack(xt[k][w]), nmt2), l2e2, nKt2);
-          const float2 p = ex2_2(lp), qv = ex2_2(lq);
-          if (MODE == kInterior) {
-            const float2 nlm = make_float2(-lam_m[k][w].x, -lam_m[k][w].y);
-            gs[w] = mul2(p, fma2(cs2, add2(lp, nlm), ncs2));
-            gt[w] = mul2(qv, fma2(ct2, add2(lq, nlm), nct2));
-          } else if (MODE == kForwardKL) {  // dS = g (p - q), dT = g q (ln q - ln p - KL)
-            gs[w] = mul2(g2, add2(p, make_float2(-qv.x, -qv.y)));
-            gt[w] = mul2(qv, fma2(ct2, add2(lq, make_float2(-lp.x, -lp.y)), nct2));
-          } else {  // dS = g p (ln p - ln q - KL), dT = g (q - p)
-            gs[w] = mul2(p, fma2(cs2, add2(lp, make_float2(-lq.x, -lq.y)), ncs2));
-            gt[w] = mul2(g2, add2(qv, make_float2(-p.x, -p.y)));
-          }
-        }
-        if (ds_row) Out<G>::store8(ds_row + static_cast<int64_t>(e0) * Out<G>::kSize, gs);
-        if (dt_row) Out<G>::store8(dt_row + static_cast<int64_t>(e0) * Out<G>::kSize, gt);
-      }
-    }
-
-    // (6) the next row into registers; its stage is then free for the row
-    // kStages further on
-    if (has_next) {
-      stage_to_regs<In, R, MODE>(stage_ptr(nst), W, len, xs, xt, viol);
-      __syncthreads();
-      const bool more = r + (kStages + 1) * Q < a.rows;
-      if (tid == 0 && bytes && more) issue(r + (kStages + 1) * Q, nst);
-      if (bytes && more) pending |= 1u << nst;
-    }
-  }
-
-  // Only after a wait gave up: copies still in flight must land before exit.
-  for (int st = 0; st < kStages; ++st)
-    if (pending & (1u << st)) mbar_wait(&tail->tma_bar[st], tma_done[st] & 1u);
-  if (!ok && tid == 0) atomicExch(&g_device_error, 1);
-  cluster_sync();  // no CTA leaves while a peer may still push into it
-}
-
-// ---------------------------------------------------------------------------
-// Host side: shape check, configuration and launch.
-// ---------------------------------------------------------------------------
-struct Config {
-  int C, R, W;
-  size_t smem;
-};
+using fused::Config;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// VPD_VERBOSE=1 in the environment logs each fused launch configuration.
+// VPD_VERBOSE=1 logs each fused launch configuration to stderr.
 bool verbose() {
   static const bool v = [] {
     const char* e = getenv("VPD_VERBOSE");
@@ -683,84 +47,45 @@ bool verbose() {
   return v;
 }
 
-bool pick_config(int64_t vocab, Config* cfg) {
+// VPD_FUSED_VARIANT=keep|recompute restricts the choice to one register
+// budget (both are complete implementations; the default tries "recompute"
+// first).
+int variant_choice() {
+  static const int v = [] {
+    const char* e = getenv("VPD_FUSED_VARIANT");
+    if (e && !strcmp(e, "keep")) return 1;
+    if (e && !strcmp(e, "recompute")) return 2;
+    return 0;
+  }();
+  return v;
+}
+
+// The smallest cluster that holds a row with at most rmax vectors of both
+// inputs per thread, for T threads per CTA.
+bool fit(int64_t vocab, int T, int rmin, int rmax, bool keep, Config* cfg) {
   for (int C : {1, 2, 4, 8, 16}) {
-    const int64_t per = (vocab + C - 1) / C;
-    const int64_t W = (per + 7) / 8 * 8;
-    const int64_t R = (W + kT * 8 - 1) / (kT * 8);
-    if (R <= kMaxR) {
+    const int64_t W = ((vocab + C - 1) / C + 7) / 8 * 8;
+    int64_t R = (W + T * 8 - 1) / (T * 8);
+    if (R < rmin) R = rmin;
+    if (R <= rmax) {
       cfg->C = C;
-      cfg->R = static_cast<int>(R < 1 ? 1 : R);
+      cfg->T = T;
+      cfg->R = static_cast<int>(R);
       cfg->W = static_cast<int>(W);
-      cfg->smem = static_cast<size_t>(kStages) * 2 * W * 2 + sizeof(Tail);
+      cfg->keep = keep;
+      const size_t tail = keep ? sizeof(fused::Tail<fused::kKeepT>) : sizeof(fused::Tail<fused::kRecomputeT>);
+      cfg->smem = static_cast<size_t>(fused::kStages) * 2 * W * 2 + tail;
       return true;
     }
   }
   return false;
 }
 
-template <class In, class G, int R, int MODE>
-cudaError_t launch_cfg(const FusedArgs& args, const Config& cfg, cudaStream_t stream) {
-  auto kern = k_jsd_fused<In, G, R, MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(cfg.smem));
-  if (e != cudaSuccess) return e;
-  if (cfg.C > 8) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return cudaErrorNotSupported;
-  }
-  cudaLaunchConfig_t lc = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cfg.C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  lc.blockDim = dim3(kT, 1, 1);
-  lc.dynamicSmemBytes = cfg.smem;
-  lc.stream = stream;
-  lc.attrs = attr;
-  lc.numAttrs = 1;
-  lc.gridDim = dim3(cfg.C, 1, 1);
-  int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, kern, &lc);
-  if (e != cudaSuccess || clusters < 1) {
-    cudaGetLastError();
-    return cudaErrorNotSupported;
-  }
-  const int64_t want = args.rows < clusters ? args.rows : clusters;
-  lc.gridDim = dim3(static_cast<unsigned>(want * cfg.C), 1, 1);
-  if (verbose())
-    fprintf(stderr, "[vpd] fused JSD: V=%lld cluster=%d R=%d W=%d smem=%zu B, %d clusters resident, grid=%u\n",
-            static_cast<long long>(args.vocab), cfg.C, cfg.R, cfg.W, cfg.smem, clusters, lc.gridDim.x);
-  e = cudaLaunchKernelEx(&lc, kern, args);
-  if (e == cudaSuccess) note_launch();
-  return e;
-}
-
-template <class In, class G, int MODE>
-cudaError_t launch_r(const FusedArgs& args, const Config& cfg, cudaStream_t stream) {
-  switch (cfg.R) {
-    case 1: return launch_cfg<In, G, 1, MODE>(args, cfg, stream);
-    case 2: return launch_cfg<In, G, 2, MODE>(args, cfg, stream);
-    case 3: return launch_cfg<In, G, 3, MODE>(args, cfg, stream);
-    case 4: return launch_cfg<In, G, 4, MODE>(args, cfg, stream);
-    case 5: return launch_cfg<In, G, 5, MODE>(args, cfg, stream);
-  }
-  return cudaErrorNotSupported;
-}
-
-template <class In, class G>
-cudaError_t launch_mode(const FusedArgs& args, const Config& cfg, double beta, cudaStream_t stream) {
-  if (beta == 0.0) return launch_r<In, G, kForwardKL>(args, cfg, stream);
-  if (beta == 1.0) return launch_r<In, G, kReverseKL>(args, cfg, stream);
-  return launch_r<In, G, kInterior>(args, cfg, stream);
-}
-
 }  // namespace
 
 cudaError_t launch_jsd_fused(const View& s, const View& t, double beta, const float* grad_loss,
                              float* loss, float* saved, const Grad& ds, const Grad& dt,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, int64_t withhold_row) {
   // 16-bit inputs only; every row of both inputs and of both gradients must
   // start on a 16-byte boundary, and V must fill whole 16-byte vectors.
   if (s.dtype == kF32 || s.vocab <= 0 || s.vocab % 8 != 0) return cudaErrorNotSupported;
@@ -777,16 +102,35 @@ cudaError_t launch_jsd_fused(const View& s, const View& t, double beta, const fl
     if (g->dtype != kF32 && g->dtype != s.dtype) return cudaErrorNotSupported;
     gdtype = g->dtype;
   }
-  Config cfg;
-  if (!pick_config(s.vocab, &cfg)) return cudaErrorNotSupported;
-  FusedArgs args{s.data, t.data, s.map, t.map, s.rows, s.vocab, cfg.W, static_cast<float>(beta),
-                 grad_loss, loss, saved, ds, dt};
+  // Candidate configurations, best first: the recompute budget (480 threads,
+  // R <= 5), then the kept-value budget (256 threads, R <= 5), which needs
+  // about twice the CTAs per row.
+  Config cand[2];
+  int n = 0;
+  const int choice = variant_choice();
+  if (choice != 1 && fit(s.vocab, fused::kRecomputeT, 1, 5, false, &cand[n])) ++n;
+  if (choice != 2 && fit(s.vocab, fused::kKeepT, 1, fused::kKeepMaxR, true, &cand[n])) ++n;
+  const int mode = beta == 0.0 ? fused::kForwardKL : beta == 1.0 ? fused::kReverseKL : fused::kInterior;
   const bool f32g = gdtype == kF32;
-  if (s.dtype == kBF16)
-    return f32g ? launch_mode<InBF16, GF32>(args, cfg, beta, stream)
-                : launch_mode<InBF16, GBF16>(args, cfg, beta, stream);
-  return f32g ? launch_mode<InF16, GF32>(args, cfg, beta, stream)
-              : launch_mode<InF16, GF16>(args, cfg, beta, stream);
+  for (int i = 0; i < n; ++i) {
+    const Config& cfg = cand[i];
+    fused::FusedArgs args{s.data, t.data, s.map, t.map, s.rows, s.vocab, cfg.W, static_cast<float>(beta),
+                          grad_loss, loss, saved, ds, dt, withhold_row};
+    int clusters = 0;
+    const cudaError_t e = s.dtype == kBF16
+                              ? fused::launch_typed<fused::InBF16>(args, cfg, mode, f32g, stream, &clusters)
+                              : fused::launch_typed<fused::InF16>(args, cfg, mode, f32g, stream, &clusters);
+    if (e == cudaErrorNotSupported) continue;
+    if (e == cudaSuccess) {
+      note_launch();
+      if (verbose())
+        fprintf(stderr, "[vpd] fused JSD: V=%lld %s cluster=%d threads=%d R=%d W=%d smem=%zu B, %d clusters\n",
+                static_cast<long long>(s.vocab), cfg.keep ? "kept" : "recompute", cfg.C, cfg.T, cfg.R, cfg.W,
+                cfg.smem, clusters);
+    }
+    return e;
+  }
+  return cudaErrorNotSupported;
 }
 
 }  // namespace vpd

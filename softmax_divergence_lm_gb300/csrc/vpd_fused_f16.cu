@@ -1,0 +1,20 @@
+// vpd_fused_f16.cu -- the fused single-read JSD kernels for fp16 logits
+// (device code in vpd_fused.cuh), and this unit's device error word.
+#include "vpd_fused.cuh"
+
+namespace vpd {
+namespace fused {
+
+template cudaError_t launch_typed<InF16>(const FusedArgs&, const Config&, int, bool, cudaStream_t, int*);
+
+cudaError_t take_error_f16(int* code) {
+  cudaError_t e = cudaMemcpyFromSymbol(code, g_fused_error, sizeof(int));
+  if (e == cudaSuccess && *code) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_fused_error, &zero, sizeof(int));
+  }
+  return e;
+}
+
+}  // namespace fused
+}  // namespace vpd

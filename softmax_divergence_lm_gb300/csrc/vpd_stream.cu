@@ -381,7 +381,7 @@ __device__ __forceinline__ KlAcc kl_init() { return {stat_init(), stat_init(), 0
 // Re-reference a partial to the maxima (Ma, Mb); 0 if it has no a-mass.
 __device__ __forceinline__ float kl_w_at(const KlAcc& x, float Ma, float Mb) {
   if (x.a.m == neg_inf() || x.b.m == neg_inf()) return 0.f;
-  return expd(x.a.m - Ma) * (x.w + ((Mb - x.b.m) - (Ma - x.a.m)) * x.a.z);
+  return exp_acc(x.a.m - Ma) * (x.w + ((Mb - x.b.m) - (Ma - x.a.m)) * x.a.z);
 }
 
 __device__ __forceinline__ KlAcc kl_merge(const KlAcc& x, const KlAcc& y) {
@@ -406,12 +406,12 @@ struct KlBody {
     }
     if (mxb > acc.b.m) {
       if (acc.b.m != neg_inf()) acc.w += (mxb - acc.b.m) * acc.a.z;
-      acc.b.z *= expd(acc.b.m - mxb);
+      acc.b.z *= exp_acc(acc.b.m - mxb);
       acc.b.m = mxb;
     }
     if (mxa > acc.a.m) {
       if (acc.a.m != neg_inf()) {
-        const float d = mxa - acc.a.m, e = expd(-d);
+        const float d = mxa - acc.a.m, e = exp_acc(-d);
         acc.w = e * (acc.w - d * acc.a.z);
         acc.a.z *= e;
       }
@@ -531,7 +531,7 @@ struct EntAcc {
 
 __device__ __forceinline__ float ent_y_at(const EntAcc& x, float M) {
   if (x.s.m == neg_inf()) return 0.f;
-  return expd(x.s.m - M) * (x.y - (M - x.s.m) * x.s.z);
+  return exp_acc(x.s.m - M) * (x.y - (M - x.s.m) * x.s.z);
 }
 
 __device__ __forceinline__ EntAcc ent_merge(const EntAcc& x, const EntAcc& y) {
@@ -548,7 +548,7 @@ struct EntBody {
     for (int i = 1; i < N; ++i) mx = fmaxf(mx, x[i]);
     if (mx > acc.s.m) {
       if (acc.s.m != neg_inf()) {
-        const float d = mx - acc.s.m, e = expd(-d);
+        const float d = mx - acc.s.m, e = exp_acc(-d);
         acc.y = e * (acc.y - d * acc.s.z);
         acc.s.z *= e;
       }

@@ -54,6 +54,7 @@ def fused_call(B, s, t, beta, g, gdtype, want_s=True, want_t=True):
     c0 = B.vpd_launch_count()
     B.vpd_jsd_fwdbwd(s, t, beta, None, g, loss, saved, ds, dt)
     torch.cuda.synchronize()
+    B.vpd_device_status()  # raises if a bounded device-side wait gave up
     launches = B.vpd_launch_count() - c0
     return loss, saved, ds, dt, launches
 
