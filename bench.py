@@ -42,7 +42,6 @@ ROWS = BATCH * SEQ - 1  # causal-shift rows 0..N-2 of the [N, V] buffer
 BYTES_PER_TOKEN = 8 * VOCAB  # read s, t (bf16) once + write dS, dT (bf16) once
 WORKLOAD = (f"qwen_vocab: JSD beta={BETA} fwd+bwd (both grads, bf16) on rows 0..N-2 of "
             f"[N={BATCH}x{SEQ}, V={VOCAB}] bf16 logits; vocab ids 151646..151935 = -inf")
-FUSED_SOURCE = os.path.join(ROOT, "softmax_divergence_lm_gb300", "csrc", "vpd_fused.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_HBM_GBS = 6800.0
 
@@ -170,9 +169,13 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+FUSED_SOURCES = ("vpd_fused.cuh", "vpd_fused_bf16.cu", "vpd_fused_f16.cu", "vpd_fused.cu", "vpd_device.cuh")
+
+
 def fused_source_hash() -> str:
+    """Hash of the sources the single-read kernel is built from."""
     h = hashlib.sha256()
-    for name in ("vpd_fused.cu", "vpd_device.cuh"):
+    for name in FUSED_SOURCES:
         with open(os.path.join(ROOT, "softmax_divergence_lm_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
