@@ -1,13 +1,14 @@
 // vpd_fused.cu -- host dispatch of the single-read fused JSD forward+backward
 // (device code and design notes in vpd_fused.cuh): shape checks, the choice of
-// cluster size and register budget, and the device error words read by
-// vpd_device_status.
+// cluster size, and the device error words read by vpd_device_status.
 
 #include <cuda_runtime.h>
 
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+
+#include <atomic>
 
 #include "vpd_fused.cuh"
 #include "vpd_internal.h"
@@ -17,6 +18,7 @@ namespace fused {
 // Instantiated in vpd_fused_bf16.cu and vpd_fused_f16.cu.
 extern template cudaError_t launch_typed<InBF16>(const FusedArgs&, const Config&, int, bool, cudaStream_t, int*);
 extern template cudaError_t launch_typed<InF16>(const FusedArgs&, const Config&, int, bool, cudaStream_t, int*);
+extern template int resident_clusters<InBF16>(int, size_t);
 cudaError_t take_error_bf16(int* code);
 cudaError_t take_error_f16(int* code);
 }  // namespace fused
@@ -47,38 +49,55 @@ bool verbose() {
   return v;
 }
 
-// VPD_FUSED_VARIANT=keep|recompute restricts the choice to one register
-// budget (both are complete implementations; the default tries "recompute"
-// first).
-int variant_choice() {
-  static const int v = [] {
-    const char* e = getenv("VPD_FUSED_VARIANT");
-    if (e && !strcmp(e, "keep")) return 1;
-    if (e && !strcmp(e, "recompute")) return 2;
-    return 0;
-  }();
-  return v;
+constexpr int kMaxDevices = 64;
+
+// Resident clusters of C CTAs on the current device (one CTA per SM; the
+// kernels of every dtype, mode and width share that shape), cached.
+int clusters_for(int C) {
+  static std::atomic<int> cache[kMaxDevices][fused::kMaxCluster + 1];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  int v = cache[dev][C].load(std::memory_order_relaxed);
+  if (v == 0) {
+    v = fused::resident_clusters<fused::InBF16>(C, fused::kMinSmem);
+    cache[dev][C].store(v < 1 ? -1 : v, std::memory_order_relaxed);
+  }
+  return v < 1 ? 0 : v;
 }
 
-// The smallest cluster that holds a row with at most rmax vectors of both
-// inputs per thread, for T threads per CTA.
-bool fit(int64_t vocab, int T, int rmin, int rmax, bool keep, Config* cfg) {
-  for (int C : {1, 2, 4, 8, 16}) {
+size_t max_smem_optin() {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess || v < 1) v = -1;
+    cache[dev].store(v, std::memory_order_relaxed);
+  }
+  return v < 1 ? 0 : static_cast<size_t>(v);
+}
+
+// The cluster size that keeps the most SMs busy on `rows` rows, among those
+// whose slice fits: at most kMaxR vectors of both inputs per thread and two
+// stages in shared memory. Ties go to the smaller cluster.
+bool choose(int64_t vocab, int64_t rows, Config* cfg) {
+  const size_t smem_cap = max_smem_optin();
+  int64_t best = 0;
+  for (int C = 1; C <= fused::kMaxCluster; ++C) {
     const int64_t W = ((vocab + C - 1) / C + 7) / 8 * 8;
-    int64_t R = (W + T * 8 - 1) / (T * 8);
-    if (R < rmin) R = rmin;
-    if (R <= rmax) {
-      cfg->C = C;
-      cfg->T = T;
-      cfg->R = static_cast<int>(R);
-      cfg->W = static_cast<int>(W);
-      cfg->keep = keep;
-      const size_t tail = keep ? sizeof(fused::Tail<fused::kKeepT>) : sizeof(fused::Tail<fused::kRecomputeT>);
-      cfg->smem = static_cast<size_t>(fused::kStages) * 2 * W * 2 + tail;
-      return true;
+    const int64_t R = (W / 8 + fused::kT - 1) / fused::kT;
+    if (R > fused::kMaxR) continue;
+    const size_t smem = fused::smem_bytes(static_cast<int>(W));
+    if (smem > smem_cap) continue;
+    const int clusters = clusters_for(C);
+    if (clusters < 1) continue;
+    const int64_t busy = (rows < clusters ? rows : clusters) * C;
+    if (busy > best) {
+      best = busy;
+      *cfg = Config{C, static_cast<int>(R), static_cast<int>(W), smem};
     }
   }
-  return false;
+  return best > 0;
 }
 
 }  // namespace
@@ -102,35 +121,23 @@ cudaError_t launch_jsd_fused(const View& s, const View& t, double beta, const fl
     if (g->dtype != kF32 && g->dtype != s.dtype) return cudaErrorNotSupported;
     gdtype = g->dtype;
   }
-  // Candidate configurations, best first: the recompute budget (480 threads,
-  // R <= 5), then the kept-value budget (256 threads, R <= 5), which needs
-  // about twice the CTAs per row.
-  Config cand[2];
-  int n = 0;
-  const int choice = variant_choice();
-  if (choice != 1 && fit(s.vocab, fused::kRecomputeT, 1, 5, false, &cand[n])) ++n;
-  if (choice != 2 && fit(s.vocab, fused::kKeepT, 1, fused::kKeepMaxR, true, &cand[n])) ++n;
+  Config cfg;
+  if (!choose(s.vocab, s.rows, &cfg)) return cudaErrorNotSupported;
   const int mode = beta == 0.0 ? fused::kForwardKL : beta == 1.0 ? fused::kReverseKL : fused::kInterior;
   const bool f32g = gdtype == kF32;
-  for (int i = 0; i < n; ++i) {
-    const Config& cfg = cand[i];
-    fused::FusedArgs args{s.data, t.data, s.map, t.map, s.rows, s.vocab, cfg.W, static_cast<float>(beta),
-                          grad_loss, loss, saved, ds, dt, withhold_row};
-    int clusters = 0;
-    const cudaError_t e = s.dtype == kBF16
-                              ? fused::launch_typed<fused::InBF16>(args, cfg, mode, f32g, stream, &clusters)
-                              : fused::launch_typed<fused::InF16>(args, cfg, mode, f32g, stream, &clusters);
-    if (e == cudaErrorNotSupported) continue;
-    if (e == cudaSuccess) {
-      note_launch();
-      if (verbose())
-        fprintf(stderr, "[vpd] fused JSD: V=%lld %s cluster=%d threads=%d R=%d W=%d smem=%zu B, %d clusters\n",
-                static_cast<long long>(s.vocab), cfg.keep ? "kept" : "recompute", cfg.C, cfg.T, cfg.R, cfg.W,
-                cfg.smem, clusters);
-    }
-    return e;
+  fused::FusedArgs args{s.data, t.data, s.map, t.map, s.rows, s.vocab, cfg.W, static_cast<float>(beta),
+                        grad_loss, loss, saved, ds, dt, withhold_row};
+  int clusters = 0;
+  const cudaError_t e = s.dtype == kBF16
+                            ? fused::launch_typed<fused::InBF16>(args, cfg, mode, f32g, stream, &clusters)
+                            : fused::launch_typed<fused::InF16>(args, cfg, mode, f32g, stream, &clusters);
+  if (e == cudaSuccess) {
+    note_launch();
+    if (verbose())
+      fprintf(stderr, "[vpd] fused JSD: V=%lld cluster=%d threads=%d R=%d W=%d smem=%zu B, %d clusters\n",
+              static_cast<long long>(s.vocab), cfg.C, fused::kT, cfg.R, cfg.W, cfg.smem, clusters);
   }
-  return cudaErrorNotSupported;
+  return e;
 }
 
 }  // namespace vpd

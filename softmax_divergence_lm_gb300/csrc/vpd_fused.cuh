@@ -10,30 +10,28 @@
 // limitations: the mixture is nonlinear in the normalised probabilities, so the
 // statistics must be global before the divergence).
 //
-// Design. One cluster of C CTAs (C in {1, 2, 4, 8, 16}) owns one token row at a
-// time; CTA c holds columns [c W, (c + 1) W) of both inputs, every thread R
-// 16-byte vectors of each, in registers. The row pair is read from HBM once:
+// Design. One cluster of C CTAs (C from 1 to 16, chosen on the host to cover
+// the most SMs) owns one token row at a time; CTA c holds columns
+// [c W, (c + 1) W) of both inputs. The row pair is read from HBM once:
 //   1. TMA bulk copies (cp.async.bulk, mbarrier completion) stage the CTA's
-//      slice of the next rows in shared memory (two stages) while the current
-//      row is computed from registers;
-//   2. statistics: NaN-propagating max of the raw 16-bit pairs (a NaN or +inf
-//      row is outside the contract, and so is a finite row max above 2^126
-//      here), then per-thread sum-exp relative to the thread max, merged over
-//      the CTA and then over the cluster: the MAX / SUM merge of per-shard
-//      statistics, with the CTA slices as shards. These are computed straight
-//      from the next row's shared-memory stage while the current row's sums
-//      are in flight;
-//   3. pass C: log2 p, log2 q, p, q and log2 M, M = (1 - beta) p + beta q; the
-//      two expectations A = KL(P_t || M) and B = KL(P_s || M) are reduced
-//      together over the CTA and the cluster;
-//   4. pass D: dS = g (1 - beta) p (ln p - ln M - B), dT = g beta q (ln q - ln M
-//      - A), stored straight from registers with 16-byte stores.
-// Two register budgets: the "kept" variant (256 threads, up to 255 registers)
-// keeps p, q, log2 p - log2 M and log2 q - log2 M in registers after pass C,
-// so pass D is a few multiply-adds per element; the "recompute" variant (480
-// threads, up to 128 registers) keeps only log2 M and recomputes p and q.
-// When the raw -inf would reach a product, it is clamped first to a finite
-// floor so that no 0 * inf forms.
+//      slice of two rows in shared memory (two stages); a stage is refilled
+//      as soon as pass C of its row has read it;
+//   2. statistics of the next row, straight from its stage while the current
+//      row's sums travel: NaN-propagating max of the raw 16-bit pairs reduced
+//      over the warp, then the sum of 2^((x - m) log2 e) relative to the warp
+//      max, merged over the CTA and then over the cluster: the MAX / SUM merge
+//      of per-shard statistics with warps and CTAs as shards;
+//   3. pass C from the stage: log2 p, log2 q, p, q and log2 M with
+//      M = (1 - beta) p + beta q; the two expectations A = KL(P_t || M) and
+//      B = KL(P_s || M) are reduced together over the CTA and the cluster.
+//      p and the two log-ratios go to tensor memory (TMEM), q stays in
+//      registers;
+//   4. pass D: dS = g (1 - beta) p (ln p - ln M - B), dT = g beta q
+//      (ln q - ln M - A) from TMEM and registers, stored with 16-byte stores.
+// Tensor memory here is plain per-thread storage: each thread owns one TMEM
+// lane and a range of 128 columns (the lane quarter of its warp), so pass D
+// needs no exponential and no logarithm. When the raw -inf would reach a
+// product, it is clamped first to a finite floor so that no 0 * inf forms.
 // Arithmetic is fp32 (packed fp32x2 where it pairs up) in base-2 logarithms,
 // so the hardware ex2 / lg2 apply without rescaling; sums are converted to
 // nats once per row.
@@ -41,7 +39,7 @@
 // Every wait on an mbarrier is bounded: when it gives up, the kernel records
 // an error in its device error word, leaves its row loop (every CTA of the
 // cluster does, since each then waits in vain for the others), waits
-// (bounded) for its own copies in flight, and returns.
+// (bounded) for its own copies in flight, frees its tensor memory and returns.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -55,11 +53,21 @@ constexpr int kStages = 2;                  // shared-memory stages per CTA
 constexpr float kTiny = 1e-37f;             // keeps M > 0 so log2 M stays finite
 constexpr float kMaxLogit = 8.5070592e37f;  // 2^126: a larger finite row max is out of contract
 constexpr int kMaxCluster = 16;
-constexpr int kKeepT = 256;     // threads per CTA of the kept-value variant (up to 255 registers each)
-constexpr int kKeepMaxR = 5;
-constexpr int kRecomputeT = 480;  // threads per CTA of the recompute variant (up to 128 registers each)
+constexpr int kT = 512;                     // threads per CTA
+constexpr int kWarps = kT / 32;
+constexpr int kMaxR = 5;                    // 16-byte vectors of each input per thread
+constexpr int kTmemCols = 512;              // the whole tensor memory of the SM
+constexpr int kMinSmem = 120 * 1024;        // keeps one CTA per SM (each takes all TMEM)
 
 enum Mode : int { kInterior = 0, kForwardKL = 1, kReverseKL = 2 };
+
+// TMEM columns a thread uses per 8-element vector: p, log2 p - log2 M and
+// log2 q - log2 M (interior); p and the log2 ratio target / other (KL).
+template <int MODE>
+struct Cols {
+  static constexpr int k = MODE == kInterior ? 24 : 16;
+};
+static_assert(Cols<kInterior>::k * kMaxR <= kTmemCols / (kWarps / 4), "TMEM columns per thread");
 
 // Set by a kernel of this translation unit whose bounded wait gave up (each
 // translation unit that includes this header has its own word).
@@ -84,18 +92,16 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a wait gives up after two seconds
-constexpr uint32_t kSuspendHintNs = 20000;        // try_wait may sleep this long per round
 
-// One try on an mbarrier phase (CTA-scope acquire); may suspend the thread for
-// up to the hint while the phase is incomplete.
+// One try on an mbarrier phase (CTA-scope acquire).
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* mb, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_addr(mb)), "r"(parity), "r"(kSuspendHintNs)
+      : "r"(smem_addr(mb)), "r"(parity)
       : "memory");
   return ok != 0;
 }
@@ -105,6 +111,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* mb, uint32_t parity) {
   const uint64_t t0 = global_ns();
   while (global_ns() - t0 < kWaitLimitNs)
     if (mbar_try_wait(mb, parity)) return true;
+  return false;
+}
+// One try with cluster-scope acquire: the partials arrive from other CTAs.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* mb, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(mb)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* mb, uint32_t parity) {
+  if (mbar_try_wait_cluster(mb, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (global_ns() - t0 < kWaitLimitNs)
+    if (mbar_try_wait_cluster(mb, parity)) return true;
   return false;
 }
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* mb) {
@@ -140,25 +165,99 @@ __device__ __forceinline__ uint32_t cluster_count() {
   asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
   return r;
 }
-// Load a float from the same shared-memory offset in CTA `rank` of the cluster.
-__device__ __forceinline__ float ld_cluster(const float* p, uint32_t rank) {
-  uint32_t remote;
-  float v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(p)), "r"(rank));
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
+__device__ __forceinline__ uint32_t map_rank(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
 }
-__device__ __forceinline__ uint4 ld_shared16(const void* p) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(smem_addr(p)));
-  return v;
+// 16 bytes into a peer's shared memory; the bytes complete on its mbarrier.
+__device__ __forceinline__ void push16(uint32_t remote, float a, float b, float c, float d, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(remote),
+      "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
+      : "memory");
 }
 __device__ __forceinline__ void st_global16(void* p, uint4 v) {
   asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
                : "memory");
+}
+
+// Tensor memory: allocation by one warp (the address lands in shared memory),
+// and per-thread 32-bit columns of the thread's own lane (32x32b shape).
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(slot)),
+               "n"(kTmemCols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t base) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "n"(kTmemCols) : "memory");
+}
+__device__ __forceinline__ void tmem_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// 8 consecutive columns from 4 packed pairs.
+__device__ __forceinline__ void tmem_st8(uint32_t ta, const float2 (&v)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(ta),
+               "f"(v[0].x), "f"(v[0].y), "f"(v[1].x), "f"(v[1].y), "f"(v[2].x), "f"(v[2].y), "f"(v[3].x),
+               "f"(v[3].y));
+}
+// 8 consecutive columns, waited for within the same statement so that no
+// register is read before the load has landed.
+__device__ __forceinline__ void tmem_ld8_wait(uint32_t ta, float2 (&v)[4]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=f"(v[0].x), "=f"(v[0].y), "=f"(v[1].x), "=f"(v[1].y), "=f"(v[2].x), "=f"(v[2].y), "=f"(v[3].x),
+        "=f"(v[3].y)
+      : "r"(ta));
+}
+// 16 + 8 columns (three groups of 8), one wait.
+__device__ __forceinline__ void tmem_ld24_wait(uint32_t ta, float2 (&a)[4], float2 (&b)[4], float2 (&c)[4]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%24];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16,%17,%18,%19,%20,%21,%22,%23}, [%25];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=f"(a[0].x), "=f"(a[0].y), "=f"(a[1].x), "=f"(a[1].y), "=f"(a[2].x), "=f"(a[2].y), "=f"(a[3].x),
+        "=f"(a[3].y), "=f"(b[0].x), "=f"(b[0].y), "=f"(b[1].x), "=f"(b[1].y), "=f"(b[2].x), "=f"(b[2].y),
+        "=f"(b[3].x), "=f"(b[3].y), "=f"(c[0].x), "=f"(c[0].y), "=f"(c[1].x), "=f"(c[1].y), "=f"(c[2].x),
+        "=f"(c[2].y), "=f"(c[3].x), "=f"(c[3].y)
+      : "r"(ta), "r"(ta + 16));
+}
+// 16 columns (two groups of 8), one wait.
+__device__ __forceinline__ void tmem_ld16_wait(uint32_t ta, float2 (&a)[4], float2 (&b)[4]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=f"(a[0].x), "=f"(a[0].y), "=f"(a[1].x), "=f"(a[1].y), "=f"(a[2].x), "=f"(a[2].y), "=f"(a[3].x),
+        "=f"(a[3].y), "=f"(b[0].x), "=f"(b[0].y), "=f"(b[1].x), "=f"(b[1].y), "=f"(b[2].x), "=f"(b[2].y),
+        "=f"(b[3].x), "=f"(b[3].y)
+      : "r"(ta));
+}
+
+// Warp-wide NaN-propagating max (every lane gets it).
+__device__ __forceinline__ float warp_max_nan(float v) {
+  float r;
+  asm volatile("redux.sync.max.NaN.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+// Sum over lanes 0..15 (the rest hold zeros), broadcast to the warp.
+__device__ __forceinline__ float sum16(float v) {
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return __shfl_sync(0xffffffffu, v, 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -262,152 +361,149 @@ struct Out<GF32> {
 };
 
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
-// A copy the compiler cannot see through: values derived from it in one pass
-// are not reused in another, so the passes recompute from the 16-bit inputs
-// instead of keeping fp32 copies alive in registers.
-__device__ __forceinline__ float2 opaque(float2 a) {
-  float2 r;
-  asm volatile("mov.b32 %0, %2;\n\tmov.b32 %1, %3;" : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y));
-  return r;
-}
+__device__ __forceinline__ float2 neg(float2 a) { return make_float2(-a.x, -a.y); }
 __device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 __device__ __forceinline__ float2 ex2_2(float2 a) { return make_float2(ex2(a.x), ex2(a.y)); }
 __device__ __forceinline__ float2 lg2_2(float2 a) { return make_float2(lg2(a.x), lg2(a.y)); }
 
+// One 16-byte vector of the stage (plain shared-memory load: ordered after
+// the mbarrier waits and barriers, free to schedule otherwise).
+__device__ __forceinline__ uint4 lds16(const unsigned char* p) { return *reinterpret_cast<const uint4*>(p); }
+
 // ---------------------------------------------------------------------------
 // Cluster reductions by push. Each CTA reduces its partial over its warps
-// (shuffles + shared memory), then one lane per peer sends it with st.async
-// into that peer's slot for this CTA; the bytes complete on the peer's
+// (warp reductions + shared memory), then lane c of warp 0 sends it with
+// st.async into CTA c's slot for this CTA; the bytes complete on the peer's
 // mbarrier. A receiver arms its own mbarrier for C partials, waits on it and
 // merges the C slots from its own shared memory. There is no cluster-wide
 // barrier and no fence on the gradient stores in flight. Slots and mbarriers
 // are double-buffered by row parity: a CTA cannot run two rows ahead of a
 // peer, since it needs that peer's partial of every row to proceed.
+//
+// Statistics travel as (m_s, z_s, m_t, z_t): z relative to m, with z = NaN
+// marking an input outside the contract (a NaN, +inf or a max above 2^126),
+// which the merges propagate. Sums travel as (A, B) in nats; a KL support
+// violation makes A = +inf.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t map_rank(uint32_t local, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void push16(uint32_t remote, float a, float b, float c, float d, uint32_t remote_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(remote),
-      "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
-      : "memory");
-}
-// One try with cluster-scope acquire: the partials arrive from other CTAs.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* mb, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_addr(mb)), "r"(parity), "r"(kSuspendHintNs)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* mb, uint32_t parity) {
-  if (mbar_try_wait_cluster(mb, parity)) return true;
-  const uint64_t t0 = global_ns();
-  while (global_ns() - t0 < kWaitLimitNs)
-    if (mbar_try_wait_cluster(mb, parity)) return true;
-  return false;
-}
-
-struct Pair {  // statistics of both inputs and their out-of-contract flags
-  float ms, zs, mt, zt, bad_s, bad_t;
-};
-struct Sums {  // A, B and the support-violation flag of the KL branches
-  float a, b, viol;
+struct Tail {
+  uint64_t tma_bar[kStages];
+  uint64_t stat_bar[2];
+  uint64_t sum_bar[2];
+  uint32_t tmem_base;
+  uint32_t pad_;
+  __align__(16) float stat_warp[kWarps][4];
+  __align__(16) float sum_warp[kWarps][2];
+  __align__(16) float stat_slot[2][kMaxCluster][4];
+  __align__(16) float sum_slot[2][kMaxCluster][4];
 };
 
-__device__ __forceinline__ float warp_max_all(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-__device__ __forceinline__ float warp_sum_all(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// Merge the statistics held by the 32 lanes of a warp: MAX of the maxima,
-// then each lane's sum rescaled once to it (accurate exp) and summed.
-__device__ __forceinline__ Pair warp_merge(const Pair& x) {
-  const float ms = warp_max_all(x.ms), mt = warp_max_all(x.mt);
-  const float zs = warp_sum_all(x.zs * exp_acc(x.ms - stat_ref(ms)));
-  const float zt = warp_sum_all(x.zt * exp_acc(x.mt - stat_ref(mt)));
-  return {ms, zs, mt, zt, warp_max_all(x.bad_s), warp_max_all(x.bad_t)};
-}
-__device__ __forceinline__ Sums warp_merge(const Sums& x) {
-  return {warp_sum_all(x.a), warp_sum_all(x.b), warp_max_all(x.viol)};
-}
-
-__device__ __forceinline__ Pair pair_identity() { return {neg_inf(), 0.f, neg_inf(), 0.f, 0.f, 0.f}; }
-__device__ __forceinline__ Sums sums_identity() { return {0.f, 0.f, 0.f}; }
-__device__ __forceinline__ void put(float* p, const Pair& v) {
-  p[0] = v.ms, p[1] = v.zs, p[2] = v.mt, p[3] = v.zt, p[4] = v.bad_s, p[5] = v.bad_t;
-}
-__device__ __forceinline__ void put(float* p, const Sums& v) { p[0] = v.a, p[1] = v.b, p[2] = v.viol; }
-__device__ __forceinline__ void get(const float* p, Pair& v) { v = {p[0], p[1], p[2], p[3], p[4], p[5]}; }
-__device__ __forceinline__ void get(const float* p, Sums& v) { v = {p[0], p[1], p[2]}; }
-__device__ __forceinline__ void identity(Pair& v) { v = pair_identity(); }
-__device__ __forceinline__ void identity(Sums& v) { v = sums_identity(); }
-template <class V> struct SlotWords;
-template <> struct SlotWords<Pair> { static constexpr int kW = 8; };
-template <> struct SlotWords<Sums> { static constexpr int kW = 4; };
-__device__ __forceinline__ void push(uint32_t dst, const Pair& v, uint32_t bar) {
-  push16(dst, v.ms, v.zs, v.mt, v.zt, bar);
-  push16(dst + 16, v.bad_s, v.bad_t, 0.f, 0.f, bar);
-}
-__device__ __forceinline__ void push(uint32_t dst, const Sums& v, uint32_t bar) {
-  push16(dst, v.a, v.b, v.viol, 0.f, bar);
-}
-
-// Reduce v over this CTA of T threads and push the result to slot `crank` of
-// every CTA of the cluster.
-template <int T, class V>
-__device__ __forceinline__ void reduce_and_push(V v, float* warp_slots, float* slots, uint64_t* bar,
-                                                uint32_t crank, uint32_t csize) {
-  constexpr int kW = SlotWords<V>::kW;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = warp_merge(v);
-  if (lane == 0) put(warp_slots + warp * kW, v);
-  __syncthreads();
-  if (warp == 0) {
-    V w;
-    if (lane < T / 32) get(warp_slots + lane * kW, w);
-    else identity(w);
-    w = warp_merge(w);
-    if (lane < static_cast<int>(csize))
-      push(map_rank(smem_addr(slots + crank * kW), lane), w, map_rank(smem_addr(bar), lane));
-  }
+// Merge (m, z) over lanes 0..15 of a warp (lanes beyond hold (-inf, 0)).
+__device__ __forceinline__ float2 merge16(float m, float z) {
+  const float mx = warp_max_nan(m);
+  return make_float2(mx, sum16(z * exp_acc(m - stat_ref(mx))));
 }
 
 // Arm this CTA's mbarrier for the C partials of one row; one thread waits
 // (bounded) while the others sleep in the CTA barrier, then every thread
-// takes the phase with cluster-scope acquire and merges the slots. `ok`
-// becomes false for every thread if the wait gave up.
-template <class V>
-__device__ __forceinline__ V collect(const float* slots, uint64_t* bar, uint32_t parity, uint32_t csize,
-                                     bool& ok) {
-  constexpr int kW = SlotWords<V>::kW;
+// takes the phase with cluster-scope acquire. `ok` becomes false for every
+// thread if the wait gave up.
+__device__ __forceinline__ void arm_and_wait(uint64_t* bar, uint32_t parity, uint32_t bytes, bool& ok) {
   bool mine = true;
   if (threadIdx.x == 0) {
-    mbar_expect_tx(bar, csize * kW * 4u);
+    mbar_expect_tx(bar, bytes);
     mine = mbar_wait_cluster(bar, parity);
   }
   ok = __syncthreads_and(mine) && ok;
   if (ok && threadIdx.x != 0) mbar_try_wait_cluster(bar, parity);
+}
+
+// Global statistics of one row: (m_s, z_s, m_t, z_t), every thread.
+__device__ __forceinline__ float4 collect_stats(const float (*slot)[4], uint64_t* bar, uint32_t parity,
+                                                uint32_t csize, bool& ok) {
+  arm_and_wait(bar, parity, csize * 16u, ok);
   const int lane = threadIdx.x & 31;
-  V c;
-  if (lane < static_cast<int>(csize)) get(slots + lane * kW, c);
-  else identity(c);
-  return warp_merge(c);
+  float4 v = make_float4(neg_inf(), 0.f, neg_inf(), 0.f);
+  if (lane < static_cast<int>(csize)) v = *reinterpret_cast<const float4*>(slot[lane]);
+  const float2 s = merge16(v.x, v.y), t = merge16(v.z, v.w);
+  return make_float4(s.x, s.y, t.x, t.y);
+}
+// Global (A, B) of one row, every thread.
+__device__ __forceinline__ float2 collect_sums(const float (*slot)[4], uint64_t* bar, uint32_t parity,
+                                               uint32_t csize, bool& ok) {
+  arm_and_wait(bar, parity, csize * 16u, ok);
+  const int lane = threadIdx.x & 31;
+  float2 v = make_float2(0.f, 0.f);
+  if (lane < static_cast<int>(csize)) v = *reinterpret_cast<const float2*>(slot[lane]);
+  return make_float2(sum16(v.x), sum16(v.y));
+}
+
+// Statistics partial of one row read from its shared-memory stage, merged over
+// the CTA and pushed to every CTA of the cluster (slot `crank`).
+template <class In, int R>
+__device__ __forceinline__ void stage_stats(const unsigned char* sb, int W, int len, Tail* tail, int par,
+                                            uint32_t crank, uint32_t csize) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t mxs = In::kNegInf2, mxt = In::kNegInf2;
+#pragma unroll
+  for (int k = 0; k < R; ++k) {
+    const int e0 = (k * kT + tid) * 8;
+    if (e0 < len) {
+      const uint4 u = lds16(sb + e0 * 2), v = lds16(sb + static_cast<size_t>(W) * 2 + e0 * 2);
+      mxs = In::max_nan(mxs, In::max_nan(In::max_nan(u.x, u.y), In::max_nan(u.z, u.w)));
+      mxt = In::max_nan(mxt, In::max_nan(In::max_nan(v.x, v.y), In::max_nan(v.z, v.w)));
+    }
+  }
+  const float2 a = In::unpack(mxs), b = In::unpack(mxt);
+  const float m_s = warp_max_nan(max_nan(a.x, a.y)), m_t = warp_max_nan(max_nan(b.x, b.y));
+  const float2 l2e2 = f2(kLog2e), ns2 = f2(-stat_ref(m_s)), nt2 = f2(-stat_ref(m_t));
+  float2 zs2 = f2(0.f), zt2 = f2(0.f);
+#pragma unroll
+  for (int k = 0; k < R; ++k) {
+    const int e0 = (k * kT + tid) * 8;
+    if (e0 < len) {
+      const uint4 u = lds16(sb + e0 * 2), v = lds16(sb + static_cast<size_t>(W) * 2 + e0 * 2);
+      const uint32_t us[4] = {u.x, u.y, u.z, u.w}, vs[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        // x - m is exact; a -inf entry gives 2^-inf = 0, a NaN gives NaN
+        zs2 = add2(zs2, ex2_2(mul2(In::sub(us[w], ns2), l2e2)));
+        zt2 = add2(zt2, ex2_2(mul2(In::sub(vs[w], nt2), l2e2)));
+      }
+    }
+  }
+  float z_s = warp_sum(zs2.x + zs2.y), z_t = warp_sum(zt2.x + zt2.y);
+  if (!(m_s <= kMaxLogit)) z_s = qnan();  // NaN, +inf or a max above 2^126
+  if (!(m_t <= kMaxLogit)) z_t = qnan();
+  if (lane == 0) *reinterpret_cast<float4*>(tail->stat_warp[warp]) = make_float4(m_s, z_s, m_t, z_t);
+  __syncthreads();
+  if (warp == 0) {
+    float4 v = make_float4(neg_inf(), 0.f, neg_inf(), 0.f);
+    if (lane < kWarps) v = *reinterpret_cast<const float4*>(tail->stat_warp[lane]);
+    const float2 s = merge16(v.x, v.y), t = merge16(v.z, v.w);
+    if (lane < static_cast<int>(csize))
+      push16(map_rank(smem_addr(tail->stat_slot[par][crank]), lane), s.x, s.y, t.x, t.y,
+             map_rank(smem_addr(&tail->stat_bar[par]), lane));
+  }
+}
+
+// Reduce (A, B) in nats over the CTA and push them to every CTA of the cluster.
+__device__ __forceinline__ void push_sums(float a, float b, Tail* tail, int par, uint32_t crank, uint32_t csize) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  a = warp_sum(a);
+  b = warp_sum(b);
+  if (lane == 0) *reinterpret_cast<float2*>(tail->sum_warp[warp]) = make_float2(a, b);
+  __syncthreads();
+  if (warp == 0) {
+    float2 v = make_float2(0.f, 0.f);
+    if (lane < kWarps) v = *reinterpret_cast<const float2*>(tail->sum_warp[lane]);
+    a = sum16(v.x);
+    b = sum16(v.y);
+    if (lane < static_cast<int>(csize))
+      push16(map_rank(smem_addr(tail->sum_slot[par][crank]), lane), a, b, 0.f, 0.f,
+             map_rank(smem_addr(&tail->sum_bar[par]), lane));
+  }
 }
 
 struct FusedArgs {
@@ -425,109 +521,23 @@ struct FusedArgs {
   int64_t withhold_row;  // test hook: CTA 0 of the owning cluster never copies this row (-1: none)
 };
 
-// Shared memory: [kStages][2 inputs][W] 16-bit elements, then this tail.
-template <int T>
-struct Tail {
-  uint64_t tma_bar[kStages];
-  uint64_t stat_bar[2];
-  uint64_t sum_bar[2];
-  float stat_warp[T / 32 * SlotWords<Pair>::kW];
-  float sum_warp[T / 32 * SlotWords<Sums>::kW];
-  __align__(16) float stat_slot[2][kMaxCluster * SlotWords<Pair>::kW];
-  __align__(16) float sum_slot[2][kMaxCluster * SlotWords<Sums>::kW];
-};
-
-// Statistics partial of one row read straight from its shared-memory stage:
-// NaN-propagating maxima of the raw pairs, then the sum of 2^((x - m) log2 e)
-// relative to this thread's max (a -inf entry contributes 2^-inf = 0; the
-// rounding of m log2 e is common to every term of the row and cancels in the
-// normalisation).
-template <class In, int T, int R>
-__device__ __forceinline__ Pair stage_stats(const unsigned char* sb, int W, int len) {
-  const int tid = threadIdx.x;
-  uint32_t mxs = In::kNegInf2, mxt = In::kNegInf2;
-#pragma unroll
-  for (int k = 0; k < R; ++k) {
-    const int e0 = (k * T + tid) * 8;
-    if (e0 < len) {
-      const uint4 u = ld_shared16(sb + e0 * 2);
-      const uint4 v = ld_shared16(sb + static_cast<size_t>(W) * 2 + e0 * 2);
-      mxs = In::max_nan(In::max_nan(mxs, u.x), In::max_nan(u.y, In::max_nan(u.z, u.w)));
-      mxt = In::max_nan(In::max_nan(mxt, v.x), In::max_nan(v.y, In::max_nan(v.z, v.w)));
-    }
-  }
-  const float2 ms2 = In::unpack(mxs), mt2 = In::unpack(mxt);
-  const float m_s = fmaxf(ms2.x, ms2.y), m_t = fmaxf(mt2.x, mt2.y);
-  const bool bad_s = isnan(ms2.x) || isnan(ms2.y) || m_s > kMaxLogit;
-  const bool bad_t = isnan(mt2.x) || isnan(mt2.y) || m_t > kMaxLogit;
-  const float2 l2e2 = f2(kLog2e), ns2 = f2(-stat_ref(m_s)), nt2 = f2(-stat_ref(m_t));
-  float2 zs2 = f2(0.f), zt2 = f2(0.f);
-#pragma unroll
-  for (int k = 0; k < R; ++k) {
-    const int e0 = (k * T + tid) * 8;
-    if (e0 < len) {
-      const uint4 u = ld_shared16(sb + e0 * 2);
-      const uint4 v = ld_shared16(sb + static_cast<size_t>(W) * 2 + e0 * 2);
-      const uint32_t us[4] = {u.x, u.y, u.z, u.w}, vs[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        // x - m is exact; a -inf entry gives 2^-inf = 0
-        zs2 = add2(zs2, ex2_2(mul2(In::sub(us[w], ns2), l2e2)));
-        zt2 = add2(zt2, ex2_2(mul2(In::sub(vs[w], nt2), l2e2)));
-      }
-    }
-  }
-  return {m_s, zs2.x + zs2.y, m_t, zt2.x + zt2.y, bad_s ? 1.f : 0.f, bad_t ? 1.f : 0.f};
-}
-
-// Copy one row's stage into registers with -inf clamped to the floor; flags a
-// KL support violation (the target finite where the other side is -inf).
-template <class In, int T, int R, int MODE>
-__device__ __forceinline__ void stage_to_regs(const unsigned char* sb, int W, int len, uint32_t (&xs)[R][4],
-                                              uint32_t (&xt)[R][4], uint32_t& viol) {
-  const int tid = threadIdx.x;
-  viol = 0;
-#pragma unroll
-  for (int k = 0; k < R; ++k) {
-    const int e0 = (k * T + tid) * 8;
-    if (e0 < len) {
-      const uint4 u = ld_shared16(sb + e0 * 2);
-      const uint4 v = ld_shared16(sb + static_cast<size_t>(W) * 2 + e0 * 2);
-      const uint32_t us[4] = {u.x, u.y, u.z, u.w}, vs[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        if (MODE != kInterior) {
-          const uint32_t tgt = MODE == kForwardKL ? vs[w] : us[w];
-          const uint32_t oth = MODE == kForwardKL ? us[w] : vs[w];
-          viol |= __vcmpeq2(oth, In::kNegInf2) & ~__vcmpeq2(tgt, In::kNegInf2);
-        }
-        xs[k][w] = In::max2(us[w], In::kNegBig2);
-        xt[k][w] = In::max2(vs[w], In::kNegBig2);
-      }
-    } else {
-#pragma unroll
-      for (int w = 0; w < 4; ++w) xs[k][w] = xt[k][w] = In::kNegBig2;
-    }
-  }
-}
-
 // log2 of the probabilities of one packed pair: (x - m) log2 e - K.
 template <class In>
 __device__ __forceinline__ float2 lam(uint32_t w, float2 nm, float2 l2e2, float2 nK) {
   return fma2(In::sub(w, nm), l2e2, nK);
 }
 
-template <class In, class G, int T, int R, int MODE, bool KEEP>
-__global__ void __launch_bounds__(T, 1) k_jsd_fused(FusedArgs a) {
+template <class In, class G, int R, int MODE>
+__global__ void __launch_bounds__(kT, 1) k_jsd_fused(FusedArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int kCols = Cols<MODE>::k;
   const int W = a.W;
-  unsigned char* stage_base = smem;
-  Tail<T>* tail = reinterpret_cast<Tail<T>*>(smem + static_cast<size_t>(kStages) * 2 * W * 2);
-  auto stage_ptr = [&](int st) { return stage_base + static_cast<size_t>(st) * 2 * W * 2; };
+  Tail* tail = reinterpret_cast<Tail*>(smem + static_cast<size_t>(kStages) * 4 * W);
+  auto stage_ptr = [&](int st) { return smem + static_cast<size_t>(st) * 4 * W; };
 
   const uint32_t crank = cluster_rank(), csize = cluster_size();
   const int64_t q = cluster_index(), Q = cluster_count();
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int64_t col0 = static_cast<int64_t>(crank) * W;
   const int64_t rest = a.vocab - col0;
   const int len = rest <= 0 ? 0 : (rest < W ? static_cast<int>(rest) : W);
@@ -552,9 +562,16 @@ __global__ void __launch_bounds__(T, 1) k_jsd_fused(FusedArgs a) {
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  if (warp == 0) tmem_alloc(&tail->tmem_base);
+  tmem_fence_before();
   __syncthreads();
-  uint32_t pending = 0;                  // bit st: a copy into stage st is in flight
-  uint32_t tma_done[kStages] = {0, 0};   // completed waits per stage
+  tmem_fence_after();
+  // This thread's TMEM lane (its warp's lane quarter) and column range.
+  const uint32_t tmem = tail->tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16) +
+                        static_cast<uint32_t>((kTmemCols / (kWarps / 4)) * (warp >> 2));
+
+  uint32_t pending = 0;                 // bit st: a copy into stage st is in flight
+  uint32_t tma_done[kStages] = {0, 0};  // completed waits per stage
   if (tid == 0 && bytes) {
     for (int st = 0; st < kStages; ++st)
       if (q + st * Q < a.rows) issue(q + st * Q, st);
@@ -576,20 +593,12 @@ __global__ void __launch_bounds__(T, 1) k_jsd_fused(FusedArgs a) {
   };
 
   const float beta = a.beta;
-  const float2 ws2 = f2(1.f - beta), wt2 = f2(beta), tiny2 = f2(kTiny), l2e2 = f2(kLog2e), neg2 = f2(-1.f);
-  uint32_t xs[R][4], xt[R][4];
-  uint32_t viol = 0;
+  const float2 ws2 = f2(1.f - beta), wt2 = f2(beta), tiny2 = f2(kTiny), l2e2 = f2(kLog2e);
 
-  // Row 0 of this cluster: statistics partial straight from its stage, then registers.
+  // Statistics of this cluster's first row.
   if (q < a.rows) {
     wait_stage(0);
-    reduce_and_push<T, Pair>(stage_stats<In, T, R>(stage_ptr(0), W, len), tail->stat_warp,
-                                tail->stat_slot[0], &tail->stat_bar[0], crank, csize);
-    stage_to_regs<In, T, R, MODE>(stage_ptr(0), W, len, xs, xt, viol);
-    __syncthreads();
-    const bool more = ok && q + kStages * Q < a.rows;  // no new copy after a failed wait
-    if (tid == 0 && bytes && more) issue(q + kStages * Q, 0);
-    if (bytes && more && !withheld(q + kStages * Q)) pending |= 1u;
+    stage_stats<In, R>(stage_ptr(0), W, len, tail, 0, crank, csize);
   }
 
   int64_t i = 0;
@@ -597,79 +606,107 @@ __global__ void __launch_bounds__(T, 1) k_jsd_fused(FusedArgs a) {
     const int par = static_cast<int>(i & 1);
     const uint32_t ph = static_cast<uint32_t>((i >> 1) & 1);
     const bool has_next = r + Q < a.rows;
-    const int nst = static_cast<int>((i + 1) % kStages);  // stage of the next row
+    const int cst = static_cast<int>(i % kStages);  // stage of this row
+    const int nst = static_cast<int>((i + 1) % kStages);
 
     // (1) global statistics of row r
-    const Pair g_st = collect<Pair>(tail->stat_slot[par], &tail->stat_bar[par], ph, csize, ok);
-    const bool row_ok = g_st.bad_s == 0.f && g_st.bad_t == 0.f && g_st.ms != neg_inf() && g_st.mt != neg_inf();
-    const float Ks = row_ok ? log2f(g_st.zs) : qnan();  // log2 Z
-    const float Kt = row_ok ? log2f(g_st.zt) : qnan();
-    const float2 nms2 = f2(-g_st.ms), nmt2 = f2(-g_st.mt), nKs2 = f2(-Ks), nKt2 = f2(-Kt);
+    const float4 g = collect_stats(tail->stat_slot[par], &tail->stat_bar[par], ph, csize, ok);
+    const bool bad_s = isnan(g.y), bad_t = isnan(g.w);
+    const bool row_ok = !bad_s && !bad_t && g.x != neg_inf() && g.z != neg_inf();
+    const float Ks = row_ok ? log2f(g.y) : qnan();  // log2 Z
+    const float Kt = row_ok ? log2f(g.w) : qnan();
+    const float2 nms2 = f2(-g.x), nmt2 = f2(-g.z), nKs2 = f2(-Ks), nKt2 = f2(-Kt);
 
-    // (2) pass C of row r from registers, in log2 units. Kept: p, q and the two
-    // log-ratios (interior: log2 p - log2 M, log2 q - log2 M; KL branches: the
-    // log2 ratio target/other). Recompute: -log2 M only.
-    float2 kp[KEEP ? R : 1][4], kq[KEEP ? R : 1][4], ku[KEEP ? R : 1][4], kv[KEEP && MODE == kInterior ? R : 1][4];
-    float2 nlm_r[KEEP ? 1 : R][4];
+    // (2) pass C of row r from its stage, in log2 units. TMEM per vector:
+    // interior p, log2 p - log2 M, log2 q - log2 M; KL p, log2 ratio. q in
+    // registers. Warps past the slice skip a vector together; inside a warp,
+    // lanes past it compute on the floor value (p = q = 0) so that the TMEM
+    // stores stay warp-uniform.
+    float2 kq[R][4];
     float2 acc_a = f2(0.f), acc_b = f2(0.f);
+    uint32_t viol = 0;
     if (row_ok) {
-      const float2 nmsC = opaque(nms2), nmtC = opaque(nmt2);
+      const unsigned char* sb = stage_ptr(cst);
 #pragma unroll
-      for (int k = 0; k < R; ++k)
+      for (int k = 0; k < R; ++k) {
+        if ((k * kT + warp * 32) * 8 >= len) continue;  // warp-uniform
+        const int e0 = (k * kT + tid) * 8;
+        uint4 u = make_uint4(In::kNegBig2, In::kNegBig2, In::kNegBig2, In::kNegBig2), v = u;
+        if (e0 < len) {
+          u = lds16(sb + e0 * 2);
+          v = lds16(sb + static_cast<size_t>(W) * 2 + e0 * 2);
+        }
+        const uint32_t us[4] = {u.x, u.y, u.z, u.w}, vs[4] = {v.x, v.y, v.z, v.w};
+        float2 t0[4], t1[4], t2[4];
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-          const float2 lp = lam<In>(xs[k][w], nmsC, l2e2, nKs2);
-          const float2 lq = lam<In>(xt[k][w], nmtC, l2e2, nKt2);
+          if (MODE != kInterior) {
+            const uint32_t tgt = MODE == kForwardKL ? vs[w] : us[w];
+            const uint32_t oth = MODE == kForwardKL ? us[w] : vs[w];
+            viol |= __vcmpeq2(oth, In::kNegInf2) & ~__vcmpeq2(tgt, In::kNegInf2);
+          }
+          const float2 lp = lam<In>(In::max2(us[w], In::kNegBig2), nms2, l2e2, nKs2);
+          const float2 lq = lam<In>(In::max2(vs[w], In::kNegBig2), nmt2, l2e2, nKt2);
           const float2 p = ex2_2(lp), qv = ex2_2(lq);
+          kq[k][w] = qv;
+          t0[w] = p;
           if (MODE == kInterior) {
-            const float2 nlm = mul2(lg2_2(fma2(ws2, p, fma2(wt2, qv, tiny2))), neg2);
-            const float2 us = add2(lp, nlm), ut = add2(lq, nlm);
-            acc_a = fma2(qv, ut, acc_a);
-            acc_b = fma2(p, us, acc_b);
-            if constexpr (KEEP) {
-              kp[k][w] = p, kq[k][w] = qv, ku[k][w] = us, kv[k][w] = ut;
-            } else {
-              nlm_r[k][w] = nlm;
-            }
+            const float2 lm = lg2_2(fma2(ws2, p, fma2(wt2, qv, tiny2)));
+            const float2 us_ = add2(lp, neg(lm)), ut_ = add2(lq, neg(lm));
+            acc_b = fma2(p, us_, acc_b);
+            acc_a = fma2(qv, ut_, acc_a);
+            t1[w] = us_;
+            t2[w] = ut_;
           } else {
             // forward KL(q || p): d = log2 q - log2 p weighted by q; reverse: mirror
-            const float2 d = MODE == kForwardKL ? add2(lq, mul2(lp, neg2)) : add2(lp, mul2(lq, neg2));
+            const float2 d = MODE == kForwardKL ? add2(lq, neg(lp)) : add2(lp, neg(lq));
             acc_a = fma2(MODE == kForwardKL ? qv : p, d, acc_a);
-            if constexpr (KEEP) kp[k][w] = p, kq[k][w] = qv, ku[k][w] = d;
+            t1[w] = d;
           }
         }
+        tmem_st8(tmem + k * kCols, t0);
+        tmem_st8(tmem + k * kCols + 8, t1);
+        if (MODE == kInterior) tmem_st8(tmem + k * kCols + 16, t2);
+      }
+      tmem_wait_st();
     }
-    reduce_and_push<T, Sums>({kLn2 * (acc_a.x + acc_a.y), kLn2 * (acc_b.x + acc_b.y), viol ? 1.f : 0.f},
-                               tail->sum_warp, tail->sum_slot[par], &tail->sum_bar[par], crank, csize);
+    float sa = kLn2 * (acc_a.x + acc_a.y);
+    if (MODE != kInterior && viol) sa = pos_inf();
+    push_sums(sa, kLn2 * (acc_b.x + acc_b.y), tail, par, crank, csize);
+    // every thread has read this row's stage: refill it with the row kStages on
+    {
+      const bool more = ok && r + kStages * Q < a.rows;  // no new copy after a failed wait
+      if (tid == 0 && bytes && more) issue(r + kStages * Q, cst);
+      if (bytes && more && !withheld(r + kStages * Q)) pending |= 1u << cst;
+    }
 
     // (3) statistics partial of the next row, straight from its stage, while
     // this row's sums travel
     if (has_next) {
       wait_stage(nst);
-      reduce_and_push<T, Pair>(stage_stats<In, T, R>(stage_ptr(nst), W, len), tail->stat_warp,
-                                  tail->stat_slot[par ^ 1], &tail->stat_bar[par ^ 1], crank, csize);
+      stage_stats<In, R>(stage_ptr(nst), W, len, tail, par ^ 1, crank, csize);
     }
 
     // (4) global sums of row r; the per-token value and saved statistics
-    const Sums g_ab = collect<Sums>(tail->sum_slot[par], &tail->sum_bar[par], ph, csize, ok);
-    float A = g_ab.a, B = g_ab.b, value;
+    const float2 ab = collect_sums(tail->sum_slot[par], &tail->sum_bar[par], ph, csize, ok);
+    float A = ab.x, B = ab.y, value;
     if (!row_ok) {
       value = qnan();
       A = B = qnan();
     } else if (MODE == kInterior) {
       value = beta * A + (1.f - beta) * B;
     } else {
-      value = g_ab.viol != 0.f ? pos_inf() : A;
+      value = A;  // +inf on a support violation
       A = MODE == kForwardKL ? value : 0.f;
       B = MODE == kForwardKL ? 0.f : value;
     }
     if (crank == 0 && tid == 0) {
       a.loss[r] = value;
       float* sv = a.saved + r * VPD_SAVED_PAIR;
-      sv[0] = g_st.bad_s != 0.f ? qnan() : g_st.ms;
-      sv[1] = g_st.bad_s != 0.f ? qnan() : (g_st.ms == neg_inf() ? neg_inf() : kLn2 * log2f(g_st.zs));
-      sv[2] = g_st.bad_t != 0.f ? qnan() : g_st.mt;
-      sv[3] = g_st.bad_t != 0.f ? qnan() : (g_st.mt == neg_inf() ? neg_inf() : kLn2 * log2f(g_st.zt));
+      sv[0] = bad_s ? qnan() : g.x;
+      sv[1] = bad_s ? qnan() : (g.x == neg_inf() ? neg_inf() : kLn2 * log2f(g.y));
+      sv[2] = bad_t ? qnan() : g.z;
+      sv[3] = bad_t ? qnan() : (g.z == neg_inf() ? neg_inf() : kLn2 * log2f(g.w));
       sv[4] = A;
       sv[5] = B;
     }
@@ -686,57 +723,38 @@ __global__ void __launch_bounds__(T, 1) k_jsd_fused(FusedArgs a) {
       const float2 ncs2 = f2(-cs * (MODE == kInterior ? B : value));
       const float2 nct2 = f2(-ct * (MODE == kInterior ? A : value));
       const float2 g2 = f2(gr);
-      const float2 nmsD = opaque(nms2), nmtD = opaque(nmt2);
 #pragma unroll
       for (int k = 0; k < R; ++k) {
-        const int e0 = (k * T + tid) * 8;
-        if (e0 >= len) continue;
+        if ((k * kT + warp * 32) * 8 >= len) continue;  // warp-uniform
+        const int e0 = (k * kT + tid) * 8;
         float2 gs[4], gt[4];
         if (!live) {
 #pragma unroll
           for (int w = 0; w < 4; ++w) gs[w] = gt[w] = f2(0.f);
         } else {
+          float2 p[4], u1[4], u2[4];
+          if (MODE == kInterior) tmem_ld24_wait(tmem + k * kCols, p, u1, u2);
+          else tmem_ld16_wait(tmem + k * kCols, p, u1);
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
-            float2 p, qv, us, ut;
-            if constexpr (KEEP) {
-              p = kp[k][w], qv = kq[k][w], us = ku[k][w];
-              ut = MODE == kInterior ? kv[k][w] : us;
-            } else {
-              const float2 lp = lam<In>(xs[k][w], nmsD, l2e2, nKs2);
-              const float2 lq = lam<In>(xt[k][w], nmtD, l2e2, nKt2);
-              p = ex2_2(lp), qv = ex2_2(lq);
-              if (MODE == kInterior) {
-                us = add2(lp, nlm_r[k][w]), ut = add2(lq, nlm_r[k][w]);
-              } else {
-                us = ut = MODE == kForwardKL ? add2(lq, mul2(lp, neg2)) : add2(lp, mul2(lq, neg2));
-              }
-            }
+            const float2 qv = kq[k][w];
             if (MODE == kInterior) {
-              gs[w] = mul2(p, fma2(cs2, us, ncs2));
-              gt[w] = mul2(qv, fma2(ct2, ut, nct2));
+              gs[w] = mul2(p[w], fma2(cs2, u1[w], ncs2));
+              gt[w] = mul2(qv, fma2(ct2, u2[w], nct2));
             } else if (MODE == kForwardKL) {  // dS = g (p - q), dT = g q (ln q - ln p - KL)
-              gs[w] = mul2(g2, add2(p, mul2(qv, neg2)));
-              gt[w] = mul2(qv, fma2(ct2, ut, nct2));
+              gs[w] = mul2(g2, add2(p[w], neg(qv)));
+              gt[w] = mul2(qv, fma2(ct2, u1[w], nct2));
             } else {  // dS = g p (ln p - ln q - KL), dT = g (q - p)
-              gs[w] = mul2(p, fma2(cs2, us, ncs2));
-              gt[w] = mul2(g2, add2(qv, mul2(p, neg2)));
+              gs[w] = mul2(p[w], fma2(cs2, u1[w], ncs2));
+              gt[w] = mul2(g2, add2(qv, neg(p[w])));
             }
           }
         }
-        if (ds_row) Out<G>::store8(ds_row + static_cast<int64_t>(e0) * Out<G>::kSize, gs);
-        if (dt_row) Out<G>::store8(dt_row + static_cast<int64_t>(e0) * Out<G>::kSize, gt);
+        if (e0 < len) {
+          if (ds_row) Out<G>::store8(ds_row + static_cast<int64_t>(e0) * Out<G>::kSize, gs);
+          if (dt_row) Out<G>::store8(dt_row + static_cast<int64_t>(e0) * Out<G>::kSize, gt);
+        }
       }
-    }
-
-    // (6) the next row into registers; its stage is then free for the row
-    // kStages further on
-    if (has_next) {
-      stage_to_regs<In, T, R, MODE>(stage_ptr(nst), W, len, xs, xt, viol);
-      __syncthreads();
-      const bool more = ok && r + (kStages + 1) * Q < a.rows;  // no new copy after a failed wait
-      if (tid == 0 && bytes && more) issue(r + (kStages + 1) * Q, nst);
-      if (bytes && more && !withheld(r + (kStages + 1) * Q)) pending |= 1u << nst;
     }
   }
 
@@ -744,6 +762,13 @@ __global__ void __launch_bounds__(T, 1) k_jsd_fused(FusedArgs a) {
   for (int st = 0; st < kStages; ++st)
     if (pending & (1u << st)) mbar_wait(&tail->tma_bar[st], tma_done[st] & 1u);
   if (!ok && tid == 0) atomicExch(&g_fused_error, 1);
+  tmem_wait_st();
+  tmem_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tmem_fence_after();
+    tmem_dealloc(tail->tmem_base);
+  }
   cluster_sync();  // no CTA leaves while a peer may still push into it
 }
 
@@ -751,10 +776,16 @@ __global__ void __launch_bounds__(T, 1) k_jsd_fused(FusedArgs a) {
 // Host side (per input dtype): one configuration, one launch.
 // ---------------------------------------------------------------------------
 struct Config {
-  int C, T, R, W;
-  bool keep;
+  int C, R, W;
   size_t smem;
 };
+
+// Shared memory of a slice width: both stages of both inputs, then the tail,
+// and at least kMinSmem so that no two CTAs share an SM's tensor memory.
+inline size_t smem_bytes(int W) {
+  const size_t s = static_cast<size_t>(kStages) * 4 * W + sizeof(Tail);
+  return s < kMinSmem ? kMinSmem : s;
+}
 
 // Launches the configured kernel; cudaErrorNotSupported (nothing launched)
 // when no cluster of that shape can be resident. `clusters_out` reports the
@@ -762,10 +793,13 @@ struct Config {
 template <class In>
 cudaError_t launch_typed(const FusedArgs& args, const Config& cfg, int mode, bool f32grad, cudaStream_t stream,
                          int* clusters_out);
+// Resident clusters of C CTAs (0 when none fit), for this dtype's kernels.
+template <class In>
+int resident_clusters(int C, size_t smem);
 
-template <class In, class G, int T, int R, int MODE, bool KEEP>
-cudaError_t launch_one(const FusedArgs& args, const Config& cfg, cudaStream_t stream, int* clusters_out) {
-  auto kern = k_jsd_fused<In, G, T, R, MODE, KEEP>;
+template <class In, class G, int R, int MODE>
+cudaError_t setup_one(const Config& cfg, cudaLaunchConfig_t* lc, cudaLaunchAttribute* attr, int* clusters) {
+  auto kern = k_jsd_fused<In, G, R, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(cfg.smem));
   if (e != cudaSuccess) return e;
@@ -776,48 +810,46 @@ cudaError_t launch_one(const FusedArgs& args, const Config& cfg, cudaStream_t st
       return cudaErrorNotSupported;
     }
   }
-  cudaLaunchConfig_t lc = {};
-  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cfg.C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  lc.blockDim = dim3(T, 1, 1);
-  lc.dynamicSmemBytes = cfg.smem;
-  lc.stream = stream;
-  lc.attrs = attr;
-  lc.numAttrs = 1;
-  lc.gridDim = dim3(cfg.C, 1, 1);
-  int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, kern, &lc);
-  if (e != cudaSuccess || clusters < 1) {
+  lc->blockDim = dim3(kT, 1, 1);
+  lc->dynamicSmemBytes = cfg.smem;
+  lc->attrs = attr;
+  lc->numAttrs = 1;
+  lc->gridDim = dim3(cfg.C, 1, 1);
+  *clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(clusters, kern, lc);
+  if (e != cudaSuccess || *clusters < 1) {
     cudaGetLastError();
     return cudaErrorNotSupported;
   }
+  return cudaSuccess;
+}
+
+template <class In, class G, int R, int MODE>
+cudaError_t launch_one(const FusedArgs& args, const Config& cfg, cudaStream_t stream, int* clusters_out) {
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute attr[1];
+  int clusters = 0;
+  cudaError_t e = setup_one<In, G, R, MODE>(cfg, &lc, attr, &clusters);
+  if (e != cudaSuccess) return e;
   *clusters_out = clusters;
   const int64_t want = args.rows < clusters ? args.rows : clusters;
   lc.gridDim = dim3(static_cast<unsigned>(want * cfg.C), 1, 1);
-  return cudaLaunchKernelEx(&lc, kern, args);
+  lc.stream = stream;
+  return cudaLaunchKernelEx(&lc, k_jsd_fused<In, G, R, MODE>, args);
 }
 
 template <class In, class G, int MODE>
 cudaError_t launch_r(const FusedArgs& args, const Config& cfg, cudaStream_t stream, int* clusters) {
-  if (cfg.keep) {
-    switch (cfg.R) {
-      case 1: return launch_one<In, G, kKeepT, 1, MODE, true>(args, cfg, stream, clusters);
-      case 2: return launch_one<In, G, kKeepT, 2, MODE, true>(args, cfg, stream, clusters);
-      case 3: return launch_one<In, G, kKeepT, 3, MODE, true>(args, cfg, stream, clusters);
-      case 4: return launch_one<In, G, kKeepT, 4, MODE, true>(args, cfg, stream, clusters);
-      case 5: return launch_one<In, G, kKeepT, 5, MODE, true>(args, cfg, stream, clusters);
-    }
-  } else {
-    switch (cfg.R) {
-      case 1: return launch_one<In, G, kRecomputeT, 1, MODE, false>(args, cfg, stream, clusters);
-      case 2: return launch_one<In, G, kRecomputeT, 2, MODE, false>(args, cfg, stream, clusters);
-      case 3: return launch_one<In, G, kRecomputeT, 3, MODE, false>(args, cfg, stream, clusters);
-      case 4: return launch_one<In, G, kRecomputeT, 4, MODE, false>(args, cfg, stream, clusters);
-      case 5: return launch_one<In, G, kRecomputeT, 5, MODE, false>(args, cfg, stream, clusters);
-    }
+  switch (cfg.R) {
+    case 1: return launch_one<In, G, 1, MODE>(args, cfg, stream, clusters);
+    case 2: return launch_one<In, G, 2, MODE>(args, cfg, stream, clusters);
+    case 3: return launch_one<In, G, 3, MODE>(args, cfg, stream, clusters);
+    case 4: return launch_one<In, G, 4, MODE>(args, cfg, stream, clusters);
+    case 5: return launch_one<In, G, 5, MODE>(args, cfg, stream, clusters);
   }
   return cudaErrorNotSupported;
 }
@@ -834,6 +866,16 @@ cudaError_t launch_typed(const FusedArgs& args, const Config& cfg, int mode, boo
                    : launch_r<In, GIn, kReverseKL>(args, cfg, stream, clusters);
   return f32grad ? launch_r<In, GF32, kInterior>(args, cfg, stream, clusters)
                  : launch_r<In, GIn, kInterior>(args, cfg, stream, clusters);
+}
+
+template <class In>
+int resident_clusters(int C, size_t smem) {
+  Config cfg{C, 1, 8, smem};
+  cudaLaunchConfig_t lc = {};
+  cudaLaunchAttribute attr[1];
+  int clusters = 0;
+  if (setup_one<In, GF32, 1, kInterior>(cfg, &lc, attr, &clusters) != cudaSuccess) return 0;
+  return clusters;
 }
 
 }  // namespace fused
