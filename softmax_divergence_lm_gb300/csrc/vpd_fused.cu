@@ -18,7 +18,7 @@ namespace fused {
 // Instantiated in vpd_fused_bf16.cu and vpd_fused_f16.cu.
 extern template cudaError_t launch_typed<InBF16>(const FusedArgs&, const Config&, int, bool, cudaStream_t, int*);
 extern template cudaError_t launch_typed<InF16>(const FusedArgs&, const Config&, int, bool, cudaStream_t, int*);
-extern template int resident_clusters<InBF16>(int, size_t);
+extern template int resident_clusters<InBF16>(int, int, size_t);
 cudaError_t take_error_bf16(int* code);
 cudaError_t take_error_f16(int* code);
 }  // namespace fused
@@ -51,15 +51,15 @@ bool verbose() {
 
 constexpr int kMaxDevices = 64;
 
-// Resident clusters of C CTAs on the current device (one CTA per SM; the
-// kernels of every dtype, mode and width share that shape), cached.
+// Resident clusters of C CTAs on the current device (one CTA per SM whatever
+// the dtype, mode, width or worker count), cached.
 int clusters_for(int C) {
   static std::atomic<int> cache[kMaxDevices][fused::kMaxCluster + 1];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
   int v = cache[dev][C].load(std::memory_order_relaxed);
   if (v == 0) {
-    v = fused::resident_clusters<fused::InBF16>(C, fused::kMinSmem);
+    v = fused::resident_clusters<fused::InBF16>(C, 16, fused::kMinSmem);
     cache[dev][C].store(v < 1 ? -1 : v, std::memory_order_relaxed);
   }
   return v < 1 ? 0 : v;
@@ -77,24 +77,34 @@ size_t max_smem_optin() {
   return v < 1 ? 0 : static_cast<size_t>(v);
 }
 
-// The cluster size that keeps the most SMs busy on `rows` rows, among those
-// whose slice fits: at most kMaxR vectors of both inputs per thread and two
-// stages in shared memory. Ties go to the smaller cluster.
+// The launch shape with the least time per row batch: for each cluster size C
+// whose slice fits (two stages in shared memory), the fewest vector slots per
+// CTA, nw worker warps x R vectors per thread covering the slice (R and nw
+// within the register and TMEM budgets), times the rows each cluster runs.
+// Ties go to the smaller cluster.
 bool choose(int64_t vocab, int64_t rows, Config* cfg) {
   const size_t smem_cap = max_smem_optin();
   int64_t best = 0;
   for (int C = 1; C <= fused::kMaxCluster; ++C) {
     const int64_t W = ((vocab + C - 1) / C + 7) / 8 * 8;
-    const int64_t R = (W / 8 + fused::kT - 1) / fused::kT;
-    if (R > fused::kMaxR) continue;
+    const int64_t nvec = W / 8;
     const size_t smem = fused::smem_bytes(static_cast<int>(W));
     if (smem > smem_cap) continue;
+    int bR = 0, bnw = 0;
+    for (int R = 1; R <= fused::kMaxR; ++R) {
+      const int64_t nw = (nvec + 32 * R - 1) / (32 * R);
+      if (nw > fused::max_workers(R)) continue;
+      if (R * fused::Cols<fused::kInterior>::k > fused::tmem_cols_per_warp(static_cast<int>(nw))) continue;
+      if (!bR || nw * R < static_cast<int64_t>(bnw) * bR) bR = R, bnw = static_cast<int>(nw);
+    }
+    if (!bR) continue;
     const int clusters = clusters_for(C);
     if (clusters < 1) continue;
-    const int64_t busy = (rows < clusters ? rows : clusters) * C;
-    if (busy > best) {
-      best = busy;
-      *cfg = Config{C, static_cast<int>(R), static_cast<int>(W), smem};
+    const int64_t used = rows < clusters ? rows : clusters;
+    const int64_t cost = (rows + used - 1) / used * bnw * bR;
+    if (!best || cost < best) {
+      best = cost;
+      *cfg = Config{C, bR, static_cast<int>(W), bnw, smem};
     }
   }
   return best > 0;
@@ -125,7 +135,7 @@ cudaError_t launch_jsd_fused(const View& s, const View& t, double beta, const fl
   if (!choose(s.vocab, s.rows, &cfg)) return cudaErrorNotSupported;
   const int mode = beta == 0.0 ? fused::kForwardKL : beta == 1.0 ? fused::kReverseKL : fused::kInterior;
   const bool f32g = gdtype == kF32;
-  fused::FusedArgs args{s.data, t.data, s.map, t.map, s.rows, s.vocab, cfg.W, static_cast<float>(beta),
+  fused::FusedArgs args{s.data, t.data, s.map, t.map, s.rows, s.vocab, cfg.W, cfg.nw, static_cast<float>(beta),
                         grad_loss, loss, saved, ds, dt, withhold_row};
   int clusters = 0;
   const cudaError_t e = s.dtype == kBF16
@@ -134,8 +144,8 @@ cudaError_t launch_jsd_fused(const View& s, const View& t, double beta, const fl
   if (e == cudaSuccess) {
     note_launch();
     if (verbose())
-      fprintf(stderr, "[vpd] fused JSD: V=%lld cluster=%d threads=%d R=%d W=%d smem=%zu B, %d clusters\n",
-              static_cast<long long>(s.vocab), cfg.C, fused::kT, cfg.R, cfg.W, cfg.smem, clusters);
+      fprintf(stderr, "[vpd] fused JSD: V=%lld cluster=%d workers=%d R=%d W=%d smem=%zu B, %d clusters\n",
+              static_cast<long long>(s.vocab), cfg.C, cfg.nw, cfg.R, cfg.W, cfg.smem, clusters);
   }
   return e;
 }

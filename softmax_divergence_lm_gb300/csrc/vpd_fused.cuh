@@ -53,11 +53,16 @@ constexpr int kStages = 2;                  // shared-memory stages per CTA
 constexpr float kTiny = 1e-37f;             // keeps M > 0 so log2 M stays finite
 constexpr float kMaxLogit = 8.5070592e37f;  // 2^126: a larger finite row max is out of contract
 constexpr int kMaxCluster = 16;
-constexpr int kT = 512;                     // threads per CTA
-constexpr int kWarps = kT / 32;
-constexpr int kMaxR = 5;                    // 16-byte vectors of each input per thread
+constexpr int kMaxR = 5;                    // 16-byte vectors of each input per worker thread
 constexpr int kTmemCols = 512;              // the whole tensor memory of the SM
 constexpr int kMinSmem = 120 * 1024;        // keeps one CTA per SM (each takes all TMEM)
+constexpr int kMaxWorkers = 17;             // worker warps per CTA (plus one control warp)
+// Worker warps per CTA for R vectors per thread: the register budget of a
+// thread is 64K / (32 (workers + 1)), 136 registers at R = 5, 112 below.
+__host__ __device__ constexpr int max_workers(int R) { return R >= 5 ? 14 : kMaxWorkers; }
+// TMEM columns of one worker warp: the warps of a lane quarter share its 512
+// columns (a multiple of 8 each).
+__host__ __device__ constexpr int tmem_cols_per_warp(int nw) { return (kTmemCols / ((nw + 3) / 4)) & ~7; }
 
 enum Mode : int { kInterior = 0, kForwardKL = 1, kReverseKL = 2 };
 
@@ -67,7 +72,8 @@ template <int MODE>
 struct Cols {
   static constexpr int k = MODE == kInterior ? 24 : 16;
 };
-static_assert(Cols<kInterior>::k * kMaxR <= kTmemCols / (kWarps / 4), "TMEM columns per thread");
+static_assert(Cols<kInterior>::k * kMaxR <= tmem_cols_per_warp(max_workers(kMaxR)), "TMEM columns per thread");
+static_assert(Cols<kInterior>::k * 4 <= tmem_cols_per_warp(max_workers(4)), "TMEM columns per thread");
 
 // Set by a kernel of this translation unit whose bounded wait gave up (each
 // translation unit that includes this header has its own word).
@@ -177,6 +183,11 @@ __device__ __forceinline__ void push16(uint32_t remote, float a, float b, float 
       "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
       : "memory");
 }
+// Named CTA barriers over n threads: arrive (no wait, release) and sync (wait, acquire).
+__device__ __forceinline__ void bar_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 __device__ __forceinline__ void st_global16(void* p, uint4 v) {
   asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
@@ -252,12 +263,6 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
-}
-// Sum over lanes 0..15 (the rest hold zeros), broadcast to the warp.
-__device__ __forceinline__ float sum16(float v) {
-#pragma unroll
-  for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return __shfl_sync(0xffffffffu, v, 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -373,82 +378,80 @@ __device__ __forceinline__ float2 lg2_2(float2 a) { return make_float2(lg2(a.x),
 __device__ __forceinline__ uint4 lds16(const unsigned char* p) { return *reinterpret_cast<const uint4*>(p); }
 
 // ---------------------------------------------------------------------------
-// Cluster reductions by push. Each CTA reduces its partial over its warps
-// (warp reductions + shared memory), then lane c of warp 0 sends it with
-// st.async into CTA c's slot for this CTA; the bytes complete on the peer's
-// mbarrier. A receiver arms its own mbarrier for C partials, waits on it and
-// merges the C slots from its own shared memory. There is no cluster-wide
-// barrier and no fence on the gradient stores in flight. Slots and mbarriers
-// are double-buffered by row parity: a CTA cannot run two rows ahead of a
-// peer, since it needs that peer's partial of every row to proceed.
+// Work split inside a CTA. nw worker warps (chosen on the host so that the
+// slice divides evenly: each worker thread holds at most R vectors of each
+// input) do the element work; one control warp does every wait on another
+// CTA, the merges, the pushes, the TMA issue and the per-row outputs. The two
+// roles hand over through shared memory and named barriers (one side arrives,
+// the other syncs), so the reductions of a row overlap the statistics pass of
+// the next and the workers never meet in a CTA-wide barrier.
+//
+// Cluster reductions by push: the control warp merges the workers' partials
+// and lane c sends the CTA's partial with st.async into CTA c's slot for this
+// CTA; the bytes complete on the peer's mbarrier. The control warp of each CTA
+// arms its own mbarrier for C partials, waits (bounded) and merges the C
+// slots. Slots and mbarriers are double-buffered by row parity: a CTA cannot
+// run two rows ahead of a peer, since it needs that peer's partial of every
+// row to proceed.
 //
 // Statistics travel as (m_s, z_s, m_t, z_t): z relative to m, with z = NaN
 // marking an input outside the contract (a NaN, +inf or a max above 2^126),
 // which the merges propagate. Sums travel as (A, B) in nats; a KL support
 // violation makes A = +inf.
 // ---------------------------------------------------------------------------
+enum NamedBar : int { kBarStatPart = 1, kBarStatReady = 2, kBarSumPart = 3, kBarSumReady = 4 };
+
 struct Tail {
   uint64_t tma_bar[kStages];
   uint64_t stat_bar[2];
   uint64_t sum_bar[2];
   uint32_t tmem_base;
-  uint32_t pad_;
-  __align__(16) float stat_warp[kWarps][4];
-  __align__(16) float sum_warp[kWarps][2];
+  int fail;  // set by a worker whose wait on a stage gave up
+  __align__(16) float stat_part[2][kMaxWorkers][4];  // per worker warp: m_s, z_s, m_t, z_t
+  __align__(16) float sum_part[2][kMaxWorkers][4];   // per worker warp: A, B (nats)
+  __align__(16) float stat_res[2][8];  // -m_s, -m_t, -log2 Z_s, -log2 Z_t, row ok, run ok
+  __align__(16) float sum_res[2][4];   // A, B, value (nats)
   __align__(16) float stat_slot[2][kMaxCluster][4];
   __align__(16) float sum_slot[2][kMaxCluster][4];
 };
 
-// Merge (m, z) over lanes 0..15 of a warp (lanes beyond hold (-inf, 0)).
-__device__ __forceinline__ float2 merge16(float m, float z) {
+// Merge (m, z) over the lanes of a warp (unused lanes hold (-inf, 0)).
+__device__ __forceinline__ float2 merge_warp(float m, float z) {
   const float mx = warp_max_nan(m);
-  return make_float2(mx, sum16(z * exp_acc(m - stat_ref(mx))));
+  return make_float2(mx, warp_sum(z * exp_acc(m - stat_ref(mx))));
 }
 
-// Arm this CTA's mbarrier for the C partials of one row; one thread waits
-// (bounded) while the others sleep in the CTA barrier, then every thread
-// takes the phase with cluster-scope acquire. `ok` becomes false for every
-// thread if the wait gave up.
-__device__ __forceinline__ void arm_and_wait(uint64_t* bar, uint32_t parity, uint32_t bytes, bool& ok) {
-  bool mine = true;
-  if (threadIdx.x == 0) {
-    mbar_expect_tx(bar, bytes);
-    mine = mbar_wait_cluster(bar, parity);
-  }
-  ok = __syncthreads_and(mine) && ok;
-  if (ok && threadIdx.x != 0) mbar_try_wait_cluster(bar, parity);
+// Control warp: arm this CTA's mbarrier for the C partials of one row and
+// wait (bounded, every lane); false if the wait gave up.
+__device__ __forceinline__ bool control_wait(uint64_t* bar, uint32_t parity, uint32_t csize) {
+  if ((threadIdx.x & 31) == 0) mbar_expect_tx(bar, csize * 16u);
+  __syncwarp();
+  const bool mine = mbar_wait_cluster(bar, parity);
+  return __all_sync(0xffffffffu, mine);
 }
 
-// Global statistics of one row: (m_s, z_s, m_t, z_t), every thread.
-__device__ __forceinline__ float4 collect_stats(const float (*slot)[4], uint64_t* bar, uint32_t parity,
-                                                uint32_t csize, bool& ok) {
-  arm_and_wait(bar, parity, csize * 16u, ok);
+// Control warp: merge the workers' statistics partials and push the CTA's to
+// every CTA of the cluster (slot `crank`).
+__device__ __forceinline__ void control_push_stats(const float (*part)[4], int nw, Tail* tail, int par,
+                                                   uint32_t crank, uint32_t csize) {
   const int lane = threadIdx.x & 31;
   float4 v = make_float4(neg_inf(), 0.f, neg_inf(), 0.f);
-  if (lane < static_cast<int>(csize)) v = *reinterpret_cast<const float4*>(slot[lane]);
-  const float2 s = merge16(v.x, v.y), t = merge16(v.z, v.w);
-  return make_float4(s.x, s.y, t.x, t.y);
-}
-// Global (A, B) of one row, every thread.
-__device__ __forceinline__ float2 collect_sums(const float (*slot)[4], uint64_t* bar, uint32_t parity,
-                                               uint32_t csize, bool& ok) {
-  arm_and_wait(bar, parity, csize * 16u, ok);
-  const int lane = threadIdx.x & 31;
-  float2 v = make_float2(0.f, 0.f);
-  if (lane < static_cast<int>(csize)) v = *reinterpret_cast<const float2*>(slot[lane]);
-  return make_float2(sum16(v.x), sum16(v.y));
+  if (lane < nw) v = *reinterpret_cast<const float4*>(part[lane]);
+  const float2 s = merge_warp(v.x, v.y), t = merge_warp(v.z, v.w);
+  if (lane < static_cast<int>(csize))
+    push16(map_rank(smem_addr(tail->stat_slot[par][crank]), lane), s.x, s.y, t.x, t.y,
+           map_rank(smem_addr(&tail->stat_bar[par]), lane));
 }
 
-// Statistics partial of one row read from its shared-memory stage, merged over
-// the CTA and pushed to every CTA of the cluster (slot `crank`).
+// Worker warps: statistics partial of one row read from its shared-memory
+// stage; lane 0 writes the warp's (m_s, z_s, m_t, z_t) to `part`.
 template <class In, int R>
-__device__ __forceinline__ void stage_stats(const unsigned char* sb, int W, int len, Tail* tail, int par,
-                                            uint32_t crank, uint32_t csize) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__device__ __forceinline__ void worker_stats(const unsigned char* sb, int W, int len, int Tw, float* part) {
+  const int tid = threadIdx.x, lane = tid & 31;
   uint32_t mxs = In::kNegInf2, mxt = In::kNegInf2;
 #pragma unroll
   for (int k = 0; k < R; ++k) {
-    const int e0 = (k * kT + tid) * 8;
+    const int e0 = (k * Tw + tid) * 8;
     if (e0 < len) {
       const uint4 u = lds16(sb + e0 * 2), v = lds16(sb + static_cast<size_t>(W) * 2 + e0 * 2);
       mxs = In::max_nan(mxs, In::max_nan(In::max_nan(u.x, u.y), In::max_nan(u.z, u.w)));
@@ -461,7 +464,7 @@ __device__ __forceinline__ void stage_stats(const unsigned char* sb, int W, int 
   float2 zs2 = f2(0.f), zt2 = f2(0.f);
 #pragma unroll
   for (int k = 0; k < R; ++k) {
-    const int e0 = (k * kT + tid) * 8;
+    const int e0 = (k * Tw + tid) * 8;
     if (e0 < len) {
       const uint4 u = lds16(sb + e0 * 2), v = lds16(sb + static_cast<size_t>(W) * 2 + e0 * 2);
       const uint32_t us[4] = {u.x, u.y, u.z, u.w}, vs[4] = {v.x, v.y, v.z, v.w};
@@ -476,34 +479,7 @@ __device__ __forceinline__ void stage_stats(const unsigned char* sb, int W, int 
   float z_s = warp_sum(zs2.x + zs2.y), z_t = warp_sum(zt2.x + zt2.y);
   if (!(m_s <= kMaxLogit)) z_s = qnan();  // NaN, +inf or a max above 2^126
   if (!(m_t <= kMaxLogit)) z_t = qnan();
-  if (lane == 0) *reinterpret_cast<float4*>(tail->stat_warp[warp]) = make_float4(m_s, z_s, m_t, z_t);
-  __syncthreads();
-  if (warp == 0) {
-    float4 v = make_float4(neg_inf(), 0.f, neg_inf(), 0.f);
-    if (lane < kWarps) v = *reinterpret_cast<const float4*>(tail->stat_warp[lane]);
-    const float2 s = merge16(v.x, v.y), t = merge16(v.z, v.w);
-    if (lane < static_cast<int>(csize))
-      push16(map_rank(smem_addr(tail->stat_slot[par][crank]), lane), s.x, s.y, t.x, t.y,
-             map_rank(smem_addr(&tail->stat_bar[par]), lane));
-  }
-}
-
-// Reduce (A, B) in nats over the CTA and push them to every CTA of the cluster.
-__device__ __forceinline__ void push_sums(float a, float b, Tail* tail, int par, uint32_t crank, uint32_t csize) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  a = warp_sum(a);
-  b = warp_sum(b);
-  if (lane == 0) *reinterpret_cast<float2*>(tail->sum_warp[warp]) = make_float2(a, b);
-  __syncthreads();
-  if (warp == 0) {
-    float2 v = make_float2(0.f, 0.f);
-    if (lane < kWarps) v = *reinterpret_cast<const float2*>(tail->sum_warp[lane]);
-    a = sum16(v.x);
-    b = sum16(v.y);
-    if (lane < static_cast<int>(csize))
-      push16(map_rank(smem_addr(tail->sum_slot[par][crank]), lane), a, b, 0.f, 0.f,
-             map_rank(smem_addr(&tail->sum_bar[par]), lane));
-  }
+  if (lane == 0) *reinterpret_cast<float4*>(part) = make_float4(m_s, z_s, m_t, z_t);
 }
 
 struct FusedArgs {
@@ -512,7 +488,8 @@ struct FusedArgs {
   RowMap ms, mt;
   int64_t rows;
   int64_t vocab;
-  int W;  // slice width per CTA (elements, multiple of 8)
+  int W;   // slice width per CTA (elements, multiple of 8)
+  int nw;  // worker warps per CTA
   float beta;
   const float* grad_loss;
   float* loss;
@@ -528,244 +505,315 @@ __device__ __forceinline__ float2 lam(uint32_t w, float2 nm, float2 l2e2, float2
 }
 
 template <class In, class G, int R, int MODE>
-__global__ void __launch_bounds__(kT, 1) k_jsd_fused(FusedArgs a) {
+__global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(FusedArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int kCols = Cols<MODE>::k;
-  const int W = a.W;
+  const int W = a.W, nw = a.nw, Tw = 32 * nw, nthreads = Tw + 32;
   Tail* tail = reinterpret_cast<Tail*>(smem + static_cast<size_t>(kStages) * 4 * W);
   auto stage_ptr = [&](int st) { return smem + static_cast<size_t>(st) * 4 * W; };
 
   const uint32_t crank = cluster_rank(), csize = cluster_size();
   const int64_t q = cluster_index(), Q = cluster_count();
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool control = warp == nw;
   const int64_t col0 = static_cast<int64_t>(crank) * W;
   const int64_t rest = a.vocab - col0;
   const int len = rest <= 0 ? 0 : (rest < W ? static_cast<int>(rest) : W);
   const uint32_t bytes = static_cast<uint32_t>(len) * 2u;
 
   // The failure-path test hook: this CTA withholds the copy of one row, so
-  // its bounded wait on that stage expires.
+  // its workers' bounded wait on that stage expires.
   auto withheld = [&](int64_t r) { return r == a.withhold_row && crank == 0; };
-  auto issue = [&](int64_t r, int st) {  // one thread: both inputs' slices of row r into stage st
-    if (withheld(r)) return;
-    unsigned char* dst = stage_ptr(st);
-    mbar_expect_tx(&tail->tma_bar[st], 2 * bytes);
-    bulk_load(dst, a.s + (a.ms.offset(r) + col0) * 2, bytes, &tail->tma_bar[st]);
-    bulk_load(dst + static_cast<size_t>(W) * 2, a.t + (a.mt.offset(r) + col0) * 2, bytes, &tail->tma_bar[st]);
+  uint32_t issued[kStages] = {0, 0};  // control warp: copies issued per stage
+  auto issue = [&](int64_t r, int st) {  // control warp: both inputs' slices of row r into stage st
+    if (!bytes || withheld(r)) return;
+    if (lane == 0) {
+      unsigned char* dst = stage_ptr(st);
+      mbar_expect_tx(&tail->tma_bar[st], 2 * bytes);
+      bulk_load(dst, a.s + (a.ms.offset(r) + col0) * 2, bytes, &tail->tma_bar[st]);
+      bulk_load(dst + static_cast<size_t>(W) * 2, a.t + (a.mt.offset(r) + col0) * 2, bytes, &tail->tma_bar[st]);
+    }
+    ++issued[st];
   };
 
-  if (tid == 0) {
-    for (int st = 0; st < kStages; ++st) mbar_init(&tail->tma_bar[st], 1);
-    for (int p = 0; p < 2; ++p) {
-      mbar_init(&tail->stat_bar[p], 1);
-      mbar_init(&tail->sum_bar[p], 1);
+  if (control) {
+    if (lane == 0) {
+      for (int st = 0; st < kStages; ++st) mbar_init(&tail->tma_bar[st], 1);
+      for (int p = 0; p < 2; ++p) {
+        mbar_init(&tail->stat_bar[p], 1);
+        mbar_init(&tail->sum_bar[p], 1);
+      }
+      tail->fail = 0;
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  if (warp == 0) tmem_alloc(&tail->tmem_base);
-  tmem_fence_before();
-  __syncthreads();
-  tmem_fence_after();
-  // This thread's TMEM lane (its warp's lane quarter) and column range.
-  const uint32_t tmem = tail->tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16) +
-                        static_cast<uint32_t>((kTmemCols / (kWarps / 4)) * (warp >> 2));
-
-  uint32_t pending = 0;                 // bit st: a copy into stage st is in flight
-  uint32_t tma_done[kStages] = {0, 0};  // completed waits per stage
-  if (tid == 0 && bytes) {
+    __syncwarp();
+    tmem_alloc(&tail->tmem_base);
     for (int st = 0; st < kStages; ++st)
       if (q + st * Q < a.rows) issue(q + st * Q, st);
   }
-  if (bytes)
-    for (int st = 0; st < kStages; ++st)
-      if (q + st * Q < a.rows && !withheld(q + st * Q)) pending |= 1u << st;
-  cluster_sync();  // every CTA's mbarriers are initialised before any push
-
-  bool ok = true;
-  auto wait_stage = [&](int st) {  // one thread waits; the others sleep in the barrier
-    if (!bytes) return;
-    bool mine = true;
-    if (tid == 0) mine = mbar_wait(&tail->tma_bar[st], tma_done[st] & 1u);
-    ok = __syncthreads_and(mine) && ok;
-    if (ok && tid != 0) mbar_try_wait(&tail->tma_bar[st], tma_done[st] & 1u);
-    ++tma_done[st];
-    pending &= ~(1u << st);
-  };
-
-  const float beta = a.beta;
-  const float2 ws2 = f2(1.f - beta), wt2 = f2(beta), tiny2 = f2(kTiny), l2e2 = f2(kLog2e);
-
-  // Statistics of this cluster's first row.
-  if (q < a.rows) {
-    wait_stage(0);
-    stage_stats<In, R>(stage_ptr(0), W, len, tail, 0, crank, csize);
-  }
-
-  int64_t i = 0;
-  for (int64_t r = q; r < a.rows && ok; r += Q, ++i) {
-    const int par = static_cast<int>(i & 1);
-    const uint32_t ph = static_cast<uint32_t>((i >> 1) & 1);
-    const bool has_next = r + Q < a.rows;
-    const int cst = static_cast<int>(i % kStages);  // stage of this row
-    const int nst = static_cast<int>((i + 1) % kStages);
-
-    // (1) global statistics of row r
-    const float4 g = collect_stats(tail->stat_slot[par], &tail->stat_bar[par], ph, csize, ok);
-    const bool bad_s = isnan(g.y), bad_t = isnan(g.w);
-    const bool row_ok = !bad_s && !bad_t && g.x != neg_inf() && g.z != neg_inf();
-    const float Ks = row_ok ? log2f(g.y) : qnan();  // log2 Z
-    const float Kt = row_ok ? log2f(g.w) : qnan();
-    const float2 nms2 = f2(-g.x), nmt2 = f2(-g.z), nKs2 = f2(-Ks), nKt2 = f2(-Kt);
-
-    // (2) pass C of row r from its stage, in log2 units. TMEM per vector:
-    // interior p, log2 p - log2 M, log2 q - log2 M; KL p, log2 ratio. q in
-    // registers. Warps past the slice skip a vector together; inside a warp,
-    // lanes past it compute on the floor value (p = q = 0) so that the TMEM
-    // stores stay warp-uniform.
-    float2 kq[R][4];
-    float2 acc_a = f2(0.f), acc_b = f2(0.f);
-    uint32_t viol = 0;
-    if (row_ok) {
-      const unsigned char* sb = stage_ptr(cst);
-#pragma unroll
-      for (int k = 0; k < R; ++k) {
-        if ((k * kT + warp * 32) * 8 >= len) continue;  // warp-uniform
-        const int e0 = (k * kT + tid) * 8;
-        uint4 u = make_uint4(In::kNegBig2, In::kNegBig2, In::kNegBig2, In::kNegBig2), v = u;
-        if (e0 < len) {
-          u = lds16(sb + e0 * 2);
-          v = lds16(sb + static_cast<size_t>(W) * 2 + e0 * 2);
-        }
-        const uint32_t us[4] = {u.x, u.y, u.z, u.w}, vs[4] = {v.x, v.y, v.z, v.w};
-        float2 t0[4], t1[4], t2[4];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          if (MODE != kInterior) {
-            const uint32_t tgt = MODE == kForwardKL ? vs[w] : us[w];
-            const uint32_t oth = MODE == kForwardKL ? us[w] : vs[w];
-            viol |= __vcmpeq2(oth, In::kNegInf2) & ~__vcmpeq2(tgt, In::kNegInf2);
-          }
-          const float2 lp = lam<In>(In::max2(us[w], In::kNegBig2), nms2, l2e2, nKs2);
-          const float2 lq = lam<In>(In::max2(vs[w], In::kNegBig2), nmt2, l2e2, nKt2);
-          const float2 p = ex2_2(lp), qv = ex2_2(lq);
-          kq[k][w] = qv;
-          t0[w] = p;
-          if (MODE == kInterior) {
-            const float2 lm = lg2_2(fma2(ws2, p, fma2(wt2, qv, tiny2)));
-            const float2 us_ = add2(lp, neg(lm)), ut_ = add2(lq, neg(lm));
-            acc_b = fma2(p, us_, acc_b);
-            acc_a = fma2(qv, ut_, acc_a);
-            t1[w] = us_;
-            t2[w] = ut_;
-          } else {
-            // forward KL(q || p): d = log2 q - log2 p weighted by q; reverse: mirror
-            const float2 d = MODE == kForwardKL ? add2(lq, neg(lp)) : add2(lp, neg(lq));
-            acc_a = fma2(MODE == kForwardKL ? qv : p, d, acc_a);
-            t1[w] = d;
-          }
-        }
-        tmem_st8(tmem + k * kCols, t0);
-        tmem_st8(tmem + k * kCols + 8, t1);
-        if (MODE == kInterior) tmem_st8(tmem + k * kCols + 16, t2);
-      }
-      tmem_wait_st();
-    }
-    float sa = kLn2 * (acc_a.x + acc_a.y);
-    if (MODE != kInterior && viol) sa = pos_inf();
-    push_sums(sa, kLn2 * (acc_b.x + acc_b.y), tail, par, crank, csize);
-    // every thread has read this row's stage: refill it with the row kStages on
-    {
-      const bool more = ok && r + kStages * Q < a.rows;  // no new copy after a failed wait
-      if (tid == 0 && bytes && more) issue(r + kStages * Q, cst);
-      if (bytes && more && !withheld(r + kStages * Q)) pending |= 1u << cst;
-    }
-
-    // (3) statistics partial of the next row, straight from its stage, while
-    // this row's sums travel
-    if (has_next) {
-      wait_stage(nst);
-      stage_stats<In, R>(stage_ptr(nst), W, len, tail, par ^ 1, crank, csize);
-    }
-
-    // (4) global sums of row r; the per-token value and saved statistics
-    const float2 ab = collect_sums(tail->sum_slot[par], &tail->sum_bar[par], ph, csize, ok);
-    float A = ab.x, B = ab.y, value;
-    if (!row_ok) {
-      value = qnan();
-      A = B = qnan();
-    } else if (MODE == kInterior) {
-      value = beta * A + (1.f - beta) * B;
-    } else {
-      value = A;  // +inf on a support violation
-      A = MODE == kForwardKL ? value : 0.f;
-      B = MODE == kForwardKL ? 0.f : value;
-    }
-    if (crank == 0 && tid == 0) {
-      a.loss[r] = value;
-      float* sv = a.saved + r * VPD_SAVED_PAIR;
-      sv[0] = bad_s ? qnan() : g.x;
-      sv[1] = bad_s ? qnan() : (g.x == neg_inf() ? neg_inf() : kLn2 * log2f(g.y));
-      sv[2] = bad_t ? qnan() : g.z;
-      sv[3] = bad_t ? qnan() : (g.z == neg_inf() ? neg_inf() : kLn2 * log2f(g.w));
-      sv[4] = A;
-      sv[5] = B;
-    }
-
-    // (5) pass D of row r: gradients, e.g. dS = p (g (1-beta) ln2 (log2 p - log2 M) - g (1-beta) B)
-    const float gr = a.grad_loss ? __ldg(a.grad_loss + r) : 1.f;
-    char* ds_row = a.ds.data ? a.ds.data + (r * a.ds.row_stride + col0) * Out<G>::kSize : nullptr;
-    char* dt_row = a.dt.data ? a.dt.data + (r * a.dt.row_stride + col0) * Out<G>::kSize : nullptr;
-    if (ds_row || dt_row) {
-      const bool live = row_ok && isfinite(value);
-      const float cs = MODE == kInterior ? gr * (1.f - beta) : gr;
-      const float ct = MODE == kInterior ? gr * beta : gr;
-      const float2 cs2 = f2(cs * kLn2), ct2 = f2(ct * kLn2);
-      const float2 ncs2 = f2(-cs * (MODE == kInterior ? B : value));
-      const float2 nct2 = f2(-ct * (MODE == kInterior ? A : value));
-      const float2 g2 = f2(gr);
-#pragma unroll
-      for (int k = 0; k < R; ++k) {
-        if ((k * kT + warp * 32) * 8 >= len) continue;  // warp-uniform
-        const int e0 = (k * kT + tid) * 8;
-        float2 gs[4], gt[4];
-        if (!live) {
-#pragma unroll
-          for (int w = 0; w < 4; ++w) gs[w] = gt[w] = f2(0.f);
-        } else {
-          float2 p[4], u1[4], u2[4];
-          if (MODE == kInterior) tmem_ld24_wait(tmem + k * kCols, p, u1, u2);
-          else tmem_ld16_wait(tmem + k * kCols, p, u1);
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const float2 qv = kq[k][w];
-            if (MODE == kInterior) {
-              gs[w] = mul2(p[w], fma2(cs2, u1[w], ncs2));
-              gt[w] = mul2(qv, fma2(ct2, u2[w], nct2));
-            } else if (MODE == kForwardKL) {  // dS = g (p - q), dT = g q (ln q - ln p - KL)
-              gs[w] = mul2(g2, add2(p[w], neg(qv)));
-              gt[w] = mul2(qv, fma2(ct2, u1[w], nct2));
-            } else {  // dS = g p (ln p - ln q - KL), dT = g (q - p)
-              gs[w] = mul2(p[w], fma2(cs2, u1[w], ncs2));
-              gt[w] = mul2(g2, add2(qv, neg(p[w])));
-            }
-          }
-        }
-        if (e0 < len) {
-          if (ds_row) Out<G>::store8(ds_row + static_cast<int64_t>(e0) * Out<G>::kSize, gs);
-          if (dt_row) Out<G>::store8(dt_row + static_cast<int64_t>(e0) * Out<G>::kSize, gt);
-        }
-      }
-    }
-  }
-
-  // Only after a wait gave up: copies still in flight must land before exit.
-  for (int st = 0; st < kStages; ++st)
-    if (pending & (1u << st)) mbar_wait(&tail->tma_bar[st], tma_done[st] & 1u);
-  if (!ok && tid == 0) atomicExch(&g_fused_error, 1);
-  tmem_wait_st();
   tmem_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  tmem_fence_after();
+  cluster_sync();  // every CTA's mbarriers are initialised before any push
+
+  const float beta = a.beta;
+  bool ok = true;
+  if (control) {
+    // ------------------------------------------------------------------
+    // Control warp.
+    // ------------------------------------------------------------------
+    if (q < a.rows) {
+      bar_sync(kBarStatPart, nthreads);
+      if (tail->fail) ok = false;
+      control_push_stats(tail->stat_part[0], nw, tail, 0, crank, csize);
+    }
+    int64_t i = 0;
+    for (int64_t r = q; r < a.rows; r += Q, ++i) {
+      const int par = static_cast<int>(i & 1);
+      const uint32_t ph = static_cast<uint32_t>((i >> 1) & 1);
+      const bool has_next = r + Q < a.rows;
+      const int cst = static_cast<int>(i % kStages);
+
+      // (C1) global statistics of row r, handed to the workers
+      float4 g = make_float4(qnan(), qnan(), qnan(), qnan());
+      if (ok) ok = control_wait(&tail->stat_bar[par], ph, csize);
+      if (ok) {
+        float4 v = make_float4(neg_inf(), 0.f, neg_inf(), 0.f);
+        if (lane < static_cast<int>(csize)) v = *reinterpret_cast<const float4*>(tail->stat_slot[par][lane]);
+        const float2 s = merge_warp(v.x, v.y), t = merge_warp(v.z, v.w);
+        g = make_float4(s.x, s.y, t.x, t.y);
+      }
+      const bool bad_s = isnan(g.y), bad_t = isnan(g.w);
+      const bool row_ok = ok && !bad_s && !bad_t && g.x != neg_inf() && g.z != neg_inf();
+      const float Ks = row_ok ? log2f(g.y) : qnan();  // log2 Z
+      const float Kt = row_ok ? log2f(g.w) : qnan();
+      if (lane == 0) {
+        float* res = tail->stat_res[par];
+        *reinterpret_cast<float4*>(res) = make_float4(-g.x, -g.z, -Ks, -Kt);
+        *reinterpret_cast<float2*>(res + 4) = make_float2(row_ok ? 1.f : 0.f, ok ? 1.f : 0.f);
+      }
+      bar_arrive(kBarStatReady, nthreads);
+      if (!ok) break;
+
+      // (C2) the workers have read this row's stage: refill it with the row
+      // kStages on; reduce and push this row's sums
+      bar_sync(kBarSumPart, nthreads);
+      if (r + kStages * Q < a.rows) issue(r + kStages * Q, cst);
+      {
+        float2 v = make_float2(0.f, 0.f);
+        if (lane < nw) v = *reinterpret_cast<const float2*>(tail->sum_part[par][lane]);
+        const float sa = warp_sum(v.x), sb = warp_sum(v.y);
+        if (lane < static_cast<int>(csize))
+          push16(map_rank(smem_addr(tail->sum_slot[par][crank]), lane), sa, sb, 0.f, 0.f,
+                 map_rank(smem_addr(&tail->sum_bar[par]), lane));
+      }
+
+      // (C3) statistics of the next row
+      if (has_next) {
+        bar_sync(kBarStatPart, nthreads);
+        if (tail->fail) ok = false;
+        control_push_stats(tail->stat_part[par ^ 1], nw, tail, par ^ 1, crank, csize);
+      }
+
+      // (C4) global sums of row r: the per-token value and saved statistics
+      float A = qnan(), B = qnan(), value = qnan();
+      const bool got = ok && control_wait(&tail->sum_bar[par], ph, csize);
+      if (!got) ok = false;
+      if (got && row_ok) {
+        float2 v = make_float2(0.f, 0.f);
+        if (lane < static_cast<int>(csize)) v = *reinterpret_cast<const float2*>(tail->sum_slot[par][lane]);
+        A = warp_sum(v.x);
+        B = warp_sum(v.y);
+        if (MODE == kInterior) {
+          value = beta * A + (1.f - beta) * B;
+        } else {
+          value = A;  // +inf on a support violation
+          A = MODE == kForwardKL ? value : 0.f;
+          B = MODE == kForwardKL ? 0.f : value;
+        }
+      }
+      if (lane == 0) {
+        *reinterpret_cast<float4*>(tail->sum_res[par]) = make_float4(A, B, value, 0.f);
+        if (crank == 0) {
+          a.loss[r] = value;
+          float* sv = a.saved + r * VPD_SAVED_PAIR;
+          sv[0] = bad_s ? qnan() : g.x;
+          sv[1] = bad_s ? qnan() : (g.x == neg_inf() ? neg_inf() : kLn2 * log2f(g.y));
+          sv[2] = bad_t ? qnan() : g.z;
+          sv[3] = bad_t ? qnan() : (g.z == neg_inf() ? neg_inf() : kLn2 * log2f(g.w));
+          sv[4] = A;
+          sv[5] = B;
+        }
+      }
+      bar_arrive(kBarSumReady, nthreads);
+    }
+    // Copies still in flight (only after a wait gave up) must land before exit.
+    if (lane == 0)
+      for (int st = 0; st < kStages; ++st)
+        if (issued[st]) mbar_wait(&tail->tma_bar[st], (issued[st] - 1) & 1u);
+    if (!ok && lane == 0) atomicExch(&g_fused_error, 1);
+  } else {
+    // ------------------------------------------------------------------
+    // Worker warps.
+    // ------------------------------------------------------------------
+    // This thread's TMEM lane (its warp's lane quarter) and column range.
+    const uint32_t tmem = tail->tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16) +
+                          static_cast<uint32_t>(tmem_cols_per_warp(nw) * (warp >> 2));
+    uint32_t tma_done[kStages] = {0, 0};  // completed waits per stage
+    auto wait_stage = [&](int st) {
+      if (!bytes) return;
+      if (!mbar_wait(&tail->tma_bar[st], tma_done[st] & 1u)) tail->fail = 1;
+      ++tma_done[st];
+    };
+    const float2 ws2 = f2(1.f - beta), wt2 = f2(beta), tiny2 = f2(kTiny), l2e2 = f2(kLog2e);
+    const int64_t gstride = static_cast<int64_t>(Tw) * 8 * Out<G>::kSize;  // bytes between vectors k, k + 1
+
+    if (q < a.rows) {
+      wait_stage(0);
+      worker_stats<In, R>(stage_ptr(0), W, len, Tw, tail->stat_part[0][warp]);
+      bar_arrive(kBarStatPart, nthreads);
+    }
+    int64_t i = 0;
+    for (int64_t r = q; r < a.rows; r += Q, ++i) {
+      const int par = static_cast<int>(i & 1);
+      const bool has_next = r + Q < a.rows;
+      const int cst = static_cast<int>(i % kStages);
+      const int nst = static_cast<int>((i + 1) % kStages);
+
+      // (W1) global statistics of row r
+      bar_sync(kBarStatReady, nthreads);
+      const float4 st4 = *reinterpret_cast<const float4*>(tail->stat_res[par]);
+      const float2 flags = *reinterpret_cast<const float2*>(tail->stat_res[par] + 4);
+      if (flags.y == 0.f) break;
+      const bool row_ok = flags.x != 0.f;
+      const float2 nms2 = f2(st4.x), nmt2 = f2(st4.y), nKs2 = f2(st4.z), nKt2 = f2(st4.w);
+
+      // (W2) pass C of row r from its stage, in log2 units. TMEM per vector:
+      // interior p, log2 p - log2 M, log2 q - log2 M; KL p, log2 ratio. q in
+      // registers. Warps past the slice skip a vector together; inside a warp,
+      // lanes past it compute on the floor value (p = q = 0) so that the TMEM
+      // stores stay warp-uniform.
+      float2 kq[R][4];
+      float2 acc_a = f2(0.f), acc_b = f2(0.f);
+      uint32_t viol = 0;
+      if (row_ok) {
+        const unsigned char* sb = stage_ptr(cst);
+#pragma unroll
+        for (int k = 0; k < R; ++k) {
+          if ((k * Tw + warp * 32) * 8 >= len) continue;  // warp-uniform
+          const int e0 = (k * Tw + tid) * 8;
+          uint4 u = make_uint4(In::kNegBig2, In::kNegBig2, In::kNegBig2, In::kNegBig2), v = u;
+          if (e0 < len) {
+            u = lds16(sb + e0 * 2);
+            v = lds16(sb + static_cast<size_t>(W) * 2 + e0 * 2);
+          }
+          const uint32_t us[4] = {u.x, u.y, u.z, u.w}, vs[4] = {v.x, v.y, v.z, v.w};
+          float2 t0[4], t1[4], t2[4];
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            if (MODE != kInterior) {
+              const uint32_t tgt = MODE == kForwardKL ? vs[w] : us[w];
+              const uint32_t oth = MODE == kForwardKL ? us[w] : vs[w];
+              viol |= __vcmpeq2(oth, In::kNegInf2) & ~__vcmpeq2(tgt, In::kNegInf2);
+            }
+            const float2 lp = lam<In>(In::max2(us[w], In::kNegBig2), nms2, l2e2, nKs2);
+            const float2 lq = lam<In>(In::max2(vs[w], In::kNegBig2), nmt2, l2e2, nKt2);
+            const float2 p = ex2_2(lp), qv = ex2_2(lq);
+            kq[k][w] = qv;
+            t0[w] = p;
+            if (MODE == kInterior) {
+              const float2 lm = lg2_2(fma2(ws2, p, fma2(wt2, qv, tiny2)));
+              const float2 us_ = add2(lp, neg(lm)), ut_ = add2(lq, neg(lm));
+              acc_b = fma2(p, us_, acc_b);
+              acc_a = fma2(qv, ut_, acc_a);
+              t1[w] = us_;
+              t2[w] = ut_;
+            } else {
+              // forward KL(q || p): d = log2 q - log2 p weighted by q; reverse: mirror
+              const float2 d = MODE == kForwardKL ? add2(lq, neg(lp)) : add2(lp, neg(lq));
+              acc_a = fma2(MODE == kForwardKL ? qv : p, d, acc_a);
+              t1[w] = d;
+            }
+          }
+          tmem_st8(tmem + k * kCols, t0);
+          tmem_st8(tmem + k * kCols + 8, t1);
+          if (MODE == kInterior) tmem_st8(tmem + k * kCols + 16, t2);
+        }
+        tmem_wait_st();
+      }
+      {
+        float sa = kLn2 * warp_sum(acc_a.x + acc_a.y);
+        if (MODE != kInterior && __any_sync(0xffffffffu, viol != 0)) sa = pos_inf();
+        const float sb = kLn2 * warp_sum(acc_b.x + acc_b.y);
+        if (lane == 0) *reinterpret_cast<float2*>(tail->sum_part[par][warp]) = make_float2(sa, sb);
+      }
+      bar_arrive(kBarSumPart, nthreads);
+
+      // (W3) statistics partial of the next row, straight from its stage,
+      // while this row's sums travel
+      if (has_next) {
+        wait_stage(nst);
+        worker_stats<In, R>(stage_ptr(nst), W, len, Tw, tail->stat_part[par ^ 1][warp]);
+        bar_arrive(kBarStatPart, nthreads);
+      }
+
+      // (W4) global sums of row r
+      bar_sync(kBarSumReady, nthreads);
+      const float4 ab = *reinterpret_cast<const float4*>(tail->sum_res[par]);
+      const float A = ab.x, B = ab.y, value = ab.z;
+
+      // (W5) pass D of row r: gradients, e.g. dS = p (g (1-beta) ln2 (log2 p - log2 M) - g (1-beta) B)
+      const float gr = a.grad_loss ? __ldg(a.grad_loss + r) : 1.f;
+      char* ds_row = a.ds.data ? a.ds.data + (r * a.ds.row_stride + col0 + tid * 8) * Out<G>::kSize : nullptr;
+      char* dt_row = a.dt.data ? a.dt.data + (r * a.dt.row_stride + col0 + tid * 8) * Out<G>::kSize : nullptr;
+      if (ds_row || dt_row) {
+        const bool live = row_ok && isfinite(value);
+        const float cs = MODE == kInterior ? gr * (1.f - beta) : gr;
+        const float ct = MODE == kInterior ? gr * beta : gr;
+        const float2 cs2 = f2(cs * kLn2), ct2 = f2(ct * kLn2);
+        const float2 ncs2 = f2(-cs * (MODE == kInterior ? B : value));
+        const float2 nct2 = f2(-ct * (MODE == kInterior ? A : value));
+        const float2 g2 = f2(gr);
+#pragma unroll
+        for (int k = 0; k < R; ++k) {
+          if ((k * Tw + warp * 32) * 8 >= len) continue;  // warp-uniform
+          const int e0 = (k * Tw + tid) * 8;
+          float2 gs[4], gt[4];
+          if (!live) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) gs[w] = gt[w] = f2(0.f);
+          } else {
+            float2 p[4], u1[4], u2[4];
+            if (MODE == kInterior) tmem_ld24_wait(tmem + k * kCols, p, u1, u2);
+            else tmem_ld16_wait(tmem + k * kCols, p, u1);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              const float2 qv = kq[k][w];
+              if (MODE == kInterior) {
+                gs[w] = mul2(p[w], fma2(cs2, u1[w], ncs2));
+                gt[w] = mul2(qv, fma2(ct2, u2[w], nct2));
+              } else if (MODE == kForwardKL) {  // dS = g (p - q), dT = g q (ln q - ln p - KL)
+                gs[w] = mul2(g2, add2(p[w], neg(qv)));
+                gt[w] = mul2(qv, fma2(ct2, u1[w], nct2));
+              } else {  // dS = g p (ln p - ln q - KL), dT = g (q - p)
+                gs[w] = mul2(p[w], fma2(cs2, u1[w], ncs2));
+                gt[w] = mul2(g2, add2(qv, neg(p[w])));
+              }
+            }
+          }
+          if (e0 < len) {
+            if (ds_row) Out<G>::store8(ds_row + k * gstride, gs);
+            if (dt_row) Out<G>::store8(dt_row + k * gstride, gt);
+          }
+        }
+      }
+    }
+    tmem_wait_st();
+  }
+
+  tmem_fence_before();
+  __syncthreads();
+  if (control) {
     tmem_fence_after();
     tmem_dealloc(tail->tmem_base);
   }
@@ -776,7 +824,7 @@ __global__ void __launch_bounds__(kT, 1) k_jsd_fused(FusedArgs a) {
 // Host side (per input dtype): one configuration, one launch.
 // ---------------------------------------------------------------------------
 struct Config {
-  int C, R, W;
+  int C, R, W, nw;
   size_t smem;
 };
 
@@ -793,13 +841,14 @@ inline size_t smem_bytes(int W) {
 template <class In>
 cudaError_t launch_typed(const FusedArgs& args, const Config& cfg, int mode, bool f32grad, cudaStream_t stream,
                          int* clusters_out);
-// Resident clusters of C CTAs (0 when none fit), for this dtype's kernels.
+// Resident clusters of C CTAs with nw worker warps (0 when none fit).
 template <class In>
-int resident_clusters(int C, size_t smem);
+int resident_clusters(int C, int nw, size_t smem);
 
 template <class In, class G, int R, int MODE>
 cudaError_t setup_one(const Config& cfg, cudaLaunchConfig_t* lc, cudaLaunchAttribute* attr, int* clusters) {
   auto kern = k_jsd_fused<In, G, R, MODE>;
+  if (cfg.nw < 1 || cfg.nw > max_workers(R)) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(cfg.smem));
   if (e != cudaSuccess) return e;
@@ -814,7 +863,7 @@ cudaError_t setup_one(const Config& cfg, cudaLaunchConfig_t* lc, cudaLaunchAttri
   attr[0].val.clusterDim.x = cfg.C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  lc->blockDim = dim3(kT, 1, 1);
+  lc->blockDim = dim3(32 * (cfg.nw + 1), 1, 1);
   lc->dynamicSmemBytes = cfg.smem;
   lc->attrs = attr;
   lc->numAttrs = 1;
@@ -869,8 +918,8 @@ cudaError_t launch_typed(const FusedArgs& args, const Config& cfg, int mode, boo
 }
 
 template <class In>
-int resident_clusters(int C, size_t smem) {
-  Config cfg{C, 1, 8, smem};
+int resident_clusters(int C, int nw, size_t smem) {
+  Config cfg{C, 1, 8, nw, smem};
   cudaLaunchConfig_t lc = {};
   cudaLaunchAttribute attr[1];
   int clusters = 0;

@@ -6,7 +6,7 @@ namespace vpd {
 namespace fused {
 
 template cudaError_t launch_typed<InF16>(const FusedArgs&, const Config&, int, bool, cudaStream_t, int*);
-template int resident_clusters<InF16>(int, size_t);
+template int resident_clusters<InF16>(int, int, size_t);
 
 cudaError_t take_error_f16(int* code) {
   cudaError_t e = cudaMemcpyFromSymbol(code, g_fused_error, sizeof(int));
