@@ -135,7 +135,12 @@ cudaError_t launch_jsd_fused(const View& s, const View& t, double beta, const fl
   if (!choose(s.vocab, s.rows, &cfg)) return cudaErrorNotSupported;
   const int mode = beta == 0.0 ? fused::kForwardKL : beta == 1.0 ? fused::kReverseKL : fused::kInterior;
   const bool f32g = gdtype == kF32;
-  fused::FusedArgs args{s.data, t.data, s.map, t.map, s.rows, s.vocab, cfg.W, cfg.nw, static_cast<float>(beta),
+  // 16-bit gradients go out through a shared-memory buffer and bulk stores
+  // when it fits beside the stages.
+  const bool gstage = gdtype >= 0 && !f32g && fused::smem_bytes(cfg.W, true) <= max_smem_optin();
+  if (gstage) cfg.smem = fused::smem_bytes(cfg.W, true);
+  fused::FusedArgs args{s.data, t.data, s.map, t.map, s.rows, s.vocab, cfg.W, cfg.nw, gstage ? 1 : 0,
+                        static_cast<float>(beta),
                         grad_loss, loss, saved, ds, dt, withhold_row};
   int clusters = 0;
   const cudaError_t e = s.dtype == kBF16
@@ -144,8 +149,9 @@ cudaError_t launch_jsd_fused(const View& s, const View& t, double beta, const fl
   if (e == cudaSuccess) {
     note_launch();
     if (verbose())
-      fprintf(stderr, "[vpd] fused JSD: V=%lld cluster=%d workers=%d R=%d W=%d smem=%zu B, %d clusters\n",
-              static_cast<long long>(s.vocab), cfg.C, cfg.nw, cfg.R, cfg.W, cfg.smem, clusters);
+      fprintf(stderr, "[vpd] fused JSD: V=%lld cluster=%d workers=%d R=%d W=%d smem=%zu B%s, %d clusters\n",
+              static_cast<long long>(s.vocab), cfg.C, cfg.nw, cfg.R, cfg.W, cfg.smem,
+              gstage ? " (staged gradients)" : "", clusters);
   }
   return e;
 }

@@ -145,6 +145,19 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       "l"(src), "r"(bytes), "r"(smem_addr(mb))
       : "memory");
 }
+// Bulk copy shared -> global (TMA store), committed as one group per call
+// site; wait_read: the shared source may be overwritten; wait_all: the global
+// writes are done.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_addr(src)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Generic-proxy shared-memory writes become visible to the bulk copies.
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile(
       "barrier.cluster.arrive.release.aligned;\n\t"
@@ -341,6 +354,9 @@ struct Out<GBF16> {
   __device__ static __forceinline__ void store8(char* p, const float2 (&v)[4]) {
     st_global16(p, make_uint4(pack(v[0]), pack(v[1]), pack(v[2]), pack(v[3])));
   }
+  __device__ static __forceinline__ void store8_shared(unsigned char* p, const float2 (&v)[4]) {
+    *reinterpret_cast<uint4*>(p) = make_uint4(pack(v[0]), pack(v[1]), pack(v[2]), pack(v[3]));
+  }
 };
 template <>
 struct Out<GF16> {
@@ -353,6 +369,9 @@ struct Out<GF16> {
   __device__ static __forceinline__ void store8(char* p, const float2 (&v)[4]) {
     st_global16(p, make_uint4(pack(v[0]), pack(v[1]), pack(v[2]), pack(v[3])));
   }
+  __device__ static __forceinline__ void store8_shared(unsigned char* p, const float2 (&v)[4]) {
+    *reinterpret_cast<uint4*>(p) = make_uint4(pack(v[0]), pack(v[1]), pack(v[2]), pack(v[3]));
+  }
 };
 template <>
 struct Out<GF32> {
@@ -363,6 +382,7 @@ struct Out<GF32> {
     st_global16(p + 16, make_uint4(__float_as_uint(v[2].x), __float_as_uint(v[2].y), __float_as_uint(v[3].x),
                                    __float_as_uint(v[3].y)));
   }
+  __device__ static __forceinline__ void store8_shared(unsigned char*, const float2 (&)[4]) {}
 };
 
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
@@ -399,7 +419,7 @@ __device__ __forceinline__ uint4 lds16(const unsigned char* p) { return *reinter
 // which the merges propagate. Sums travel as (A, B) in nats; a KL support
 // violation makes A = +inf.
 // ---------------------------------------------------------------------------
-enum NamedBar : int { kBarStatPart = 1, kBarStatReady = 2, kBarSumPart = 3, kBarSumReady = 4 };
+enum NamedBar : int { kBarStatPart = 1, kBarStatReady = 2, kBarSumPart = 3, kBarSumReady = 4, kBarGradFull = 5 };
 
 struct Tail {
   uint64_t tma_bar[kStages];
@@ -488,8 +508,9 @@ struct FusedArgs {
   RowMap ms, mt;
   int64_t rows;
   int64_t vocab;
-  int W;   // slice width per CTA (elements, multiple of 8)
-  int nw;  // worker warps per CTA
+  int W;      // slice width per CTA (elements, multiple of 8)
+  int nw;     // worker warps per CTA
+  int gstage; // 16-bit gradients go through a shared-memory buffer and bulk stores
   float beta;
   const float* grad_loss;
   float* loss;
@@ -509,7 +530,11 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int kCols = Cols<MODE>::k;
   const int W = a.W, nw = a.nw, Tw = 32 * nw, nthreads = Tw + 32;
-  Tail* tail = reinterpret_cast<Tail*>(smem + static_cast<size_t>(kStages) * 4 * W);
+  // Shared memory: kStages x [s, t] slices, then (staged gradients) the dS and
+  // dT slices of one row, then the tail.
+  unsigned char* gbuf = smem + static_cast<size_t>(kStages) * 4 * W;
+  const bool staged = a.gstage != 0 && (a.ds.data || a.dt.data);
+  Tail* tail = reinterpret_cast<Tail*>(gbuf + (a.gstage ? static_cast<size_t>(4) * W : 0));
   auto stage_ptr = [&](int st) { return smem + static_cast<size_t>(st) * 4 * W; };
 
   const uint32_t crank = cluster_rank(), csize = cluster_size();
@@ -534,6 +559,15 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
       bulk_load(dst + static_cast<size_t>(W) * 2, a.t + (a.mt.offset(r) + col0) * 2, bytes, &tail->tma_bar[st]);
     }
     ++issued[st];
+  };
+
+  // Control warp: bulk stores of the staged gradients of row r.
+  auto store_grads = [&](int64_t r) {
+    if (lane == 0 && bytes) {
+      if (a.ds.data) bulk_store(a.ds.data + (r * a.ds.row_stride + col0) * 2, gbuf, bytes);
+      if (a.dt.data) bulk_store(a.dt.data + (r * a.dt.row_stride + col0) * 2, gbuf + static_cast<size_t>(W) * 2, bytes);
+      bulk_commit();
+    }
   };
 
   if (control) {
@@ -568,6 +602,7 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
       control_push_stats(tail->stat_part[0], nw, tail, 0, crank, csize);
     }
     int64_t i = 0;
+    int64_t owed = -1;  // row whose staged gradients the workers write next (not yet stored)
     for (int64_t r = q; r < a.rows; r += Q, ++i) {
       const int par = static_cast<int>(i & 1);
       const uint32_t ph = static_cast<uint32_t>((i >> 1) & 1);
@@ -595,6 +630,14 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
       bar_arrive(kBarStatReady, nthreads);
       if (!ok) break;
 
+      // The previous row's gradients are staged (the workers finished its
+      // pass D before taking this row's statistics): store them.
+      if (owed >= 0) {
+        bar_sync(kBarGradFull, nthreads);
+        store_grads(owed);
+        owed = -1;
+      }
+
       // (C2) the workers have read this row's stage: refill it with the row
       // kStages on; reduce and push this row's sums
       bar_sync(kBarSumPart, nthreads);
@@ -608,14 +651,8 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
                  map_rank(smem_addr(&tail->sum_bar[par]), lane));
       }
 
-      // (C3) statistics of the next row
-      if (has_next) {
-        bar_sync(kBarStatPart, nthreads);
-        if (tail->fail) ok = false;
-        control_push_stats(tail->stat_part[par ^ 1], nw, tail, par ^ 1, crank, csize);
-      }
-
-      // (C4) global sums of row r: the per-token value and saved statistics
+      // (C3) global sums of row r, handed to the workers as soon as they
+      // arrive; then the per-token value and saved statistics
       float A = qnan(), B = qnan(), value = qnan();
       const bool got = ok && control_wait(&tail->sum_bar[par], ph, csize);
       if (!got) ok = false;
@@ -632,21 +669,34 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
           B = MODE == kForwardKL ? 0.f : value;
         }
       }
-      if (lane == 0) {
-        *reinterpret_cast<float4*>(tail->sum_res[par]) = make_float4(A, B, value, 0.f);
-        if (crank == 0) {
-          a.loss[r] = value;
-          float* sv = a.saved + r * VPD_SAVED_PAIR;
-          sv[0] = bad_s ? qnan() : g.x;
-          sv[1] = bad_s ? qnan() : (g.x == neg_inf() ? neg_inf() : kLn2 * log2f(g.y));
-          sv[2] = bad_t ? qnan() : g.z;
-          sv[3] = bad_t ? qnan() : (g.z == neg_inf() ? neg_inf() : kLn2 * log2f(g.w));
-          sv[4] = A;
-          sv[5] = B;
-        }
-      }
+      if (lane == 0) *reinterpret_cast<float4*>(tail->sum_res[par]) = make_float4(A, B, value, 0.f);
+      // the workers overwrite the staging buffer once they have this row's sums
+      if (staged && lane == 0) bulk_wait_read();
       bar_arrive(kBarSumReady, nthreads);
+      if (staged) owed = r;
+      if (lane == 0 && crank == 0) {
+        a.loss[r] = value;
+        float* sv = a.saved + r * VPD_SAVED_PAIR;
+        sv[0] = bad_s ? qnan() : g.x;
+        sv[1] = bad_s ? qnan() : (g.x == neg_inf() ? neg_inf() : (row_ok ? kLn2 * Ks : kLn2 * log2f(g.y)));
+        sv[2] = bad_t ? qnan() : g.z;
+        sv[3] = bad_t ? qnan() : (g.z == neg_inf() ? neg_inf() : (row_ok ? kLn2 * Kt : kLn2 * log2f(g.w)));
+        sv[4] = A;
+        sv[5] = B;
+      }
+
+      // (C4) statistics of the next row
+      if (has_next) {
+        bar_sync(kBarStatPart, nthreads);
+        if (tail->fail) ok = false;
+        control_push_stats(tail->stat_part[par ^ 1], nw, tail, par ^ 1, crank, csize);
+      }
     }
+    if (owed >= 0) {
+      bar_sync(kBarGradFull, nthreads);
+      store_grads(owed);
+    }
+    if (lane == 0) bulk_wait_all();
     // Copies still in flight (only after a wait gave up) must land before exit.
     if (lane == 0)
       for (int st = 0; st < kStages; ++st)
@@ -679,6 +729,9 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
       const bool has_next = r + Q < a.rows;
       const int cst = static_cast<int>(i % kStages);
       const int nst = static_cast<int>((i + 1) % kStages);
+
+      // upstream gradient of row r, loaded well before pass D needs it
+      const float gr = a.grad_loss ? __ldg(a.grad_loss + r) : 1.f;
 
       // (W1) global statistics of row r
       bar_sync(kBarStatReady, nthreads);
@@ -763,7 +816,6 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
       const float A = ab.x, B = ab.y, value = ab.z;
 
       // (W5) pass D of row r: gradients, e.g. dS = p (g (1-beta) ln2 (log2 p - log2 M) - g (1-beta) B)
-      const float gr = a.grad_loss ? __ldg(a.grad_loss + r) : 1.f;
       char* ds_row = a.ds.data ? a.ds.data + (r * a.ds.row_stride + col0 + tid * 8) * Out<G>::kSize : nullptr;
       char* dt_row = a.dt.data ? a.dt.data + (r * a.dt.row_stride + col0 + tid * 8) * Out<G>::kSize : nullptr;
       if (ds_row || dt_row) {
@@ -802,9 +854,18 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
             }
           }
           if (e0 < len) {
-            if (ds_row) Out<G>::store8(ds_row + k * gstride, gs);
-            if (dt_row) Out<G>::store8(dt_row + k * gstride, gt);
+            if (staged) {
+              if (ds_row) Out<G>::store8_shared(gbuf + e0 * 2, gs);
+              if (dt_row) Out<G>::store8_shared(gbuf + static_cast<size_t>(W) * 2 + e0 * 2, gt);
+            } else {
+              if (ds_row) Out<G>::store8(ds_row + k * gstride, gs);
+              if (dt_row) Out<G>::store8(dt_row + k * gstride, gt);
+            }
           }
+        }
+        if (staged) {
+          fence_proxy_async();
+          bar_arrive(kBarGradFull, nthreads);
         }
       }
     }
@@ -830,8 +891,8 @@ struct Config {
 
 // Shared memory of a slice width: both stages of both inputs, then the tail,
 // and at least kMinSmem so that no two CTAs share an SM's tensor memory.
-inline size_t smem_bytes(int W) {
-  const size_t s = static_cast<size_t>(kStages) * 4 * W + sizeof(Tail);
+inline size_t smem_bytes(int W, bool gstage = false) {
+  const size_t s = static_cast<size_t>(kStages) * 4 * W + (gstage ? static_cast<size_t>(4) * W : 0) + sizeof(Tail);
   return s < kMinSmem ? kMinSmem : s;
 }
 
