@@ -59,6 +59,9 @@ def parse_args():
     p.add_argument("--sweep", action="store_true",
                    help="instead of the headline line, print one JSONL record per workload x op x phase")
     p.add_argument("--sweep-steps", type=int, default=10)
+    p.add_argument("--profile-rows", type=int, default=0,
+                   help="profiling mode: only the fused step on this many rows of the same vocabulary, "
+                        "--warmup + --steps launches, one short line (for ncu captures of a small case)")
     return p.parse_args()
 
 
@@ -563,8 +566,36 @@ def run_sweep(args):
         torch.cuda.empty_cache()
 
 
+def run_profile(args):
+    """The headline step on a smaller row count, for profiler captures: the same
+    kernel and launch shape per row, a few GB on the device."""
+    from softmax_divergence_lm_gb300 import binding as B
+    from softmax_divergence_lm_gb300 import build as cuda_build
+    from softmax_divergence_lm_gb300 import synth
+
+    dev = torch.device("cuda", 0)
+    cuda_build.build()
+    B.load()
+    n = args.profile_rows
+    s3, t3 = synth.qwen_vocab(device=dev, batch=1, seq=n)
+    s, t = s3.view(n, VOCAB), t3.view(n, VOCAB)
+    g = torch.full((n,), 1.0 / n, device=dev)
+    loss = torch.empty(n, device=dev)
+    saved = torch.empty(n, B.SAVED_PAIR, device=dev)
+    ds = torch.empty(n, VOCAB, dtype=torch.bfloat16, device=dev)
+    dt = torch.empty(n, VOCAB, dtype=torch.bfloat16, device=dev)
+    for _ in range(args.warmup + args.steps):
+        B.vpd_jsd_fwdbwd(s, t, BETA, None, g, loss, saved, ds, dt)
+    torch.cuda.synchronize(dev)
+    B.vpd_device_status()
+    print(json.dumps({"profile_rows": n, "launches": args.warmup + args.steps, "vocab": VOCAB}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.profile_rows:
+        run_profile(args)
+        return
     if args.sweep:
         run_sweep(args)
         return
