@@ -44,6 +44,8 @@
 
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "vpd_internal.h"
 
 namespace vpd {
@@ -463,17 +465,34 @@ __device__ __forceinline__ void control_push_stats(const float (*part)[4], int n
            map_rank(smem_addr(&tail->stat_bar[par]), lane));
 }
 
+// Which of its R vectors (k Tw + tid, k = 0..R-1) a worker thread holds: the
+// first `kv`; every lane of its warp holds the first `kfull`, some lane the
+// first `kwarp` (both warp-uniform).
+struct Span {
+  int kv, kfull, kwarp;
+};
+template <int R>
+__device__ __forceinline__ Span span_of(int len, int Tw) {
+  const int nv = len >> 3, tid = threadIdx.x, w0 = tid & ~31;
+  auto kv_of = [&](int t) {
+    const int k = (nv - t + Tw - 1) / Tw;
+    return k < 0 ? 0 : (k > R ? R : k);
+  };
+  return {kv_of(tid), kv_of(w0 + 31), kv_of(w0)};
+}
+
 // Worker warps: statistics partial of one row read from its shared-memory
 // stage; lane 0 writes the warp's (m_s, z_s, m_t, z_t) to `part`.
 template <class In, int R>
-__device__ __forceinline__ void worker_stats(const unsigned char* sb, int W, int len, int Tw, float* part) {
+__device__ __forceinline__ void worker_stats(const unsigned char* sb, int W, const Span& sp, int Tw, float* part) {
   const int tid = threadIdx.x, lane = tid & 31;
+  const unsigned char* ps = sb + tid * 16;
+  const size_t tofs = static_cast<size_t>(W) * 2;
   uint32_t mxs = In::kNegInf2, mxt = In::kNegInf2;
 #pragma unroll
   for (int k = 0; k < R; ++k) {
-    const int e0 = (k * Tw + tid) * 8;
-    if (e0 < len) {
-      const uint4 u = lds16(sb + e0 * 2), v = lds16(sb + static_cast<size_t>(W) * 2 + e0 * 2);
+    if (k < sp.kv) {
+      const uint4 u = lds16(ps + k * Tw * 16), v = lds16(ps + tofs + k * Tw * 16);
       mxs = In::max_nan(mxs, In::max_nan(In::max_nan(u.x, u.y), In::max_nan(u.z, u.w)));
       mxt = In::max_nan(mxt, In::max_nan(In::max_nan(v.x, v.y), In::max_nan(v.z, v.w)));
     }
@@ -484,9 +503,8 @@ __device__ __forceinline__ void worker_stats(const unsigned char* sb, int W, int
   float2 zs2 = f2(0.f), zt2 = f2(0.f);
 #pragma unroll
   for (int k = 0; k < R; ++k) {
-    const int e0 = (k * Tw + tid) * 8;
-    if (e0 < len) {
-      const uint4 u = lds16(sb + e0 * 2), v = lds16(sb + static_cast<size_t>(W) * 2 + e0 * 2);
+    if (k < sp.kv) {
+      const uint4 u = lds16(ps + k * Tw * 16), v = lds16(ps + tofs + k * Tw * 16);
       const uint32_t us[4] = {u.x, u.y, u.z, u.w}, vs[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
@@ -717,10 +735,11 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
     };
     const float2 ws2 = f2(1.f - beta), wt2 = f2(beta), tiny2 = f2(kTiny), l2e2 = f2(kLog2e);
     const int64_t gstride = static_cast<int64_t>(Tw) * 8 * Out<G>::kSize;  // bytes between vectors k, k + 1
+    const Span sp = span_of<R>(len, Tw);
 
     if (q < a.rows) {
       wait_stage(0);
-      worker_stats<In, R>(stage_ptr(0), W, len, Tw, tail->stat_part[0][warp]);
+      worker_stats<In, R>(stage_ptr(0), W, sp, Tw, tail->stat_part[0][warp]);
       bar_arrive(kBarStatPart, nthreads);
     }
     int64_t i = 0;
@@ -750,15 +769,18 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
       float2 acc_a = f2(0.f), acc_b = f2(0.f);
       uint32_t viol = 0;
       if (row_ok) {
-        const unsigned char* sb = stage_ptr(cst);
-#pragma unroll
-        for (int k = 0; k < R; ++k) {
-          if ((k * Tw + warp * 32) * 8 >= len) continue;  // warp-uniform
-          const int e0 = (k * Tw + tid) * 8;
-          uint4 u = make_uint4(In::kNegBig2, In::kNegBig2, In::kNegBig2, In::kNegBig2), v = u;
-          if (e0 < len) {
-            u = lds16(sb + e0 * 2);
-            v = lds16(sb + static_cast<size_t>(W) * 2 + e0 * 2);
+        const unsigned char* ps = stage_ptr(cst) + tid * 16;
+        const size_t tofs = static_cast<size_t>(W) * 2;
+        // One vector: PARTIAL marks the warp that straddles the slice end,
+        // whose lanes past it compute on the floor value.
+        auto vec_c = [&](int k, auto partial) {
+          constexpr bool PARTIAL = decltype(partial)::value;
+          uint4 u, v;
+          if (!PARTIAL || k < sp.kv) {
+            u = lds16(ps + k * Tw * 16);
+            v = lds16(ps + tofs + k * Tw * 16);
+          } else {
+            u = v = make_uint4(In::kNegBig2, In::kNegBig2, In::kNegBig2, In::kNegBig2);
           }
           const uint32_t us[4] = {u.x, u.y, u.z, u.w}, vs[4] = {v.x, v.y, v.z, v.w};
           float2 t0[4], t1[4], t2[4];
@@ -791,6 +813,11 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
           tmem_st8(tmem + k * kCols, t0);
           tmem_st8(tmem + k * kCols + 8, t1);
           if (MODE == kInterior) tmem_st8(tmem + k * kCols + 16, t2);
+        };
+#pragma unroll
+        for (int k = 0; k < R; ++k) {
+          if (k < sp.kfull) vec_c(k, std::false_type{});
+          else if (k < sp.kwarp) vec_c(k, std::true_type{});  // warp-uniform branches
         }
         tmem_wait_st();
       }
@@ -806,7 +833,7 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
       // while this row's sums travel
       if (has_next) {
         wait_stage(nst);
-        worker_stats<In, R>(stage_ptr(nst), W, len, Tw, tail->stat_part[par ^ 1][warp]);
+        worker_stats<In, R>(stage_ptr(nst), W, sp, Tw, tail->stat_part[par ^ 1][warp]);
         bar_arrive(kBarStatPart, nthreads);
       }
 
@@ -826,43 +853,66 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
         const float2 ncs2 = f2(-cs * (MODE == kInterior ? B : value));
         const float2 nct2 = f2(-ct * (MODE == kInterior ? A : value));
         const float2 g2 = f2(gr);
-#pragma unroll
-        for (int k = 0; k < R; ++k) {
-          if ((k * Tw + warp * 32) * 8 >= len) continue;  // warp-uniform
-          const int e0 = (k * Tw + tid) * 8;
+        // One vector: TMEM loads stay warp-uniform; only lanes holding the
+        // vector store it.
+        auto vec_d = [&](int k, auto staged_t) {
+          constexpr bool STAGED = decltype(staged_t)::value;
           float2 gs[4], gt[4];
-          if (!live) {
+          float2 p[4], u1[4], u2[4];
+          if (MODE == kInterior) tmem_ld24_wait(tmem + k * kCols, p, u1, u2);
+          else tmem_ld16_wait(tmem + k * kCols, p, u1);
 #pragma unroll
-            for (int w = 0; w < 4; ++w) gs[w] = gt[w] = f2(0.f);
-          } else {
-            float2 p[4], u1[4], u2[4];
-            if (MODE == kInterior) tmem_ld24_wait(tmem + k * kCols, p, u1, u2);
-            else tmem_ld16_wait(tmem + k * kCols, p, u1);
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              const float2 qv = kq[k][w];
-              if (MODE == kInterior) {
-                gs[w] = mul2(p[w], fma2(cs2, u1[w], ncs2));
-                gt[w] = mul2(qv, fma2(ct2, u2[w], nct2));
-              } else if (MODE == kForwardKL) {  // dS = g (p - q), dT = g q (ln q - ln p - KL)
-                gs[w] = mul2(g2, add2(p[w], neg(qv)));
-                gt[w] = mul2(qv, fma2(ct2, u1[w], nct2));
-              } else {  // dS = g p (ln p - ln q - KL), dT = g (q - p)
-                gs[w] = mul2(p[w], fma2(cs2, u1[w], ncs2));
-                gt[w] = mul2(g2, add2(qv, neg(p[w])));
-              }
+          for (int w = 0; w < 4; ++w) {
+            const float2 qv = kq[k][w];
+            if (MODE == kInterior) {
+              gs[w] = mul2(p[w], fma2(cs2, u1[w], ncs2));
+              gt[w] = mul2(qv, fma2(ct2, u2[w], nct2));
+            } else if (MODE == kForwardKL) {  // dS = g (p - q), dT = g q (ln q - ln p - KL)
+              gs[w] = mul2(g2, add2(p[w], neg(qv)));
+              gt[w] = mul2(qv, fma2(ct2, u1[w], nct2));
+            } else {  // dS = g p (ln p - ln q - KL), dT = g (q - p)
+              gs[w] = mul2(p[w], fma2(cs2, u1[w], ncs2));
+              gt[w] = mul2(g2, add2(qv, neg(p[w])));
             }
           }
-          if (e0 < len) {
-            if (staged) {
-              if (ds_row) Out<G>::store8_shared(gbuf + e0 * 2, gs);
-              if (dt_row) Out<G>::store8_shared(gbuf + static_cast<size_t>(W) * 2 + e0 * 2, gt);
+          if (k < sp.kv) {
+            if constexpr (STAGED) {
+              unsigned char* pg = gbuf + (k * Tw + tid) * 16;
+              if (ds_row) Out<G>::store8_shared(pg, gs);
+              if (dt_row) Out<G>::store8_shared(pg + static_cast<size_t>(W) * 2, gt);
             } else {
               if (ds_row) Out<G>::store8(ds_row + k * gstride, gs);
               if (dt_row) Out<G>::store8(dt_row + k * gstride, gt);
             }
           }
-        }
+        };
+        // Rows with no defined value get zero gradients.
+        auto zero_d = [&](int k, auto staged_t) {
+          constexpr bool STAGED = decltype(staged_t)::value;
+          float2 z[4] = {f2(0.f), f2(0.f), f2(0.f), f2(0.f)};
+          if (k < sp.kv) {
+            if constexpr (STAGED) {
+              unsigned char* pg = gbuf + (k * Tw + tid) * 16;
+              if (ds_row) Out<G>::store8_shared(pg, z);
+              if (dt_row) Out<G>::store8_shared(pg + static_cast<size_t>(W) * 2, z);
+            } else {
+              if (ds_row) Out<G>::store8(ds_row + k * gstride, z);
+              if (dt_row) Out<G>::store8(dt_row + k * gstride, z);
+            }
+          }
+        };
+        auto run_d = [&](auto staged_t) {
+          if (live) {
+#pragma unroll
+            for (int k = 0; k < R; ++k)
+              if (k < sp.kwarp) vec_d(k, staged_t);  // warp-uniform
+          } else {
+#pragma unroll
+            for (int k = 0; k < R; ++k) zero_d(k, staged_t);
+          }
+        };
+        if (Out<G>::kSize == 2 && staged) run_d(std::true_type{});
+        else run_d(std::false_type{});
         if (staged) {
           fence_proxy_async();
           bar_arrive(kBarGradFull, nthreads);
