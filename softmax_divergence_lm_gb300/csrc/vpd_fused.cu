@@ -77,11 +77,16 @@ size_t max_smem_optin() {
   return v < 1 ? 0 : static_cast<size_t>(v);
 }
 
-// The launch shape with the least time per row batch: for each cluster size C
-// whose slice fits (two stages in shared memory), the fewest vector slots per
-// CTA, nw worker warps x R vectors per thread covering the slice (R and nw
-// within the register and TMEM budgets), times the rows each cluster runs.
-// Ties go to the smaller cluster.
+// Per-row cost of the cluster exchanges, in units of one 16-byte vector pair
+// of work on an SM (about 1.5 us of hand-overs against about 4 ns a vector).
+constexpr int64_t kRowOverheadVectors = 400;
+
+// The launch shape: the cluster size C with the least time per row batch,
+// rows per cluster x (slice vectors + exchange overhead), among those whose
+// slice fits (two stages in shared memory; at most kMaxR vectors per worker
+// thread within the register and TMEM budgets); then the smallest R that
+// covers the slice and as many workers as the budgets allow without idle
+// warps (more warps hide more latency). Ties go to the smaller cluster.
 bool choose(int64_t vocab, int64_t rows, Config* cfg) {
   const size_t smem_cap = max_smem_optin();
   int64_t best = 0;
@@ -91,17 +96,20 @@ bool choose(int64_t vocab, int64_t rows, Config* cfg) {
     const size_t smem = fused::smem_bytes(static_cast<int>(W));
     if (smem > smem_cap) continue;
     int bR = 0, bnw = 0;
-    for (int R = 1; R <= fused::kMaxR; ++R) {
-      const int64_t nw = (nvec + 32 * R - 1) / (32 * R);
-      if (nw > fused::max_workers(R)) continue;
+    for (int R = 1; R <= fused::kMaxR && !bR; ++R) {
+      const int64_t cap = fused::max_workers(R);
+      if (nvec > 32 * cap * R) continue;
+      int64_t nw = R == 1 ? (nvec + 31) / 32 : (nvec + 32 * (R - 1) - 1) / (32 * (R - 1));
+      if (nw > cap) nw = cap;
+      if (nw < 1) nw = 1;
       if (R * fused::Cols<fused::kInterior>::k > fused::tmem_cols_per_warp(static_cast<int>(nw))) continue;
-      if (!bR || nw * R < static_cast<int64_t>(bnw) * bR) bR = R, bnw = static_cast<int>(nw);
+      bR = R, bnw = static_cast<int>(nw);
     }
     if (!bR) continue;
     const int clusters = clusters_for(C);
     if (clusters < 1) continue;
     const int64_t used = rows < clusters ? rows : clusters;
-    const int64_t cost = (rows + used - 1) / used * bnw * bR;
+    const int64_t cost = (rows + used - 1) / used * (nvec + kRowOverheadVectors);
     if (!best || cost < best) {
       best = cost;
       *cfg = Config{C, bR, static_cast<int>(W), bnw, smem};

@@ -58,9 +58,11 @@ constexpr int kMaxCluster = 16;
 constexpr int kMaxR = 5;                    // 16-byte vectors of each input per worker thread
 constexpr int kTmemCols = 512;              // the whole tensor memory of the SM
 constexpr int kMinSmem = 120 * 1024;        // keeps one CTA per SM (each takes all TMEM)
-constexpr int kMaxWorkers = 17;             // worker warps per CTA (plus one control warp)
-// Worker warps per CTA for R vectors per thread: the register budget of a
-// thread is 64K / (32 (workers + 1)), 136 registers at R = 5, 112 below.
+constexpr int kMaxWorkers = 19;             // worker warps per CTA (plus one control warp)
+// Worker warps per CTA for R vectors per thread. A warp scheduler (SM
+// sub-partition) holds a quarter of the register file, so the budget of a
+// thread is 16K / (32 ceil((workers + 1) / 4)): 136 registers at R = 5 (15
+// warps), 96 below (20 warps).
 __host__ __device__ constexpr int max_workers(int R) { return R >= 5 ? 14 : kMaxWorkers; }
 // TMEM columns of one worker warp: the warps of a lane quarter share its 512
 // columns (a multiple of 8 each).
