@@ -481,8 +481,12 @@ def run_sweep(args):
         dt_name = str(s.dtype).replace("torch.", "")
         for beta in betas:
             if not fused_only:
+                c0 = B.vpd_launch_count()
+                B.vpd_jsd_fwd(s, t, beta, segments, loss, saved)
+                torch.cuda.synchronize()
+                fpath = "single-read" if B.vpd_launch_count() - c0 == 1 else "two-pass"
                 ms = _time_call(lambda: B.vpd_jsd_fwd(s, t, beta, segments, loss, saved), steps, 3, stream)
-                emit(name, "jsd", "fwd (two-pass)", dt_name, beta, n, v, rd, ms)
+                emit(name, "jsd", f"fwd ({fpath})", dt_name, beta, n, v, rd, ms)
                 ms = _time_call(lambda: B.vpd_jsd_bwd(s, t, beta, segments, g, saved, ds, dt), steps, 3, stream)
                 emit(name, "jsd", "bwd", dt_name, beta, n, v, rd + wr, ms)
             c0 = B.vpd_launch_count()
@@ -495,7 +499,7 @@ def run_sweep(args):
             for rev in (False, True):
                 opn = "kl_reverse" if rev else "kl_forward"
                 ms = _time_call(lambda: B.vpd_kl_fwd(s, t, rev, segments, loss, saved), steps, 3, stream)
-                emit(name, opn, "fwd (single pass)", dt_name, None, n, v, rd, ms)
+                emit(name, opn, "fwd (one read)", dt_name, None, n, v, rd, ms)
                 ms = _time_call(lambda: B.vpd_kl_bwd(s, t, rev, segments, g, saved, ds, dt), steps, 3, stream)
                 emit(name, opn, "bwd", dt_name, None, n, v, rd + wr, ms)
         del ds, dt

@@ -59,7 +59,7 @@ typedef enum {
     VPD_ERR_ARG = 1,     /* NULL pointer, beta outside [0, 1], k < 1, misaligned pointer ... */
     VPD_ERR_DTYPE = 2,   /* unknown dtype, or student and teacher dtypes differ */
     VPD_ERR_SHAPE = 3,   /* rows/vocab mismatch, stride < vocab, segment widths not summing to vocab */
-    VPD_ERR_INDEX = 4,   /* reported by the host-side index helpers only */
+    VPD_ERR_INDEX = 4,   /* an index outside [0, V) (vpd_logprobs_fwd without err_flag) */
     VPD_ERR_CUDA = 5,    /* a CUDA call or launch failed */
     VPD_ERR_TIMEOUT = 6, /* a bounded device-side wait gave up (see vpd_device_status) */
     VPD_ERR_UNSUPPORTED = 7
@@ -127,13 +127,16 @@ typedef struct {
  *   segment table. beta in [0, 1].
  * ------------------------------------------------------------------------- */
 
-/* Forward in two input passes, the pages' design ([JSD page], "Scope and
- * limitations": statistics, then divergence): a paired-statistics kernel merges
- * per-segment (max, sum-exp) of both inputs, then a divergence kernel reduces the
- * two KL-to-mixture expectations together ([JSD page], "Changes").
+/* Forward. The statistics must be global before the divergence ([JSD page],
+ * "Scope and limitations"): when the single-read conditions of vpd_jsd_fwdbwd
+ * hold (one segment, 16-bit inputs, aligned rows), one cluster kernel reads each
+ * row pair once and keeps it on chip for both steps; otherwise the pages' design
+ * in two input passes: a paired-statistics kernel merges per-segment (max,
+ * sum-exp) of both inputs, then a divergence kernel reduces the two
+ * KL-to-mixture expectations together ([JSD page], "Changes").
  * loss:  device float[N], the per-token divergence.
- * saved: device float[N, 6] (see above), required: it also carries the
- *        statistics from the first kernel to the second. */
+ * saved: device float[N, 6] (see above), required: it carries the statistics
+ *        to the backward (and between the two streaming kernels). */
 vpd_status vpd_jsd_fwd(const vpd_view *s, const vpd_view *t, double beta, const vpd_segments *seg,
                        float *loss, float *saved, void *stream);
 
@@ -169,9 +172,11 @@ vpd_status vpd_jsd_fwdbwd(const vpd_view *s, const vpd_view *t, double beta,
 
 /* ---------------------------------------------------------------------------
  * Forward / reverse KL ([ops page], "What"): reverse = 0 gives KL(P_t || P_s)
- * (the teacher is the target), reverse = 1 gives KL(P_s || P_t). The forward is
- * one online pass over the inputs (running maxima with rescaled sums). Saved
- * layout and backward are those of the JSD beta = 0 / 1 branches.
+ * (the teacher is the target), reverse = 1 gives KL(P_s || P_t). The forward
+ * reads the inputs once: the single-read cluster kernel's KL branch when its
+ * conditions hold (see vpd_jsd_fwdbwd), else one online pass (running maxima
+ * with rescaled sums). saved may be NULL. Saved layout and backward are those
+ * of the JSD beta = 0 / 1 branches.
  * ------------------------------------------------------------------------- */
 vpd_status vpd_kl_fwd(const vpd_view *s, const vpd_view *t, int32_t reverse,
                       const vpd_segments *seg, float *loss, float *saved, void *stream);
@@ -196,11 +201,14 @@ vpd_status vpd_entropy_bwd(const vpd_view *x, const vpd_segments *seg, const flo
  *   takes no gradient.
  * index: device int64[N, k] (row-major, k >= 1).
  * out: device float[N, k]; saved: device float[N, 2] or NULL.
- * err_flag: device int32[1], required. The call sets it to 0, and to 1 if any
- *   index outside [0, V) (other than ignore_index) is found; such positions
- *   output NaN. Reading the flag is the caller's synchronisation point (the
- *   pages' wrapper syncs on this check, [ops page], review thread "Provide a path
- *   for reusing validated shard metadata").
+ * err_flag: device int32[1] or NULL. Given, the call sets it to 0, and to 1 if
+ *   any index outside [0, V) (other than ignore_index) is found; such positions
+ *   output NaN, and reading the flag is the caller's synchronisation point.
+ *   NULL: the call copies the indices to the host on `stream`, synchronises,
+ *   and returns VPD_ERR_INDEX before any launch (nothing written) if one is
+ *   out of range. Either way the check is the pages' synchronising index
+ *   validation ([ops page], review thread "Provide a path for reusing validated
+ *   shard metadata").
  * Backward: dX_j = sum_k g_rk [j == index_rk] - p_j sum_k g_rk over the positions
  *   with a finite output. grad_out: device float[N, k] (NULL means 1).
  * ------------------------------------------------------------------------- */

@@ -245,12 +245,15 @@ def _index_ptr(index: torch.Tensor):
 
 
 def vpd_logprobs_fwd(x, segments, index, k, ignore_index, out, saved, err_flag, stream=None):
+    """err_flag: int32 CUDA tensor, or None (the library then checks the
+    indices on the host and raises VPD_ERR_INDEX before launching)."""
     vx = make_view(x)
     seg, _keep = make_segments(segments)
-    if err_flag.dtype != torch.int32 or not err_flag.is_cuda:
-        raise ValueError("err_flag must be an int32 CUDA tensor")
+    if err_flag is not None and (err_flag.dtype != torch.int32 or not err_flag.is_cuda):
+        raise ValueError("err_flag must be an int32 CUDA tensor or None")
     _check(load().vpd_logprobs_fwd(ctypes.byref(vx), _ref(seg), _index_ptr(index), int(k), int(ignore_index),
-                                   _fptr(out), _fptr(saved), err_flag.data_ptr(), _stream(stream)))
+                                   _fptr(out), _fptr(saved), err_flag.data_ptr() if err_flag is not None else None,
+                                   _stream(stream)))
 
 
 def vpd_logprobs_bwd(x, segments, index, k, ignore_index, grad_out, saved, dx, stream=None):

@@ -8,6 +8,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <vector>
 
 #include "vpd.h"
 #include "vpd_internal.h"
@@ -149,6 +150,12 @@ vpd_status check_grads_pair(const vpd_grad* ds, const vpd_grad* dt, const vpd::V
 
 extern "C" {
 
+// Forward-only calls take the single-read kernel only in clusters of at most
+// this many CTAs: on this GPU larger clusters leave a quarter of the SMs idle
+// (16-CTA clusters cover 112 of 152), and without a backward the streaming
+// kernels on every SM are faster there.
+constexpr int kForwardMaxCluster = 10;
+
 vpd_status vpd_jsd_fwd(const vpd_view* s, const vpd_view* t, double beta, const vpd_segments* seg,
                        float* loss, float* saved, void* stream) {
   vpd::View vs, vt;
@@ -159,6 +166,16 @@ vpd_status vpd_jsd_fwd(const vpd_view* s, const vpd_view* t, double beta, const 
   if (vs.rows == 0) return ok();
   if (!loss || !saved) return fail(VPD_ERR_ARG, "vpd_jsd_fwd: loss and saved are required");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // One read of the inputs when the single-read kernel takes the shape (no
+  // gradients wanted) in clusters that still cover most SMs; otherwise the two
+  // streaming passes, which use every SM.
+  if (sg.count == 1) {
+    const vpd::Grad none{nullptr, 0, 0};
+    cudaError_t e = vpd::launch_jsd_fused(vs, vt, beta, nullptr, loss, saved, none, none, st, -1,
+                                          kForwardMaxCluster);
+    if (e == cudaSuccess) return ok();
+    if (e != cudaErrorNotSupported) return cuda_fail(e, "fused single-read kernel");
+  }
   VPD_CUDA(vpd::launch_pair_stats(vs, vt, sg, saved, st), "paired statistics kernel");
   VPD_CUDA(vpd::launch_jsd_div(vs, vt, beta, loss, saved, st), "divergence kernel");
   return ok();
@@ -218,6 +235,15 @@ vpd_status vpd_kl_fwd(const vpd_view* s, const vpd_view* t, int32_t reverse,
   VPD_TRY(check_segments(seg, vs.vocab, &sg));
   if (vs.rows == 0) return ok();
   if (!loss) return fail(VPD_ERR_ARG, "vpd_kl_fwd: loss is required");
+  // The KL branches of the single-read kernel (beta = 0 / 1) when it takes the
+  // shape; otherwise the online single-pass kernel.
+  if (sg.count == 1) {
+    const vpd::Grad none{nullptr, 0, 0};
+    cudaError_t e = vpd::launch_jsd_fused(vs, vt, reverse ? 1.0 : 0.0, nullptr, loss, saved, none, none,
+                                          static_cast<cudaStream_t>(stream), -1, kForwardMaxCluster);
+    if (e == cudaSuccess) return ok();
+    if (e != cudaErrorNotSupported) return cuda_fail(e, "fused single-read kernel");
+  }
   VPD_CUDA(vpd::launch_kl_fwd(vs, vt, reverse ? 1 : 0, sg, loss, saved,
                               static_cast<cudaStream_t>(stream)),
            "single-pass KL kernel");
@@ -277,11 +303,23 @@ vpd_status vpd_logprobs_fwd(const vpd_view* x, const vpd_segments* seg, const in
   VPD_TRY(check_view(x, "x", &vx));
   VPD_TRY(check_segments(seg, vx.vocab, &sg));
   if (k < 1) return fail(VPD_ERR_ARG, "vpd_logprobs_fwd: k must be >= 1");
-  if (!err_flag) return fail(VPD_ERR_ARG, "vpd_logprobs_fwd: err_flag is required");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  VPD_CUDA(cudaMemsetAsync(err_flag, 0, sizeof(int32_t), st), "clearing err_flag");
+  if (err_flag) VPD_CUDA(cudaMemsetAsync(err_flag, 0, sizeof(int32_t), st), "clearing err_flag");
   if (vx.rows == 0) return ok();
   if (!index || !out) return fail(VPD_ERR_ARG, "vpd_logprobs_fwd: index and out are required");
+  if (!err_flag) {
+    // No flag: the indices are checked on the host first (a copy on the
+    // caller's stream, then a synchronisation), so a bad index is an error
+    // before anything is launched or written.
+    std::vector<int64_t> h(static_cast<size_t>(vx.rows) * static_cast<size_t>(k));
+    VPD_CUDA(cudaMemcpyAsync(h.data(), index, h.size() * sizeof(int64_t), cudaMemcpyDeviceToHost, st),
+             "reading index");
+    VPD_CUDA(cudaStreamSynchronize(st), "reading index");
+    for (size_t i = 0; i < h.size(); ++i)
+      if (h[i] != ignore_index && (h[i] < 0 || h[i] >= vx.vocab))
+        return fail(VPD_ERR_INDEX, "vpd_logprobs_fwd: index[%lld] = %lld outside [0, %lld)",
+                    static_cast<long long>(i), static_cast<long long>(h[i]), static_cast<long long>(vx.vocab));
+  }
   VPD_CUDA(vpd::launch_logprobs_fwd(vx, sg, index, k, ignore_index, out, saved, err_flag, st),
            "log-prob kernel");
   return ok();

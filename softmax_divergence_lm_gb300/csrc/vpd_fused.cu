@@ -87,10 +87,10 @@ constexpr int64_t kRowOverheadVectors = 400;
 // thread within the register and TMEM budgets); then the smallest R that
 // covers the slice and as many workers as the budgets allow without idle
 // warps (more warps hide more latency). Ties go to the smaller cluster.
-bool choose(int64_t vocab, int64_t rows, Config* cfg) {
+bool choose(int64_t vocab, int64_t rows, int max_cluster, Config* cfg) {
   const size_t smem_cap = max_smem_optin();
   int64_t best = 0;
-  for (int C = 1; C <= fused::kMaxCluster; ++C) {
+  for (int C = 1; C <= fused::kMaxCluster && C <= max_cluster; ++C) {
     const int64_t W = ((vocab + C - 1) / C + 7) / 8 * 8;
     const int64_t nvec = W / 8;
     const size_t smem = fused::smem_bytes(static_cast<int>(W));
@@ -122,7 +122,7 @@ bool choose(int64_t vocab, int64_t rows, Config* cfg) {
 
 cudaError_t launch_jsd_fused(const View& s, const View& t, double beta, const float* grad_loss,
                              float* loss, float* saved, const Grad& ds, const Grad& dt,
-                             cudaStream_t stream, int64_t withhold_row) {
+                             cudaStream_t stream, int64_t withhold_row, int max_cluster) {
   // 16-bit inputs only; every row of both inputs and of both gradients must
   // start on a 16-byte boundary, and V must fill whole 16-byte vectors.
   if (s.dtype == kF32 || s.vocab <= 0 || s.vocab % 8 != 0) return cudaErrorNotSupported;
@@ -140,7 +140,7 @@ cudaError_t launch_jsd_fused(const View& s, const View& t, double beta, const fl
     gdtype = g->dtype;
   }
   Config cfg;
-  if (!choose(s.vocab, s.rows, &cfg)) return cudaErrorNotSupported;
+  if (!choose(s.vocab, s.rows, max_cluster, &cfg)) return cudaErrorNotSupported;
   const int mode = beta == 0.0 ? fused::kForwardKL : beta == 1.0 ? fused::kReverseKL : fused::kInterior;
   const bool f32g = gdtype == kF32;
   // 16-bit gradients go out through a shared-memory buffer and bulk stores

@@ -694,8 +694,8 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
       if (staged && lane == 0) bulk_wait_read();
       bar_arrive(kBarSumReady, nthreads);
       if (staged) owed = r;
-      if (lane == 0 && crank == 0) {
-        a.loss[r] = value;
+      if (lane == 0 && crank == 0) a.loss[r] = value;
+      if (lane == 0 && crank == 0 && a.saved) {
         float* sv = a.saved + r * VPD_SAVED_PAIR;
         sv[0] = bad_s ? qnan() : g.x;
         sv[1] = bad_s ? qnan() : (g.x == neg_inf() ? neg_inf() : (row_ok ? kLn2 * Ks : kLn2 * log2f(g.y)));
@@ -771,6 +771,7 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
       float2 acc_a = f2(0.f), acc_b = f2(0.f);
       uint32_t viol = 0;
       if (row_ok) {
+        const bool keep = a.ds.data || a.dt.data;  // gradients wanted: pass D follows
         const unsigned char* ps = stage_ptr(cst) + tid * 16;
         const size_t tofs = static_cast<size_t>(W) * 2;
         // One vector: PARTIAL marks the warp that straddles the slice end,
@@ -812,9 +813,11 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
               t1[w] = d;
             }
           }
-          tmem_st8(tmem + k * kCols, t0);
-          tmem_st8(tmem + k * kCols + 8, t1);
-          if (MODE == kInterior) tmem_st8(tmem + k * kCols + 16, t2);
+          if (keep) {  // warp-uniform: pass D reads these
+            tmem_st8(tmem + k * kCols, t0);
+            tmem_st8(tmem + k * kCols + 8, t1);
+            if (MODE == kInterior) tmem_st8(tmem + k * kCols + 16, t2);
+          }
         };
 #pragma unroll
         for (int k = 0; k < R; ++k) {

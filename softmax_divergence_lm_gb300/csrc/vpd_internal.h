@@ -54,11 +54,12 @@ cudaError_t launch_logprobs_bwd(const View& x, const int64_t* index, int k, int6
 
 // Single-read fused JSD forward+backward on thread-block clusters. Returns
 // cudaErrorNotSupported (without launching) when the row pair does not fit on
-// chip or the layout does not allow it; the caller then uses the streaming path.
-// withhold_row >= 0 is the failure-path test hook (vpd_test_withhold_copy).
+// chip in clusters of at most max_cluster CTAs or the layout does not allow it;
+// the caller then uses the streaming path. withhold_row >= 0 is the
+// failure-path test hook (vpd_test_withhold_copy).
 cudaError_t launch_jsd_fused(const View& s, const View& t, double beta, const float* grad_loss,
                              float* loss, float* saved, const Grad& ds, const Grad& dt,
-                             cudaStream_t stream, int64_t withhold_row);
+                             cudaStream_t stream, int64_t withhold_row, int max_cluster = 16);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

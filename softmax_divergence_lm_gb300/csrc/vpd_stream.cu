@@ -693,7 +693,7 @@ __global__ void __launch_bounds__(kThreads) k_logprobs_fwd(View x, Segs seg, con
         v = 0.f;
       } else if (i < 0 || i >= x.vocab) {
         v = qnan();
-        atomicExch(err, 1);
+        if (err) atomicExch(err, 1);
       } else if (!stat_ok(st)) {
         v = qnan();
       } else {

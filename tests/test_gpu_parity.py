@@ -248,6 +248,30 @@ def test_logprobs_out_of_range_sets_flag(B):
     assert np.isfinite(o[0, 0]) and np.isnan(o[1, 0]) and np.isnan(o[2, 0]) and o[3, 0] == 0.0
 
 
+def test_logprobs_without_flag(B):
+    """With no err_flag the indices are validated on the host: valid indices
+    give the same outputs as the flagged call; a bad one is an error and
+    nothing is written."""
+    x = torch.randn(4, 100, device="cuda")
+    idx = torch.tensor([[1, 7], [99, -100], [0, 5], [-100, 42]], device="cuda")
+    out_f = torch.empty(4, 2, device="cuda")
+    out_n = torch.empty(4, 2, device="cuda")
+    err = torch.empty(1, dtype=torch.int32, device="cuda")
+    B.vpd_logprobs_fwd(x, None, idx, 2, -100, out_f, None, err)
+    B.vpd_logprobs_fwd(x, None, idx, 2, -100, out_n, None, None)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(out_f, out_n)
+    bad = idx.clone()
+    bad[2, 1] = 100
+    out_b = torch.full((4, 2), 7.0, device="cuda")
+    with pytest.raises(B.VpdError) as e:
+        B.vpd_logprobs_fwd(x, None, bad, 2, -100, out_b, None, None)
+    assert e.value.status == 4  # VPD_ERR_INDEX
+    torch.cuda.synchronize()
+    assert bool((out_b == 7.0).all()), "nothing is written when an index is rejected"
+
+
 def test_degenerate_shapes(B):
     # N = 0: nothing to do, nothing written
     e = torch.empty(0, 10, device="cuda")
