@@ -778,20 +778,29 @@ __global__ void __launch_bounds__(kThreads) k_logprobs_bwd(View x, const int64_t
 // ---------------------------------------------------------------------------
 // Launch helpers.
 // ---------------------------------------------------------------------------
+// Threads per CTA for rows of `vocab` elements of `esize` bytes: about 16
+// 16-byte vectors per thread, a multiple of 64 from 64 to kThreads. Short rows
+// get small CTAs, several per SM, so per-row reductions stay cheap.
+int threads_for(int64_t vocab, int esize) {
+  const int64_t nv = vocab * esize / 16;
+  const int64_t t = (nv / 16 + 63) / 64 * 64;
+  return t < 64 ? 64 : (t > kThreads ? kThreads : static_cast<int>(t));
+}
+
 template <class Kern>
-int grid_for(Kern kernel, int64_t rows) {
+int grid_for(Kern kernel, int64_t rows, int threads) {
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0) != cudaSuccess ||
-      per_sm < 1)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess || per_sm < 1)
     per_sm = 1;
   const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
   return static_cast<int>(rows < cap ? rows : cap);
 }
 
+// One CTA per row at a time (grid-stride over rows), `threads` per CTA.
 template <class Kern, class... Args>
-cudaError_t launch_rows(Kern kernel, int64_t rows, cudaStream_t stream, Args... args) {
+cudaError_t launch_rows(Kern kernel, int64_t rows, int threads, cudaStream_t stream, Args... args) {
   if (rows <= 0) return cudaSuccess;
-  kernel<<<grid_for(kernel, rows), kThreads, 0, stream>>>(args...);
+  kernel<<<grid_for(kernel, rows, threads), threads, 0, stream>>>(args...);
   note_launch();
   return cudaGetLastError();
 }
@@ -819,7 +828,7 @@ cudaError_t by_grad(int gdtype, Args&&... args) {
 template <class T>
 struct PairStatsL {
   static cudaError_t run(const View& s, const View& t, const Segs& seg, float* saved, cudaStream_t st) {
-    return launch_rows(k_pair_stats<T>, s.rows, st, s, t, seg, saved);
+    return launch_rows(k_pair_stats<T>, s.rows, threads_for(s.vocab, T::kSize), st, s, t, seg, saved);
   }
 };
 
@@ -828,9 +837,9 @@ struct DivL {
   static cudaError_t run(const View& s, const View& t, double beta, float* loss, float* saved,
                          cudaStream_t st) {
     const float b = static_cast<float>(beta);
-    if (beta == 0.0) return launch_rows(k_jsd_div<T, kForwardKL>, s.rows, st, s, t, b, loss, saved);
-    if (beta == 1.0) return launch_rows(k_jsd_div<T, kReverseKL>, s.rows, st, s, t, b, loss, saved);
-    return launch_rows(k_jsd_div<T, kInterior>, s.rows, st, s, t, b, loss, saved);
+    if (beta == 0.0) return launch_rows(k_jsd_div<T, kForwardKL>, s.rows, threads_for(s.vocab, T::kSize), st, s, t, b, loss, saved);
+    if (beta == 1.0) return launch_rows(k_jsd_div<T, kReverseKL>, s.rows, threads_for(s.vocab, T::kSize), st, s, t, b, loss, saved);
+    return launch_rows(k_jsd_div<T, kInterior>, s.rows, threads_for(s.vocab, T::kSize), st, s, t, b, loss, saved);
   }
 };
 
@@ -840,10 +849,10 @@ struct BwdL {
                          const float* saved, const Grad& ds, const Grad& dt, cudaStream_t st) {
     const float b = static_cast<float>(beta);
     if (beta == 0.0)
-      return launch_rows(k_pair_bwd<T, G, kForwardKL>, s.rows, st, s, t, b, g, saved, ds, dt);
+      return launch_rows(k_pair_bwd<T, G, kForwardKL>, s.rows, threads_for(s.vocab, T::kSize), st, s, t, b, g, saved, ds, dt);
     if (beta == 1.0)
-      return launch_rows(k_pair_bwd<T, G, kReverseKL>, s.rows, st, s, t, b, g, saved, ds, dt);
-    return launch_rows(k_pair_bwd<T, G, kInterior>, s.rows, st, s, t, b, g, saved, ds, dt);
+      return launch_rows(k_pair_bwd<T, G, kReverseKL>, s.rows, threads_for(s.vocab, T::kSize), st, s, t, b, g, saved, ds, dt);
+    return launch_rows(k_pair_bwd<T, G, kInterior>, s.rows, threads_for(s.vocab, T::kSize), st, s, t, b, g, saved, ds, dt);
   }
 };
 
@@ -860,14 +869,14 @@ template <class T>
 struct KlL {
   static cudaError_t run(const View& a, const View& b, const Segs& seg, int a_is_teacher, float* loss,
                          float* saved, cudaStream_t st) {
-    return launch_rows(k_kl_fwd<T>, a.rows, st, a, b, seg, a_is_teacher, loss, saved);
+    return launch_rows(k_kl_fwd<T>, a.rows, threads_for(a.vocab, T::kSize), st, a, b, seg, a_is_teacher, loss, saved);
   }
 };
 
 template <class T>
 struct EntL {
   static cudaError_t run(const View& x, const Segs& seg, float* out, float* saved, cudaStream_t st) {
-    return launch_rows(k_entropy_fwd<T>, x.rows, st, x, seg, out, saved);
+    return launch_rows(k_entropy_fwd<T>, x.rows, threads_for(x.vocab, T::kSize), st, x, seg, out, saved);
   }
 };
 
@@ -875,7 +884,7 @@ template <class T, class G>
 struct EntBwdL {
   static cudaError_t run(const View& x, const float* g, const float* saved, const Grad& dx,
                          cudaStream_t st) {
-    return launch_rows(k_entropy_bwd<T, G>, x.rows, st, x, g, saved, dx);
+    return launch_rows(k_entropy_bwd<T, G>, x.rows, threads_for(x.vocab, T::kSize), st, x, g, saved, dx);
   }
 };
 
@@ -891,7 +900,7 @@ template <class T>
 struct LpL {
   static cudaError_t run(const View& x, const Segs& seg, const int64_t* idx, int k, int64_t ignore,
                          float* out, float* saved, int32_t* err, cudaStream_t st) {
-    return launch_rows(k_logprobs_fwd<T>, x.rows, st, x, seg, idx, k, ignore, out, saved, err);
+    return launch_rows(k_logprobs_fwd<T>, x.rows, threads_for(x.vocab, T::kSize), st, x, seg, idx, k, ignore, out, saved, err);
   }
 };
 
@@ -899,7 +908,7 @@ template <class T, class G>
 struct LpBwdL {
   static cudaError_t run(const View& x, const int64_t* idx, int k, int64_t ignore, const float* g,
                          const float* saved, const Grad& dx, cudaStream_t st) {
-    return launch_rows(k_logprobs_bwd<T, G>, x.rows, st, x, idx, k, ignore, g, saved, dx);
+    return launch_rows(k_logprobs_bwd<T, G>, x.rows, threads_for(x.vocab, T::kSize), st, x, idx, k, ignore, g, saved, dx);
   }
 };
 
