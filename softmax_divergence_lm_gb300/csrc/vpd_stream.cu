@@ -25,13 +25,36 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "vpd_internal.h"
+#include "vpd_packed.cuh"
 
 namespace vpd {
 namespace {
 
 constexpr int kUnroll = 4;  // 16-byte vectors per input in flight per thread
+
+// 16-bit inputs can be handed to a body as raw 16-byte vectors (Body::kRaw),
+// which it consumes with packed arithmetic instead of unpacked floats.
+template <class T>
+struct Packed {
+  using type = void;
+};
+template <>
+struct Packed<BF16> {
+  using type = InBF16;
+};
+template <>
+struct Packed<F16> {
+  using type = InF16;
+};
+template <class B, class = void>
+struct HasRaw : std::false_type {};
+template <class B>
+struct HasRaw<B, std::void_t<decltype(B::kRaw)>> : std::bool_constant<B::kRaw> {};
+template <class T, class Body>
+constexpr bool kUseRaw = T::kSize == 2 && HasRaw<Body>::value;
 
 // ---------------------------------------------------------------------------
 // Row sweeps. The range [0, n) of one row (or of a row pair with the same
@@ -63,17 +86,25 @@ __device__ __forceinline__ void visit2(const char* a, const char* b, int64_t n, 
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      float xa[V], xb[V];
-      T::unpack(ra[u], xa);
-      T::unpack(rb[u], xb);
-      body.vec(head + (i + u * nt) * V, xa, xb);
+      if constexpr (kUseRaw<T, Body>) {
+        body.template raw<typename Packed<T>::type>(head + (i + u * nt) * V, ra[u], rb[u]);
+      } else {
+        float xa[V], xb[V];
+        T::unpack(ra[u], xa);
+        T::unpack(rb[u], xb);
+        body.vec(head + (i + u * nt) * V, xa, xb);
+      }
     }
   }
   for (; i < nv; i += nt) {
-    float xa[V], xb[V];
-    T::unpack(ldg16(va + i * 16), xa);
-    T::unpack(ldg16(vb + i * 16), xb);
-    body.vec(head + i * V, xa, xb);
+    if constexpr (kUseRaw<T, Body>) {
+      body.template raw<typename Packed<T>::type>(head + i * V, ldg16(va + i * 16), ldg16(vb + i * 16));
+    } else {
+      float xa[V], xb[V];
+      T::unpack(ldg16(va + i * 16), xa);
+      T::unpack(ldg16(vb + i * 16), xb);
+      body.vec(head + i * V, xa, xb);
+    }
   }
   for (int64_t j = head + nv * V + tid; j < n; j += nt) body.one(j, T::load(a, j), T::load(b, j));
 }
@@ -95,15 +126,23 @@ __device__ __forceinline__ void visit1(const char* a, int64_t n, Body& body) {
     for (int u = 0; u < kUnroll; ++u) ra[u] = ldg16(va + (i + u * nt) * 16);
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      float xa[V];
-      T::unpack(ra[u], xa);
-      body.vec(head + (i + u * nt) * V, xa);
+      if constexpr (kUseRaw<T, Body>) {
+        body.template raw<typename Packed<T>::type>(head + (i + u * nt) * V, ra[u]);
+      } else {
+        float xa[V];
+        T::unpack(ra[u], xa);
+        body.vec(head + (i + u * nt) * V, xa);
+      }
     }
   }
   for (; i < nv; i += nt) {
-    float xa[V];
-    T::unpack(ldg16(va + i * 16), xa);
-    body.vec(head + i * V, xa);
+    if constexpr (kUseRaw<T, Body>) {
+      body.template raw<typename Packed<T>::type>(head + i * V, ldg16(va + i * 16));
+    } else {
+      float xa[V];
+      T::unpack(ldg16(va + i * 16), xa);
+      body.vec(head + i * V, xa);
+    }
   }
   for (int64_t j = head + nv * V + tid; j < n; j += nt) body.one(j, T::load(a, j));
 }
@@ -149,11 +188,52 @@ __device__ __forceinline__ RowStat finish_stat(Stat st) {
 
 __device__ __forceinline__ bool stat_ok(RowStat r) { return isfinite(r.m); }
 
+// Online statistics of one raw vector of 8 packed 16-bit values. First the
+// running max: the NaN-propagating packed max of the vector (a NaN makes z NaN
+// for good); when it grows, `grow(old_m, new_m)` rescales whatever the body
+// keeps relative to it, then m moves. Then the exponentials relative to the
+// running max with x - m exact: d[w] = (x - m) log2 e and e[w] = 2^d[w] for
+// the four packed pairs, and z += sum e. With CLAMP, -inf entries enter as the
+// finite floor (e = 0 still, d finite), for bodies that multiply e by d.
+template <class In, bool CLAMP, class Grow>
+__device__ __forceinline__ void stat_raw(Stat& st, const uint4& v, float2 (&d)[4], float2 (&e)[4], Grow&& grow) {
+  const uint32_t mx = In::max_nan(In::max_nan(v.x, v.y), In::max_nan(v.z, v.w));
+  const float2 m2 = In::unpack(mx);
+  const float vm = max_nan(m2.x, m2.y);
+  if (isnan(vm)) {
+    st.z = qnan();
+  } else if (vm > st.m) {
+    grow(st.m, vm);
+    if (st.m != neg_inf()) st.z *= exp_acc(st.m - vm);
+    st.m = vm;
+  }
+  const float2 nr2 = f2(-stat_ref(st.m)), l2e2 = f2(kLog2e);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float2 z2 = f2(0.f);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    d[i] = mul2(In::sub(CLAMP ? In::max2(w[i], In::kNegBig2) : w[i], nr2), l2e2);
+    e[i] = ex2_2(d[i]);
+    z2 = add2(z2, e[i]);
+  }
+  st.z += z2.x + z2.y;
+}
+struct NoGrow {
+  __device__ __forceinline__ void operator()(float, float) const {}
+};
+
 // ===========================================================================
 // Paired statistics (first input pass of the JSD forward).
 // ===========================================================================
 struct PairStatBody {
+  static constexpr bool kRaw = true;
   Stat s, t;
+  template <class In>
+  __device__ __forceinline__ void raw(int64_t, const uint4& a, const uint4& b) {
+    float2 d[4], e[4];
+    stat_raw<In, false>(s, a, d, e, NoGrow{});
+    stat_raw<In, false>(t, b, d, e, NoGrow{});
+  }
   template <int N>
   __device__ __forceinline__ void vec(int64_t, const float (&xs)[N], const float (&xt)[N]) {
     stat_add<N>(s, xs);
@@ -395,7 +475,34 @@ __device__ __forceinline__ KlAcc kl_merge(const KlAcc& x, const KlAcc& y) {
 }
 
 struct KlBody {
+  static constexpr bool kRaw = true;
   KlAcc acc;
+  // w is kept relative to both maxima (see kl_w_at); the target a weights it.
+  template <class In>
+  __device__ __forceinline__ void raw(int64_t, const uint4& va, const uint4& vb) {
+    float2 da[4], ea[4], db[4], eb[4];
+    stat_raw<In, true>(acc.b, vb, db, eb, [&](float old_m, float new_m) {
+      if (old_m != neg_inf()) acc.w += (new_m - old_m) * acc.a.z;
+    });
+    stat_raw<In, true>(acc.a, va, da, ea, [&](float old_m, float new_m) {
+      if (old_m != neg_inf()) {
+        const float dd = new_m - old_m, f = exp_acc(-dd);
+        acc.w = f * (acc.w - dd * acc.a.z);
+      }
+    });
+    // sum over the pairs of e_a (d_a - d_b), in log2 units; a masked target
+    // gives e_a = 0, a target with a masked other side is a support violation
+    const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+    float2 w2 = f2(0.f);
+    uint32_t viol = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w2 = fma2(ea[i], add2(da[i], neg(db[i])), w2);
+      viol |= __vcmpeq2(wb[i], In::kNegInf2) & ~__vcmpeq2(wa[i], In::kNegInf2);
+    }
+    acc.w += kLn2 * (w2.x + w2.y);
+    acc.viol |= viol != 0;
+  }
   template <int N>
   __device__ __forceinline__ void vec(int64_t, const float (&xa)[N], const float (&xb)[N]) {
     float mxa = xa[0], mxb = xb[0];
@@ -540,7 +647,22 @@ __device__ __forceinline__ EntAcc ent_merge(const EntAcc& x, const EntAcc& y) {
 }
 
 struct EntBody {
+  static constexpr bool kRaw = true;
   EntAcc acc;
+  template <class In>
+  __device__ __forceinline__ void raw(int64_t, const uint4& v) {
+    float2 d[4], e[4];
+    stat_raw<In, true>(acc.s, v, d, e, [&](float old_m, float new_m) {
+      if (old_m != neg_inf()) {
+        const float dd = new_m - old_m, f = exp_acc(-dd);
+        acc.y = f * (acc.y - dd * acc.s.z);
+      }
+    });
+    float2 y2 = f2(0.f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) y2 = fma2(e[i], d[i], y2);  // masked: e = 0, d finite
+    acc.y += kLn2 * (y2.x + y2.y);
+  }
   template <int N>
   __device__ __forceinline__ void vec(int64_t, const float (&x)[N]) {
     float mx = x[0];
@@ -661,7 +783,13 @@ __global__ void __launch_bounds__(kThreads) k_entropy_bwd(View x, const float* g
 // Selected / top-k log-probabilities.
 // ===========================================================================
 struct StatBody {
+  static constexpr bool kRaw = true;
   Stat s;
+  template <class In>
+  __device__ __forceinline__ void raw(int64_t, const uint4& a) {
+    float2 d[4], e[4];
+    stat_raw<In, false>(s, a, d, e, NoGrow{});
+  }
   template <int N>
   __device__ __forceinline__ void vec(int64_t, const float (&x)[N]) {
     stat_add<N>(s, x);
