@@ -173,10 +173,10 @@ vpd_status vpd_jsd_fwdbwd(const vpd_view *s, const vpd_view *t, double beta,
 /* ---------------------------------------------------------------------------
  * Forward / reverse KL ([ops page], "What"): reverse = 0 gives KL(P_t || P_s)
  * (the teacher is the target), reverse = 1 gives KL(P_s || P_t). The forward
- * reads the inputs once: the single-read cluster kernel's KL branch when its
- * conditions hold (see vpd_jsd_fwdbwd), else one online pass (running maxima
- * with rescaled sums). saved may be NULL. Saved layout and backward are those
- * of the JSD beta = 0 / 1 branches.
+ * reads the inputs once: one online pass (running maxima with rescaled sums),
+ * or for short rows (V <= 32768) under the conditions of vpd_jsd_fwdbwd the
+ * single-read cluster kernel's KL branch. saved may be NULL. Saved layout and
+ * backward are those of the JSD beta = 0 / 1 branches.
  * ------------------------------------------------------------------------- */
 vpd_status vpd_kl_fwd(const vpd_view *s, const vpd_view *t, int32_t reverse,
                       const vpd_segments *seg, float *loss, float *saved, void *stream);
