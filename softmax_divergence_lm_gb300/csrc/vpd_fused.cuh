@@ -700,7 +700,6 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
       float2 acc_a = f2(0.f), acc_b = f2(0.f);
       uint32_t viol = 0;
       if (row_ok) {
-        const bool keep = a.ds.data || a.dt.data;  // gradients wanted: pass D follows
         const unsigned char* ps = stage_ptr(cst) + tid * 16;
         const size_t tofs = static_cast<size_t>(W) * 2;
         // One vector: PARTIAL marks the warp that straddles the slice end,
@@ -742,11 +741,9 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
               t1[w] = d;
             }
           }
-          if (keep) {  // warp-uniform: pass D reads these
-            tmem_st8(tmem + k * kCols, t0);
-            tmem_st8(tmem + k * kCols + 8, t1);
-            if (MODE == kInterior) tmem_st8(tmem + k * kCols + 16, t2);
-          }
+          tmem_st8(tmem + k * kCols, t0);
+          tmem_st8(tmem + k * kCols + 8, t1);
+          if (MODE == kInterior) tmem_st8(tmem + k * kCols + 16, t2);
         };
 #pragma unroll
         for (int k = 0; k < R; ++k) {
