@@ -172,7 +172,7 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-FUSED_SOURCES = ("vpd_fused.cuh", "vpd_fused_bf16.cu", "vpd_fused_f16.cu", "vpd_fused.cu", "vpd_device.cuh")
+FUSED_SOURCES = ("vpd_fused.cuh", "vpd_fused_bf16.cu", "vpd_fused_f16.cu", "vpd_fused.cu", "vpd_device.cuh", "vpd_packed.cuh")
 
 
 def fused_source_hash() -> str:
