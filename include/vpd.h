@@ -159,7 +159,7 @@ vpd_status vpd_jsd_bwd(const vpd_view *s, const vpd_view *t, double beta, const 
  * The single-read path runs when the inputs are bf16 or fp16, V is a multiple
  * of 8, every row of the inputs and gradients starts on a 16-byte boundary,
  * the gradients are float32 or the input dtype, there is one segment, and the
- * row fits on a thread-block cluster (V <= 307200). There a cluster of up to
+ * row fits on a thread-block cluster (V <= 311296). There a cluster of up to
  * 16 CTAs holds each row pair on chip and statistics, divergence and
  * gradients come from one HBM read; a bf16 row whose finite max exceeds 2^126
  * is treated as out of contract (NaN, zero gradient). Otherwise the call runs

@@ -176,3 +176,72 @@ def test_fused_one_hot_against_broad_fp32_floor(B):
         assert np.all(err <= 1e-6 + 1e-4 * np.abs(ref) + floor), f"beta={beta}: max excess {np.max(err - 1e-6 - 1e-4*np.abs(ref) - floor):.3e}"
         other = to64(dt) if beta == 1.0 else to64(ds)
         assert_grad(other, rdt if beta == 1.0 else rds, f"one-hot beta={beta} other gradient")
+
+
+def launches_of(B, fn):
+    c0 = B.vpd_launch_count()
+    fn()
+    torch.cuda.synchronize()
+    B.vpd_device_status()
+    return B.vpd_launch_count() - c0
+
+
+@pytest.mark.parametrize("v", [8, 16, 24])
+def test_fused_tiny_vocabularies(B, v):
+    """A slice of one vector per CTA, most lanes of the single worker warp
+    past the slice end."""
+    g = torch.Generator(device="cpu").manual_seed(v)
+    s = (torch.randn(40, v, generator=g) * 3).to(torch.bfloat16).cuda()
+    t = (torch.randn(40, v, generator=g) * 3).to(torch.bfloat16).cuda()
+    for beta in (0.5, 0.0, 1.0):
+        check(B, s, t, beta, torch.bfloat16, label=f"V={v}")
+
+
+def test_fused_size_limit(B):
+    """The widest row the single-read kernel takes (16 CTAs x 19 warps x 32
+    threads x 4 vectors x 8 = 311296 columns) runs as one launch; one vector
+    more falls back to the two streaming passes and the backward."""
+    for v, fused in ((311296, True), (311304, False)):
+        g = torch.Generator(device="cpu").manual_seed(v % 1000)
+        s0 = torch.randn(6, v, generator=g) * 4
+        s = s0.to(torch.bfloat16).cuda()
+        t = (s0 + torch.randn(6, v, generator=g) * 2).to(torch.bfloat16).cuda()
+        n = s.shape[0]
+        gr = torch.rand(n, device="cuda")
+        loss = torch.empty(n, device="cuda")
+        saved = torch.empty(n, 6, device="cuda")
+        ds = torch.empty(n, v, dtype=torch.bfloat16, device="cuda")
+        dt = torch.empty_like(ds)
+        k = launches_of(B, lambda: B.vpd_jsd_fwdbwd(s, t, 0.5, None, gr, loss, saved, ds, dt))
+        assert (k == 1) == fused, f"V={v}: {k} launches"
+        rl, _, _, rds, rdt = O.jsd(to64(s), to64(t), 0.5, to64(gr), threads=8)
+        assert_loss(to64(loss), rl, f"V={v} loss")
+        assert_grad(to64(ds), rds, f"V={v} dS", torch.bfloat16)
+        assert_grad(to64(dt), rdt, f"V={v} dT", torch.bfloat16)
+
+
+@pytest.mark.parametrize("v", [16032, 151936])
+def test_forward_calls_through_single_read(B, v):
+    """vpd_jsd_fwd takes the single-read kernel (one launch) and matches the
+    oracle's loss and saved statistics; vpd_kl_fwd matches the oracle's KL
+    on either of its paths."""
+    s, t = make_rows(12, v, torch.bfloat16, seed=v % 89)
+    n = s.shape[0]
+    loss = torch.empty(n, device="cuda")
+    saved = torch.empty(n, 6, device="cuda")
+    k = launches_of(B, lambda: B.vpd_jsd_fwd(s, t, 0.5, None, loss, saved))
+    assert k == 1, f"V={v}: the JSD forward took {k} launches"
+    rl, _, _, _, _ = O.jsd(to64(s), to64(t), 0.5, None, grad=False, threads=8)
+    assert_loss(to64(loss), rl, f"V={v} forward loss")
+    sv = to64(saved)
+    for col, x in ((0, s), (2, t)):
+        m, lse, code = O.row_stats(to64(x))
+        ok = code == 0
+        assert np.array_equal(sv[ok, col], m[ok])
+        assert np.allclose(sv[ok, col + 1], lse[ok], rtol=1e-5, atol=5e-6)
+    for rev in (0, 1):
+        kl = torch.empty(n, device="cuda")
+        B.vpd_kl_fwd(s, t, rev, None, kl, None)
+        torch.cuda.synchronize()
+        rk, _, _, _, _ = O.jsd(to64(s), to64(t), float(rev), None, grad=False, threads=8)
+        assert_loss(to64(kl), rk, f"V={v} KL reverse={rev}")
