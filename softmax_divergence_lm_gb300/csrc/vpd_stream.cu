@@ -299,15 +299,58 @@ __device__ __forceinline__ void mix_terms(float lp, float lq, const Mix& c, floa
 
 enum Mode : int { kInterior = 0, kForwardKL = 1, kReverseKL = 2 };
 
+// Raw 16-bit vectors of a row pair with known statistics, in log2 units:
+// log2 p = (s - m_s) log2 e - L_s log2 e (x - m exact), p = 2^log2 p, and the
+// same for q. -inf logits enter as the finite floor, so their p or q is 0 and
+// every product with a log-ratio stays finite.
+constexpr float kTinyMix = 1e-37f;  // keeps M > 0 so log2 M stays finite
+template <class In>
+__device__ __forceinline__ void pair_log2(uint32_t ws, uint32_t wt, float2 nms2, float2 nmt2, float2 nKs2,
+                                          float2 nKt2, float2& lp, float2& lq, float2& p, float2& q) {
+  const float2 l2e2 = f2(kLog2e);
+  lp = fma2(In::sub(In::max2(ws, In::kNegBig2), nms2), l2e2, nKs2);
+  lq = fma2(In::sub(In::max2(wt, In::kNegBig2), nmt2), l2e2, nKt2);
+  p = ex2_2(lp);
+  q = ex2_2(lq);
+}
+
 // ===========================================================================
 // Divergence pass (second input pass of the JSD forward).
 // ===========================================================================
 template <int MODE>
 struct DivBody {
+  static constexpr bool kRaw = true;
   float ms, Ls, mt, Lt;
   Mix mix;
   float A, B;  // interior: the two KL-to-mixture sums; endpoints: A holds the KL sum
   int viol;    // endpoints: the target has a finite logit where the other is -inf
+
+  template <class In>
+  __device__ __forceinline__ void raw(int64_t, const uint4& a, const uint4& b) {
+    const float2 nms2 = f2(-ms), nmt2 = f2(-mt), nKs2 = f2(-Ls * kLog2e), nKt2 = f2(-Lt * kLog2e);
+    const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+    float2 acc_a = f2(0.f), acc_b = f2(0.f);
+    uint32_t v = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 lp, lq, p, q;
+      pair_log2<In>(wa[i], wb[i], nms2, nmt2, nKs2, nKt2, lp, lq, p, q);
+      if (MODE == kInterior) {
+        const float2 lm = lg2_2(fma2(f2(mix.ws), p, fma2(f2(mix.wt), q, f2(kTinyMix))));
+        acc_a = fma2(q, add2(lq, neg(lm)), acc_a);
+        acc_b = fma2(p, add2(lp, neg(lm)), acc_b);
+      } else if (MODE == kForwardKL) {  // KL(q || p)
+        acc_a = fma2(q, add2(lq, neg(lp)), acc_a);
+        v |= __vcmpeq2(wa[i], In::kNegInf2) & ~__vcmpeq2(wb[i], In::kNegInf2);
+      } else {  // KL(p || q)
+        acc_a = fma2(p, add2(lp, neg(lq)), acc_a);
+        v |= __vcmpeq2(wb[i], In::kNegInf2) & ~__vcmpeq2(wa[i], In::kNegInf2);
+      }
+    }
+    A += kLn2 * (acc_a.x + acc_a.y);
+    if (MODE == kInterior) B += kLn2 * (acc_b.x + acc_b.y);
+    viol |= v != 0;
+  }
 
   __device__ __forceinline__ void one(int64_t, float s, float t) {
     const bool fs = s != neg_inf(), ft = t != neg_inf();
@@ -382,6 +425,7 @@ struct BwdBody {
   float cs, ct;    // g (1 - beta), g beta (interior); g (endpoints)
   char* ds;
   char* dt;
+
 
   __device__ __forceinline__ void grads(float s, float t, float& gs, float& gt) const {
     const bool fs = s != neg_inf(), ft = t != neg_inf();
