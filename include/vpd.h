@@ -128,10 +128,10 @@ typedef struct {
  * ------------------------------------------------------------------------- */
 
 /* Forward. The statistics must be global before the divergence ([JSD page],
- * "Scope and limitations"): when the single-read conditions of vpd_jsd_fwdbwd
- * hold (one segment, 16-bit inputs, aligned rows), one cluster kernel reads each
- * row pair once and keeps it on chip for both steps; otherwise the pages' design
- * in two input passes: a paired-statistics kernel merges per-segment (max,
+ * "Scope and limitations"): for short rows (V <= 32768) under the single-read
+ * conditions of vpd_jsd_fwdbwd (one segment, 16-bit inputs, aligned rows), one
+ * cluster kernel reads each row pair once and keeps it on chip for both steps;
+ * otherwise the pages' design in two input passes: a paired-statistics kernel merges per-segment (max,
  * sum-exp) of both inputs, then a divergence kernel reduces the two
  * KL-to-mixture expectations together ([JSD page], "Changes").
  * loss:  device float[N], the per-token divergence.

@@ -150,15 +150,14 @@ vpd_status check_grads_pair(const vpd_grad* ds, const vpd_grad* dt, const vpd::V
 
 extern "C" {
 
-// Forward-only calls take the single-read kernel only in clusters of at most
-// this many CTAs: on this GPU larger clusters leave a quarter of the SMs idle
-// (16-CTA clusters cover 112 of 152), and without a backward the streaming
-// kernels on every SM are faster there.
+// Forward-only calls (JSD and KL) take the single-read kernel only for rows up
+// to this vocabulary, in clusters of at most kForwardMaxCluster CTAs: without a
+// backward, its per-row cluster exchanges are exposed, and on this GPU the
+// streaming kernels on every SM are faster for longer rows (V = 151936, 8191
+// rows: JSD 1.69 ms two-pass against 1.88 single-read, KL 1.36 against 1.75;
+// V = 16032: JSD 0.19 against 0.21, KL 0.18 against 0.19).
+constexpr int64_t kForwardFusedMaxVocab = 32768;
 constexpr int kForwardMaxCluster = 10;
-// The KL forward takes the single-read kernel only up to this vocabulary: on
-// this GPU the online single-pass kernel is faster for longer rows (V = 151936:
-// 1.35 against 1.75 ms for 8191 rows; V = 16032: 0.19 against 0.18 ms).
-constexpr int64_t kKlFusedMaxVocab = 32768;
 
 vpd_status vpd_jsd_fwd(const vpd_view* s, const vpd_view* t, double beta, const vpd_segments* seg,
                        float* loss, float* saved, void* stream) {
@@ -170,10 +169,9 @@ vpd_status vpd_jsd_fwd(const vpd_view* s, const vpd_view* t, double beta, const 
   if (vs.rows == 0) return ok();
   if (!loss || !saved) return fail(VPD_ERR_ARG, "vpd_jsd_fwd: loss and saved are required");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // One read of the inputs when the single-read kernel takes the shape (no
-  // gradients wanted) in clusters that still cover most SMs; otherwise the two
-  // streaming passes, which use every SM.
-  if (sg.count == 1) {
+  // Short rows: one read of the inputs by the single-read kernel (no gradients
+  // wanted); longer rows: the two streaming passes on every SM.
+  if (sg.count == 1 && vs.vocab <= kForwardFusedMaxVocab) {
     const vpd::Grad none{nullptr, 0, 0};
     cudaError_t e = vpd::launch_jsd_fused(vs, vt, beta, nullptr, loss, saved, none, none, st, -1,
                                           kForwardMaxCluster);
@@ -241,7 +239,7 @@ vpd_status vpd_kl_fwd(const vpd_view* s, const vpd_view* t, int32_t reverse,
   if (!loss) return fail(VPD_ERR_ARG, "vpd_kl_fwd: loss is required");
   // Short rows: the KL branch of the single-read kernel (beta = 0 / 1); longer
   // rows: the online single-pass kernel on every SM, which is faster there.
-  if (sg.count == 1 && vs.vocab <= kKlFusedMaxVocab) {
+  if (sg.count == 1 && vs.vocab <= kForwardFusedMaxVocab) {
     const vpd::Grad none{nullptr, 0, 0};
     cudaError_t e = vpd::launch_jsd_fused(vs, vt, reverse ? 1.0 : 0.0, nullptr, loss, saved, none, none,
                                           static_cast<cudaStream_t>(stream), -1, kForwardMaxCluster);

@@ -222,15 +222,17 @@ def test_fused_size_limit(B):
 
 @pytest.mark.parametrize("v", [16032, 151936])
 def test_forward_calls_through_single_read(B, v):
-    """vpd_jsd_fwd takes the single-read kernel (one launch) and matches the
-    oracle's loss and saved statistics; vpd_kl_fwd matches the oracle's KL
-    on either of its paths."""
+    """vpd_jsd_fwd takes the single-read kernel (one launch) for rows up to
+    V = 32768 and the two streaming passes (two launches) above, and matches
+    the oracle's loss and saved statistics either way; vpd_kl_fwd matches the
+    oracle's KL on either of its paths."""
     s, t = make_rows(12, v, torch.bfloat16, seed=v % 89)
     n = s.shape[0]
     loss = torch.empty(n, device="cuda")
     saved = torch.empty(n, 6, device="cuda")
     k = launches_of(B, lambda: B.vpd_jsd_fwd(s, t, 0.5, None, loss, saved))
-    assert k == 1, f"V={v}: the JSD forward took {k} launches"
+    want = 1 if v <= 32768 else 2
+    assert k == want, f"V={v}: the JSD forward took {k} launches, not {want}"
     rl, _, _, _, _ = O.jsd(to64(s), to64(t), 0.5, None, grad=False, threads=8)
     assert_loss(to64(loss), rl, f"V={v} forward loss")
     sv = to64(saved)
