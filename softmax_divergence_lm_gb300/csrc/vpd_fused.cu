@@ -81,8 +81,23 @@ size_t max_smem_optin() {
 // of work on an SM (about 1.5 us of hand-overs against about 4 ns a vector).
 constexpr int64_t kRowOverheadVectors = 400;
 
+// Per-row work of a CTA in vectors, as its busiest warp scheduler sets it:
+// each per-row phase ends when the sub-partition (warp % 4) with the most
+// warp-wide vectors has issued them, so the cost is 4 x 32 x that count.
+int64_t sched_vectors(int64_t nvec, int R, int nw) {
+  int64_t load[4] = {0, 0, 0, 0};
+  for (int w = 0; w < nw; ++w) {
+    const int64_t j = fused::vector_order(w, nw, R);
+    for (int k = 0; k < R; ++k)
+      if (static_cast<int64_t>(k) * 32 * nw + 32 * j < nvec) ++load[w & 3];
+  }
+  int64_t m = 0;
+  for (int s = 0; s < 4; ++s) m = load[s] > m ? load[s] : m;
+  return 128 * m;
+}
+
 // The launch shape: the cluster size C with the least time per row batch,
-// rows per cluster x (slice vectors + exchange overhead), among those whose
+// rows per cluster x (slice work + exchange overhead), among those whose
 // slice fits (two stages in shared memory; at most kMaxR vectors per worker
 // thread within the register and TMEM budgets); then the smallest R that
 // covers the slice and as many workers as the budgets allow without idle
@@ -109,7 +124,7 @@ bool choose(int64_t vocab, int64_t rows, int max_cluster, Config* cfg) {
     const int clusters = clusters_for(C);
     if (clusters < 1) continue;
     const int64_t used = rows < clusters ? rows : clusters;
-    const int64_t cost = (rows + used - 1) / used * (nvec + kRowOverheadVectors);
+    const int64_t cost = (rows + used - 1) / used * (sched_vectors(nvec, bR, bnw) + kRowOverheadVectors);
     if (!best || cost < best) {
       best = cost;
       *cfg = Config{C, bR, static_cast<int>(W), bnw, smem};

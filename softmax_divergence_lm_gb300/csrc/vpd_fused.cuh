@@ -396,28 +396,64 @@ __device__ __forceinline__ void control_push_stats(const float (*part)[4], int n
            map_rank(smem_addr(&tail->stat_bar[par]), lane));
 }
 
-// Which of its R vectors (k Tw + tid, k = 0..R-1) a worker thread holds: the
-// first `kv`; every lane of its warp holds the first `kfull`, some lane the
-// first `kwarp` (both warp-uniform).
+// Which of its R vectors (k Tw + vt, k = 0..R-1, vt the thread's place in the
+// vector order) a worker thread holds: the first `kv`; every lane of its warp
+// holds the first `kfull`, some lane the first `kwarp` (both warp-uniform).
 struct Span {
   int kv, kfull, kwarp;
 };
 template <int R>
-__device__ __forceinline__ Span span_of(int len, int Tw) {
-  const int nv = len >> 3, tid = threadIdx.x, w0 = tid & ~31;
+__device__ __forceinline__ Span span_of(int len, int Tw, int vt) {
+  const int nv = len >> 3, w0 = vt & ~31;
   auto kv_of = [&](int t) {
     const int k = (nv - t + Tw - 1) / Tw;
     return k < 0 ? 0 : (k > R ? R : k);
   };
-  return {kv_of(tid), kv_of(w0 + 31), kv_of(w0)};
+  return {kv_of(vt), kv_of(w0 + 31), kv_of(w0)};
+}
+
+// The position of worker warp `warp` in the order in which the workers take
+// the slice's vectors (vector k Tw + 32 j + lane goes to lane `lane` of the
+// j-th warp). A warp scheduler (SM sub-partition, warp % 4) issues only for
+// its own warps, and every per-row phase ends with its busiest scheduler, so
+// the last, partial round of R vectors goes first to the schedulers with the
+// least work: each next warp comes from the scheduler with the fewest vectors
+// so far, ties away from the control warp's.
+__host__ __device__ __forceinline__ int vector_order(int warp, int nw, int R) {
+  int load[4], next[4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    load[s] = (nw - s + 3) / 4 * (R - 1);
+    next[s] = s;
+  }
+  const int ctrl = nw & 3;
+  for (int j = 0; j < nw; ++j) {
+    int b = -1, lb = 0;
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+      if (next[s] < nw && (b < 0 || load[s] < lb || (load[s] == lb && b == ctrl))) {
+        b = s;
+        lb = load[s];
+      }
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {  // constant indices keep the arrays in registers
+      if (s != b) continue;
+      if (next[s] == warp) return j;
+      next[s] += 4;
+      ++load[s];
+    }
+  }
+  return warp;
 }
 
 // Worker warps: statistics partial of one row read from its shared-memory
-// stage; lane 0 writes the warp's (m_s, z_s, m_t, z_t) to `part`.
+// stage (`vt`: this thread's place in the vector order); lane 0 writes the
+// warp's (m_s, z_s, m_t, z_t) to `part`.
 template <class In, int R>
-__device__ __forceinline__ void worker_stats(const unsigned char* sb, int W, const Span& sp, int Tw, float* part) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  const unsigned char* ps = sb + tid * 16;
+__device__ __forceinline__ void worker_stats(const unsigned char* sb, int W, const Span& sp, int Tw, int vt,
+                                             float* part) {
+  const int lane = threadIdx.x & 31;
+  const unsigned char* ps = sb + vt * 16;
   const size_t tofs = static_cast<size_t>(W) * 2;
   uint32_t mxs = In::kNegInf2, mxt = In::kNegInf2;
 #pragma unroll
@@ -498,7 +534,8 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
   // The failure-path test hook: this CTA withholds the copy of one row, so
   // its workers' bounded wait on that stage expires.
   auto withheld = [&](int64_t r) { return r == a.withhold_row && crank == 0; };
-  uint32_t issued[kStages] = {0, 0};  // control warp: copies issued per stage
+  // control warp, bit st: copies were issued into stage st / their count is odd
+  uint32_t issued_any = 0, issued_odd = 0;
   auto issue = [&](int64_t r, int st) {  // control warp: both inputs' slices of row r into stage st
     if (!bytes || withheld(r)) return;
     if (lane == 0) {
@@ -507,7 +544,8 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
       bulk_load(dst, a.s + (a.ms.offset(r) + col0) * 2, bytes, &tail->tma_bar[st]);
       bulk_load(dst + static_cast<size_t>(W) * 2, a.t + (a.mt.offset(r) + col0) * 2, bytes, &tail->tma_bar[st]);
     }
-    ++issued[st];
+    issued_any |= 1u << st;
+    issued_odd ^= 1u << st;
   };
 
   // Control warp: bulk stores of the staged gradients of row r.
@@ -649,7 +687,7 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
     // Copies still in flight (only after a wait gave up) must land before exit.
     if (lane == 0)
       for (int st = 0; st < kStages; ++st)
-        if (issued[st]) mbar_wait(&tail->tma_bar[st], (issued[st] - 1) & 1u);
+        if ((issued_any >> st) & 1u) mbar_wait(&tail->tma_bar[st], ((issued_odd >> st) & 1u) ^ 1u);
     if (!ok && lane == 0) atomicExch(&g_fused_error, 1);
   } else {
     // ------------------------------------------------------------------
@@ -658,19 +696,20 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
     // This thread's TMEM lane (its warp's lane quarter) and column range.
     const uint32_t tmem = tail->tmem_base + (static_cast<uint32_t>(32 * (warp & 3)) << 16) +
                           static_cast<uint32_t>(tmem_cols_per_warp(nw) * (warp >> 2));
-    uint32_t tma_done[kStages] = {0, 0};  // completed waits per stage
+    uint32_t tma_parity = 0;  // bit st: parity of the next wait on stage st
     auto wait_stage = [&](int st) {
       if (!bytes) return;
-      if (!mbar_wait(&tail->tma_bar[st], tma_done[st] & 1u)) tail->fail = 1;
-      ++tma_done[st];
+      if (!mbar_wait(&tail->tma_bar[st], (tma_parity >> st) & 1u)) tail->fail = 1;
+      tma_parity ^= 1u << st;
     };
     const float2 ws2 = f2(1.f - beta), wt2 = f2(beta), tiny2 = f2(kTiny), l2e2 = f2(kLog2e);
     const int64_t gstride = static_cast<int64_t>(Tw) * 8 * Out<G>::kSize;  // bytes between vectors k, k + 1
-    const Span sp = span_of<R>(len, Tw);
+    const int vt = 32 * vector_order(warp, nw, R) + lane;  // this thread's place in the vector order
+    const Span sp = span_of<R>(len, Tw, vt);
 
     if (q < a.rows) {
       wait_stage(0);
-      worker_stats<In, R>(stage_ptr(0), W, sp, Tw, tail->stat_part[0][warp]);
+      worker_stats<In, R>(stage_ptr(0), W, sp, Tw, vt, tail->stat_part[0][warp]);
       bar_arrive(kBarStatPart, nthreads);
     }
     int64_t i = 0;
@@ -700,7 +739,7 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
       float2 acc_a = f2(0.f), acc_b = f2(0.f);
       uint32_t viol = 0;
       if (row_ok) {
-        const unsigned char* ps = stage_ptr(cst) + tid * 16;
+        const unsigned char* ps = stage_ptr(cst) + vt * 16;
         const size_t tofs = static_cast<size_t>(W) * 2;
         // One vector: PARTIAL marks the warp that straddles the slice end,
         // whose lanes past it compute on the floor value.
@@ -764,7 +803,7 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
       // while this row's sums travel
       if (has_next) {
         wait_stage(nst);
-        worker_stats<In, R>(stage_ptr(nst), W, sp, Tw, tail->stat_part[par ^ 1][warp]);
+        worker_stats<In, R>(stage_ptr(nst), W, sp, Tw, vt, tail->stat_part[par ^ 1][warp]);
         bar_arrive(kBarStatPart, nthreads);
       }
 
@@ -774,8 +813,8 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
       const float A = ab.x, B = ab.y, value = ab.z;
 
       // (W5) pass D of row r: gradients, e.g. dS = p (g (1-beta) ln2 (log2 p - log2 M) - g (1-beta) B)
-      char* ds_row = a.ds.data ? a.ds.data + (r * a.ds.row_stride + col0 + tid * 8) * Out<G>::kSize : nullptr;
-      char* dt_row = a.dt.data ? a.dt.data + (r * a.dt.row_stride + col0 + tid * 8) * Out<G>::kSize : nullptr;
+      char* ds_row = a.ds.data ? a.ds.data + (r * a.ds.row_stride + col0 + vt * 8) * Out<G>::kSize : nullptr;
+      char* dt_row = a.dt.data ? a.dt.data + (r * a.dt.row_stride + col0 + vt * 8) * Out<G>::kSize : nullptr;
       if (ds_row || dt_row) {
         const bool live = row_ok && isfinite(value);
         const float cs = MODE == kInterior ? gr * (1.f - beta) : gr;
@@ -808,7 +847,7 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
           }
           if (k < sp.kv) {
             if constexpr (STAGED) {
-              unsigned char* pg = gbuf + (k * Tw + tid) * 16;
+              unsigned char* pg = gbuf + (k * Tw + vt) * 16;
               if (ds_row) Out<G>::store8_shared(pg, gs);
               if (dt_row) Out<G>::store8_shared(pg + static_cast<size_t>(W) * 2, gt);
             } else {
@@ -823,7 +862,7 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
           float2 z[4] = {f2(0.f), f2(0.f), f2(0.f), f2(0.f)};
           if (k < sp.kv) {
             if constexpr (STAGED) {
-              unsigned char* pg = gbuf + (k * Tw + tid) * 16;
+              unsigned char* pg = gbuf + (k * Tw + vt) * 16;
               if (ds_row) Out<G>::store8_shared(pg, z);
               if (dt_row) Out<G>::store8_shared(pg + static_cast<size_t>(W) * 2, z);
             } else {
