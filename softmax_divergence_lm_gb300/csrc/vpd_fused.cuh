@@ -280,6 +280,16 @@ __device__ __forceinline__ float warp_sum(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
+// Warp sums of a and of b in one butterfly: the half-warps first swap the
+// other value, then each reduces its own; lanes 0-15 return the sum of a,
+// lanes 16-31 that of b.
+__device__ __forceinline__ float warp_sum_pair(float a, float b) {
+  const bool hi = (threadIdx.x & 16) != 0;
+  float v = (hi ? b : a) + __shfl_xor_sync(0xffffffffu, hi ? a : b, 16);
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
 
 // Gradient formats for 8 values (one 16-byte input vector).
 template <class G>
@@ -481,10 +491,11 @@ __device__ __forceinline__ void worker_stats(const unsigned char* sb, int W, con
       }
     }
   }
-  float z_s = warp_sum(zs2.x + zs2.y), z_t = warp_sum(zt2.x + zt2.y);
-  if (!(m_s <= kMaxLogit)) z_s = qnan();  // NaN, +inf or a max above 2^126
-  if (!(m_t <= kMaxLogit)) z_t = qnan();
-  if (lane == 0) *reinterpret_cast<float4*>(part) = make_float4(m_s, z_s, m_t, z_t);
+  // z_s on lanes 0-15, z_t on lanes 16-31
+  float z = warp_sum_pair(zs2.x + zs2.y, zt2.x + zt2.y);
+  const float m = lane < 16 ? m_s : m_t;
+  if (!(m <= kMaxLogit)) z = qnan();  // NaN, +inf or a max above 2^126
+  if ((lane & 15) == 0) *reinterpret_cast<float2*>(part + (lane >> 3)) = make_float2(m, z);
 }
 
 struct FusedArgs {
@@ -791,11 +802,13 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
         }
         tmem_wait_st();
       }
-      {
+      if constexpr (MODE == kInterior) {  // A partial on lanes 0-15, B partial on lanes 16-31
+        const float v = kLn2 * warp_sum_pair(acc_a.x + acc_a.y, acc_b.x + acc_b.y);
+        if ((lane & 15) == 0) tail->sum_part[par][warp][lane >> 4] = v;
+      } else {
         float sa = kLn2 * warp_sum(acc_a.x + acc_a.y);
-        if (MODE != kInterior && __any_sync(0xffffffffu, viol != 0)) sa = pos_inf();
-        const float sb = kLn2 * warp_sum(acc_b.x + acc_b.y);
-        if (lane == 0) *reinterpret_cast<float2*>(tail->sum_part[par][warp]) = make_float2(sa, sb);
+        if (__any_sync(0xffffffffu, viol != 0)) sa = pos_inf();
+        if (lane == 0) *reinterpret_cast<float2*>(tail->sum_part[par][warp]) = make_float2(sa, 0.f);
       }
       bar_arrive(kBarSumPart, nthreads);
 
