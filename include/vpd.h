@@ -128,10 +128,12 @@ typedef struct {
  * ------------------------------------------------------------------------- */
 
 /* Forward. The statistics must be global before the divergence ([JSD page],
- * "Scope and limitations"): for short rows (V <= 32768) under the single-read
- * conditions of vpd_jsd_fwdbwd (one segment, 16-bit inputs, aligned rows), one
- * cluster kernel reads each row pair once and keeps it on chip for both steps;
- * otherwise the pages' design in two input passes: a paired-statistics kernel merges per-segment (max,
+ * "Scope and limitations"): under the single-read conditions of vpd_jsd_fwdbwd
+ * (one segment, 16-bit inputs, aligned rows), when the row fits in clusters of
+ * at most 10 CTAs (V <= 191040 with 227 KB of shared memory per CTA), a
+ * forward-only cluster kernel reads each row pair once and keeps it on chip
+ * for both steps; otherwise the pages' design in two input passes: a
+ * paired-statistics kernel merges per-segment (max,
  * sum-exp) of both inputs, then a divergence kernel reduces the two
  * KL-to-mixture expectations together ([JSD page], "Changes").
  * loss:  device float[N], the per-token divergence.
@@ -163,8 +165,9 @@ vpd_status vpd_jsd_bwd(const vpd_view *s, const vpd_view *t, double beta, const 
  * 16 CTAs holds each row pair on chip and statistics, divergence and
  * gradients come from one HBM read; a bf16 row whose finite max exceeds 2^126
  * is treated as out of contract (NaN, zero gradient). Otherwise the call runs
- * the two forward kernels and the backward kernel in turn. Outputs as
- * vpd_jsd_fwd (loss, and saved, which is required) plus the gradients as
+ * the two forward kernels and the backward kernel in turn. With both
+ * gradients absent the single-read path is the forward-only kernel. Outputs
+ * as vpd_jsd_fwd (loss, and saved, which is required) plus the gradients as
  * vpd_jsd_bwd. */
 vpd_status vpd_jsd_fwdbwd(const vpd_view *s, const vpd_view *t, double beta,
                           const vpd_segments *seg, const float *grad_loss, float *loss,
@@ -175,7 +178,7 @@ vpd_status vpd_jsd_fwdbwd(const vpd_view *s, const vpd_view *t, double beta,
  * (the teacher is the target), reverse = 1 gives KL(P_s || P_t). The forward
  * reads the inputs once: one online pass (running maxima with rescaled sums),
  * or for short rows (V <= 32768) under the conditions of vpd_jsd_fwdbwd the
- * single-read cluster kernel's KL branch. saved may be NULL. Saved layout and
+ * forward-only cluster kernel's KL branch. saved may be NULL. Saved layout and
  * backward are those of the JSD beta = 0 / 1 branches.
  * ------------------------------------------------------------------------- */
 vpd_status vpd_kl_fwd(const vpd_view *s, const vpd_view *t, int32_t reverse,

@@ -150,14 +150,16 @@ vpd_status check_grads_pair(const vpd_grad* ds, const vpd_grad* dt, const vpd::V
 
 extern "C" {
 
-// Forward-only calls (JSD and KL) take the single-read kernel only for rows up
-// to this vocabulary, in clusters of at most kForwardMaxCluster CTAs: without a
-// backward, its per-row cluster exchanges are exposed, and on this GPU the
-// streaming kernels on every SM are faster for longer rows (V = 151936, 8191
-// rows: JSD 1.69 ms two-pass against 1.88 single-read, KL 1.36 against 1.75;
-// V = 16032: JSD 0.19 against 0.21, KL 0.18 against 0.19).
-constexpr int64_t kForwardFusedMaxVocab = 32768;
+// Forward-only calls take the single-read forward kernel in clusters of at
+// most kForwardMaxCluster CTAs (130 or more SMs on this GPU); a row that needs
+// larger clusters (V = 262144: 16 CTAs, 112 SMs) takes the streaming kernels,
+// which use every SM (JSD: 10.7 ms two-pass against 12.4 single-read for
+// 32768 rows). At V = 151936 the JSD forward takes 1.49 ms single-read against
+// 1.69 two-pass for 8191 rows. The KL forward has a one-read streaming kernel
+// of its own, faster above kKlFusedMaxVocab (V = 151936: 1.35 against 1.46
+// ms; V = 16032: 0.155 single-read against 0.18).
 constexpr int kForwardMaxCluster = 10;
+constexpr int64_t kKlFusedMaxVocab = 32768;
 
 vpd_status vpd_jsd_fwd(const vpd_view* s, const vpd_view* t, double beta, const vpd_segments* seg,
                        float* loss, float* saved, void* stream) {
@@ -169,9 +171,9 @@ vpd_status vpd_jsd_fwd(const vpd_view* s, const vpd_view* t, double beta, const 
   if (vs.rows == 0) return ok();
   if (!loss || !saved) return fail(VPD_ERR_ARG, "vpd_jsd_fwd: loss and saved are required");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // Short rows: one read of the inputs by the single-read kernel (no gradients
-  // wanted); longer rows: the two streaming passes on every SM.
-  if (sg.count == 1 && vs.vocab <= kForwardFusedMaxVocab) {
+  // One read of the inputs by the single-read forward kernel when it fits in
+  // clusters that cover most SMs; else the two streaming passes on every SM.
+  if (sg.count == 1) {
     const vpd::Grad none{nullptr, 0, 0};
     cudaError_t e = vpd::launch_jsd_fused(vs, vt, beta, nullptr, loss, saved, none, none, st, -1,
                                           kForwardMaxCluster);
@@ -239,7 +241,7 @@ vpd_status vpd_kl_fwd(const vpd_view* s, const vpd_view* t, int32_t reverse,
   if (!loss) return fail(VPD_ERR_ARG, "vpd_kl_fwd: loss is required");
   // Short rows: the KL branch of the single-read kernel (beta = 0 / 1); longer
   // rows: the online single-pass kernel on every SM, which is faster there.
-  if (sg.count == 1 && vs.vocab <= kForwardFusedMaxVocab) {
+  if (sg.count == 1 && vs.vocab <= kKlFusedMaxVocab) {
     const vpd::Grad none{nullptr, 0, 0};
     cudaError_t e = vpd::launch_jsd_fused(vs, vt, reverse ? 1.0 : 0.0, nullptr, loss, saved, none, none,
                                           static_cast<cudaStream_t>(stream), -1, kForwardMaxCluster);

@@ -16,8 +16,8 @@
 namespace vpd {
 namespace fused {
 // Instantiated in vpd_fused_bf16.cu and vpd_fused_f16.cu.
-extern template cudaError_t launch_typed<InBF16>(const FusedArgs&, const Config&, int, bool, cudaStream_t, int*);
-extern template cudaError_t launch_typed<InF16>(const FusedArgs&, const Config&, int, bool, cudaStream_t, int*);
+extern template cudaError_t launch_typed<InBF16>(const FusedArgs&, const Config&, int, bool, bool, cudaStream_t, int*);
+extern template cudaError_t launch_typed<InF16>(const FusedArgs&, const Config&, int, bool, bool, cudaStream_t, int*);
 extern template int resident_clusters<InBF16>(int, int, size_t);
 cudaError_t take_error_bf16(int* code);
 cudaError_t take_error_f16(int* code);
@@ -102,22 +102,23 @@ int64_t sched_vectors(int64_t nvec, int R, int nw) {
 // thread within the register and TMEM budgets); then the smallest R that
 // covers the slice and as many workers as the budgets allow without idle
 // warps (more warps hide more latency). Ties go to the smaller cluster.
-bool choose(int64_t vocab, int64_t rows, int max_cluster, Config* cfg) {
+// `fwd`: the forward-only kernel (three stages, no tensor memory).
+bool choose(int64_t vocab, int64_t rows, int max_cluster, bool fwd, Config* cfg) {
   const size_t smem_cap = max_smem_optin();
   int64_t best = 0;
   for (int C = 1; C <= fused::kMaxCluster && C <= max_cluster; ++C) {
     const int64_t W = ((vocab + C - 1) / C + 7) / 8 * 8;
     const int64_t nvec = W / 8;
-    const size_t smem = fused::smem_bytes(static_cast<int>(W));
+    const size_t smem = fwd ? fused::smem_bytes_fwd(static_cast<int>(W)) : fused::smem_bytes(static_cast<int>(W));
     if (smem > smem_cap) continue;
     int bR = 0, bnw = 0;
     for (int R = 1; R <= fused::kMaxR && !bR; ++R) {
-      const int64_t cap = fused::max_workers(R);
+      const int64_t cap = fwd ? fused::kMaxWorkersFwd : fused::max_workers(R);
       if (nvec > 32 * cap * R) continue;
       int64_t nw = R == 1 ? (nvec + 31) / 32 : (nvec + 32 * (R - 1) - 1) / (32 * (R - 1));
       if (nw > cap) nw = cap;
       if (nw < 1) nw = 1;
-      if (R * fused::Cols<fused::kInterior>::k > fused::tmem_cols_per_warp(static_cast<int>(nw))) continue;
+      if (!fwd && R * fused::Cols<fused::kInterior>::k > fused::tmem_cols_per_warp(static_cast<int>(nw))) continue;
       bR = R, bnw = static_cast<int>(nw);
     }
     if (!bR) continue;
@@ -154,8 +155,9 @@ cudaError_t launch_jsd_fused(const View& s, const View& t, double beta, const fl
     if (g->dtype != kF32 && g->dtype != s.dtype) return cudaErrorNotSupported;
     gdtype = g->dtype;
   }
+  const bool fwd = gdtype < 0;  // no gradient wanted: the forward-only kernel
   Config cfg;
-  if (!choose(s.vocab, s.rows, max_cluster, &cfg)) return cudaErrorNotSupported;
+  if (!choose(s.vocab, s.rows, max_cluster, fwd, &cfg)) return cudaErrorNotSupported;
   const int mode = beta == 0.0 ? fused::kForwardKL : beta == 1.0 ? fused::kReverseKL : fused::kInterior;
   const bool f32g = gdtype == kF32;
   // 16-bit gradients go out through a shared-memory buffer and bulk stores
@@ -167,13 +169,13 @@ cudaError_t launch_jsd_fused(const View& s, const View& t, double beta, const fl
                         grad_loss, loss, saved, ds, dt, withhold_row};
   int clusters = 0;
   const cudaError_t e = s.dtype == kBF16
-                            ? fused::launch_typed<fused::InBF16>(args, cfg, mode, f32g, stream, &clusters)
-                            : fused::launch_typed<fused::InF16>(args, cfg, mode, f32g, stream, &clusters);
+                            ? fused::launch_typed<fused::InBF16>(args, cfg, mode, f32g, fwd, stream, &clusters)
+                            : fused::launch_typed<fused::InF16>(args, cfg, mode, f32g, fwd, stream, &clusters);
   if (e == cudaSuccess) {
     note_launch();
     if (verbose())
-      fprintf(stderr, "[vpd] fused JSD: V=%lld cluster=%d workers=%d R=%d W=%d smem=%zu B%s, %d clusters\n",
-              static_cast<long long>(s.vocab), cfg.C, cfg.nw, cfg.R, cfg.W, cfg.smem,
+      fprintf(stderr, "[vpd] fused JSD%s: V=%lld cluster=%d workers=%d R=%d W=%d smem=%zu B%s, %d clusters\n",
+              fwd ? " forward" : "", static_cast<long long>(s.vocab), cfg.C, cfg.nw, cfg.R, cfg.W, cfg.smem,
               gstage ? " (staged gradients)" : "", clusters);
   }
   return e;

@@ -55,7 +55,9 @@ namespace fused {
 using vpd::InBF16;
 using vpd::InF16;
 
-constexpr int kStages = 2;                  // shared-memory stages per CTA
+constexpr int kStages = 2;                  // shared-memory stages per CTA (forward + backward)
+constexpr int kFwdStages = 3;               // stages of the forward-only kernel
+constexpr int kRing = 3;                    // cluster slots and their mbarriers, by row
 constexpr float kTiny = 1e-37f;             // keeps M > 0 so log2 M stays finite
 constexpr float kMaxLogit = 8.5070592e37f;  // 2^126: a larger finite row max is out of contract
 constexpr int kMaxCluster = 16;
@@ -68,6 +70,10 @@ constexpr int kMaxWorkers = 19;             // worker warps per CTA (plus one co
 // thread is 16K / (32 ceil((workers + 1) / 4)): 136 registers at R = 5 (15
 // warps), 96 below (20 warps).
 __host__ __device__ constexpr int max_workers(int R) { return R >= 5 ? 14 : kMaxWorkers; }
+// The forward-only kernel keeps nothing across passes (about 70 registers), so
+// it runs up to 23 worker warps at any R: more warps hide more of each row's
+// hand-over latency.
+constexpr int kMaxWorkersFwd = 23;
 // TMEM columns of one worker warp: the warps of a lane quarter share its 512
 // columns (a multiple of 8 each).
 __host__ __device__ constexpr int tmem_cols_per_warp(int nw) { return (kTmemCols / ((nw + 3) / 4)) & ~7; }
@@ -362,20 +368,27 @@ __device__ __forceinline__ uint4 lds16(const unsigned char* p) { return *reinter
 // which the merges propagate. Sums travel as (A, B) in nats; a KL support
 // violation makes A = +inf.
 // ---------------------------------------------------------------------------
-enum NamedBar : int { kBarStatPart = 1, kBarStatReady = 2, kBarSumPart = 3, kBarSumReady = 4, kBarGradFull = 5 };
+enum NamedBar : int {
+  kBarStatPart = 1,
+  kBarStatReady = 2,
+  kBarSumPart = 3,
+  kBarSumReady = 4,
+  kBarGradFull = 5,
+  kBarStatPartOdd = 6,  // forward-only kernel: statistics partials of odd rows
+};
 
 struct Tail {
-  uint64_t tma_bar[kStages];
-  uint64_t stat_bar[2];
-  uint64_t sum_bar[2];
+  uint64_t tma_bar[kFwdStages];
+  uint64_t stat_bar[kRing];
+  uint64_t sum_bar[kRing];
   uint32_t tmem_base;
   int fail;  // set by a worker whose wait on a stage gave up
-  __align__(16) float stat_part[2][kMaxWorkers][4];  // per worker warp: m_s, z_s, m_t, z_t
-  __align__(16) float sum_part[2][kMaxWorkers][4];   // per worker warp: A, B (nats)
+  __align__(16) float stat_part[2][kMaxWorkersFwd][4];  // per worker warp: m_s, z_s, m_t, z_t
+  __align__(16) float sum_part[2][kMaxWorkersFwd][4];   // per worker warp: A, B (nats)
   __align__(16) float stat_res[2][8];  // -m_s, -m_t, -log2 Z_s, -log2 Z_t, row ok, run ok
   __align__(16) float sum_res[2][4];   // A, B, value (nats)
-  __align__(16) float stat_slot[2][kMaxCluster][4];
-  __align__(16) float sum_slot[2][kMaxCluster][4];
+  __align__(16) float stat_slot[kRing][kMaxCluster][4];
+  __align__(16) float sum_slot[kRing][kMaxCluster][4];
 };
 
 // Merge (m, z) over the lanes of a warp (unused lanes hold (-inf, 0)).
@@ -394,7 +407,7 @@ __device__ __forceinline__ bool control_wait(uint64_t* bar, uint32_t parity, uin
 }
 
 // Control warp: merge the workers' statistics partials and push the CTA's to
-// every CTA of the cluster (slot `crank`).
+// every CTA of the cluster (ring slot `par`, entry `crank`).
 __device__ __forceinline__ void control_push_stats(const float (*part)[4], int nw, Tail* tail, int par,
                                                    uint32_t crank, uint32_t csize) {
   const int lane = threadIdx.x & 31;
@@ -571,7 +584,7 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
   if (control) {
     if (lane == 0) {
       for (int st = 0; st < kStages; ++st) mbar_init(&tail->tma_bar[st], 1);
-      for (int p = 0; p < 2; ++p) {
+      for (int p = 0; p < kRing; ++p) {
         mbar_init(&tail->stat_bar[p], 1);
         mbar_init(&tail->sum_bar[p], 1);
       }
@@ -915,6 +928,281 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
 }
 
 // ---------------------------------------------------------------------------
+// Forward only (no gradient wanted): the statistics, pass C and the cluster
+// reductions of the kernel above without pass D, so nothing goes to tensor
+// memory and q is not kept. With no pass D, the exchanges are hidden another
+// way: each worker computes the statistics partial of row i + 1 before pass C
+// of row i, so that their cluster exchange travels during pass C; and the
+// control warp takes the cluster's sums of a row two rows later, when they are
+// in, so that this wait never delays a hand-over. Three shared-memory stages
+// keep two rows ahead of pass C in flight (a stage is refilled with row i + 3
+// once pass C of row i has read it, and is needed again two rows later).
+//
+// Row indices below count this cluster's rows (row q + i Q is row i).
+// Workers, per row i: the statistics partial of row i + 1 from its stage;
+// wait for the statistics of row i; pass C of row i (the partials of A and B).
+// Control warp, per row i: (C1) merge the cluster's statistics of row i and
+// hand them over; (C3) wait for the cluster's sums of row i - 2 and write its
+// loss and saved statistics; (C4) merge and push the statistics of row i + 1;
+// (C2) once pass C of row i is in, refill its stage with row i + 3 and push
+// this CTA's sums. Cluster slots and their mbarriers form rings of three by
+// row: a CTA pushes into the slot of row i + 3 only after its own hand-over of
+// row i + 3 or i + 2, which needs partials that every peer sends only after
+// reading that slot for row i.
+// ---------------------------------------------------------------------------
+template <class In, int R, int MODE>
+__global__ void __launch_bounds__(32 * (kMaxWorkersFwd + 1), 1) k_jsd_fused_fwd(FusedArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int W = a.W, nw = a.nw, Tw = 32 * nw, nthreads = Tw + 32;
+  Tail* tail = reinterpret_cast<Tail*>(smem + static_cast<size_t>(kFwdStages) * 4 * W);
+  auto stage_ptr = [&](int st) { return smem + static_cast<size_t>(st) * 4 * W; };
+
+  const uint32_t crank = cluster_rank(), csize = cluster_size();
+  const int64_t q = cluster_index(), Q = cluster_count();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool control = warp == nw;
+  const int64_t col0 = static_cast<int64_t>(crank) * W;
+  const int64_t rest = a.vocab - col0;
+  const int len = rest <= 0 ? 0 : (rest < W ? static_cast<int>(rest) : W);
+  const uint32_t bytes = static_cast<uint32_t>(len) * 2u;
+  // statistics partials of row i hand over on a named barrier of its parity:
+  // the workers may arrive for row i + 1 before the control warp took row i
+  auto stat_part_bar = [](int64_t i) { return (i & 1) ? kBarStatPartOdd : kBarStatPart; };
+
+  auto withheld = [&](int64_t r) { return r == a.withhold_row && crank == 0; };
+  // control warp, bit st: copies were issued into stage st / their count is odd
+  uint32_t issued_any = 0, issued_odd = 0;
+  auto issue = [&](int64_t r, int st) {  // control warp: both inputs' slices of row r into stage st
+    if (!bytes || withheld(r)) return;
+    if (lane == 0) {
+      unsigned char* dst = stage_ptr(st);
+      mbar_expect_tx(&tail->tma_bar[st], 2 * bytes);
+      bulk_load(dst, a.s + (a.ms.offset(r) + col0) * 2, bytes, &tail->tma_bar[st]);
+      bulk_load(dst + static_cast<size_t>(W) * 2, a.t + (a.mt.offset(r) + col0) * 2, bytes, &tail->tma_bar[st]);
+    }
+    issued_any |= 1u << st;
+    issued_odd ^= 1u << st;
+  };
+
+  if (control) {
+    if (lane == 0) {
+      for (int st = 0; st < kFwdStages; ++st) mbar_init(&tail->tma_bar[st], 1);
+      for (int p = 0; p < kRing; ++p) {
+        mbar_init(&tail->stat_bar[p], 1);
+        mbar_init(&tail->sum_bar[p], 1);
+      }
+      tail->fail = 0;
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    for (int st = 0; st < kFwdStages; ++st)
+      if (q + st * Q < a.rows) issue(q + st * Q, st);
+  }
+  __syncthreads();
+  cluster_sync();  // every CTA's mbarriers are initialised before any push
+
+  const float beta = a.beta;
+  bool ok = true;
+  if (control) {
+    // ------------------------------------------------------------------
+    // Control warp.
+    // ------------------------------------------------------------------
+    struct RowStats {
+      float4 g;  // m_s, Z_s, m_t, Z_t
+      float Ks, Kt;
+      bool bad_s, bad_t, row_ok;
+    };
+    // (C4) merge the workers' statistics partials of row i and push them
+    auto push_stats = [&](int64_t i) {
+      bar_sync(stat_part_bar(i), nthreads);
+      if (tail->fail) ok = false;
+      control_push_stats(tail->stat_part[i & 1], nw, tail, static_cast<int>(i % kRing), crank, csize);
+    };
+    // (C1) the cluster's statistics of row i, handed to the workers
+    auto publish = [&](int64_t i) {
+      const int slot = static_cast<int>(i % kRing), par = static_cast<int>(i & 1);
+      RowStats rs;
+      rs.g = make_float4(qnan(), qnan(), qnan(), qnan());
+      if (ok) ok = control_wait(&tail->stat_bar[slot], static_cast<uint32_t>((i / kRing) & 1), csize);
+      if (ok) {
+        float4 v = make_float4(neg_inf(), 0.f, neg_inf(), 0.f);
+        if (lane < static_cast<int>(csize)) v = *reinterpret_cast<const float4*>(tail->stat_slot[slot][lane]);
+        const float2 ms = merge_warp(v.x, v.y), mt = merge_warp(v.z, v.w);
+        rs.g = make_float4(ms.x, ms.y, mt.x, mt.y);
+      }
+      rs.bad_s = isnan(rs.g.y);
+      rs.bad_t = isnan(rs.g.w);
+      rs.row_ok = ok && !rs.bad_s && !rs.bad_t && rs.g.x != neg_inf() && rs.g.z != neg_inf();
+      rs.Ks = rs.row_ok ? log2f(rs.g.y) : qnan();  // log2 Z
+      rs.Kt = rs.row_ok ? log2f(rs.g.w) : qnan();
+      if (lane == 0) {
+        float* res = tail->stat_res[par];
+        *reinterpret_cast<float4*>(res) = make_float4(-rs.g.x, -rs.g.z, -rs.Ks, -rs.Kt);
+        *reinterpret_cast<float2*>(res + 4) = make_float2(rs.row_ok ? 1.f : 0.f, ok ? 1.f : 0.f);
+      }
+      bar_arrive(kBarStatReady, nthreads);
+      return rs;
+    };
+    // (C3) the cluster's sums of row j (row r): the per-token value and saved statistics
+    auto finish = [&](int64_t j, int64_t r, const RowStats& rs) {
+      const int slot = static_cast<int>(j % kRing);
+      float A = qnan(), B = qnan(), value = qnan();
+      const bool got = ok && control_wait(&tail->sum_bar[slot], static_cast<uint32_t>((j / kRing) & 1), csize);
+      if (!got) ok = false;
+      if (got && rs.row_ok) {
+        float2 v = make_float2(0.f, 0.f);
+        if (lane < static_cast<int>(csize)) v = *reinterpret_cast<const float2*>(tail->sum_slot[slot][lane]);
+        A = warp_sum(v.x);
+        B = warp_sum(v.y);
+        if (MODE == kInterior) {
+          value = beta * A + (1.f - beta) * B;
+        } else {
+          value = A;  // +inf on a support violation
+          A = MODE == kForwardKL ? value : 0.f;
+          B = MODE == kForwardKL ? 0.f : value;
+        }
+      }
+      if (lane == 0 && crank == 0) a.loss[r] = value;
+      if (lane == 0 && crank == 0 && a.saved) {
+        const float4 g = rs.g;
+        float* sv = a.saved + r * VPD_SAVED_PAIR;
+        sv[0] = rs.bad_s ? qnan() : g.x;
+        sv[1] = rs.bad_s ? qnan() : (g.x == neg_inf() ? neg_inf() : (rs.row_ok ? kLn2 * rs.Ks : kLn2 * log2f(g.y)));
+        sv[2] = rs.bad_t ? qnan() : g.z;
+        sv[3] = rs.bad_t ? qnan() : (g.z == neg_inf() ? neg_inf() : (rs.row_ok ? kLn2 * rs.Kt : kLn2 * log2f(g.w)));
+        sv[4] = A;
+        sv[5] = B;
+      }
+    };
+    // Rows whose sums are still to be taken: rows i - 2 (old) and i - 1 (new).
+    RowStats old_s{}, new_s{};
+    int64_t old_r = -1, new_r = -1;
+    if (q < a.rows) push_stats(0);
+    int64_t i = 0;
+    for (int64_t r = q; r < a.rows; r += Q, ++i) {
+      const int par = static_cast<int>(i & 1), slot = static_cast<int>(i % kRing);
+      const bool has_next = r + Q < a.rows;
+
+      // (C1) statistics of row i (pushed a row earlier) to the workers, who
+      // take the row only if no wait gave up
+      const RowStats cur = publish(i);
+      const bool live = ok;
+      // (C3) sums of row i - 2, in by now (every peer pushed them before the
+      // statistics of row i that were just merged)
+      if (old_r >= 0) finish(i - 2, old_r, old_s);
+      old_r = -1;
+      // (C4) statistics of row i + 1, which the workers computed before taking row i
+      if (has_next) push_stats(i + 1);
+      if (!live) break;
+
+      // (C2) pass C of row i is in: refill its stage with row i + 3, push the sums
+      bar_sync(kBarSumPart, nthreads);
+      if (r + kFwdStages * Q < a.rows) issue(r + kFwdStages * Q, static_cast<int>(i % kFwdStages));
+      {
+        float2 v = make_float2(0.f, 0.f);
+        if (lane < nw) v = *reinterpret_cast<const float2*>(tail->sum_part[par][lane]);
+        const float sa = warp_sum(v.x), sb = warp_sum(v.y);
+        if (lane < static_cast<int>(csize))
+          push16(map_rank(smem_addr(tail->sum_slot[slot][crank]), lane), sa, sb, 0.f, 0.f,
+                 map_rank(smem_addr(&tail->sum_bar[slot]), lane));
+      }
+      old_s = new_s;
+      old_r = new_r;
+      new_s = cur;
+      new_r = r;
+    }
+    // the last two rows' sums
+    if (old_r >= 0) finish(i - 2, old_r, old_s);
+    if (new_r >= 0) finish(i - 1, new_r, new_s);
+    // Copies still in flight (only after a wait gave up) must land before exit.
+    if (lane == 0)
+      for (int st = 0; st < kFwdStages; ++st)
+        if ((issued_any >> st) & 1u) mbar_wait(&tail->tma_bar[st], ((issued_odd >> st) & 1u) ^ 1u);
+  } else {
+    // ------------------------------------------------------------------
+    // Worker warps.
+    // ------------------------------------------------------------------
+    uint32_t tma_parity = 0;  // bit st: parity of the next wait on stage st
+    const float2 ws2 = f2(1.f - beta), wt2 = f2(beta), tiny2 = f2(kTiny), l2e2 = f2(kLog2e);
+    const int vt = 32 * vector_order(warp, nw, R) + lane;  // this thread's place in the vector order
+    const Span sp = span_of<R>(len, Tw, vt);
+    // statistics partial of row i from its stage
+    auto stats_of = [&](int64_t i) {
+      const int st = static_cast<int>(i % kFwdStages);
+      if (bytes) {
+        if (!mbar_wait(&tail->tma_bar[st], (tma_parity >> st) & 1u)) tail->fail = 1;
+        tma_parity ^= 1u << st;
+      }
+      worker_stats<In, R>(stage_ptr(st), W, sp, Tw, vt, tail->stat_part[i & 1][warp]);
+      bar_arrive(stat_part_bar(i), nthreads);
+    };
+    if (q < a.rows) stats_of(0);
+    int64_t i = 0;
+    for (int64_t r = q; r < a.rows; r += Q, ++i) {
+      const int par = static_cast<int>(i & 1);
+
+      // (W3) statistics partial of row i + 1: its exchange travels during pass C of row i
+      if (r + Q < a.rows) stats_of(i + 1);
+
+      // (W1) global statistics of row i
+      bar_sync(kBarStatReady, nthreads);
+      const float4 st4 = *reinterpret_cast<const float4*>(tail->stat_res[par]);
+      const float2 flags = *reinterpret_cast<const float2*>(tail->stat_res[par] + 4);
+      if (flags.y == 0.f) break;
+      const float2 nms2 = f2(st4.x), nmt2 = f2(st4.y), nKs2 = f2(st4.z), nKt2 = f2(st4.w);
+
+      // (W2) pass C of row i from its stage, in log2 units
+      float2 acc_a = f2(0.f), acc_b = f2(0.f);
+      uint32_t viol = 0;
+      if (flags.x != 0.f) {
+        const unsigned char* ps = stage_ptr(static_cast<int>(i % kFwdStages)) + vt * 16;
+        const size_t tofs = static_cast<size_t>(W) * 2;
+#pragma unroll
+        for (int k = 0; k < R; ++k) {
+          if (k < sp.kv) {
+            const uint4 u = lds16(ps + k * Tw * 16), v = lds16(ps + tofs + k * Tw * 16);
+            const uint32_t us[4] = {u.x, u.y, u.z, u.w}, vs[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              if (MODE != kInterior) {
+                const uint32_t tgt = MODE == kForwardKL ? vs[w] : us[w];
+                const uint32_t oth = MODE == kForwardKL ? us[w] : vs[w];
+                viol |= __vcmpeq2(oth, In::kNegInf2) & ~__vcmpeq2(tgt, In::kNegInf2);
+              }
+              const float2 lp = lam<In>(In::max2(us[w], In::kNegBig2), nms2, l2e2, nKs2);
+              const float2 lq = lam<In>(In::max2(vs[w], In::kNegBig2), nmt2, l2e2, nKt2);
+              const float2 p = ex2_2(lp), qv = ex2_2(lq);
+              if (MODE == kInterior) {
+                const float2 lm = lg2_2(fma2(ws2, p, fma2(wt2, qv, tiny2)));
+                acc_b = fma2(p, add2(lp, neg(lm)), acc_b);
+                acc_a = fma2(qv, add2(lq, neg(lm)), acc_a);
+              } else {
+                // forward KL(q || p): d = log2 q - log2 p weighted by q; reverse: mirror
+                const float2 d = MODE == kForwardKL ? add2(lq, neg(lp)) : add2(lp, neg(lq));
+                acc_a = fma2(MODE == kForwardKL ? qv : p, d, acc_a);
+              }
+            }
+          }
+        }
+      }
+      if constexpr (MODE == kInterior) {  // A partial on lanes 0-15, B partial on lanes 16-31
+        const float v = kLn2 * warp_sum_pair(acc_a.x + acc_a.y, acc_b.x + acc_b.y);
+        if ((lane & 15) == 0) tail->sum_part[par][warp][lane >> 4] = v;
+      } else {
+        float sa = kLn2 * warp_sum(acc_a.x + acc_a.y);
+        if (__any_sync(0xffffffffu, viol != 0)) sa = pos_inf();
+        if (lane == 0) *reinterpret_cast<float2*>(tail->sum_part[par][warp]) = make_float2(sa, 0.f);
+      }
+      bar_arrive(kBarSumPart, nthreads);
+    }
+  }
+
+  __syncthreads();
+  if (control && lane == 0 && (!ok || tail->fail)) atomicExch(&g_fused_error, 1);
+  cluster_sync();  // no CTA leaves while a peer may still push into it
+}
+
+// ---------------------------------------------------------------------------
 // Host side (per input dtype): one configuration, one launch.
 // ---------------------------------------------------------------------------
 struct Config {
@@ -928,21 +1216,29 @@ inline size_t smem_bytes(int W, bool gstage = false) {
   const size_t s = static_cast<size_t>(kStages) * 4 * W + (gstage ? static_cast<size_t>(4) * W : 0) + sizeof(Tail);
   return s < kMinSmem ? kMinSmem : s;
 }
+// The forward-only kernel: three stages, then the tail (one CTA per SM too).
+inline size_t smem_bytes_fwd(int W) {
+  const size_t s = static_cast<size_t>(kFwdStages) * 4 * W + sizeof(Tail);
+  return s < kMinSmem ? kMinSmem : s;
+}
 
 // Launches the configured kernel; cudaErrorNotSupported (nothing launched)
 // when no cluster of that shape can be resident. `clusters_out` reports the
 // number of resident clusters.
+// `fwd`: no gradient wanted, the forward-only kernel.
 template <class In>
-cudaError_t launch_typed(const FusedArgs& args, const Config& cfg, int mode, bool f32grad, cudaStream_t stream,
-                         int* clusters_out);
+cudaError_t launch_typed(const FusedArgs& args, const Config& cfg, int mode, bool f32grad, bool fwd,
+                         cudaStream_t stream, int* clusters_out);
 // Resident clusters of C CTAs with nw worker warps (0 when none fit).
 template <class In>
 int resident_clusters(int C, int nw, size_t smem);
 
-template <class In, class G, int R, int MODE>
-cudaError_t setup_one(const Config& cfg, cudaLaunchConfig_t* lc, cudaLaunchAttribute* attr, int* clusters) {
-  auto kern = k_jsd_fused<In, G, R, MODE>;
-  if (cfg.nw < 1 || cfg.nw > max_workers(R)) return cudaErrorNotSupported;
+using Kernel = void (*)(FusedArgs);
+
+// Cluster launch of `kern` (at most `maxw` worker warps) in shape `cfg`.
+inline cudaError_t setup_one(Kernel kern, int maxw, const Config& cfg, cudaLaunchConfig_t* lc,
+                             cudaLaunchAttribute* attr, int* clusters) {
+  if (cfg.nw < 1 || cfg.nw > maxw) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(cfg.smem));
   if (e != cudaSuccess) return e;
@@ -971,35 +1267,52 @@ cudaError_t setup_one(const Config& cfg, cudaLaunchConfig_t* lc, cudaLaunchAttri
   return cudaSuccess;
 }
 
-template <class In, class G, int R, int MODE>
-cudaError_t launch_one(const FusedArgs& args, const Config& cfg, cudaStream_t stream, int* clusters_out) {
+inline cudaError_t launch_kernel(Kernel kern, int maxw, const FusedArgs& args, const Config& cfg,
+                                 cudaStream_t stream, int* clusters_out) {
   cudaLaunchConfig_t lc = {};
   cudaLaunchAttribute attr[1];
   int clusters = 0;
-  cudaError_t e = setup_one<In, G, R, MODE>(cfg, &lc, attr, &clusters);
+  cudaError_t e = setup_one(kern, maxw, cfg, &lc, attr, &clusters);
   if (e != cudaSuccess) return e;
   *clusters_out = clusters;
   const int64_t want = args.rows < clusters ? args.rows : clusters;
   lc.gridDim = dim3(static_cast<unsigned>(want * cfg.C), 1, 1);
   lc.stream = stream;
-  return cudaLaunchKernelEx(&lc, k_jsd_fused<In, G, R, MODE>, args);
+  return cudaLaunchKernelEx(&lc, kern, args);
 }
 
 template <class In, class G, int MODE>
 cudaError_t launch_r(const FusedArgs& args, const Config& cfg, cudaStream_t stream, int* clusters) {
   switch (cfg.R) {
-    case 1: return launch_one<In, G, 1, MODE>(args, cfg, stream, clusters);
-    case 2: return launch_one<In, G, 2, MODE>(args, cfg, stream, clusters);
-    case 3: return launch_one<In, G, 3, MODE>(args, cfg, stream, clusters);
-    case 4: return launch_one<In, G, 4, MODE>(args, cfg, stream, clusters);
-    case 5: return launch_one<In, G, 5, MODE>(args, cfg, stream, clusters);
+    case 1: return launch_kernel(k_jsd_fused<In, G, 1, MODE>, max_workers(1), args, cfg, stream, clusters);
+    case 2: return launch_kernel(k_jsd_fused<In, G, 2, MODE>, max_workers(2), args, cfg, stream, clusters);
+    case 3: return launch_kernel(k_jsd_fused<In, G, 3, MODE>, max_workers(3), args, cfg, stream, clusters);
+    case 4: return launch_kernel(k_jsd_fused<In, G, 4, MODE>, max_workers(4), args, cfg, stream, clusters);
+    case 5: return launch_kernel(k_jsd_fused<In, G, 5, MODE>, max_workers(5), args, cfg, stream, clusters);
+  }
+  return cudaErrorNotSupported;
+}
+
+template <class In, int MODE>
+cudaError_t launch_fwd(const FusedArgs& args, const Config& cfg, cudaStream_t stream, int* clusters) {
+  switch (cfg.R) {
+    case 1: return launch_kernel(k_jsd_fused_fwd<In, 1, MODE>, kMaxWorkersFwd, args, cfg, stream, clusters);
+    case 2: return launch_kernel(k_jsd_fused_fwd<In, 2, MODE>, kMaxWorkersFwd, args, cfg, stream, clusters);
+    case 3: return launch_kernel(k_jsd_fused_fwd<In, 3, MODE>, kMaxWorkersFwd, args, cfg, stream, clusters);
+    case 4: return launch_kernel(k_jsd_fused_fwd<In, 4, MODE>, kMaxWorkersFwd, args, cfg, stream, clusters);
+    case 5: return launch_kernel(k_jsd_fused_fwd<In, 5, MODE>, kMaxWorkersFwd, args, cfg, stream, clusters);
   }
   return cudaErrorNotSupported;
 }
 
 template <class In>
-cudaError_t launch_typed(const FusedArgs& args, const Config& cfg, int mode, bool f32grad, cudaStream_t stream,
-                         int* clusters) {
+cudaError_t launch_typed(const FusedArgs& args, const Config& cfg, int mode, bool f32grad, bool fwd,
+                         cudaStream_t stream, int* clusters) {
+  if (fwd) {
+    if (mode == kForwardKL) return launch_fwd<In, kForwardKL>(args, cfg, stream, clusters);
+    if (mode == kReverseKL) return launch_fwd<In, kReverseKL>(args, cfg, stream, clusters);
+    return launch_fwd<In, kInterior>(args, cfg, stream, clusters);
+  }
   using GIn = typename In::GSame;
   if (mode == kForwardKL)
     return f32grad ? launch_r<In, GF32, kForwardKL>(args, cfg, stream, clusters)
@@ -1017,7 +1330,8 @@ int resident_clusters(int C, int nw, size_t smem) {
   cudaLaunchConfig_t lc = {};
   cudaLaunchAttribute attr[1];
   int clusters = 0;
-  if (setup_one<In, GF32, 1, kInterior>(cfg, &lc, attr, &clusters) != cudaSuccess) return 0;
+  if (setup_one(k_jsd_fused<In, GF32, 1, kInterior>, max_workers(1), cfg, &lc, attr, &clusters) != cudaSuccess)
+    return 0;
   return clusters;
 }
 

@@ -5,7 +5,7 @@
 namespace vpd {
 namespace fused {
 
-template cudaError_t launch_typed<InF16>(const FusedArgs&, const Config&, int, bool, cudaStream_t, int*);
+template cudaError_t launch_typed<InF16>(const FusedArgs&, const Config&, int, bool, bool, cudaStream_t, int*);
 template int resident_clusters<InF16>(int, int, size_t);
 
 cudaError_t take_error_f16(int* code) {

@@ -25,12 +25,12 @@ def B():
     return binding
 
 
-def _call(B, s, t):
+def _call(B, s, t, grads=True):
     n, v = s.shape
     loss = torch.empty(n, device="cuda")
     saved = torch.empty(n, 6, device="cuda")
-    ds = torch.empty(n, v, dtype=s.dtype, device="cuda")
-    dt = torch.empty(n, v, dtype=s.dtype, device="cuda")
+    ds = torch.empty(n, v, dtype=s.dtype, device="cuda") if grads else None
+    dt = torch.empty(n, v, dtype=s.dtype, device="cuda") if grads else None
     c0 = B.vpd_launch_count()
     B.vpd_jsd_fwdbwd(s, t, 0.5, None, None, loss, saved, ds, dt)
     torch.cuda.synchronize()
@@ -38,20 +38,21 @@ def _call(B, s, t):
     return loss
 
 
+@pytest.mark.parametrize("grads", [True, False])  # the forward+backward and the forward-only kernel
 @pytest.mark.parametrize("v", [8192, 151936])  # one CTA per row, and a cluster of CTAs per row
-def test_bounded_wait_reports_timeout_and_device_recovers(B, v):
+def test_bounded_wait_reports_timeout_and_device_recovers(B, v, grads):
     g = torch.Generator(device="cpu").manual_seed(3)
     s = (torch.randn(24, v, generator=g) * 3).to(torch.bfloat16).cuda()
     t = (torch.randn(24, v, generator=g) * 3).to(torch.bfloat16).cuda()
-    _call(B, s, t)
+    _call(B, s, t, grads)
     B.vpd_device_status()  # clean before the injected failure
     B.vpd_test_withhold_copy(5)
-    _call(B, s, t)
+    _call(B, s, t, grads)
     with pytest.raises(B.VpdError) as err:
         B.vpd_device_status()
     assert err.value.status == B.VPD_ERR_TIMEOUT
     B.vpd_device_status()  # the error word was cleared by the read
-    loss = _call(B, s, t)  # the context is still usable and the result is right
+    loss = _call(B, s, t, grads)  # the context is still usable and the result is right
     B.vpd_device_status()
     rl = O.jsd(to64(s), to64(t), 0.5, grad=False, threads=8)[0]
     assert_loss(to64(loss), rl, "after recovery")
