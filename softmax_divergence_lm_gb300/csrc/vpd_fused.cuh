@@ -534,11 +534,13 @@ __device__ __forceinline__ float2 lam(uint32_t w, float2 nm, float2 l2e2, float2
   return fma2(In::sub(w, nm), l2e2, nK);
 }
 
-template <class In, class G, int R, int MODE>
+// NW > 0 fixes the worker count at compile time (the common shapes), so that
+// the vector offsets k 32 NW are immediates; NW = 0 takes it from the args.
+template <class In, class G, int R, int MODE, int NW = 0>
 __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(FusedArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int kCols = Cols<MODE>::k;
-  const int W = a.W, nw = a.nw, Tw = 32 * nw, nthreads = Tw + 32;
+  const int W = a.W, nw = NW > 0 ? NW : a.nw, Tw = 32 * nw, nthreads = Tw + 32;
   // Shared memory: kStages x [s, t] slices, then (staged gradients) the dS and
   // dT slices of one row, then the tail.
   unsigned char* gbuf = smem + static_cast<size_t>(kStages) * 4 * W;
@@ -950,10 +952,10 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
 // row i + 3 or i + 2, which needs partials that every peer sends only after
 // reading that slot for row i.
 // ---------------------------------------------------------------------------
-template <class In, int R, int MODE>
+template <class In, int R, int MODE, int NW = 0>  // NW: as for k_jsd_fused
 __global__ void __launch_bounds__(32 * (kMaxWorkersFwd + 1), 1) k_jsd_fused_fwd(FusedArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  const int W = a.W, nw = a.nw, Tw = 32 * nw, nthreads = Tw + 32;
+  const int W = a.W, nw = NW > 0 ? NW : a.nw, Tw = 32 * nw, nthreads = Tw + 32;
   Tail* tail = reinterpret_cast<Tail*>(smem + static_cast<size_t>(kFwdStages) * 4 * W);
   auto stage_ptr = [&](int st) { return smem + static_cast<size_t>(st) * 4 * W; };
 
@@ -1287,7 +1289,10 @@ cudaError_t launch_r(const FusedArgs& args, const Config& cfg, cudaStream_t stre
     case 1: return launch_kernel(k_jsd_fused<In, G, 1, MODE>, max_workers(1), args, cfg, stream, clusters);
     case 2: return launch_kernel(k_jsd_fused<In, G, 2, MODE>, max_workers(2), args, cfg, stream, clusters);
     case 3: return launch_kernel(k_jsd_fused<In, G, 3, MODE>, max_workers(3), args, cfg, stream, clusters);
-    case 4: return launch_kernel(k_jsd_fused<In, G, 4, MODE>, max_workers(4), args, cfg, stream, clusters);
+    case 4:
+      if (cfg.nw == kMaxWorkers && MODE == kInterior)
+        return launch_kernel(k_jsd_fused<In, G, 4, MODE, kMaxWorkers>, max_workers(4), args, cfg, stream, clusters);
+      return launch_kernel(k_jsd_fused<In, G, 4, MODE>, max_workers(4), args, cfg, stream, clusters);
     case 5: return launch_kernel(k_jsd_fused<In, G, 5, MODE>, max_workers(5), args, cfg, stream, clusters);
   }
   return cudaErrorNotSupported;
@@ -1298,7 +1303,11 @@ cudaError_t launch_fwd(const FusedArgs& args, const Config& cfg, cudaStream_t st
   switch (cfg.R) {
     case 1: return launch_kernel(k_jsd_fused_fwd<In, 1, MODE>, kMaxWorkersFwd, args, cfg, stream, clusters);
     case 2: return launch_kernel(k_jsd_fused_fwd<In, 2, MODE>, kMaxWorkersFwd, args, cfg, stream, clusters);
-    case 3: return launch_kernel(k_jsd_fused_fwd<In, 3, MODE>, kMaxWorkersFwd, args, cfg, stream, clusters);
+    case 3:
+      if (cfg.nw == kMaxWorkersFwd)
+        return launch_kernel(k_jsd_fused_fwd<In, 3, MODE, kMaxWorkersFwd>, kMaxWorkersFwd, args, cfg, stream,
+                             clusters);
+      return launch_kernel(k_jsd_fused_fwd<In, 3, MODE>, kMaxWorkersFwd, args, cfg, stream, clusters);
     case 4: return launch_kernel(k_jsd_fused_fwd<In, 4, MODE>, kMaxWorkersFwd, args, cfg, stream, clusters);
     case 5: return launch_kernel(k_jsd_fused_fwd<In, 5, MODE>, kMaxWorkersFwd, args, cfg, stream, clusters);
   }
