@@ -62,6 +62,8 @@ def parse_args():
     p.add_argument("--profile-rows", type=int, default=0,
                    help="profiling mode: only the fused step on this many rows of the same vocabulary, "
                         "--warmup + --steps launches, one short line (for ncu captures of a small case)")
+    p.add_argument("--profile-forward", action="store_true",
+                   help="with --profile-rows: the forward-only call (no gradients) instead of fwd+bwd")
     return p.parse_args()
 
 
@@ -586,13 +588,18 @@ def run_profile(args):
     g = torch.full((n,), 1.0 / n, device=dev)
     loss = torch.empty(n, device=dev)
     saved = torch.empty(n, B.SAVED_PAIR, device=dev)
-    ds = torch.empty(n, VOCAB, dtype=torch.bfloat16, device=dev)
-    dt = torch.empty(n, VOCAB, dtype=torch.bfloat16, device=dev)
-    for _ in range(args.warmup + args.steps):
-        B.vpd_jsd_fwdbwd(s, t, BETA, None, g, loss, saved, ds, dt)
+    if args.profile_forward:
+        for _ in range(args.warmup + args.steps):
+            B.vpd_jsd_fwd(s, t, BETA, None, loss, saved)
+    else:
+        ds = torch.empty(n, VOCAB, dtype=torch.bfloat16, device=dev)
+        dt = torch.empty(n, VOCAB, dtype=torch.bfloat16, device=dev)
+        for _ in range(args.warmup + args.steps):
+            B.vpd_jsd_fwdbwd(s, t, BETA, None, g, loss, saved, ds, dt)
     torch.cuda.synchronize(dev)
     B.vpd_device_status()
-    print(json.dumps({"profile_rows": n, "launches": args.warmup + args.steps, "vocab": VOCAB}), flush=True)
+    print(json.dumps({"profile_rows": n, "launches": args.warmup + args.steps, "vocab": VOCAB,
+                      "step": "forward" if args.profile_forward else "fwd+bwd"}), flush=True)
 
 
 def main():
