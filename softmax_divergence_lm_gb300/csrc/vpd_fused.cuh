@@ -471,18 +471,25 @@ __host__ __device__ __forceinline__ int vector_order(int warp, int nw, int R) {
 
 // Worker warps: statistics partial of one row read from its shared-memory
 // stage (`vt`: this thread's place in the vector order); lane 0 writes the
-// warp's (m_s, z_s, m_t, z_t) to `part`.
-template <class In, int R>
+// warp's (m_s, z_s, m_t, z_t) to `part`. KEEP holds the vectors in registers
+// between the max and the exponential sweeps (one shared-memory read instead
+// of two) where the kernel has registers to spare.
+template <class In, int R, bool KEEP = false>
 __device__ __forceinline__ void worker_stats(const unsigned char* sb, int W, const Span& sp, int Tw, int vt,
                                              float* part) {
   const int lane = threadIdx.x & 31;
   const unsigned char* ps = sb + vt * 16;
   const size_t tofs = static_cast<size_t>(W) * 2;
   uint32_t mxs = In::kNegInf2, mxt = In::kNegInf2;
+  uint4 ku[R], kv[R];
 #pragma unroll
   for (int k = 0; k < R; ++k) {
     if (k < sp.kv) {
       const uint4 u = lds16(ps + k * Tw * 16), v = lds16(ps + tofs + k * Tw * 16);
+      if (KEEP) {
+        ku[k] = u;
+        kv[k] = v;
+      }
       mxs = In::max_nan(mxs, In::max_nan(In::max_nan(u.x, u.y), In::max_nan(u.z, u.w)));
       mxt = In::max_nan(mxt, In::max_nan(In::max_nan(v.x, v.y), In::max_nan(v.z, v.w)));
     }
@@ -494,7 +501,7 @@ __device__ __forceinline__ void worker_stats(const unsigned char* sb, int W, con
 #pragma unroll
   for (int k = 0; k < R; ++k) {
     if (k < sp.kv) {
-      const uint4 u = lds16(ps + k * Tw * 16), v = lds16(ps + tofs + k * Tw * 16);
+      const uint4 u = KEEP ? ku[k] : lds16(ps + k * Tw * 16), v = KEEP ? kv[k] : lds16(ps + tofs + k * Tw * 16);
       const uint32_t us[4] = {u.x, u.y, u.z, u.w}, vs[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
@@ -1135,7 +1142,7 @@ __global__ void __launch_bounds__(32 * (kMaxWorkersFwd + 1), 1) k_jsd_fused_fwd(
         if (!mbar_wait(&tail->tma_bar[st], (tma_parity >> st) & 1u)) tail->fail = 1;
         tma_parity ^= 1u << st;
       }
-      worker_stats<In, R>(stage_ptr(st), W, sp, Tw, vt, tail->stat_part[i & 1][warp]);
+      worker_stats<In, R, true>(stage_ptr(st), W, sp, Tw, vt, tail->stat_part[i & 1][warp]);
       bar_arrive(stat_part_bar(i), nthreads);
     };
     if (q < a.rows) stats_of(0);
