@@ -163,6 +163,14 @@ def test_fused_causal_view_and_many_rows(B):
     check(B, base_s[:, :-1], base_t[:, :-1], 0.5, torch.bfloat16, rows=rows, label="causal")
 
 
+def test_fused_many_rows_at_cluster_width(B):
+    """Many rows per cluster at the Qwen vocabulary (clusters of 9 CTAs, 19
+    workers x R = 4): every stage and cluster slot ring wraps many times."""
+    s, t = make_rows(240, 151936, torch.bfloat16, seed=13)
+    rows = np.arange(0, 240, 7)
+    check(B, s, t, 0.5, torch.bfloat16, rows=rows, label="240 rows")
+
+
 def test_fused_equals_streaming_path(B):
     """The fused single-read call and the two-pass forward + backward agree."""
     s, t = make_rows(32, 151936, torch.bfloat16, seed=7)
