@@ -153,11 +153,12 @@ extern "C" {
 // Forward-only calls take the single-read forward kernel in clusters of at
 // most kForwardMaxCluster CTAs (130 or more SMs on this GPU); a row that needs
 // larger clusters (V = 262144: 16 CTAs, 112 SMs) takes the streaming kernels,
-// which use every SM (JSD: 10.7 ms two-pass against 12.4 single-read for
-// 32768 rows). At V = 151936 the JSD forward takes 1.49 ms single-read against
+// which use every SM (JSD: 10.7 ms two-pass against 12.1 single-read for
+// 32768 rows). At V = 151936 the JSD forward takes 1.43 ms single-read against
 // 1.69 two-pass for 8191 rows. The KL forward has a one-read streaming kernel
-// of its own, faster above kKlFusedMaxVocab (V = 151936: 1.35 against 1.46
-// ms; V = 16032: 0.155 single-read against 0.18).
+// of its own, as fast on long rows (V = 151936: 1.355 against 1.361 ms) and
+// slower on short ones (V = 16032: 0.18 against 0.149 single-read), hence
+// kKlFusedMaxVocab.
 constexpr int kForwardMaxCluster = 10;
 constexpr int64_t kKlFusedMaxVocab = 32768;
 
