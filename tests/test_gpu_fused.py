@@ -266,6 +266,39 @@ def test_fused_size_limit(B):
         assert_grad(to64(dt), rdt, f"V={v} dT", torch.bfloat16)
 
 
+@pytest.mark.parametrize("v", [8, 16, 24])
+def test_forward_kernel_tiny_vocabularies(B, v):
+    """The forward-only kernel with one vector per CTA slice: most lanes of
+    its single worker warp are past the slice end."""
+    g = torch.Generator(device="cpu").manual_seed(v + 100)
+    s = (torch.randn(40, v, generator=g) * 3).to(torch.bfloat16).cuda()
+    t = (torch.randn(40, v, generator=g) * 3).to(torch.bfloat16).cuda()
+    for beta in (0.5, 0.0, 1.0):
+        loss, _, _, _, launches = fused_call(B, s, t, beta, None, torch.bfloat16, want_s=False, want_t=False)
+        assert launches == 1
+        rl = O.jsd(to64(s), to64(t), beta, grad=False, threads=4)[0]
+        assert_loss(to64(loss), rl, f"forward V={v} beta={beta}")
+
+
+def test_forward_size_limit(B):
+    """vpd_jsd_fwd: the widest row the forward-only kernel takes in clusters of
+    at most 10 CTAs (three stages of 4 x 19104 bytes plus the tail fill the
+    232448 bytes of shared memory a CTA can have) is one launch; one vector
+    more takes the two streaming passes."""
+    for v, fused in ((191040, True), (191048, False)):
+        g = torch.Generator(device="cpu").manual_seed(v % 1000)
+        s0 = torch.randn(6, v, generator=g) * 4
+        s = s0.to(torch.bfloat16).cuda()
+        t = (s0 + torch.randn(6, v, generator=g) * 2).to(torch.bfloat16).cuda()
+        n = s.shape[0]
+        loss = torch.empty(n, device="cuda")
+        saved = torch.empty(n, 6, device="cuda")
+        k = launches_of(B, lambda: B.vpd_jsd_fwd(s, t, 0.5, None, loss, saved))
+        assert (k == 1) == fused, f"V={v}: {k} launches"
+        rl = O.jsd(to64(s), to64(t), 0.5, grad=False, threads=8)[0]
+        assert_loss(to64(loss), rl, f"V={v} forward loss")
+
+
 @pytest.mark.parametrize("v", [16032, 151936])
 def test_forward_calls_through_single_read(B, v):
     """vpd_jsd_fwd takes the single-read forward kernel (one launch) at both
