@@ -24,6 +24,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -177,12 +178,20 @@ def measured_peak():
 FUSED_SOURCES = ("vpd_fused.cuh", "vpd_fused_bf16.cu", "vpd_fused_f16.cu", "vpd_fused.cu", "vpd_device.cuh", "vpd_packed.cuh")
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and with whitespace runs collapsed, so that
+    the hash follows the code and not its comments."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def fused_source_hash() -> str:
-    """Hash of the sources the single-read kernel is built from."""
+    """Hash of the code of the sources the single-read kernels are built from."""
     h = hashlib.sha256()
     for name in FUSED_SOURCES:
-        with open(os.path.join(ROOT, "softmax_divergence_lm_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "softmax_divergence_lm_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,6 +1,8 @@
-// vpd_fused.cuh -- device code of the single-read fused JSD forward+backward
-// on thread-block clusters (instantiated per input dtype in
-// vpd_fused_bf16.cu / vpd_fused_f16.cu; host dispatch in vpd_fused.cu).
+// vpd_fused.cuh -- device code of the single-read fused JSD on thread-block
+// clusters: the forward+backward kernel (k_jsd_fused) and, for calls that
+// want no gradient, the forward-only kernel (k_jsd_fused_fwd, further below);
+// instantiated per input dtype in vpd_fused_bf16.cu / vpd_fused_f16.cu, host
+// dispatch in vpd_fused.cu.
 //
 // Source: DeepSpeed pull request #8958, "[VocabTP] Add vocabulary-parallel
 // generalized JSD with Triton kernels": the op (section Changes: paired softmax
