@@ -171,6 +171,20 @@ def test_fused_many_rows_at_cluster_width(B):
     check(B, s, t, 0.5, torch.bfloat16, rows=rows, label="240 rows")
 
 
+def test_forward_kernel_many_rows_at_cluster_width(B):
+    """The forward-only kernel on 240 rows at the Qwen vocabulary (clusters of
+    9 CTAs, 23 workers x R = 3): its stages and slot rings wrap many times."""
+    s, t = make_rows(240, 151936, torch.bfloat16, seed=17)
+    for beta in (0.5, 1.0):
+        loss, saved, _, _, launches = fused_call(B, s, t, beta, None, torch.bfloat16, want_s=False, want_t=False)
+        assert launches == 1
+        rl, ra, rb, _, _ = O.jsd(to64(s), to64(t), beta, grad=False, threads=8)
+        assert_loss(to64(loss), rl, f"forward 240 rows beta={beta}")
+        if beta == 0.5:
+            live = np.isfinite(rl)
+            assert_loss(to64(saved)[live, 4], ra[live], "forward 240 rows saved KL(P_t||M)")
+
+
 def test_fused_equals_streaming_path(B):
     """The fused single-read call and the two-pass forward + backward agree."""
     s, t = make_rows(32, 151936, torch.bfloat16, seed=7)
