@@ -136,6 +136,9 @@ typedef struct {
  * paired-statistics kernel merges per-segment (max,
  * sum-exp) of both inputs, then a divergence kernel reduces the two
  * KL-to-mixture expectations together ([JSD page], "Changes").
+ * On the single-read path a bf16 row whose largest finite logit exceeds 2^126
+ * is out of contract and comes back NaN (the streaming path and the oracle give
+ * a finite value there); the limit keeps every clamped log-difference finite.
  * loss:  device float[N], the per-token divergence.
  * saved: device float[N, 6] (see above), required: it carries the statistics
  *        to the backward (and between the two streaming kernels). */
@@ -178,8 +181,9 @@ vpd_status vpd_jsd_fwdbwd(const vpd_view *s, const vpd_view *t, double beta,
  * (the teacher is the target), reverse = 1 gives KL(P_s || P_t). The forward
  * reads the inputs once: one online pass (running maxima with rescaled sums),
  * or for short rows (V <= 32768) under the conditions of vpd_jsd_fwdbwd the
- * forward-only cluster kernel's KL branch. saved may be NULL. Saved layout and
- * backward are those of the JSD beta = 0 / 1 branches.
+ * forward-only cluster kernel's KL branch (where, as in vpd_jsd_fwd, a bf16 row
+ * whose largest finite logit exceeds 2^126 comes back NaN). saved may be NULL.
+ * Saved layout and backward are those of the JSD beta = 0 / 1 branches.
  * ------------------------------------------------------------------------- */
 vpd_status vpd_kl_fwd(const vpd_view *s, const vpd_view *t, int32_t reverse,
                       const vpd_segments *seg, float *loss, float *saved, void *stream);
@@ -243,8 +247,11 @@ uint64_t vpd_launch_count(void);
  * negative row clears the hook. Returns VPD_OK. */
 vpd_status vpd_test_withhold_copy(int64_t row);
 /* Synchronises `stream`, then reads and clears the device error word that the
- * library's kernels set when a bounded wait gives up. Returns VPD_OK, or
- * VPD_ERR_TIMEOUT with the failure described in vpd_last_error(). */
+ * library's kernels set when a bounded wait gives up. The read and the clear
+ * are one atomic exchange on the device, ordered on `stream`, so a failure that
+ * a kernel on another stream records meanwhile is reported by this call or the
+ * next, never lost. Returns VPD_OK, or VPD_ERR_TIMEOUT with the failure
+ * described in vpd_last_error(). */
 vpd_status vpd_device_status(void *stream);
 
 #ifdef __cplusplus

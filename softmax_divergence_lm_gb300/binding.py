@@ -124,11 +124,24 @@ def _check(status: int):
 # ---------------------------------------------------------------------------
 # Marshalling.
 # ---------------------------------------------------------------------------
+def _on_current_device(x: torch.Tensor, what: str):
+    """The library launches on the current CUDA device: every tensor it is
+    given must live there (a pointer into another GPU's memory would be read
+    by kernels of this one)."""
+    if not x.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if x.device.index != torch.cuda.current_device():
+        raise ValueError(f"{what} is on {x.device}, the current device is cuda:{torch.cuda.current_device()}")
+
+
+def _rows_vocab(view: vpd_view) -> tuple[int, int]:
+    return int(view.rows), int(view.vocab)
+
+
 def make_view(x: torch.Tensor) -> vpd_view:
     if x.dtype not in _DTYPES:
         raise TypeError(f"logits dtype {x.dtype} is not float32/bfloat16/float16")
-    if not x.is_cuda:
-        raise ValueError("logits must be CUDA tensors")
+    _on_current_device(x, "logits")
     if x.dim() == 2:
         n, v = x.shape
         if v > 1 and x.stride(1) != 1:
@@ -143,17 +156,21 @@ def make_view(x: torch.Tensor) -> vpd_view:
     raise ValueError("logits must be [N, V] or [B, T, V]")
 
 
-def make_grad(g: torch.Tensor | None) -> vpd_grad | None:
+def make_grad(g: torch.Tensor | None, rows: int | None = None, vocab: int | None = None) -> vpd_grad | None:
+    """Gradient descriptor; with rows / vocab given, the tensor must be exactly
+    [rows, vocab] (after flattening [B, T, V]), so that no row the kernels
+    write lies past its allocation."""
     if g is None:
         return None
     if g.dtype not in _DTYPES:
         raise TypeError(f"gradient dtype {g.dtype} is not float32/bfloat16/float16")
-    if not g.is_cuda:
-        raise ValueError("gradients must be CUDA tensors")
+    _on_current_device(g, "gradient")
     if g.dim() == 3:
         g = g.view(-1, g.shape[-1])
     if g.dim() != 2 or (g.shape[1] > 1 and g.stride(1) != 1):
         raise ValueError("gradient must be a dense [N, V] (or [B, T, V]) tensor with unit vocab stride")
+    if rows is not None and (g.shape[0] != rows or g.shape[1] != vocab):
+        raise ValueError(f"gradient shape {tuple(g.shape)} does not match the logits [{rows}, {vocab}]")
     return vpd_grad(g.data_ptr(), _DTYPES[g.dtype], g.stride(0) if g.shape[0] > 1 else g.shape[1])
 
 
@@ -164,17 +181,25 @@ def make_segments(widths) -> tuple[vpd_segments | None, object]:
     return vpd_segments(len(widths), arr), arr  # keep arr alive alongside
 
 
-def _fptr(t: torch.Tensor | None):
+def _fptr(t: torch.Tensor | None, numel: int | None = None, what: str = "per-row buffer"):
+    """Device pointer of a contiguous float32 buffer of exactly `numel`
+    elements (when given)."""
     if t is None:
         return None
-    if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
-        raise ValueError("float32 per-row buffers must be contiguous CUDA tensors")
+    if t.dtype != torch.float32 or not t.is_contiguous():
+        raise ValueError(f"{what} must be a contiguous float32 CUDA tensor")
+    _on_current_device(t, what)
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{what} has {t.numel()} elements, {numel} expected")
     return t.data_ptr()
 
 
 def _stream(stream) -> int | None:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
+    dev = getattr(stream, "device", None)
+    if dev is not None and getattr(dev, "index", None) is not None and dev.index != torch.cuda.current_device():
+        raise ValueError(f"stream is on {dev}, the current device is cuda:{torch.cuda.current_device()}")
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
 
 
@@ -183,64 +208,82 @@ def _ref(x):
 
 
 # ---------------------------------------------------------------------------
-# Entry points (same names and argument order as include/vpd.h).
+# Entry points (same names and argument order as include/vpd.h). Each checks,
+# before the call, that every buffer lives on the current device and has the
+# size the kernels will read or write for the view's N, V (and k).
 # ---------------------------------------------------------------------------
-def vpd_jsd_fwd(s, t, beta, segments, loss, saved, stream=None):
+def _pair(s, t):
     vs, vt = make_view(s), make_view(t)
+    n, v = _rows_vocab(vs)
+    if _rows_vocab(vt) != (n, v):
+        raise ValueError(f"student [{n}, {v}] and teacher {tuple(_rows_vocab(vt))} differ")
+    return vs, vt, n, v
+
+
+def vpd_jsd_fwd(s, t, beta, segments, loss, saved, stream=None):
+    vs, vt, n, _ = _pair(s, t)
     seg, _keep = make_segments(segments)
     _check(load().vpd_jsd_fwd(ctypes.byref(vs), ctypes.byref(vt), float(beta), _ref(seg),
-                              _fptr(loss), _fptr(saved), _stream(stream)))
+                              _fptr(loss, n, "loss"), _fptr(saved, n * SAVED_PAIR, "saved"), _stream(stream)))
 
 
 def vpd_jsd_bwd(s, t, beta, segments, grad_loss, saved, ds, dt, stream=None):
-    vs, vt = make_view(s), make_view(t)
+    vs, vt, n, v = _pair(s, t)
     seg, _keep = make_segments(segments)
-    gs, gt = make_grad(ds), make_grad(dt)
+    gs, gt = make_grad(ds, n, v), make_grad(dt, n, v)
     _check(load().vpd_jsd_bwd(ctypes.byref(vs), ctypes.byref(vt), float(beta), _ref(seg),
-                              _fptr(grad_loss), _fptr(saved), _ref(gs), _ref(gt), _stream(stream)))
+                              _fptr(grad_loss, n, "grad_loss"), _fptr(saved, n * SAVED_PAIR, "saved"),
+                              _ref(gs), _ref(gt), _stream(stream)))
 
 
 def vpd_jsd_fwdbwd(s, t, beta, segments, grad_loss, loss, saved, ds, dt, stream=None):
-    vs, vt = make_view(s), make_view(t)
+    vs, vt, n, v = _pair(s, t)
     seg, _keep = make_segments(segments)
-    gs, gt = make_grad(ds), make_grad(dt)
+    gs, gt = make_grad(ds, n, v), make_grad(dt, n, v)
     _check(load().vpd_jsd_fwdbwd(ctypes.byref(vs), ctypes.byref(vt), float(beta), _ref(seg),
-                                 _fptr(grad_loss), _fptr(loss), _fptr(saved), _ref(gs), _ref(gt),
-                                 _stream(stream)))
+                                 _fptr(grad_loss, n, "grad_loss"), _fptr(loss, n, "loss"),
+                                 _fptr(saved, n * SAVED_PAIR, "saved"), _ref(gs), _ref(gt), _stream(stream)))
 
 
 def vpd_kl_fwd(s, t, reverse, segments, loss, saved, stream=None):
-    vs, vt = make_view(s), make_view(t)
+    vs, vt, n, _ = _pair(s, t)
     seg, _keep = make_segments(segments)
     _check(load().vpd_kl_fwd(ctypes.byref(vs), ctypes.byref(vt), int(bool(reverse)), _ref(seg),
-                             _fptr(loss), _fptr(saved), _stream(stream)))
+                             _fptr(loss, n, "loss"), _fptr(saved, n * SAVED_PAIR, "saved"), _stream(stream)))
 
 
 def vpd_kl_bwd(s, t, reverse, segments, grad_loss, saved, ds, dt, stream=None):
-    vs, vt = make_view(s), make_view(t)
+    vs, vt, n, v = _pair(s, t)
     seg, _keep = make_segments(segments)
-    gs, gt = make_grad(ds), make_grad(dt)
+    gs, gt = make_grad(ds, n, v), make_grad(dt, n, v)
     _check(load().vpd_kl_bwd(ctypes.byref(vs), ctypes.byref(vt), int(bool(reverse)), _ref(seg),
-                             _fptr(grad_loss), _fptr(saved), _ref(gs), _ref(gt), _stream(stream)))
+                             _fptr(grad_loss, n, "grad_loss"), _fptr(saved, n * SAVED_PAIR, "saved"),
+                             _ref(gs), _ref(gt), _stream(stream)))
 
 
 def vpd_entropy_fwd(x, segments, out, saved, stream=None):
     vx = make_view(x)
+    n, _ = _rows_vocab(vx)
     seg, _keep = make_segments(segments)
-    _check(load().vpd_entropy_fwd(ctypes.byref(vx), _ref(seg), _fptr(out), _fptr(saved), _stream(stream)))
+    _check(load().vpd_entropy_fwd(ctypes.byref(vx), _ref(seg), _fptr(out, n, "out"),
+                                  _fptr(saved, n * SAVED_ENTROPY, "saved"), _stream(stream)))
 
 
 def vpd_entropy_bwd(x, segments, grad_out, saved, dx, stream=None):
     vx = make_view(x)
+    n, v = _rows_vocab(vx)
     seg, _keep = make_segments(segments)
-    gx = make_grad(dx)
-    _check(load().vpd_entropy_bwd(ctypes.byref(vx), _ref(seg), _fptr(grad_out), _fptr(saved), _ref(gx),
-                                  _stream(stream)))
+    gx = make_grad(dx, n, v)
+    _check(load().vpd_entropy_bwd(ctypes.byref(vx), _ref(seg), _fptr(grad_out, n, "grad_out"),
+                                  _fptr(saved, n * SAVED_ENTROPY, "saved"), _ref(gx), _stream(stream)))
 
 
-def _index_ptr(index: torch.Tensor):
-    if index.dtype != torch.int64 or not index.is_cuda or not index.is_contiguous():
+def _index_ptr(index: torch.Tensor, numel: int):
+    if index.dtype != torch.int64 or not index.is_contiguous():
         raise ValueError("index must be a contiguous int64 CUDA tensor")
+    _on_current_device(index, "index")
+    if index.numel() != numel:
+        raise ValueError(f"index has {index.numel()} elements, {numel} expected")
     return index.data_ptr()
 
 
@@ -248,20 +291,26 @@ def vpd_logprobs_fwd(x, segments, index, k, ignore_index, out, saved, err_flag, 
     """err_flag: int32 CUDA tensor, or None (the library then checks the
     indices on the host and raises VPD_ERR_INDEX before launching)."""
     vx = make_view(x)
+    n, _ = _rows_vocab(vx)
     seg, _keep = make_segments(segments)
-    if err_flag is not None and (err_flag.dtype != torch.int32 or not err_flag.is_cuda):
-        raise ValueError("err_flag must be an int32 CUDA tensor or None")
-    _check(load().vpd_logprobs_fwd(ctypes.byref(vx), _ref(seg), _index_ptr(index), int(k), int(ignore_index),
-                                   _fptr(out), _fptr(saved), err_flag.data_ptr() if err_flag is not None else None,
-                                   _stream(stream)))
+    if err_flag is not None:
+        if err_flag.dtype != torch.int32 or err_flag.numel() < 1:
+            raise ValueError("err_flag must be an int32 CUDA tensor of at least one element, or None")
+        _on_current_device(err_flag, "err_flag")
+    _check(load().vpd_logprobs_fwd(ctypes.byref(vx), _ref(seg), _index_ptr(index, n * int(k)), int(k),
+                                   int(ignore_index), _fptr(out, n * int(k), "out"),
+                                   _fptr(saved, n * SAVED_LOGPROBS, "saved"),
+                                   err_flag.data_ptr() if err_flag is not None else None, _stream(stream)))
 
 
 def vpd_logprobs_bwd(x, segments, index, k, ignore_index, grad_out, saved, dx, stream=None):
     vx = make_view(x)
+    n, v = _rows_vocab(vx)
     seg, _keep = make_segments(segments)
-    gx = make_grad(dx)
-    _check(load().vpd_logprobs_bwd(ctypes.byref(vx), _ref(seg), _index_ptr(index), int(k), int(ignore_index),
-                                   _fptr(grad_out), _fptr(saved), _ref(gx), _stream(stream)))
+    gx = make_grad(dx, n, v)
+    _check(load().vpd_logprobs_bwd(ctypes.byref(vx), _ref(seg), _index_ptr(index, n * int(k)), int(k),
+                                   int(ignore_index), _fptr(grad_out, n * int(k), "grad_out"),
+                                   _fptr(saved, n * SAVED_LOGPROBS, "saved"), _ref(gx), _stream(stream)))
 
 
 def vpd_device_status(stream=None):

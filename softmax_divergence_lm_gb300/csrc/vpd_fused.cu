@@ -19,17 +19,17 @@ namespace fused {
 extern template cudaError_t launch_typed<InBF16>(const FusedArgs&, const Config&, int, bool, bool, cudaStream_t, int*);
 extern template cudaError_t launch_typed<InF16>(const FusedArgs&, const Config&, int, bool, bool, cudaStream_t, int*);
 extern template int resident_clusters<InBF16>(int, int, size_t);
-cudaError_t take_error_bf16(int* code);
-cudaError_t take_error_f16(int* code);
+cudaError_t take_error_bf16(cudaStream_t stream, int* code);
+cudaError_t take_error_f16(cudaStream_t stream, int* code);
 }  // namespace fused
 
 cudaError_t take_device_error(cudaStream_t stream, int* code) {
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return e;
   int a = 0, b = 0;
-  e = fused::take_error_bf16(&a);
+  e = fused::take_error_bf16(stream, &a);
   if (e != cudaSuccess) return e;
-  e = fused::take_error_f16(&b);
+  e = fused::take_error_f16(stream, &b);
   *code = a | b;
   return e;
 }

@@ -94,6 +94,22 @@ static_assert(Cols<kInterior>::k * 4 <= tmem_cols_per_warp(max_workers(4)), "TME
 // Set by a kernel of this translation unit whose bounded wait gave up (each
 // translation unit that includes this header has its own word).
 static __device__ int g_fused_error = 0;
+// The value g_fused_error held when k_take_error last swapped it for 0.
+static __device__ int g_fused_taken = 0;
+
+// Reads and clears the error word in one atomic step, so that a failure
+// recorded by a kernel on another stream in between is never lost.
+static __global__ void k_take_error() { g_fused_taken = atomicExch(&g_fused_error, 0); }
+
+// Host side: the word's value (0 if no wait gave up), cleared, in stream order.
+static inline cudaError_t take_error_local(cudaStream_t stream, int* code) {
+  k_take_error<<<1, 1, 0, stream>>>();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbolAsync(code, g_fused_taken, sizeof(int), 0, cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(stream);
+}
 
 // ---------------------------------------------------------------------------
 // PTX wrappers

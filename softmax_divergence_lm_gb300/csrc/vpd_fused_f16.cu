@@ -8,14 +8,7 @@ namespace fused {
 template cudaError_t launch_typed<InF16>(const FusedArgs&, const Config&, int, bool, bool, cudaStream_t, int*);
 template int resident_clusters<InF16>(int, int, size_t);
 
-cudaError_t take_error_f16(int* code) {
-  cudaError_t e = cudaMemcpyFromSymbol(code, g_fused_error, sizeof(int));
-  if (e == cudaSuccess && *code) {
-    const int zero = 0;
-    e = cudaMemcpyToSymbol(g_fused_error, &zero, sizeof(int));
-  }
-  return e;
-}
+cudaError_t take_error_f16(cudaStream_t stream, int* code) { return take_error_local(stream, code); }
 
 }  // namespace fused
 }  // namespace vpd

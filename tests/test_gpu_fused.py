@@ -338,3 +338,40 @@ def test_forward_calls_through_single_read(B, v):
         torch.cuda.synchronize()
         rk, _, _, _, _ = O.jsd(to64(s), to64(t), float(rev), None, grad=False, threads=8)
         assert_loss(to64(kl), rk, f"V={v} KL reverse={rev}")
+
+
+def test_bf16_row_max_above_2_126(B):
+    """A bf16 row whose largest finite logit exceeds 2^126 is out of contract
+    on the single-read kernels: NaN with zero gradients (the limit keeps every
+    clamped log-difference finite). The streaming kernels, reached here through
+    a two-segment call, and the oracle give the finite value."""
+    v = 4096
+    g0 = torch.Generator(device="cpu").manual_seed(21)
+    s = torch.randn(4, v, generator=g0) * 3
+    t = s + torch.randn(4, v, generator=g0)
+    s[0, 5] = 2.0**127
+    t[1, 9] = 2.0**127
+    s, t = s.to(torch.bfloat16).cuda(), t.to(torch.bfloat16).cuda()
+    g = torch.ones(4, device="cuda")
+    for beta in (0.5, 0.0):
+        loss, _, ds, dt, launches = fused_call(B, s, t, beta, g, torch.float32)
+        assert launches == 1
+        lo = to64(loss)
+        assert np.all(np.isnan(lo[:2])) and np.all(np.isfinite(lo[2:]))
+        assert_zero_rows(to64(ds), [0, 1], "2^127 row dS")
+        assert_zero_rows(to64(dt), [0, 1], "2^127 row dT")
+        rl, _, _, rds, rdt = O.jsd(to64(s), to64(t), beta, to64(g), threads=4)
+        assert_loss(lo[2:], rl[2:], f"beta={beta} in-contract rows")
+        fwd = torch.empty(4, device="cuda")
+        k = launches_of(B, lambda: B.vpd_jsd_fwd(s, t, beta, None, fwd, torch.empty(4, 6, device="cuda")))
+        assert k == 1 and np.all(np.isnan(to64(fwd)[:2]))
+        # two segments: the streaming kernels, finite and equal to the oracle
+        ls = torch.empty(4, device="cuda")
+        sv = torch.empty(4, 6, device="cuda")
+        ds2 = torch.empty(4, v, device="cuda")
+        dt2 = torch.empty(4, v, device="cuda")
+        B.vpd_jsd_fwdbwd(s, t, beta, [v // 2, v - v // 2], g, ls, sv, ds2, dt2)
+        torch.cuda.synchronize()
+        assert_loss(to64(ls), rl, f"beta={beta} streaming loss")
+        assert_grad(to64(ds2), rds, f"beta={beta} streaming dS")
+        assert_grad(to64(dt2), rdt, f"beta={beta} streaming dT")

@@ -356,6 +356,9 @@ def test_qwen_vocab_workload(B):
     check_pair(B, flat_s[:-1], flat_t[:-1], 0.5, rows=rows, gdtype=torch.bfloat16, fused=True,
                label="qwen rows")
     check_pair(B, flat_s[:-1], flat_t[:-1], 0.5, rows=rows, want_t=False, fused=True, label="qwen detached")
+    # float32 gradients pin the on-chip gradient arithmetic at the stated
+    # tolerance, without the rounding of a 16-bit store
+    check_pair(B, flat_s[:-1], flat_t[:-1], 0.5, rows=rows, fused=True, label="qwen fp32 grads")
     check_pair(B, flat_s[:-1], flat_t[:-1], 0.5, rows=rows, label="qwen two-pass")
     # (ii) the causal-shift view [4, 2047, V]
     cs, ct = s3[:, :-1], t3[:, :-1]
@@ -392,14 +395,21 @@ def test_large_sweep_workload(B, dtype):
     n, v = s.shape
     rows = _sample(n, count=8)
     check_pair(B, s, t, 0.5, rows=rows, gdtype=dtype, fused=True, label="sweep fused")
+    check_pair(B, s, t, 0.5, rows=rows, fused=True, label="sweep fused fp32 grads")
     check_pair(B, s, t, 0.5, rows=rows, gdtype=dtype, label="sweep two-pass")
     check_pair(B, s, t, None, op="kl-fwd", rows=rows, gdtype=dtype, label="sweep")
     out = torch.empty(n, device="cuda")
     saved = torch.empty(n, 3, device="cuda")
+    dx = torch.empty(n, v, dtype=dtype, device="cuda")
+    gen = torch.Generator(device="cpu").manual_seed(9)
+    g = torch.randn(n, generator=gen).cuda()
     B.vpd_entropy_fwd(s, None, out, saved)
+    B.vpd_entropy_bwd(s, None, g, saved, dx)
     torch.cuda.synchronize()
     r = torch.as_tensor(rows, device="cuda")
-    ro, _ = O.entropy(to64(s[r]), grad=False, threads=8)
+    ro, rdx = O.entropy(to64(s[r]), to64(g)[rows], threads=8)
     assert_loss(to64(out)[rows], ro, "sweep entropy")
+    assert_grad(to64(dx[r]), rdx, "sweep entropy grad", dtype)
+    del dx
     del s, t
     torch.cuda.empty_cache()
