@@ -425,4 +425,106 @@ def pin_torch_fp64_autograd():
         _close(dt, tt.grad.numpy(), 1e-10, 1e-14, f"torch dt {beta}")
 
 
+# ---------------------------------------------------------------------------
+# Compositions: fused-linear JSD, cross-entropy, teacher top-k forward KL.
+# ---------------------------------------------------------------------------
+def pin_linear_logits_brute_force():
+    """The logits step of the fused-linear oracle against explicit loops over
+    the hidden dimension (pins which operand is transposed)."""
+    rng = np.random.default_rng(31)
+    n, v, hs, ht = 2, 5, 3, 4
+    h_s, w_s = rng.normal(size=(n, hs)), rng.normal(size=(v, hs))
+    h_t, w_t = rng.normal(size=(n, ht)), rng.normal(size=(v, ht))
+    s = np.array([[sum(h_s[r, k] * w_s[j, k] for k in range(hs)) for j in range(v)] for r in range(n)])
+    t = np.array([[sum(h_t[r, k] * w_t[j, k] for k in range(ht)) for j in range(v)] for r in range(n)])
+    for beta in (0.0, 0.4, 1.0):
+        lin = O.jsd_linear(h_s, w_s, h_t, w_t, beta, grad=False)[0]
+        _close(lin, O.jsd(s, t, beta, grad=False)[0], 1e-13, 1e-15, f"linear logits beta={beta}")
+
+
+def pin_linear_finite_differences():
+    """Central differences of the fused-linear loss with respect to every entry
+    of both hidden-state matrices and both head weights."""
+    rng = np.random.default_rng(32)
+    n, v, hs, ht = 3, 6, 4, 3
+    h_s, w_s = rng.normal(size=(n, hs)), rng.normal(0, 0.8, (v, hs))
+    h_t, w_t = rng.normal(size=(n, ht)), rng.normal(0, 0.8, (v, ht))
+    g = rng.normal(size=n)
+    for beta in (0.3, 0.0, 1.0):
+        _, _, _, dhs, dws, dht, dwt = O.jsd_linear(h_s, w_s, h_t, w_t, beta, g)
+        f = lambda a, b, c, d: float(np.dot(g, O.jsd_linear(a, b, c, d, beta, grad=False)[0]))  # noqa: E731
+        _fd_check(lambda x: f(x, w_s, h_t, w_t), h_s, dhs, f"linear dh_s {beta}")
+        _fd_check(lambda x: f(h_s, x, h_t, w_t), w_s, dws, f"linear dw_s {beta}")
+        _fd_check(lambda x: f(h_s, w_s, x, w_t), h_t, dht, f"linear dh_t {beta}")
+        _fd_check(lambda x: f(h_s, w_s, h_t, x), w_t, dwt, f"linear dw_t {beta}")
+
+
+def pin_linear_identical_heads():
+    """Identical student and teacher heads and hidden states: JSD 0 and every
+    gradient 0 (the JSD of a distribution with itself)."""
+    rng = np.random.default_rng(33)
+    h, w = rng.normal(size=(4, 6)), rng.normal(size=(9, 6))
+    loss, _, _, dhs, dws, dht, dwt = O.jsd_linear(h, w, h, w, 0.5, rng.normal(size=4))
+    assert np.all(np.abs(loss) < 1e-15)
+    for d in (dhs, dws, dht, dwt):
+        assert np.all(np.abs(d) < 1e-14)
+
+
+def pin_cross_entropy():
+    """Cross-entropy: ln V on equal logits; -log_softmax(x / T) at the label
+    from SciPy; 0 and no gradient at ignore_index; central differences."""
+    rng = np.random.default_rng(34)
+    x = rng.normal(0, 2, (5, 11))
+    x[1, 3] = -np.inf
+    labels = np.array([2, 4, -100, 10, 0])
+    for temp in (1.0, 1.7):
+        loss, dx, errs = O.cross_entropy(x, labels, -100, temp)
+        assert errs == 0
+        ref = -special.log_softmax(x / temp, axis=1)[np.arange(5), np.where(labels < 0, 0, labels)]
+        ref[2] = 0.0
+        _close(loss, ref, 1e-13, 1e-15, f"ce T={temp}")
+        assert np.all(dx[2] == 0.0)
+        g = rng.normal(size=5)
+        _, dxg, _ = O.cross_entropy(x, labels, -100, temp, g)
+        _fd_check(lambda y: float(np.dot(g, O.cross_entropy(y, labels, -100, temp, grad=False)[0])), x, dxg,
+                  f"ce fd T={temp}")
+    flat = np.zeros((2, 13))
+    _close(O.cross_entropy(flat, [0, 12])[0], [math.log(13)] * 2, 1e-15, 0, "ce uniform")
+
+
+def pin_topk_kl_full_vocabulary():
+    """With every id selected (k = V) and the teacher's full log-softmax, the
+    top-k forward KL is the full forward KL(P_t || P_s), value and student
+    gradient, from the KL row oracle."""
+    rng = np.random.default_rng(35)
+    s = rng.normal(0, 2, (4, 9))
+    t = rng.normal(0, 2, (4, 9))
+    g = rng.normal(size=4)
+    ids = np.tile(np.arange(9), (4, 1))
+    tl = special.log_softmax(t, axis=1)
+    kl, ds, errs = O.topk_forward_kl(s, ids, tl, -100, 1.0, g)
+    assert errs == 0
+    ref, rds, _ = O.kl(s, t, False, g)
+    _close(kl, ref, 1e-12, 1e-14, "top-k = full KL")
+    _close(ds, rds, 1e-11, 1e-14, "top-k = full KL, student gradient")
+
+
+def pin_topk_kl_finite_differences_and_classes():
+    """Central differences of the top-k forward KL (temperature 1.5, an ignored
+    position, a duplicate id); +inf with zero gradient when the student masks
+    an id the teacher gives mass."""
+    rng = np.random.default_rng(36)
+    s = rng.normal(0, 2, (3, 8))
+    ids = np.array([[1, 5, 5], [0, -100, 7], [2, 3, 4]])
+    tl = np.log(np.array([[0.5, 0.2, 0.1], [0.4, 0.3, 0.2], [0.6, 0.2, 0.1]]))
+    g = rng.normal(size=3)
+    _, ds, _ = O.topk_forward_kl(s, ids, tl, -100, 1.5, g)
+    _fd_check(lambda y: float(np.dot(g, O.topk_forward_kl(y, ids, tl, -100, 1.5, grad=False)[0])), s, ds,
+              "top-k kl fd")
+    sm = s.copy()
+    sm[2, 3] = -np.inf
+    kl, dsm, _ = O.topk_forward_kl(sm, ids, tl, -100, 1.0, g)
+    assert np.isposinf(kl[2]) and np.all(dsm[2] == 0.0) and np.all(np.isfinite(kl[:2]))
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_") and callable(v)]

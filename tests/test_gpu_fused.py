@@ -344,7 +344,11 @@ def test_bf16_row_max_above_2_126(B):
     """A bf16 row whose largest finite logit exceeds 2^126 is out of contract
     on the single-read kernels: NaN with zero gradients (the limit keeps every
     clamped log-difference finite). The streaming kernels, reached here through
-    a two-segment call, and the oracle give the finite value."""
+    a two-segment call, and the oracle give the finite value. At beta = 0 the
+    teacher gradient of such a row is a difference of two log-ratios near
+    2^127 that fp32 cannot resolve (the same floor as for near one-hot rows),
+    so there only the loss and the student gradient of those rows are
+    compared."""
     v = 4096
     g0 = torch.Generator(device="cpu").manual_seed(21)
     s = torch.randn(4, v, generator=g0) * 3
@@ -374,4 +378,5 @@ def test_bf16_row_max_above_2_126(B):
         torch.cuda.synchronize()
         assert_loss(to64(ls), rl, f"beta={beta} streaming loss")
         assert_grad(to64(ds2), rds, f"beta={beta} streaming dS")
-        assert_grad(to64(dt2), rdt, f"beta={beta} streaming dT")
+        keep = slice(None) if beta > 0.0 else slice(2, None)
+        assert_grad(to64(dt2)[keep], rdt[keep], f"beta={beta} streaming dT")

@@ -52,3 +52,38 @@ def test_planted_mistake_is_caught(name, tmp_path, monkeypatch):
         except (AssertionError, ValueError, FloatingPointError):
             failed.append(pin.__name__)
     assert failed, f"no pin caught the planted mistake '{name}'"
+
+
+# Planted mistakes in the Python compositions of the oracle (fused-linear JSD,
+# cross-entropy, teacher top-k forward KL): the function is re-created from its
+# own source with one edit and swapped in for the duration of the test.
+PY_MUTANTS = {
+    "linear: teacher gradient used for the student head": ("jsd_linear", "ds.T @ h_s", "dt.T @ h_s"),
+    "linear: student head used for the teacher logits": ("jsd_linear", "t = h_t @ w_t.T", "t = h_t @ w_t.T + s * 0.01"),
+    "cross-entropy: temperature multiplies the gradient": ("cross_entropy", "dx = dx / float(temperature)",
+                                                            "dx = dx * float(temperature)"),
+    "cross-entropy: sign": ("cross_entropy", "loss = -out[:, 0]", "loss = out[:, 0]"),
+    "top-k KL: log-probs used as weights": ("topk_forward_kl", "np.exp(np.where(live, tl, 0.0))",
+                                            "np.where(live, tl, 0.0)"),
+    "top-k KL: temperature ignored": ("topk_forward_kl", "logprobs(s / float(temperature)", "logprobs(s"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_planted_composition_mistake_is_caught(name, monkeypatch):
+    import inspect
+    import textwrap
+
+    fn_name, old, new = PY_MUTANTS[name]
+    src = textwrap.dedent(inspect.getsource(getattr(O, fn_name)))
+    assert src.count(old) == 1, f"mutation site for '{name}' must be unique"
+    namespace = dict(vars(O))
+    exec(compile(src.replace(old, new), f"<mutant {fn_name}>", "exec"), namespace)
+    monkeypatch.setattr(O, fn_name, namespace[fn_name])
+    failed = []
+    for pin in oracle_pins.PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, FloatingPointError):
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught the planted mistake '{name}'"
