@@ -227,6 +227,62 @@ vpd_status vpd_logprobs_bwd(const vpd_view *x, const vpd_segments *seg, const in
                             const float *saved, const vpd_grad *dx, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * Fused-linear generalized JSD ([JSD page], "Scope and limitations" and [ops
+ * page], "Limitations": the fused-linear divergence the pages leave for later).
+ * The logits of two linear heads, s = h_s w_s^T and t = h_t w_t^T, are formed
+ * tile by tile on the tensor cores and consumed on chip: the [N, V] logits are
+ * never written to memory. The divergence, its beta = 0 / 1 branches, the
+ * saved [N, 6] statistics and the special values are those of vpd_jsd_fwd /
+ * vpd_jsd_bwd applied to s and t, where the logits are the fp32 sums of the
+ * exact bf16 products.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    const void *h_s;   /* device bf16 [rows, hidden_s] student hidden states, row stride ld_hs */
+    const void *w_s;   /* device bf16 [vocab, hidden_s] student head weight, row stride ld_ws */
+    const void *h_t;   /* device bf16 [rows, hidden_t] teacher hidden states, row stride ld_ht */
+    const void *w_t;   /* device bf16 [vocab, hidden_t] teacher head weight, row stride ld_wt */
+    int64_t rows;      /* N >= 0 */
+    int64_t vocab;     /* V >= 1, a multiple of 8 */
+    int64_t hidden_s;  /* a positive multiple of 64 */
+    int64_t hidden_t;  /* a positive multiple of 64 */
+    int64_t ld_hs, ld_ws, ld_ht, ld_wt; /* row strides in elements: >= the hidden size, multiples of 8 */
+} vpd_linear_heads;
+
+/* Workspace sizes (bytes) of vpd_jsd_linear_fwd and of vpd_jsd_linear_bwd
+ * with the given gradients wanted (nonzero flags). The backward works through
+ * the rows in chunks of 1024 and keeps, per head, that chunk's gradient of the
+ * logits split in two bf16 parts (row-major and transposed), the head weight
+ * transposed and the chunk's hidden states transposed. Either output pointer
+ * may be NULL. */
+vpd_status vpd_jsd_linear_workspace(const vpd_linear_heads *heads, int32_t student_grads,
+                                    int32_t teacher_grads, size_t *fwd_bytes, size_t *bwd_bytes);
+
+/* Forward: two passes of tensor-core tiles over the vocabulary, the first for
+ * the statistics of both heads (per-chunk (max, sum-exp) partials merged in
+ * chunk order), the second for the two KL-to-mixture sums ([JSD page],
+ * "Scope and limitations": the mixture needs global statistics).
+ * loss: device float[N]; saved: device float[N, 6] as vpd_jsd_fwd's.
+ * workspace: device memory of at least the forward size above (caller-owned,
+ * 16-byte aligned; its contents on entry do not matter). */
+vpd_status vpd_jsd_linear_fwd(const vpd_linear_heads *heads, double beta, float *loss, float *saved,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/* Backward: recomputes the logits tiles, forms dS and dT as vpd_jsd_bwd does
+ * and contracts them on the tensor cores: dh = dS w, dw = dS^T h per head. The
+ * gradient of the logits enters the contractions as a bf16 high part plus a
+ * bf16 low part (16 bits of mantissa together). Outputs are device float32,
+ * dense: dh_s [N, hidden_s], dw_s [V, hidden_s], dh_t [N, hidden_t], dw_t [V,
+ * hidden_t]; each may be NULL (not wanted; a detached teacher passes NULL for
+ * both of its own). They are overwritten (set to zero, then accumulated).
+ * grad_loss: device float[N] or NULL (ones); loss and saved: as written by
+ * vpd_jsd_linear_fwd with the same heads and beta. workspace: at least the
+ * backward size above for the gradients wanted. */
+vpd_status vpd_jsd_linear_bwd(const vpd_linear_heads *heads, double beta, const float *grad_loss,
+                              const float *loss, const float *saved, float *dh_s, float *dw_s,
+                              float *dh_t, float *dw_t, void *workspace, size_t workspace_bytes,
+                              void *stream);
+
+/* ---------------------------------------------------------------------------
  * Utilities.
  * ------------------------------------------------------------------------- */
 /* Name of a status code (static string). */

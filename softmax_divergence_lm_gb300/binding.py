@@ -32,7 +32,8 @@ _DTYPES = {torch.float32: VPD_F32, torch.bfloat16: VPD_BF16, torch.float16: VPD_
 SYMBOLS = ("vpd_jsd_fwd", "vpd_jsd_bwd", "vpd_jsd_fwdbwd", "vpd_kl_fwd", "vpd_kl_bwd",
            "vpd_entropy_fwd", "vpd_entropy_bwd", "vpd_logprobs_fwd", "vpd_logprobs_bwd",
            "vpd_status_string", "vpd_last_error", "vpd_abi_version", "vpd_device_status",
-           "vpd_launch_count", "vpd_test_withhold_copy")
+           "vpd_launch_count", "vpd_test_withhold_copy", "vpd_jsd_linear_workspace", "vpd_jsd_linear_fwd",
+           "vpd_jsd_linear_bwd")
 
 
 class VpdError(RuntimeError):
@@ -53,6 +54,13 @@ class vpd_segments(ctypes.Structure):
 
 class vpd_grad(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("row_stride", ctypes.c_int64)]
+
+
+class vpd_linear_heads(ctypes.Structure):
+    _fields_ = [("h_s", ctypes.c_void_p), ("w_s", ctypes.c_void_p), ("h_t", ctypes.c_void_p),
+                ("w_t", ctypes.c_void_p), ("rows", ctypes.c_int64), ("vocab", ctypes.c_int64),
+                ("hidden_s", ctypes.c_int64), ("hidden_t", ctypes.c_int64), ("ld_hs", ctypes.c_int64),
+                ("ld_ws", ctypes.c_int64), ("ld_ht", ctypes.c_int64), ("ld_wt", ctypes.c_int64)]
 
 
 _lock = threading.Lock()
@@ -91,6 +99,9 @@ def _declare(lib):
         "vpd_logprobs_fwd": [V, S, f, i32, i64, f, f, f, vp],
         "vpd_logprobs_bwd": [V, S, f, i32, i64, f, f, G, vp],
         "vpd_device_status": [vp],
+        "vpd_jsd_linear_workspace": [P(vpd_linear_heads), i32, i32, P(ctypes.c_size_t), P(ctypes.c_size_t)],
+        "vpd_jsd_linear_fwd": [P(vpd_linear_heads), dbl, f, f, vp, ctypes.c_size_t, vp],
+        "vpd_jsd_linear_bwd": [P(vpd_linear_heads), dbl, f, f, f, f, f, f, f, vp, ctypes.c_size_t, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -311,6 +322,61 @@ def vpd_logprobs_bwd(x, segments, index, k, ignore_index, grad_out, saved, dx, s
     _check(load().vpd_logprobs_bwd(ctypes.byref(vx), _ref(seg), _index_ptr(index, n * int(k)), int(k),
                                    int(ignore_index), _fptr(grad_out, n * int(k), "grad_out"),
                                    _fptr(saved, n * SAVED_LOGPROBS, "saved"), _ref(gx), _stream(stream)))
+
+
+def make_heads(h_s, w_s, h_t, w_t) -> vpd_linear_heads:
+    """Descriptor of two bf16 linear heads: hidden states [N, H] and head
+    weights [V, H] with unit stride along H, all on the current device."""
+    for x, what in ((h_s, "h_s"), (w_s, "w_s"), (h_t, "h_t"), (w_t, "w_t")):
+        if x.dtype != torch.bfloat16 or x.dim() != 2 or (x.shape[1] > 1 and x.stride(1) != 1):
+            raise ValueError(f"{what} must be a bf16 [rows, hidden] tensor with unit stride along hidden")
+        _on_current_device(x, what)
+    if h_s.shape[1] != w_s.shape[1] or h_t.shape[1] != w_t.shape[1]:
+        raise ValueError("hidden sizes of the hidden states and their head differ")
+    if h_s.shape[0] != h_t.shape[0] or w_s.shape[0] != w_t.shape[0]:
+        raise ValueError("student and teacher must share rows and vocabulary")
+    ld = lambda x: x.stride(0) if x.shape[0] > 1 else x.shape[1]  # noqa: E731
+    return vpd_linear_heads(h_s.data_ptr(), w_s.data_ptr(), h_t.data_ptr(), w_t.data_ptr(), h_s.shape[0],
+                            w_s.shape[0], h_s.shape[1], h_t.shape[1], ld(h_s), ld(w_s), ld(h_t), ld(w_t))
+
+
+def vpd_jsd_linear_workspace(heads: vpd_linear_heads, student_grads=True, teacher_grads=False) -> tuple[int, int]:
+    f, b = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load().vpd_jsd_linear_workspace(ctypes.byref(heads), int(bool(student_grads)), int(bool(teacher_grads)),
+                                           ctypes.byref(f), ctypes.byref(b)))
+    return int(f.value), int(b.value)
+
+
+def _workspace(ws: torch.Tensor | None, need: int):
+    if ws is None:
+        raise ValueError("a workspace tensor is required")
+    _on_current_device(ws, "workspace")
+    nbytes = ws.numel() * ws.element_size()
+    if not ws.is_contiguous() or nbytes < need:
+        raise ValueError(f"workspace must be a contiguous tensor of at least {need} bytes")
+    return ws.data_ptr(), nbytes
+
+
+def vpd_jsd_linear_fwd(heads: vpd_linear_heads, beta, loss, saved, workspace, stream=None):
+    n = int(heads.rows)
+    need, _ = vpd_jsd_linear_workspace(heads, False, False)
+    wp, wn = _workspace(workspace, need)
+    _check(load().vpd_jsd_linear_fwd(ctypes.byref(heads), float(beta), _fptr(loss, n, "loss"),
+                                     _fptr(saved, n * SAVED_PAIR, "saved"), wp, wn, _stream(stream)))
+
+
+def vpd_jsd_linear_bwd(heads: vpd_linear_heads, beta, grad_loss, loss, saved, dh_s, dw_s, dh_t, dw_t, workspace,
+                       stream=None):
+    n, v = int(heads.rows), int(heads.vocab)
+    hs, ht = int(heads.hidden_s), int(heads.hidden_t)
+    _, need = vpd_jsd_linear_workspace(heads, dh_s is not None or dw_s is not None,
+                                       dh_t is not None or dw_t is not None)
+    wp, wn = _workspace(workspace, need)
+    _check(load().vpd_jsd_linear_bwd(ctypes.byref(heads), float(beta), _fptr(grad_loss, n, "grad_loss"),
+                                     _fptr(loss, n, "loss"), _fptr(saved, n * SAVED_PAIR, "saved"),
+                                     _fptr(dh_s, n * hs, "dh_s"), _fptr(dw_s, v * hs, "dw_s"),
+                                     _fptr(dh_t, n * ht, "dh_t"), _fptr(dw_t, v * ht, "dw_t"), wp, wn,
+                                     _stream(stream)))
 
 
 def vpd_device_status(stream=None):

@@ -12,6 +12,7 @@
 
 #include "vpd.h"
 #include "vpd_internal.h"
+#include "vpd_linear.h"
 
 namespace vpd {
 // Reads and clears the device error word (defined with the fused kernel).
@@ -348,6 +349,81 @@ vpd_status vpd_logprobs_bwd(const vpd_view* x, const vpd_segments* seg, const in
   return ok();
 }
 
+}  // extern "C"
+
+namespace {
+
+vpd_status check_heads(const vpd_linear_heads* p, vpd::LinearProblem* out) {
+  if (!p) return fail(VPD_ERR_ARG, "NULL heads");
+  if (p->rows < 0 || p->vocab < 1) return fail(VPD_ERR_SHAPE, "rows must be >= 0 and vocab >= 1");
+  if (p->vocab % 8) return fail(VPD_ERR_SHAPE, "vocab %lld is not a multiple of 8", (long long)p->vocab);
+  if (p->hidden_s < 64 || p->hidden_s % 64 || p->hidden_t < 64 || p->hidden_t % 64)
+    return fail(VPD_ERR_SHAPE, "hidden sizes must be positive multiples of 64");
+  const int64_t ld[4] = {p->ld_hs, p->ld_ws, p->ld_ht, p->ld_wt};
+  const int64_t hid[4] = {p->hidden_s, p->hidden_s, p->hidden_t, p->hidden_t};
+  const void* ptr[4] = {p->h_s, p->w_s, p->h_t, p->w_t};
+  for (int i = 0; i < 4; ++i) {
+    if (ld[i] < hid[i] || ld[i] % 8) return fail(VPD_ERR_SHAPE, "row stride %d must be >= hidden and a multiple of 8", i);
+    if (p->rows > 0 && (!ptr[i] || (reinterpret_cast<uintptr_t>(ptr[i]) & 15u)))
+      return fail(VPD_ERR_ARG, "heads: NULL or not 16-byte aligned operand %d", i);
+  }
+  *out = vpd::LinearProblem{p->h_s, p->w_s, p->h_t, p->w_t, p->rows, p->vocab, p->hidden_s, p->hidden_t,
+                            p->ld_hs, p->ld_ws, p->ld_ht, p->ld_wt, 0.0};
+  return VPD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+vpd_status vpd_jsd_linear_workspace(const vpd_linear_heads* heads, int32_t student_grads, int32_t teacher_grads,
+                                    size_t* fwd_bytes, size_t* bwd_bytes) {
+  vpd::LinearProblem p;
+  VPD_TRY(check_heads(heads, &p));
+  if (fwd_bytes) *fwd_bytes = p.rows ? vpd::linear_fwd_workspace(p.rows, p.vocab) : 0;
+  if (bwd_bytes)
+    *bwd_bytes = p.rows ? vpd::linear_bwd_workspace(p.rows, p.vocab, p.hs, p.ht, student_grads != 0,
+                                                    teacher_grads != 0, vpd::kLinearChunkRows)
+                        : 0;
+  return ok();
+}
+
+vpd_status vpd_jsd_linear_fwd(const vpd_linear_heads* heads, double beta, float* loss, float* saved,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  vpd::LinearProblem p;
+  VPD_TRY(check_heads(heads, &p));
+  VPD_TRY(check_beta(beta));
+  if (p.rows == 0) return ok();
+  if (!loss || !saved || !workspace) return fail(VPD_ERR_ARG, "vpd_jsd_linear_fwd: loss, saved and workspace are required");
+  if (reinterpret_cast<uintptr_t>(workspace) & 15u) return fail(VPD_ERR_ARG, "workspace not 16-byte aligned");
+  if (workspace_bytes < vpd::linear_fwd_workspace(p.rows, p.vocab))
+    return fail(VPD_ERR_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes,
+                vpd::linear_fwd_workspace(p.rows, p.vocab));
+  p.beta = beta;
+  VPD_CUDA(vpd::linear_jsd_forward(p, loss, saved, workspace, workspace_bytes, static_cast<cudaStream_t>(stream)),
+           "fused-linear forward");
+  return ok();
+}
+
+vpd_status vpd_jsd_linear_bwd(const vpd_linear_heads* heads, double beta, const float* grad_loss, const float* loss,
+                              const float* saved, float* dh_s, float* dw_s, float* dh_t, float* dw_t, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  vpd::LinearProblem p;
+  VPD_TRY(check_heads(heads, &p));
+  VPD_TRY(check_beta(beta));
+  const bool student = dh_s || dw_s, teacher = dh_t || dw_t;
+  if (p.rows == 0 || (!student && !teacher)) return ok();
+  if (!loss || !saved || !workspace) return fail(VPD_ERR_ARG, "vpd_jsd_linear_bwd: loss, saved and workspace are required");
+  if (reinterpret_cast<uintptr_t>(workspace) & 15u) return fail(VPD_ERR_ARG, "workspace not 16-byte aligned");
+  const size_t need = vpd::linear_bwd_workspace(p.rows, p.vocab, p.hs, p.ht, student, teacher, vpd::kLinearChunkRows);
+  if (workspace_bytes < need) return fail(VPD_ERR_ARG, "workspace of %zu bytes, %zu needed", workspace_bytes, need);
+  p.beta = beta;
+  VPD_CUDA(vpd::linear_jsd_backward(p, grad_loss, loss, saved, dh_s, dw_s, dh_t, dw_t, workspace, workspace_bytes,
+                                    vpd::kLinearChunkRows, static_cast<cudaStream_t>(stream)),
+           "fused-linear backward");
+  return ok();
+}
+
 const char* vpd_status_string(vpd_status status) {
   switch (status) {
     case VPD_OK: return "VPD_OK";
@@ -376,6 +452,9 @@ vpd_status vpd_test_withhold_copy(int64_t row) {
 vpd_status vpd_device_status(void* stream) {
   int code = 0;
   VPD_CUDA(vpd::take_device_error(static_cast<cudaStream_t>(stream), &code), "reading device status");
+  int lin = 0;
+  VPD_CUDA(vpd::take_linear_error(static_cast<cudaStream_t>(stream), &lin), "reading device status");
+  code |= lin;
   if (code)
     return fail(VPD_ERR_TIMEOUT, "a bounded device-side wait gave up (code %d)", code);
   return ok();

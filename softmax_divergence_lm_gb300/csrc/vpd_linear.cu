@@ -1,0 +1,921 @@
+// vpd_linear.cu -- the fused-linear generalized JSD: student and teacher
+// logits s = h_s W_s^T and t = h_t W_t^T are formed tile by tile on the
+// tensor cores (tcgen05.mma, bf16 operands staged by TMA, fp32 accumulators in
+// tensor memory) and consumed in the epilogue, so the [N, V] logits are never
+// written to memory.
+//
+// Sources (web pages):
+//   [JSD page] DeepSpeed pull request #8958, "[VocabTP] Add vocabulary-parallel
+//              generalized JSD with Triton kernels": section Scope and
+//              limitations names the fused-linear divergence as not included
+//              and explains why JSD needs the statistics before the divergence.
+//   [ops page] DeepSpeed pull request #8791, "Add vocabulary-parallel logprobs,
+//              entropy and KL ops": section Limitations, the fused-linear
+//              variant as future work; section How, the (max, sum-exp) merge.
+//
+// One persistent kernel, k_linear, in four epilogue modes:
+//   kStats  logits tiles of both heads -> online (max, sum-exp) per row over
+//           the unit's vocabulary tiles -> partials per (vocabulary chunk, row);
+//   kDiv    logits tiles again -> the two KL-to-mixture partial sums with the
+//           merged statistics (the second of the two passes JSD needs);
+//   kGrad   logits tiles again -> dS and dT of a chunk of rows, each split into
+//           a bf16 high part and a bf16 low part (x = hi + lo to 16 bits of
+//           mantissa) and stored row-major and transposed;
+//   kGemm   a plain C += A B^T over one or two (A, B) operand pairs (used for
+//           dh = dS W and dW = dS^T h from the split gradients, hi and lo as the
+//           two pairs), split along K, accumulated into fp32 C by atomics.
+// Small kernels merge the per-chunk partials and transpose bf16 matrices.
+//
+// Warp roles of k_linear (192 threads): warp 0 issues the TMA loads into a
+// ring of shared-memory stages; warp 1 issues the MMAs (one elected lane) into
+// one of two tensor-memory accumulator buffers; warps 2-5 are the epilogue,
+// thread i of the epilogue owning TMEM lane (and tile row) 32 (warp % 4) + lane.
+// Stages hand over through mbarriers (TMA completion -> MMA; tcgen05.commit ->
+// producer), and so do the accumulator buffers (commit -> epilogue; epilogue
+// arrivals -> MMA), so the epilogue of one tile overlaps the MMAs of the next.
+// Every mbarrier wait gives up after two seconds, sets the device error word
+// and leaves the loops; the CTA waits for copies and MMAs in flight before it
+// frees its tensor memory.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "vpd_internal.h"
+#include "vpd_linear.h"
+
+namespace vpd {
+namespace linear {
+
+constexpr int BM = 128;                     // tile rows (tensor-memory lanes)
+constexpr int BN = 128;                     // tile columns
+constexpr int BK = 64;                      // k per stage: one 128-byte swizzle row of bf16
+constexpr int kStages = 6;
+constexpr int kTileBytes = BM * BK * 2;     // 16 KB per operand tile
+constexpr int kStageBytes = 2 * kTileBytes;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr float kTinyL = 1e-37f;
+constexpr float kLog2eL = 1.4426950408889634f;
+constexpr float kLn2L = 0.6931471805599453f;
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+enum Mode : int { kStats = 0, kDiv = 1, kGrad = 2, kGemm = 3 };
+
+static __device__ int g_linear_error = 0;
+
+struct Args {
+  int mode;
+  int jmode;          // 0 interior, 1 forward KL (beta = 0), 2 reverse KL (beta = 1)
+  int64_t rows;       // valid rows of the A operands (M)
+  int64_t cols;       // valid columns of the output (V for the JSD modes, the N of C for kGemm)
+  int nk0, nk1;       // k-blocks of operand pair 0 and 1 (nk1 = 0: one pair)
+  int mtiles, ntiles;
+  int tiles_per_unit; // JSD modes: vocabulary tiles per work unit
+  int ksplit;         // kGemm: parts of the k range
+  int64_t units;
+  float beta;
+  // JSD modes
+  const float* saved;      // [rows, 6] merged statistics and sums (kDiv, kGrad)
+  const float* loss;       // [rows] (kGrad, endpoint branches)
+  const float* grad_loss;  // [rows] or NULL (kGrad)
+  float* part;             // [chunks, rows, 4] (kStats) / [chunks, rows, 2] (kDiv)
+  // kGrad outputs, chunk-local: row-major [rows, cols] and transposed [cols, ld_t]
+  __nv_bfloat16 *gs_hi, *gs_lo, *gst_hi, *gst_lo;
+  __nv_bfloat16 *gt_hi, *gt_lo, *gtt_hi, *gtt_lo;
+  int64_t ld_t;
+  // kGemm output
+  float* C;
+  int64_t ldc;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t saddr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+__device__ __forceinline__ uint64_t now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mb_init(uint64_t* b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mb_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mb_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
+}
+__device__ __forceinline__ bool mb_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(saddr(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for the phase of `parity`, giving up after kWaitNs or when another role
+// has already given up.
+__device__ __forceinline__ bool mb_wait(uint64_t* b, uint32_t parity, volatile int* abort) {
+  if (mb_try(b, parity)) return true;
+  const uint64_t t0 = now_ns();
+  while (true) {
+    if (mb_try(b, parity)) return true;
+    if (*abort || now_ns() - t0 > kWaitNs) return false;
+  }
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          saddr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(saddr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_all(uint32_t* slot) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(slot)), "n"(kTmemCols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_free_all(uint32_t base) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "n"(kTmemCols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Shared-memory matrix descriptor of a K-major bf16 tile stored as rows of 128
+// bytes with the 128-byte swizzle (the layout TMA writes for a {64, rows} box):
+// 8-row groups 1024 bytes apart (stride byte offset), leading byte offset
+// unused for this layout, fixed version bits 0b001 at 46-48, swizzle mode 2.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+  uint64_t d = static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(16u >> 4) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+// Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A
+// and B (bits 7-9, 10-12 = 1), both K-major, N >> 3 at bits 17-22, M >> 4 at
+// bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((BN >> 3) << 17) | ((BM >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(saddr(bar))
+               : "memory");
+}
+// 32 consecutive fp32 columns of this thread's lane, waited for in the same statement.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2f(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
+
+// ---------------------------------------------------------------------------
+// The sequence of work every role walks through in the same order.
+// ---------------------------------------------------------------------------
+struct Unit {
+  int mt;        // row tile
+  int nt0, nt1;  // column tiles [nt0, nt1)
+  int kb0, kb1;  // kGemm: k-blocks [kb0, kb1) of the concatenated pairs
+  int chunk;     // JSD modes: vocabulary chunk index
+};
+
+__device__ __forceinline__ Unit unit_of(const Args& a, int64_t u) {
+  Unit w;
+  if (a.mode == kGemm) {
+    w.mt = static_cast<int>(u % a.mtiles);
+    const int64_t rest = u / a.mtiles;
+    w.nt0 = static_cast<int>(rest % a.ntiles);
+    w.nt1 = w.nt0 + 1;
+    const int ks = static_cast<int>(rest / a.ntiles);
+    const int nk = a.nk0 + a.nk1;
+    w.kb0 = static_cast<int>(static_cast<int64_t>(nk) * ks / a.ksplit);
+    w.kb1 = static_cast<int>(static_cast<int64_t>(nk) * (ks + 1) / a.ksplit);
+    w.chunk = 0;
+  } else {
+    w.mt = static_cast<int>(u % a.mtiles);
+    w.chunk = static_cast<int>(u / a.mtiles);
+    w.nt0 = w.chunk * a.tiles_per_unit;
+    w.nt1 = w.nt0 + a.tiles_per_unit < a.ntiles ? w.nt0 + a.tiles_per_unit : a.ntiles;
+    w.kb0 = 0;
+    w.kb1 = a.nk0 + a.nk1;
+  }
+  return w;
+}
+
+struct __align__(8) Bars {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_linear(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap b0,
+             const __grid_constant__ CUtensorMap a1, const __grid_constant__ CUtensorMap b1, Args a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Bars bars;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort = &bars.abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mb_init(&bars.full[s], 1);
+      mb_init(&bars.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mb_init(&bars.acc_full[b], 1);
+      mb_init(&bars.acc_empty[b], 4);
+    }
+    bars.abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  if (warp == 0) tmem_alloc_all(&bars.tmem_base);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  const bool gemm = a.mode == kGemm;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+        const Unit w = unit_of(a, u);
+        for (int nt = w.nt0; nt < w.nt1 && ok; ++nt) {
+          for (int kb = w.kb0; kb < w.kb1; ++kb) {
+            if (!mb_wait(&bars.empty[stage], phase ^ 1u, abort)) {
+              ok = false;
+              break;
+            }
+            const bool second = kb >= a.nk0;
+            const int kk = second ? kb - a.nk0 : kb;
+            uint8_t* sa = smem + stage * kStageBytes;
+            mb_expect_tx(&bars.full[stage], kStageBytes);
+            tma_load_2d(sa, second ? &a1 : &a0, kk * BK, w.mt * BM, &bars.full[stage]);
+            tma_load_2d(sa + kTileBytes, second ? &b1 : &b0, kk * BK, nt * BN, &bars.full[stage]);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) bars.abort = 1;
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int buf = 0;
+      uint32_t acc_phase[2] = {0, 0};
+      bool ok = true;
+      for (int64_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+        const Unit w = unit_of(a, u);
+        for (int nt = w.nt0; nt < w.nt1 && ok; ++nt) {
+          if (!mb_wait(&bars.acc_empty[buf], acc_phase[buf] ^ 1u, abort)) {
+            ok = false;
+            break;
+          }
+          acc_phase[buf] ^= 1u;
+          tc_fence_after();
+          const uint32_t acc0 = tmem + 256u * buf;  // kGemm: the one accumulator; JSD modes: S
+          for (int kb = w.kb0; kb < w.kb1; ++kb) {
+            if (!mb_wait(&bars.full[stage], phase, abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const bool second = kb >= a.nk0;
+            const uint32_t dst = (!gemm && second) ? acc0 + BN : acc0;
+            // accumulate unless this is the first k-block into this accumulator
+            const bool first = gemm ? kb == w.kb0 : (second ? kb == a.nk0 : kb == 0);
+            const uint32_t sa = saddr(smem + stage * kStageBytes);
+            const uint64_t da = sw128_desc(sa), db = sw128_desc(sa + kTileBytes);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)  // 16 bf16 = 32 bytes per MMA: +2 in the address field
+              mma_bf16(dst, da + 2u * k, db + 2u * k, (first && k == 0) ? 0u : 1u);
+            mma_commit(&bars.empty[stage]);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          mma_commit(&bars.acc_full[buf]);
+          buf ^= 1;
+        }
+      }
+      if (!ok) bars.abort = 1;
+    }
+  } else {
+    // ---------------- epilogue (warps 2-5) ----------------
+    const int q = warp & 3;                     // lane quarter of tensor memory
+    const int rloc = 32 * q + lane;             // row within the tile
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+    int buf = 0;
+    uint32_t acc_phase[2] = {0, 0};
+    bool ok = true;
+    const float beta = a.beta;
+    for (int64_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
+      const Unit w = unit_of(a, u);
+      const int64_t row = static_cast<int64_t>(w.mt) * BM + rloc;
+      const bool rv = row < a.rows;
+      // per-row state
+      float ms = ninf(), zs = 0.f, mt = ninf(), zt = 0.f;  // kStats
+      float accA = 0.f, accB = 0.f;                       // kDiv (log2 units)
+      float nms = 0.f, nmt = 0.f, nKs = 0.f, nKt = 0.f;   // -m, -L log2 e
+      float cs = 0.f, ct = 0.f, ks_ = 0.f, kt_ = 0.f;     // kGrad coefficients
+      bool live = false;
+      if (!gemm && a.mode != kStats && rv) {
+        const float* sv = a.saved + row * 6;
+        nms = -sv[0];
+        nKs = -sv[1] * kLog2eL;
+        nmt = -sv[2];
+        nKt = -sv[3] * kLog2eL;
+        live = isfinite(sv[0]) && isfinite(sv[1]) && isfinite(sv[2]) && isfinite(sv[3]);
+        if (a.mode == kGrad) {
+          const float g = a.grad_loss ? a.grad_loss[row] : 1.f;
+          const float A = sv[4], B = sv[5], value = a.loss[row];
+          live = live && isfinite(value);
+          if (a.jmode == 0) {
+            cs = g * (1.f - beta);
+            ct = g * beta;
+            ks_ = -cs * B;
+            kt_ = -ct * A;
+          } else {
+            cs = ct = g;
+            ks_ = -g * value;
+            kt_ = -g * value;
+          }
+        }
+      }
+      for (int nt = w.nt0; nt < w.nt1; ++nt) {
+        // every lane waits; the warp goes on only together (the tensor-memory
+        // loads below are warp-collective)
+        if (!__all_sync(0xffffffffu, mb_wait(&bars.acc_full[buf], acc_phase[buf], abort))) {
+          ok = false;
+          break;
+        }
+        acc_phase[buf] ^= 1u;
+        tc_fence_after();
+        const uint32_t accS = tmem + lane_addr + 256u * buf;
+        const int64_t col0 = static_cast<int64_t>(nt) * BN;
+        for (int c = 0; c < BN; c += 32) {
+          float x[32];
+          tmem_ld32(accS + c, x);
+          if (gemm) {
+            if (rv) {
+              float* crow = a.C + row * a.ldc;
+#pragma unroll
+              for (int i = 0; i < 32; i += 4) {
+                const int64_t j = col0 + c + i;
+                if (j + 3 < a.cols) {
+                  atomicAdd(reinterpret_cast<float4*>(crow + j), make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]));
+                } else {
+                  for (int e = 0; e < 4; ++e)
+                    if (j + e < a.cols) atomicAdd(crow + j + e, x[i + e]);
+                }
+              }
+            }
+            continue;
+          }
+          float y[32];
+          tmem_ld32(accS + BN + c, y);
+          const int nvalid = static_cast<int>(a.cols - (col0 + c) < 32 ? a.cols - (col0 + c) : 32);
+          if (a.mode == kStats) {
+            float cm = ninf(), cmt = ninf();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < nvalid) {
+                cm = fmaxf(cm, x[i]);
+                cmt = fmaxf(cmt, y[i]);
+              }
+            if (cm > ms) {
+              zs = ms == ninf() ? 0.f : zs * expf(ms - cm);
+              ms = cm;
+            }
+            if (cmt > mt) {
+              zt = mt == ninf() ? 0.f : zt * expf(mt - cmt);
+              mt = cmt;
+            }
+            float es = 0.f, et = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < nvalid) {
+                es += ex2f((x[i] - ms) * kLog2eL);
+                et += ex2f((y[i] - mt) * kLog2eL);
+              }
+            zs += es;
+            zt += et;
+          } else if (a.mode == kDiv) {
+            if (!live) continue;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (i >= nvalid) continue;
+              const float lp = fmaf(x[i] + nms, kLog2eL, nKs), lq = fmaf(y[i] + nmt, kLog2eL, nKt);
+              const float p = ex2f(lp), qv = ex2f(lq);
+              if (a.jmode == 0) {
+                const float lm = lg2f(fmaf(1.f - beta, p, fmaf(beta, qv, kTinyL)));
+                accA = fmaf(qv, lq - lm, accA);
+                accB = fmaf(p, lp - lm, accB);
+              } else if (a.jmode == 1) {
+                accA = fmaf(qv, lq - lp, accA);
+              } else {
+                accB = fmaf(p, lp - lq, accB);
+              }
+            }
+          } else {  // kGrad
+            // rows past the chunk's end (inside its last row tile) are zero in
+            // the transposed arrays, whose columns the dW product sums over
+            const int64_t rl = row;  // the operand maps start at the chunk's first row
+            if (!rv) {
+              const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
+#pragma unroll 4
+              for (int i = 0; i < 32; ++i) {
+                const int64_t j = col0 + c + i;
+                if (i >= nvalid) continue;
+                if (a.gst_hi) {
+                  a.gst_hi[j * a.ld_t + rl] = z;
+                  a.gst_lo[j * a.ld_t + rl] = z;
+                }
+                if (a.gtt_hi) {
+                  a.gtt_hi[j * a.ld_t + rl] = z;
+                  a.gtt_lo[j * a.ld_t + rl] = z;
+                }
+              }
+              continue;
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int64_t j = col0 + c + i;
+              if (i >= nvalid) continue;
+              float gs = 0.f, gt = 0.f;
+              if (live) {
+                const float lp = fmaf(x[i] + nms, kLog2eL, nKs), lq = fmaf(y[i] + nmt, kLog2eL, nKt);
+                const float p = ex2f(lp), qv = ex2f(lq);
+                if (a.jmode == 0) {
+                  const float lm = lg2f(fmaf(1.f - beta, p, fmaf(beta, qv, kTinyL)));
+                  gs = p * fmaf(cs * kLn2L, lp - lm, ks_);
+                  gt = qv * fmaf(ct * kLn2L, lq - lm, kt_);
+                } else if (a.jmode == 1) {  // dS = g (p - q), dT = g q (ln q - ln p - KL)
+                  gs = cs * (p - qv);
+                  gt = qv * fmaf(ct * kLn2L, lq - lp, kt_);
+                } else {  // dS = g p (ln p - ln q - KL), dT = g (q - p)
+                  gs = p * fmaf(cs * kLn2L, lp - lq, ks_);
+                  gt = ct * (qv - p);
+                }
+              }
+              if (a.gst_hi) {
+                const __nv_bfloat16 hi = __float2bfloat16_rn(gs);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(gs - __bfloat162float(hi));
+                a.gs_hi[rl * a.cols + j] = hi;
+                a.gs_lo[rl * a.cols + j] = lo;
+                a.gst_hi[j * a.ld_t + rl] = hi;
+                a.gst_lo[j * a.ld_t + rl] = lo;
+              }
+              if (a.gtt_hi) {
+                const __nv_bfloat16 hi = __float2bfloat16_rn(gt);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(gt - __bfloat162float(hi));
+                a.gt_hi[rl * a.cols + j] = hi;
+                a.gt_lo[rl * a.cols + j] = lo;
+                a.gtt_hi[j * a.ld_t + rl] = hi;
+                a.gtt_lo[j * a.ld_t + rl] = lo;
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mb_arrive(&bars.acc_empty[buf]);
+        buf ^= 1;
+      }
+      if (!ok) break;
+      if (rv && a.mode == kStats) {
+        reinterpret_cast<float4*>(a.part)[static_cast<int64_t>(w.chunk) * a.rows + row] = make_float4(ms, zs, mt, zt);
+      } else if (rv && a.mode == kDiv) {
+        reinterpret_cast<float2*>(a.part)[static_cast<int64_t>(w.chunk) * a.rows + row] = make_float2(accA, accB);
+      }
+    }
+    if (!ok) bars.abort = 1;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (bars.abort) {
+    // a wait gave up: let copies and MMAs already issued land before the
+    // shared and tensor memory are released
+    const uint64_t t0 = now_ns();
+    while (now_ns() - t0 < 10000000ull) {
+    }
+    if (threadIdx.x == 0) atomicExch(&g_linear_error, 1);
+  }
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_free_all(tmem);
+  }
+}
+
+// Per row: merge the (m, z) partials of both heads over the vocabulary chunks
+// in chunk order (MAX of maxima, SUM of sums rescaled to it) and store
+// (m_s, ln Z_s, m_t, ln Z_t) in `saved`.
+__global__ void k_linear_merge_stats(const float4* part, int chunks, int64_t rows, float* saved) {
+  const int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (r >= rows) return;
+  float ms = ninf(), mt = ninf();
+  for (int c = 0; c < chunks; ++c) {
+    const float4 p = part[c * rows + r];
+    ms = fmaxf(ms, p.x);
+    mt = fmaxf(mt, p.z);
+  }
+  float zs = 0.f, zt = 0.f;
+  for (int c = 0; c < chunks; ++c) {
+    const float4 p = part[c * rows + r];
+    if (p.x != ninf()) zs += p.y * expf(p.x - ms);
+    if (p.z != ninf()) zt += p.w * expf(p.z - mt);
+  }
+  float* sv = saved + r * 6;
+  const bool bad_s = !isfinite(ms) || !isfinite(zs), bad_t = !isfinite(mt) || !isfinite(zt);
+  sv[0] = bad_s ? __int_as_float(0x7fffffff) : ms;
+  sv[1] = bad_s ? __int_as_float(0x7fffffff) : logf(zs);
+  sv[2] = bad_t ? __int_as_float(0x7fffffff) : mt;
+  sv[3] = bad_t ? __int_as_float(0x7fffffff) : logf(zt);
+}
+
+// Per row: the sums of the two KL-to-mixture partials (log2 units) over the
+// chunks, in nats; the per-token value beta A + (1 - beta) B (or the KL of an
+// endpoint branch).
+__global__ void k_linear_merge_div(const float2* part, int chunks, int64_t rows, int jmode, float beta, float* saved,
+                                   float* loss) {
+  const int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (r >= rows) return;
+  float A = 0.f, B = 0.f;
+  for (int c = 0; c < chunks; ++c) {
+    const float2 p = part[c * rows + r];
+    A += p.x;
+    B += p.y;
+  }
+  A *= kLn2L;
+  B *= kLn2L;
+  float* sv = saved + r * 6;
+  const bool ok = isfinite(sv[0]) && isfinite(sv[2]);
+  float value;
+  if (!ok) {
+    A = B = value = __int_as_float(0x7fffffff);
+  } else if (jmode == 0) {
+    value = beta * A + (1.f - beta) * B;
+  } else if (jmode == 1) {
+    value = A;
+    B = 0.f;
+  } else {
+    value = B;
+    A = 0.f;
+  }
+  sv[4] = A;
+  sv[5] = B;
+  loss[r] = value;
+}
+
+// out[c, r] = in[r, c] for a bf16 [rows, cols] matrix (32 x 32 tiles through
+// shared memory; rows and cols of the output are those of the transposed view).
+__global__ void k_transpose_bf16(const __nv_bfloat16* in, int64_t rows, int64_t cols, int64_t ld_in,
+                                 __nv_bfloat16* out, int64_t ld_out) {
+  __shared__ __nv_bfloat16 tile[32][33];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32, c0 = static_cast<int64_t>(blockIdx.x) * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int64_t r = r0 + i, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) tile[i][threadIdx.x] = in[r * ld_in + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int64_t c = c0 + i, r = r0 + threadIdx.x;
+    if (r < rows && c < cols) out[c * ld_out + r] = tile[threadIdx.x][i];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// A K-major bf16 operand [rows, k] with row stride `ld` elements, tiled in
+// {64, 128} boxes with the 128-byte swizzle; rows and k past the ends read 0.
+cudaError_t make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t k, int64_t ld) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) || (ld * 2) % 16) return cudaErrorInvalidValue;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
+  const cuuint32_t box[2] = {BK, BM};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1, const CUtensorMap& b1,
+                   const Args& args, cudaStream_t stream) {
+  if (args.units <= 0) return cudaSuccess;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(k_linear, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const int64_t grid = args.units < sm_count() ? args.units : sm_count();
+  k_linear<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(a0, b0, a1, b1, args);
+  note_launch();
+  return cudaGetLastError();
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Vocabulary tiles per work unit of the JSD modes: enough units to fill the
+// GPU a few times over, each long enough that its fixed cost is small.
+int tiles_per_unit(int64_t mtiles, int64_t ntiles) {
+  const int64_t want_units = 4 * static_cast<int64_t>(sm_count());
+  int64_t per_m = cdiv(want_units, mtiles);  // chunks per row tile
+  if (per_m < 1) per_m = 1;
+  int64_t t = cdiv(ntiles, per_m);
+  if (t < 4) t = ntiles < 4 ? ntiles : 4;
+  return static_cast<int>(t);
+}
+
+}  // namespace linear
+
+using namespace linear;
+
+size_t linear_fwd_workspace(int64_t rows, int64_t vocab) {
+  const int64_t mtiles = cdiv(rows, BM), ntiles = cdiv(vocab, BN);
+  const int64_t chunks = cdiv(ntiles, tiles_per_unit(mtiles, ntiles));
+  return static_cast<size_t>(chunks) * static_cast<size_t>(rows) * 16u;
+}
+
+size_t linear_bwd_workspace(int64_t rows, int64_t vocab, int64_t hs, int64_t ht, bool student, bool teacher,
+                            int64_t chunk_rows) {
+  const int64_t nc = rows < chunk_rows ? cdiv(rows, BM) * BM : chunk_rows;
+  size_t b = 0;
+  const size_t g = static_cast<size_t>(nc) * static_cast<size_t>(vocab) * 2u;  // one bf16 [nc, V]
+  if (student) b += 4 * g + static_cast<size_t>(hs) * vocab * 2u + static_cast<size_t>(hs) * nc * 2u;
+  if (teacher) b += 4 * g + static_cast<size_t>(ht) * vocab * 2u + static_cast<size_t>(ht) * nc * 2u;
+  return b + 1024;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+cudaError_t linear_jsd_forward(const LinearProblem& p, float* loss, float* saved, void* ws, size_t ws_bytes,
+                               cudaStream_t stream) {
+  const int64_t mtiles = cdiv(p.rows, BM), ntiles = cdiv(p.vocab, BN);
+  const int tpu = tiles_per_unit(mtiles, ntiles);
+  const int64_t chunks = cdiv(ntiles, tpu);
+  if (ws_bytes < linear_fwd_workspace(p.rows, p.vocab)) return cudaErrorInvalidValue;
+  CUtensorMap hs, wsm, ht, wt;
+  cudaError_t e;
+  if ((e = make_map(&hs, p.h_s, p.rows, p.hs, p.ld_hs)) != cudaSuccess) return e;
+  if ((e = make_map(&wsm, p.w_s, p.vocab, p.hs, p.ld_ws)) != cudaSuccess) return e;
+  if ((e = make_map(&ht, p.h_t, p.rows, p.ht, p.ld_ht)) != cudaSuccess) return e;
+  if ((e = make_map(&wt, p.w_t, p.vocab, p.ht, p.ld_wt)) != cudaSuccess) return e;
+  Args a{};
+  a.jmode = p.beta == 0.0 ? 1 : p.beta == 1.0 ? 2 : 0;
+  a.rows = p.rows;
+  a.cols = p.vocab;
+  a.nk0 = static_cast<int>(p.hs / BK);
+  a.nk1 = static_cast<int>(p.ht / BK);
+  a.mtiles = static_cast<int>(mtiles);
+  a.ntiles = static_cast<int>(ntiles);
+  a.tiles_per_unit = tpu;
+  a.units = mtiles * chunks;
+  a.beta = static_cast<float>(p.beta);
+  a.part = static_cast<float*>(ws);
+  a.saved = saved;
+  a.mode = kStats;
+  if ((e = launch(hs, wsm, ht, wt, a, stream)) != cudaSuccess) return e;
+  const unsigned mg = static_cast<unsigned>(cdiv(p.rows, 256));
+  k_linear_merge_stats<<<mg, 256, 0, stream>>>(reinterpret_cast<const float4*>(ws), static_cast<int>(chunks), p.rows,
+                                               saved);
+  note_launch();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  a.mode = kDiv;
+  if ((e = launch(hs, wsm, ht, wt, a, stream)) != cudaSuccess) return e;
+  k_linear_merge_div<<<mg, 256, 0, stream>>>(reinterpret_cast<const float2*>(ws), static_cast<int>(chunks), p.rows,
+                                             a.jmode, a.beta, saved, loss);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t transpose_bf16(const void* in, int64_t rows, int64_t cols, int64_t ld_in, void* out, int64_t ld_out,
+                           cudaStream_t stream) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  dim3 grid(static_cast<unsigned>(cdiv(cols, 32)), static_cast<unsigned>(cdiv(rows, 32)));
+  k_transpose_bf16<<<grid, dim3(32, 8), 0, stream>>>(static_cast<const __nv_bfloat16*>(in), rows, cols, ld_in,
+                                                       static_cast<__nv_bfloat16*>(out), ld_out);
+  note_launch();
+  return cudaGetLastError();
+}
+
+// C[rows, n] += A0 B0^T + A1 B1^T with K-major bf16 operands (A [rows, k],
+// B [n, k]), split along k so that about four units run per SM.
+cudaError_t gemm_acc(const void* a0p, const void* a1p, int64_t lda, const void* bp, int64_t ldb, int64_t rows,
+                     int64_t n, int64_t k, float* C, int64_t ldc, cudaStream_t stream) {
+  CUtensorMap a0, a1, b0;
+  cudaError_t e;
+  if ((e = make_map(&a0, a0p, rows, k, lda)) != cudaSuccess) return e;
+  if ((e = make_map(&a1, a1p, rows, k, lda)) != cudaSuccess) return e;
+  if ((e = make_map(&b0, bp, n, k, ldb)) != cudaSuccess) return e;
+  Args a{};
+  a.mode = kGemm;
+  a.rows = rows;
+  a.cols = n;
+  a.nk0 = a.nk1 = static_cast<int>(cdiv(k, BK));
+  a.mtiles = static_cast<int>(cdiv(rows, BM));
+  a.ntiles = static_cast<int>(cdiv(n, BN));
+  const int64_t tiles = static_cast<int64_t>(a.mtiles) * a.ntiles;
+  int64_t ks = cdiv(4 * static_cast<int64_t>(sm_count()), tiles);
+  const int64_t nk = a.nk0 + a.nk1;
+  if (ks > nk / 8) ks = nk / 8;  // at least 8 k-blocks per unit
+  if (ks < 1) ks = 1;
+  a.ksplit = static_cast<int>(ks);
+  a.units = tiles * ks;
+  a.C = C;
+  a.ldc = ldc;
+  return launch(a0, b0, a1, b0, a, stream);
+}
+
+cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, const float* loss,
+                                const float* saved, float* dh_s, float* dw_s, float* dh_t, float* dw_t, void* ws,
+                                size_t ws_bytes, int64_t chunk_rows, cudaStream_t stream) {
+  const bool student = dh_s || dw_s, teacher = dh_t || dw_t;
+  if (!student && !teacher) return cudaSuccess;
+  const int64_t nc = p.rows < chunk_rows ? cdiv(p.rows, BM) * BM : chunk_rows;
+  if (ws_bytes < linear_bwd_workspace(p.rows, p.vocab, p.hs, p.ht, student, teacher, chunk_rows))
+    return cudaErrorInvalidValue;
+  // workspace: per head [hi, lo, hi^T, lo^T] gradients of one chunk, the head
+  // weight transposed [H, V], the chunk's hidden states transposed [H, nc]
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const size_t g = align256(static_cast<size_t>(nc) * p.vocab * 2u);
+  auto take = [&](size_t bytes) {
+    uint8_t* r = w;
+    w += align256(bytes);
+    return r;
+  };
+  __nv_bfloat16* G[2][4] = {};
+  void* wT[2] = {nullptr, nullptr};
+  void* hT[2] = {nullptr, nullptr};
+  const int64_t H[2] = {p.hs, p.ht};
+  const void* hp[2] = {p.h_s, p.h_t};
+  const int64_t ldh[2] = {p.ld_hs, p.ld_ht};
+  const void* wp[2] = {p.w_s, p.w_t};
+  const int64_t ldw[2] = {p.ld_ws, p.ld_wt};
+  const bool want[2] = {student, teacher};
+  float* dh[2] = {dh_s, dh_t};
+  float* dw[2] = {dw_s, dw_t};
+  cudaError_t e;
+  for (int x = 0; x < 2; ++x) {
+    if (!want[x]) continue;
+    for (int i = 0; i < 4; ++i) G[x][i] = reinterpret_cast<__nv_bfloat16*>(take(g));
+    wT[x] = take(static_cast<size_t>(H[x]) * p.vocab * 2u);
+    hT[x] = take(static_cast<size_t>(H[x]) * nc * 2u);
+    // dh and dW accumulate by atomics: start from zero
+    if (dh[x] && (e = cudaMemsetAsync(dh[x], 0, static_cast<size_t>(p.rows) * H[x] * 4u, stream)) != cudaSuccess)
+      return e;
+    if (dw[x] && (e = cudaMemsetAsync(dw[x], 0, static_cast<size_t>(p.vocab) * H[x] * 4u, stream)) != cudaSuccess)
+      return e;
+    if (dh[x] && (e = transpose_bf16(wp[x], p.vocab, H[x], ldw[x], wT[x], p.vocab, stream)) != cudaSuccess) return e;
+  }
+  CUtensorMap hsm, wsm, htm, wtm;
+  for (int64_t r0 = 0; r0 < p.rows; r0 += nc) {
+    const int64_t n = p.rows - r0 < nc ? p.rows - r0 : nc;
+    const void* hs0 = static_cast<const char*>(p.h_s) + r0 * p.ld_hs * 2;
+    const void* ht0 = static_cast<const char*>(p.h_t) + r0 * p.ld_ht * 2;
+    if ((e = make_map(&hsm, hs0, n, p.hs, p.ld_hs)) != cudaSuccess) return e;
+    if ((e = make_map(&wsm, p.w_s, p.vocab, p.hs, p.ld_ws)) != cudaSuccess) return e;
+    if ((e = make_map(&htm, ht0, n, p.ht, p.ld_ht)) != cudaSuccess) return e;
+    if ((e = make_map(&wtm, p.w_t, p.vocab, p.ht, p.ld_wt)) != cudaSuccess) return e;
+    Args a{};
+    a.mode = kGrad;
+    a.jmode = p.beta == 0.0 ? 1 : p.beta == 1.0 ? 2 : 0;
+    a.rows = n;
+    a.cols = p.vocab;
+    a.nk0 = static_cast<int>(p.hs / BK);
+    a.nk1 = static_cast<int>(p.ht / BK);
+    a.mtiles = static_cast<int>(cdiv(n, BM));
+    a.ntiles = static_cast<int>(cdiv(p.vocab, BN));
+    a.tiles_per_unit = tiles_per_unit(a.mtiles, a.ntiles);
+    a.units = static_cast<int64_t>(a.mtiles) * cdiv(a.ntiles, a.tiles_per_unit);
+    a.beta = static_cast<float>(p.beta);
+    a.saved = saved + r0 * 6;
+    a.loss = loss + r0;
+    a.grad_loss = grad_loss ? grad_loss + r0 : nullptr;
+    a.ld_t = nc;
+    if (student) {
+      a.gs_hi = G[0][0];
+      a.gs_lo = G[0][1];
+      a.gst_hi = G[0][2];
+      a.gst_lo = G[0][3];
+    }
+    if (teacher) {
+      a.gt_hi = G[1][0];
+      a.gt_lo = G[1][1];
+      a.gtt_hi = G[1][2];
+      a.gtt_lo = G[1][3];
+    }
+    if ((e = launch(hsm, wsm, htm, wtm, a, stream)) != cudaSuccess) return e;
+    for (int x = 0; x < 2; ++x) {
+      if (!want[x]) continue;
+      // dh[r0:r0+n] += G_hi W + G_lo W  (K = V; B = W^T [H, V])
+      if (dh[x] &&
+          (e = gemm_acc(G[x][0], G[x][1], p.vocab, wT[x], p.vocab, n, H[x], p.vocab, dh[x] + r0 * H[x], H[x],
+                        stream)) != cudaSuccess)
+        return e;
+      // dW += G_hi^T h + G_lo^T h  (K = chunk rows; A = G^T [V, nc], B = h^T [H, nc])
+      if (dw[x]) {
+        const void* h0 = static_cast<const char*>(hp[x]) + r0 * ldh[x] * 2;
+        if ((e = transpose_bf16(h0, n, H[x], ldh[x], hT[x], nc, stream)) != cudaSuccess) return e;
+        if (n < nc &&
+            (e = cudaMemset2DAsync(static_cast<char*>(hT[x]) + n * 2, nc * 2, 0, (nc - n) * 2, H[x], stream)) !=
+                cudaSuccess)
+          return e;
+        if ((e = gemm_acc(G[x][2], G[x][3], nc, hT[x], nc, p.vocab, H[x], nc, dw[x], H[x], stream)) != cudaSuccess)
+          return e;
+      }
+    }
+  }
+  return cudaSuccess;
+}
+
+cudaError_t take_linear_error(cudaStream_t stream, int* code);
+
+}  // namespace vpd
+
+namespace vpd {
+static __device__ int g_linear_taken = 0;
+static __global__ void k_take_linear_error2() { g_linear_taken = atomicExch(&linear::g_linear_error, 0); }
+cudaError_t take_linear_error(cudaStream_t stream, int* code) {
+  k_take_linear_error2<<<1, 1, 0, stream>>>();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbolAsync(code, g_linear_taken, sizeof(int), 0, cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(stream);
+}
+}  // namespace vpd

@@ -1,0 +1,36 @@
+// vpd_linear.h -- host interface of the fused-linear JSD kernels (vpd_linear.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace vpd {
+
+// Student and teacher heads: logits s = h_s w_s^T, t = h_t w_t^T; every matrix
+// bf16, row-major, K-major (hidden index contiguous), rows 16-byte aligned.
+struct LinearProblem {
+  const void* h_s;  // [rows, hs], row stride ld_hs
+  const void* w_s;  // [vocab, hs], row stride ld_ws
+  const void* h_t;  // [rows, ht]
+  const void* w_t;  // [vocab, ht]
+  int64_t rows, vocab, hs, ht;
+  int64_t ld_hs, ld_ws, ld_ht, ld_wt;
+  double beta;
+};
+
+// Rows of one backward chunk (a multiple of the 128-row tile).
+constexpr int64_t kLinearChunkRows = 1024;
+
+size_t linear_fwd_workspace(int64_t rows, int64_t vocab);
+size_t linear_bwd_workspace(int64_t rows, int64_t vocab, int64_t hs, int64_t ht, bool student, bool teacher,
+                            int64_t chunk_rows);
+cudaError_t linear_jsd_forward(const LinearProblem& p, float* loss, float* saved, void* ws, size_t ws_bytes,
+                               cudaStream_t stream);
+cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, const float* loss,
+                                const float* saved, float* dh_s, float* dw_s, float* dh_t, float* dw_t, void* ws,
+                                size_t ws_bytes, int64_t chunk_rows, cudaStream_t stream);
+// Reads and clears the device error word of the fused-linear kernels.
+cudaError_t take_linear_error(cudaStream_t stream, int* code);
+
+}  // namespace vpd
