@@ -282,6 +282,32 @@ vpd_status vpd_jsd_linear_bwd(const vpd_linear_heads *heads, double beta, const 
                               float *dh_t, float *dw_t, void *workspace, size_t workspace_bytes,
                               void *stream);
 
+/* Largest forward workspace (bytes) vpd_jsd_linear_fwd_noalloc can serve. */
+#define VPD_LINEAR_NOALLOC_MAX_BYTES (4u << 20)
+
+/* vpd_jsd_linear_fwd for callers that cannot allocate device memory: for
+ * example an engine that owns all device memory and hands each op only its
+ * inputs and outputs, or a latency-critical loop where cudaMalloc / cudaFree
+ * would stall the device. The pages have no counterpart of this entry point.
+ * Same arguments, results and errors as vpd_jsd_linear_fwd, without the
+ * workspace: the statistics partials go to one array of
+ * VPD_LINEAR_NOALLOC_MAX_BYTES bytes that the library keeps in device memory
+ * for the life of the process (each GPU that loads the library holds one). A
+ * problem whose forward workspace (vpd_jsd_linear_workspace) is larger returns
+ * VPD_ERR_SHAPE before anything is launched. That workspace is 16 bytes per row
+ * and vocabulary chunk, and the chunk count falls as rows grow (to one chunk
+ * once the row tiles alone fill the GPU four times), so on a 152-SM GPU the
+ * array serves up to about 260000 rows. Nothing is allocated: no cudaMalloc,
+ * no cudaFree. The first call on a
+ * device looks up the array's device address on that device (make that device
+ * current first); make this first call before any stream capture. Every call
+ * shares the one array: calls whose work overlaps on the GPU (other streams,
+ * other threads, other devices are separate arrays) race and give undefined
+ * results, so serialise them. Nothing from an earlier call needs clearing:
+ * every entry a call reads, the same call writes first. */
+vpd_status vpd_jsd_linear_fwd_noalloc(const vpd_linear_heads *heads, double beta, float *loss,
+                                      float *saved, void *stream);
+
 /* ---------------------------------------------------------------------------
  * Utilities.
  * ------------------------------------------------------------------------- */

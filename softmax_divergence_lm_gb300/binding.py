@@ -33,7 +33,7 @@ SYMBOLS = ("vpd_jsd_fwd", "vpd_jsd_bwd", "vpd_jsd_fwdbwd", "vpd_kl_fwd", "vpd_kl
            "vpd_entropy_fwd", "vpd_entropy_bwd", "vpd_logprobs_fwd", "vpd_logprobs_bwd",
            "vpd_status_string", "vpd_last_error", "vpd_abi_version", "vpd_device_status",
            "vpd_launch_count", "vpd_test_withhold_copy", "vpd_jsd_linear_workspace", "vpd_jsd_linear_fwd",
-           "vpd_jsd_linear_bwd")
+           "vpd_jsd_linear_bwd", "vpd_jsd_linear_fwd_noalloc")
 
 
 class VpdError(RuntimeError):
@@ -102,6 +102,7 @@ def _declare(lib):
         "vpd_jsd_linear_workspace": [P(vpd_linear_heads), i32, i32, P(ctypes.c_size_t), P(ctypes.c_size_t)],
         "vpd_jsd_linear_fwd": [P(vpd_linear_heads), dbl, f, f, vp, ctypes.c_size_t, vp],
         "vpd_jsd_linear_bwd": [P(vpd_linear_heads), dbl, f, f, f, f, f, f, f, vp, ctypes.c_size_t, vp],
+        "vpd_jsd_linear_fwd_noalloc": [P(vpd_linear_heads), dbl, f, f, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -363,6 +364,15 @@ def vpd_jsd_linear_fwd(heads: vpd_linear_heads, beta, loss, saved, workspace, st
     wp, wn = _workspace(workspace, need)
     _check(load().vpd_jsd_linear_fwd(ctypes.byref(heads), float(beta), _fptr(loss, n, "loss"),
                                      _fptr(saved, n * SAVED_PAIR, "saved"), wp, wn, _stream(stream)))
+
+
+def vpd_jsd_linear_fwd_noalloc(heads: vpd_linear_heads, beta, loss, saved, stream=None):
+    """vpd_jsd_linear_fwd without a workspace argument, for callers that may not
+    allocate device memory (the library's built-in scratch array is used; calls
+    that overlap on the GPU must not share it)."""
+    n = int(heads.rows)
+    _check(load().vpd_jsd_linear_fwd_noalloc(ctypes.byref(heads), float(beta), _fptr(loss, n, "loss"),
+                                             _fptr(saved, n * SAVED_PAIR, "saved"), _stream(stream)))
 
 
 def vpd_jsd_linear_bwd(heads: vpd_linear_heads, beta, grad_loss, loss, saved, dh_s, dw_s, dh_t, dw_t, workspace,

@@ -405,6 +405,28 @@ vpd_status vpd_jsd_linear_fwd(const vpd_linear_heads* heads, double beta, float*
   return ok();
 }
 
+vpd_status vpd_jsd_linear_fwd_noalloc(const vpd_linear_heads* heads, double beta, float* loss, float* saved,
+                                      void* stream) {
+  vpd::LinearProblem p;
+  VPD_TRY(check_heads(heads, &p));
+  VPD_TRY(check_beta(beta));
+  if (p.rows == 0) return ok();
+  if (!loss || !saved) return fail(VPD_ERR_ARG, "vpd_jsd_linear_fwd_noalloc: loss and saved are required");
+  const size_t need = vpd::linear_fwd_workspace(p.rows, p.vocab);
+  if (need > vpd::kLinearNoAllocMaxBytes)
+    return fail(VPD_ERR_SHAPE,
+                "vpd_jsd_linear_fwd_noalloc: this problem needs %zu bytes of scratch, the built-in array holds %zu; "
+                "use vpd_jsd_linear_fwd with a workspace",
+                need, vpd::kLinearNoAllocMaxBytes);
+  void* scratch = nullptr;
+  VPD_CUDA(vpd::linear_scratch(&scratch), "looking up the built-in scratch array");
+  p.beta = beta;
+  VPD_CUDA(vpd::linear_jsd_forward(p, loss, saved, scratch, vpd::kLinearNoAllocMaxBytes,
+                                   static_cast<cudaStream_t>(stream)),
+           "fused-linear forward");
+  return ok();
+}
+
 vpd_status vpd_jsd_linear_bwd(const vpd_linear_heads* heads, double beta, const float* grad_loss, const float* loss,
                               const float* saved, float* dh_s, float* dw_s, float* dh_t, float* dw_t, void* workspace,
                               size_t workspace_bytes, void* stream) {

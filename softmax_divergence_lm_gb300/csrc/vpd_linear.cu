@@ -905,6 +905,35 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
 
 cudaError_t take_linear_error(cudaStream_t stream, int* code);
 
+// ---------------------------------------------------------------------------
+// Forward without caller workspace: the per-chunk statistics partials live in
+// one file-scope device array (each GPU that loads the library holds its own
+// copy until the process exits). Every entry of it that the forward reads is
+// first written by the same call, so nothing needs clearing; two calls that
+// overlap on the GPU would write the same entries and race.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_linear_scratch[kLinearNoAllocMaxBytes];
+
+cudaError_t linear_scratch(void** out) {
+  static std::mutex mu;
+  static void* ptr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptr[dev]) {
+    // the array's device address on the current device (its host-side name is
+    // only a stand-in and must never reach a kernel)
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_linear_scratch);
+    if (e != cudaSuccess) return e;
+    ptr[dev] = p;
+  }
+  *out = ptr[dev];
+  return cudaSuccess;
+}
+
 }  // namespace vpd
 
 namespace vpd {

@@ -30,6 +30,10 @@ cudaError_t linear_jsd_forward(const LinearProblem& p, float* loss, float* saved
 cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, const float* loss,
                                 const float* saved, float* dh_s, float* dw_s, float* dh_t, float* dw_t, void* ws,
                                 size_t ws_bytes, int64_t chunk_rows, cudaStream_t stream);
+// Size of the file-scope device array the workspace-free forward uses.
+constexpr size_t kLinearNoAllocMaxBytes = size_t(4) << 20;
+// Device address of that array on the current device (looked up once per device).
+cudaError_t linear_scratch(void** out);
 // Reads and clears the device error word of the fused-linear kernels.
 cudaError_t take_linear_error(cudaStream_t stream, int* code);
 
