@@ -9,6 +9,8 @@
  *               generalized JSD with Triton kernels".
  *   [ops page]  DeepSpeed pull request #8791, "Add vocabulary-parallel logprobs,
  *               entropy and KL ops".
+ *   [OPSD page] DeepSpeedExamples pull request #1019, "Add an opt-in
+ *               vocabulary-parallel KL route to OPSD".
  *
  * Notation for one token row r of logits s (student) and t (teacher), or x:
  *   S_x = { j : x_j > -inf },  m_x = max_{S_x} x_j,  Z_x = sum_{S_x} e^{x_j - m_x},
@@ -225,6 +227,44 @@ vpd_status vpd_logprobs_fwd(const vpd_view *x, const vpd_segments *seg, const in
 vpd_status vpd_logprobs_bwd(const vpd_view *x, const vpd_segments *seg, const int64_t *index,
                             int32_t k, int64_t ignore_index, const float *grad_out,
                             const float *saved, const vpd_grad *dx, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Two thin ops on the selected log-probabilities ([ops page], "What": the
+ * teacher top-k forward KL written with the log-prob op; "How": the
+ * cross-entropy op that validates its shard layout the same way), each with an
+ * optional temperature T > 0 that divides the logits before the softmax (T = 1:
+ * none; [OPSD page] divides by it in fp32 before the op). The statistics saved
+ * for the backward ([N, 2] as for log-probs, or NULL) are those of x / T.
+ * Index checking, err_flag and ignore_index behave as in vpd_logprobs_fwd.
+ * ------------------------------------------------------------------------- */
+
+/* Cross-entropy per token: loss[r] = -ln softmax(x_r / T)[labels[r]]; a label
+ * equal to ignore_index gives 0 and no gradient; a label whose logit is -inf
+ * gives +inf and no gradient. labels: device int64[N]; loss: device float[N].
+ * Backward: dx_j = (g / T) (p_j - [j == label]); grad_loss device float[N] or
+ * NULL (ones). */
+vpd_status vpd_cross_entropy_fwd(const vpd_view *x, const vpd_segments *seg, const int64_t *labels,
+                                 int64_t ignore_index, double temperature, float *loss, float *saved,
+                                 int32_t *err_flag, void *stream);
+vpd_status vpd_cross_entropy_bwd(const vpd_view *x, const vpd_segments *seg, const int64_t *labels,
+                                 int64_t ignore_index, double temperature, const float *grad_loss,
+                                 const float *saved, const vpd_grad *dx, void *stream);
+
+/* Teacher top-k forward KL per token:
+ *   kl[r] = sum_k e^{tl[r,k]} (tl[r,k] - ln softmax(s_r / T)[index[r,k]]),
+ * with tl the teacher's log-probabilities at its top-k ids (device float[N, k],
+ * computed by the caller; the teacher is detached). Positions equal to
+ * ignore_index, and teacher log-probs of -inf, contribute nothing; an id the
+ * teacher gives mass but the student masks (-inf logit) makes the row +inf.
+ * Backward to the student only: ds_j = (g / T) (p_j W - sum_k e^{tl_k}
+ * [j == index_k]) with W = sum_k e^{tl_k} over the contributing positions; a
+ * +inf or NaN row gets a zero gradient. grad_kl device float[N] or NULL. */
+vpd_status vpd_topk_kl_fwd(const vpd_view *s, const vpd_segments *seg, const int64_t *index, int32_t k,
+                           int64_t ignore_index, const float *teacher_logp, double temperature, float *kl,
+                           float *saved, int32_t *err_flag, void *stream);
+vpd_status vpd_topk_kl_bwd(const vpd_view *s, const vpd_segments *seg, const int64_t *index, int32_t k,
+                           int64_t ignore_index, const float *teacher_logp, double temperature,
+                           const float *grad_kl, const float *saved, const vpd_grad *ds, void *stream);
 
 /* ---------------------------------------------------------------------------
  * Fused-linear generalized JSD ([JSD page], "Scope and limitations" and [ops

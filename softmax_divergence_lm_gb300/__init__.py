@@ -11,12 +11,13 @@ the built library.
 """
 import importlib
 
-__all__ = ["binding", "ops", "synth", "build", "jsd", "kl_div", "entropy", "logprobs", "jsd_fwdbwd"]
+__all__ = ["binding", "ops", "synth", "build", "jsd", "kl_div", "entropy", "logprobs", "jsd_fwdbwd", "cross_entropy",
+           "topk_forward_kl"]
 
 
 def __getattr__(name):
     if name in ("binding", "ops", "synth", "build"):
         return importlib.import_module(f"{__name__}.{name}")
-    if name in ("jsd", "kl_div", "entropy", "logprobs", "jsd_fwdbwd"):
+    if name in ("jsd", "kl_div", "entropy", "logprobs", "jsd_fwdbwd", "cross_entropy", "topk_forward_kl"):
         return getattr(importlib.import_module(f"{__name__}.ops"), name)
     raise AttributeError(name)

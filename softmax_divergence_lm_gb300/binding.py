@@ -33,7 +33,8 @@ SYMBOLS = ("vpd_jsd_fwd", "vpd_jsd_bwd", "vpd_jsd_fwdbwd", "vpd_kl_fwd", "vpd_kl
            "vpd_entropy_fwd", "vpd_entropy_bwd", "vpd_logprobs_fwd", "vpd_logprobs_bwd",
            "vpd_status_string", "vpd_last_error", "vpd_abi_version", "vpd_device_status",
            "vpd_launch_count", "vpd_test_withhold_copy", "vpd_jsd_linear_workspace", "vpd_jsd_linear_fwd",
-           "vpd_jsd_linear_bwd", "vpd_jsd_linear_fwd_noalloc")
+           "vpd_jsd_linear_bwd", "vpd_jsd_linear_fwd_noalloc", "vpd_cross_entropy_fwd", "vpd_cross_entropy_bwd",
+           "vpd_topk_kl_fwd", "vpd_topk_kl_bwd")
 
 
 class VpdError(RuntimeError):
@@ -103,6 +104,10 @@ def _declare(lib):
         "vpd_jsd_linear_fwd": [P(vpd_linear_heads), dbl, f, f, vp, ctypes.c_size_t, vp],
         "vpd_jsd_linear_bwd": [P(vpd_linear_heads), dbl, f, f, f, f, f, f, f, vp, ctypes.c_size_t, vp],
         "vpd_jsd_linear_fwd_noalloc": [P(vpd_linear_heads), dbl, f, f, vp],
+        "vpd_cross_entropy_fwd": [V, S, f, i64, dbl, f, f, f, vp],
+        "vpd_cross_entropy_bwd": [V, S, f, i64, dbl, f, f, G, vp],
+        "vpd_topk_kl_fwd": [V, S, f, i32, i64, f, dbl, f, f, f, vp],
+        "vpd_topk_kl_bwd": [V, S, f, i32, i64, f, dbl, f, f, G, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -387,6 +392,58 @@ def vpd_jsd_linear_bwd(heads: vpd_linear_heads, beta, grad_loss, loss, saved, dh
                                      _fptr(dh_s, n * hs, "dh_s"), _fptr(dw_s, v * hs, "dw_s"),
                                      _fptr(dh_t, n * ht, "dh_t"), _fptr(dw_t, v * ht, "dw_t"), wp, wn,
                                      _stream(stream)))
+
+
+def _flag_ptr(err_flag):
+    if err_flag is None:
+        return None
+    if err_flag.dtype != torch.int32 or err_flag.numel() < 1:
+        raise ValueError("err_flag must be an int32 CUDA tensor of at least one element, or None")
+    _on_current_device(err_flag, "err_flag")
+    return err_flag.data_ptr()
+
+
+def vpd_cross_entropy_fwd(x, segments, labels, ignore_index, temperature, loss, saved, err_flag, stream=None):
+    vx = make_view(x)
+    n, _ = _rows_vocab(vx)
+    seg, _keep = make_segments(segments)
+    _check(load().vpd_cross_entropy_fwd(ctypes.byref(vx), _ref(seg), _index_ptr(labels, n), int(ignore_index),
+                                        float(temperature), _fptr(loss, n, "loss"),
+                                        _fptr(saved, n * SAVED_LOGPROBS, "saved"), _flag_ptr(err_flag),
+                                        _stream(stream)))
+
+
+def vpd_cross_entropy_bwd(x, segments, labels, ignore_index, temperature, grad_loss, saved, dx, stream=None):
+    vx = make_view(x)
+    n, v = _rows_vocab(vx)
+    seg, _keep = make_segments(segments)
+    gx = make_grad(dx, n, v)
+    _check(load().vpd_cross_entropy_bwd(ctypes.byref(vx), _ref(seg), _index_ptr(labels, n), int(ignore_index),
+                                        float(temperature), _fptr(grad_loss, n, "grad_loss"),
+                                        _fptr(saved, n * SAVED_LOGPROBS, "saved"), _ref(gx), _stream(stream)))
+
+
+def vpd_topk_kl_fwd(s, segments, index, k, ignore_index, teacher_logp, temperature, kl, saved, err_flag,
+                    stream=None):
+    vs = make_view(s)
+    n, _ = _rows_vocab(vs)
+    seg, _keep = make_segments(segments)
+    _check(load().vpd_topk_kl_fwd(ctypes.byref(vs), _ref(seg), _index_ptr(index, n * int(k)), int(k),
+                                  int(ignore_index), _fptr(teacher_logp, n * int(k), "teacher_logp"),
+                                  float(temperature), _fptr(kl, n, "kl"), _fptr(saved, n * SAVED_LOGPROBS, "saved"),
+                                  _flag_ptr(err_flag), _stream(stream)))
+
+
+def vpd_topk_kl_bwd(s, segments, index, k, ignore_index, teacher_logp, temperature, grad_kl, saved, ds,
+                    stream=None):
+    vs = make_view(s)
+    n, v = _rows_vocab(vs)
+    seg, _keep = make_segments(segments)
+    gs = make_grad(ds, n, v)
+    _check(load().vpd_topk_kl_bwd(ctypes.byref(vs), _ref(seg), _index_ptr(index, n * int(k)), int(k),
+                                  int(ignore_index), _fptr(teacher_logp, n * int(k), "teacher_logp"),
+                                  float(temperature), _fptr(grad_kl, n, "grad_kl"),
+                                  _fptr(saved, n * SAVED_LOGPROBS, "saved"), _ref(gs), _stream(stream)))
 
 
 def vpd_device_status(stream=None):

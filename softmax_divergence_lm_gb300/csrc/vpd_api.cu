@@ -301,52 +301,121 @@ vpd_status vpd_entropy_bwd(const vpd_view* x, const vpd_segments* seg, const flo
   return ok();
 }
 
-vpd_status vpd_logprobs_fwd(const vpd_view* x, const vpd_segments* seg, const int64_t* index,
-                            int32_t k, int64_t ignore_index, float* out, float* saved,
-                            int32_t* err_flag, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The pages' synchronising index check ([ops page], review thread "Provide a
+// path for reusing validated shard metadata"): without a device flag the
+// indices are copied to the host on the caller's stream and checked before
+// anything is launched or written.
+vpd_status check_indices_on_host(const int64_t* index, int64_t count, int64_t ignore_index, int64_t vocab,
+                                 cudaStream_t st, const char* who) {
+  std::vector<int64_t> h(static_cast<size_t>(count));
+  VPD_CUDA(cudaMemcpyAsync(h.data(), index, h.size() * sizeof(int64_t), cudaMemcpyDeviceToHost, st), "reading index");
+  VPD_CUDA(cudaStreamSynchronize(st), "reading index");
+  for (size_t i = 0; i < h.size(); ++i)
+    if (h[i] != ignore_index && (h[i] < 0 || h[i] >= vocab))
+      return fail(VPD_ERR_INDEX, "%s: index[%lld] = %lld outside [0, %lld)", who, static_cast<long long>(i),
+                  static_cast<long long>(h[i]), static_cast<long long>(vocab));
+  return VPD_OK;
+}
+
+vpd_status check_temperature(double temperature, float* inv) {
+  if (!(temperature > 0.0) || !std::isfinite(temperature))
+    return fail(VPD_ERR_ARG, "temperature %g must be positive and finite", temperature);
+  *inv = static_cast<float>(1.0 / temperature);
+  return VPD_OK;
+}
+
+// Shared forward of the selection ops: validation, the flag or the host index
+// check, then the kernel.
+vpd_status select_fwd(const vpd_view* x, const vpd_segments* seg, const int64_t* index, int32_t k,
+                      int64_t ignore_index, double temperature, int mode, const float* teacher_logp, float* out,
+                      float* row_out, float* saved, int32_t* err_flag, void* stream, const char* who) {
   vpd::View vx;
   vpd::Segs sg;
+  float inv = 1.f;
   VPD_TRY(check_view(x, "x", &vx));
   VPD_TRY(check_segments(seg, vx.vocab, &sg));
-  if (k < 1) return fail(VPD_ERR_ARG, "vpd_logprobs_fwd: k must be >= 1");
+  VPD_TRY(check_temperature(temperature, &inv));
+  if (k < 1) return fail(VPD_ERR_ARG, "%s: k must be >= 1", who);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (err_flag) VPD_CUDA(cudaMemsetAsync(err_flag, 0, sizeof(int32_t), st), "clearing err_flag");
   if (vx.rows == 0) return ok();
-  if (!index || !out) return fail(VPD_ERR_ARG, "vpd_logprobs_fwd: index and out are required");
-  if (!err_flag) {
-    // No flag: the indices are checked on the host first (a copy on the
-    // caller's stream, then a synchronisation), so a bad index is an error
-    // before anything is launched or written.
-    std::vector<int64_t> h(static_cast<size_t>(vx.rows) * static_cast<size_t>(k));
-    VPD_CUDA(cudaMemcpyAsync(h.data(), index, h.size() * sizeof(int64_t), cudaMemcpyDeviceToHost, st),
-             "reading index");
-    VPD_CUDA(cudaStreamSynchronize(st), "reading index");
-    for (size_t i = 0; i < h.size(); ++i)
-      if (h[i] != ignore_index && (h[i] < 0 || h[i] >= vx.vocab))
-        return fail(VPD_ERR_INDEX, "vpd_logprobs_fwd: index[%lld] = %lld outside [0, %lld)",
-                    static_cast<long long>(i), static_cast<long long>(h[i]), static_cast<long long>(vx.vocab));
-  }
-  VPD_CUDA(vpd::launch_logprobs_fwd(vx, sg, index, k, ignore_index, out, saved, err_flag, st),
-           "log-prob kernel");
+  if (!index || (mode == 0 && !out) || (mode != 0 && !row_out) || (mode == 2 && !teacher_logp))
+    return fail(VPD_ERR_ARG, "%s: a required pointer is NULL", who);
+  if (!err_flag) VPD_TRY(check_indices_on_host(index, vx.rows * k, ignore_index, vx.vocab, st, who));
+  VPD_CUDA(vpd::launch_select_fwd(vx, sg, index, k, ignore_index, inv, mode, teacher_logp, out, row_out, saved,
+                                  err_flag, st),
+           "selection kernel");
   return ok();
 }
 
-vpd_status vpd_logprobs_bwd(const vpd_view* x, const vpd_segments* seg, const int64_t* index,
-                            int32_t k, int64_t ignore_index, const float* grad_out,
-                            const float* saved, const vpd_grad* dx, void* stream) {
+vpd_status select_bwd(const vpd_view* x, const vpd_segments* seg, const int64_t* index, int32_t k,
+                      int64_t ignore_index, double temperature, int mode, const float* teacher_logp,
+                      const float* grad, const float* saved, const vpd_grad* dx, void* stream, const char* who) {
   vpd::View vx;
   vpd::Segs sg;
   vpd::Grad gx;
+  float inv = 1.f;
   VPD_TRY(check_view(x, "x", &vx));
   VPD_TRY(check_segments(seg, vx.vocab, &sg));
   VPD_TRY(check_grad(dx, "dx", vx.vocab, vx.rows, &gx));
-  if (k < 1) return fail(VPD_ERR_ARG, "vpd_logprobs_bwd: k must be >= 1");
+  VPD_TRY(check_temperature(temperature, &inv));
+  if (k < 1) return fail(VPD_ERR_ARG, "%s: k must be >= 1", who);
   if (vx.rows == 0 || !gx.data) return ok();
-  if (!index || !saved) return fail(VPD_ERR_ARG, "vpd_logprobs_bwd: index and saved are required");
-  VPD_CUDA(vpd::launch_logprobs_bwd(vx, index, k, ignore_index, grad_out, saved, gx,
-                                    static_cast<cudaStream_t>(stream)),
-           "log-prob backward kernel");
+  if (!index || !saved || (mode == 2 && !teacher_logp))
+    return fail(VPD_ERR_ARG, "%s: index, saved (and the teacher log-probs) are required", who);
+  VPD_CUDA(vpd::launch_select_bwd(vx, index, k, ignore_index, inv, mode, teacher_logp, grad, saved, gx,
+                                  static_cast<cudaStream_t>(stream)),
+           "selection backward kernel");
   return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+vpd_status vpd_logprobs_fwd(const vpd_view* x, const vpd_segments* seg, const int64_t* index, int32_t k,
+                            int64_t ignore_index, float* out, float* saved, int32_t* err_flag, void* stream) {
+  return select_fwd(x, seg, index, k, ignore_index, 1.0, 0, nullptr, out, nullptr, saved, err_flag, stream,
+                    "vpd_logprobs_fwd");
+}
+
+vpd_status vpd_logprobs_bwd(const vpd_view* x, const vpd_segments* seg, const int64_t* index, int32_t k,
+                            int64_t ignore_index, const float* grad_out, const float* saved, const vpd_grad* dx,
+                            void* stream) {
+  return select_bwd(x, seg, index, k, ignore_index, 1.0, 0, nullptr, grad_out, saved, dx, stream,
+                    "vpd_logprobs_bwd");
+}
+
+vpd_status vpd_cross_entropy_fwd(const vpd_view* x, const vpd_segments* seg, const int64_t* labels,
+                                 int64_t ignore_index, double temperature, float* loss, float* saved,
+                                 int32_t* err_flag, void* stream) {
+  return select_fwd(x, seg, labels, 1, ignore_index, temperature, 1, nullptr, nullptr, loss, saved, err_flag, stream,
+                    "vpd_cross_entropy_fwd");
+}
+
+vpd_status vpd_cross_entropy_bwd(const vpd_view* x, const vpd_segments* seg, const int64_t* labels,
+                                 int64_t ignore_index, double temperature, const float* grad_loss, const float* saved,
+                                 const vpd_grad* dx, void* stream) {
+  return select_bwd(x, seg, labels, 1, ignore_index, temperature, 1, nullptr, grad_loss, saved, dx, stream,
+                    "vpd_cross_entropy_bwd");
+}
+
+vpd_status vpd_topk_kl_fwd(const vpd_view* s, const vpd_segments* seg, const int64_t* index, int32_t k,
+                           int64_t ignore_index, const float* teacher_logp, double temperature, float* kl,
+                           float* saved, int32_t* err_flag, void* stream) {
+  return select_fwd(s, seg, index, k, ignore_index, temperature, 2, teacher_logp, nullptr, kl, saved, err_flag,
+                    stream, "vpd_topk_kl_fwd");
+}
+
+vpd_status vpd_topk_kl_bwd(const vpd_view* s, const vpd_segments* seg, const int64_t* index, int32_t k,
+                           int64_t ignore_index, const float* teacher_logp, double temperature,
+                           const float* grad_kl, const float* saved, const vpd_grad* ds, void* stream) {
+  return select_bwd(s, seg, index, k, ignore_index, temperature, 2, teacher_logp, grad_kl, saved, ds, stream,
+                    "vpd_topk_kl_bwd");
 }
 
 }  // extern "C"

@@ -45,12 +45,17 @@ cudaError_t launch_entropy_fwd(const View& x, const Segs& seg, float* out, float
                                cudaStream_t stream);
 cudaError_t launch_entropy_bwd(const View& x, const float* grad, const float* saved, const Grad& dx,
                                cudaStream_t stream);
-cudaError_t launch_logprobs_fwd(const View& x, const Segs& seg, const int64_t* index, int k,
-                                int64_t ignore_index, float* out, float* saved, int32_t* err_flag,
-                                cudaStream_t stream);
-cudaError_t launch_logprobs_bwd(const View& x, const int64_t* index, int k, int64_t ignore_index,
-                                const float* grad, const float* saved, const Grad& dx,
-                                cudaStream_t stream);
+// Selected log-probabilities and the ops built on them: mode 0 the log-probs
+// at index [N, k] into out [N, k]; mode 1 the cross-entropy at one label per
+// row (k = 1) into row_out [N]; mode 2 the teacher top-k forward KL with the
+// teacher's log-probs teacher_logp [N, k] into row_out [N]. inv_temperature
+// scales the logits before the softmax (1: none).
+cudaError_t launch_select_fwd(const View& x, const Segs& seg, const int64_t* index, int k, int64_t ignore_index,
+                              float inv_temperature, int mode, const float* teacher_logp, float* out,
+                              float* row_out, float* saved, int32_t* err_flag, cudaStream_t stream);
+cudaError_t launch_select_bwd(const View& x, const int64_t* index, int k, int64_t ignore_index,
+                              float inv_temperature, int mode, const float* teacher_logp, const float* grad,
+                              const float* saved, const Grad& dx, cudaStream_t stream);
 
 // Single-read fused JSD forward+backward on thread-block clusters. Returns
 // cudaErrorNotSupported (without launching) when the row pair does not fit on

@@ -824,7 +824,12 @@ __global__ void __launch_bounds__(kThreads) k_entropy_bwd(View x, const float* g
 }
 
 // ===========================================================================
-// Selected / top-k log-probabilities.
+// Selected / top-k log-probabilities, and the two thin ops built on them
+// ([ops page], "What"): the per-token cross-entropy at a label (-ln p_label)
+// and the teacher top-k forward KL, sum_k e^{tl_k} (tl_k - ln p_{i_k}) with the
+// teacher's log-probs tl at its top-k ids. An optional temperature T divides
+// the logits before the softmax: the statistics are then taken of x / T (sc =
+// 1 / T), in the scaled domain.
 // ===========================================================================
 struct StatBody {
   static constexpr bool kRaw = true;
@@ -841,27 +846,69 @@ struct StatBody {
   __device__ __forceinline__ void one(int64_t, float x) { stat_add1(s, x); }
 };
 
-template <class T>
-__global__ void __launch_bounds__(kThreads) k_logprobs_fwd(View x, Segs seg, const int64_t* index,
-                                                           int K, int64_t ignore, float* out,
-                                                           float* saved, int32_t* err) {
+// Statistics of x / T (x * sc): (max, sum-exp) of the scaled logits.
+struct ScaledStatBody {
+  Stat s;
+  float sc;
+  template <int N>
+  __device__ __forceinline__ void vec(int64_t, const float (&x)[N]) {
+    float y[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) y[i] = x[i] * sc;
+    stat_add<N>(s, y);
+  }
+  __device__ __forceinline__ void one(int64_t, float x) { stat_add1(s, x * sc); }
+};
+
+// What the selection computes: the log-probs themselves, the cross-entropy at
+// one label per row, or the teacher top-k forward KL.
+enum SelMode : int { kSelLogprobs = 0, kSelCrossEntropy = 1, kSelTopkKL = 2 };
+
+struct Sel {
+  const int64_t* index;  // [N, K]
+  int K;
+  int64_t ignore;
+  float sc;              // 1 / T
+  int mode;
+  const float* tl;       // kSelTopkKL: teacher log-probs [N, K]
+};
+
+// Weight of position k of row r in the top-k KL: e^{tl}, or 0 where the id is
+// ignored or the teacher has no mass.
+__device__ __forceinline__ float topk_weight(const Sel& q, int64_t r, int k, int64_t i) {
+  if (i == q.ignore) return 0.f;
+  const float t = q.tl[r * q.K + k];
+  return t == neg_inf() ? 0.f : expf(t);
+}
+
+template <class T, bool SCALED>
+__global__ void __launch_bounds__(kThreads) k_select_fwd(View x, Segs seg, Sel q, float* out, float* row_out,
+                                                         float* saved, int32_t* err) {
   __shared__ float scratch[64];
   for (int64_t r = blockIdx.x; r < x.rows; r += gridDim.x) {
     const char* px = row_ptr<T>(x, r);
     Stat run[1] = {stat_init()};
     for (int k = 0; k < seg.count; ++k) {
       const int64_t off = seg.off[k], w = seg.off[k + 1] - off;
-      StatBody body{stat_init()};
-      visit1<T>(px + off * T::kSize, w, body);
-      Stat part[1] = {body.s};
+      Stat part[1];
+      if constexpr (SCALED) {
+        ScaledStatBody body{stat_init(), q.sc};
+        visit1<T>(px + off * T::kSize, w, body);
+        part[0] = body.s;
+      } else {
+        StatBody body{stat_init()};
+        visit1<T>(px + off * T::kSize, w, body);
+        part[0] = body.s;
+      }
       block_stat<1>(part, scratch);
       run[0] = stat_merge(run[0], part[0]);
     }
-    const RowStat st = finish_stat(run[0]);
-    for (int k = threadIdx.x; k < K; k += blockDim.x) {
-      const int64_t i = index[r * K + k];
+    const RowStat st = finish_stat(run[0]);  // of x * sc when SCALED
+    float acc[1] = {0.f};
+    for (int k = threadIdx.x; k < q.K; k += blockDim.x) {
+      const int64_t i = q.index[r * q.K + k];
       float v;
-      if (i == ignore) {
+      if (i == q.ignore) {
         v = 0.f;
       } else if (i < 0 || i >= x.vocab) {
         v = qnan();
@@ -870,9 +917,22 @@ __global__ void __launch_bounds__(kThreads) k_logprobs_fwd(View x, Segs seg, con
         v = qnan();
       } else {
         const float xi = T::load(px, i);
-        v = xi == neg_inf() ? neg_inf() : (xi - st.m) - st.L;
+        v = xi == neg_inf() ? neg_inf() : ((SCALED ? xi * q.sc : xi) - st.m) - st.L;
       }
-      out[r * K + k] = v;
+      if (q.mode == kSelLogprobs) {
+        out[r * q.K + k] = v;
+      } else if (q.mode == kSelCrossEntropy) {
+        acc[0] += -v;  // K = 1
+      } else {
+        const float wk = (i >= 0 && i < x.vocab) || i == q.ignore ? topk_weight(q, r, k, i) : 0.f;
+        const float tk = i == q.ignore ? 0.f : q.tl[r * q.K + k];
+        if (isnan(v)) acc[0] += v;
+        else if (wk > 0.f) acc[0] += wk * (tk - v);  // v = -inf with teacher mass: +inf
+      }
+    }
+    if (q.mode != kSelLogprobs) {
+      block_sum<1>(acc, scratch);
+      if (threadIdx.x == 0) row_out[r] = stat_ok(st) ? acc[0] : qnan();
     }
     if (saved && threadIdx.x == 0) {
       saved[r * VPD_SAVED_LOGPROBS] = st.m;
@@ -881,11 +941,12 @@ __global__ void __launch_bounds__(kThreads) k_logprobs_fwd(View x, Segs seg, con
   }
 }
 
-template <class G>
+template <class G, bool SCALED>
 struct LpBwdBody {
-  float m, L, G_;
+  float m, L, G_, sc;
   char* dx;
   __device__ __forceinline__ float grad(float x) const {
+    if (SCALED) return x != neg_inf() ? -G_ * sc * expd((x * sc - m) - L) : 0.f;
     return x != neg_inf() ? -G_ * expd((x - m) - L) : 0.f;
   }
   __device__ __forceinline__ void one(int64_t j, float x) { G::store(dx, j, grad(x)); }
@@ -898,11 +959,11 @@ struct LpBwdBody {
   }
 };
 
-template <class T, class G>
-__global__ void __launch_bounds__(kThreads) k_logprobs_bwd(View x, const int64_t* index, int K,
-                                                           int64_t ignore, const float* grad,
-                                                           const float* saved, Grad dx) {
+template <class T, class G, bool SCALED>
+__global__ void __launch_bounds__(kThreads) k_select_bwd(View x, Sel q, const float* grad, const float* saved,
+                                                         Grad dx) {
   __shared__ float scratch[32];
+  __shared__ int iscratch[32];
   for (int64_t r = blockIdx.x; r < x.rows; r += gridDim.x) {
     const char* px = row_ptr<T>(x, r);
     char* rd = dx.data + r * dx.row_stride * G::kSize;
@@ -913,35 +974,55 @@ __global__ void __launch_bounds__(kThreads) k_logprobs_bwd(View x, const int64_t
     }
     // a position takes gradient when its index is valid and its log-prob finite
     auto takes = [&](int k, int64_t& i) -> bool {
-      i = index[r * K + k];
-      if (i == ignore || i < 0 || i >= x.vocab) return false;
+      i = q.index[r * q.K + k];
+      if (i == q.ignore || i < 0 || i >= x.vocab) return false;
       return T::load(px, i) != neg_inf();
     };
+    // the upstream gradient of position k
+    auto up = [&](int k, int64_t i) -> float {
+      if (q.mode == kSelLogprobs) return grad ? grad[r * q.K + k] : 1.f;
+      const float g = grad ? grad[r] : 1.f;
+      if (q.mode == kSelCrossEntropy) return -g;
+      return -g * topk_weight(q, r, k, i);
+    };
+    if (q.mode == kSelTopkKL) {
+      // +inf KL (an id the teacher gives mass that the student masks): no gradient
+      int inf_row = 0;
+      for (int k = threadIdx.x; k < q.K; k += blockDim.x) {
+        const int64_t i = q.index[r * q.K + k];
+        if (i != q.ignore && i >= 0 && i < x.vocab && topk_weight(q, r, k, i) > 0.f && T::load(px, i) == neg_inf())
+          inf_row = 1;
+      }
+      if (block_or(inf_row, iscratch)) {
+        zero_row<G>(rd, x.vocab);
+        continue;
+      }
+    }
     float gsum[1] = {0.f};
-    for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    for (int k = threadIdx.x; k < q.K; k += blockDim.x) {
       int64_t i;
-      if (takes(k, i)) gsum[0] += grad ? grad[r * K + k] : 1.f;
+      if (takes(k, i)) gsum[0] += up(k, i);
     }
     block_sum<1>(gsum, scratch);
-    LpBwdBody<G> b{st.m, st.L, gsum[0], rd};
+    LpBwdBody<G, SCALED> b{st.m, st.L, gsum[0], q.sc, rd};
     visit1<T>(px, x.vocab, b);
     __syncthreads();
-    // the selected tokens: sum of their upstream gradients minus p_j G
-    for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    // the selected tokens: the sum of their upstream gradients minus p_j G (times sc)
+    for (int k = threadIdx.x; k < q.K; k += blockDim.x) {
       int64_t i;
       if (!takes(k, i)) continue;
       bool first = true;
       float gi = 0.f;
-      for (int k2 = 0; k2 < K; ++k2) {
+      for (int k2 = 0; k2 < q.K; ++k2) {
         int64_t i2;
         if (!takes(k2, i2) || i2 != i) continue;
         if (k2 < k) {
           first = false;
           break;
         }
-        gi += grad ? grad[r * K + k2] : 1.f;
+        gi += up(k2, i2);
       }
-      if (first) G::store(rd, i, gi + b.grad(T::load(px, i)));
+      if (first) G::store(rd, i, (SCALED ? q.sc : 1.f) * gi + b.grad(T::load(px, i)));
     }
     __syncthreads();
   }
@@ -1069,26 +1150,32 @@ struct EntBwdByGrad {
 };
 
 template <class T>
-struct LpL {
-  static cudaError_t run(const View& x, const Segs& seg, const int64_t* idx, int k, int64_t ignore,
-                         float* out, float* saved, int32_t* err, cudaStream_t st) {
-    return launch_rows(k_logprobs_fwd<T>, x.rows, threads_for(x.vocab, T::kSize), st, x, seg, idx, k, ignore, out, saved, err);
+struct SelL {
+  static cudaError_t run(const View& x, const Segs& seg, const Sel& q, float* out, float* row_out, float* saved,
+                         int32_t* err, cudaStream_t st) {
+    if (q.sc != 1.f)
+      return launch_rows(k_select_fwd<T, true>, x.rows, threads_for(x.vocab, T::kSize), st, x, seg, q, out, row_out,
+                         saved, err);
+    return launch_rows(k_select_fwd<T, false>, x.rows, threads_for(x.vocab, T::kSize), st, x, seg, q, out, row_out,
+                       saved, err);
   }
 };
 
 template <class T, class G>
-struct LpBwdL {
-  static cudaError_t run(const View& x, const int64_t* idx, int k, int64_t ignore, const float* g,
-                         const float* saved, const Grad& dx, cudaStream_t st) {
-    return launch_rows(k_logprobs_bwd<T, G>, x.rows, threads_for(x.vocab, T::kSize), st, x, idx, k, ignore, g, saved, dx);
+struct SelBwdL {
+  static cudaError_t run(const View& x, const Sel& q, const float* g, const float* saved, const Grad& dx,
+                         cudaStream_t st) {
+    if (q.sc != 1.f)
+      return launch_rows(k_select_bwd<T, G, true>, x.rows, threads_for(x.vocab, T::kSize), st, x, q, g, saved, dx);
+    return launch_rows(k_select_bwd<T, G, false>, x.rows, threads_for(x.vocab, T::kSize), st, x, q, g, saved, dx);
   }
 };
 
 template <class T>
-struct LpBwdByGrad {
-  static cudaError_t run(const View& x, const int64_t* idx, int k, int64_t ignore, const float* g,
-                         const float* saved, const Grad& dx, cudaStream_t st) {
-    return by_grad<T, LpBwdL>(dx.dtype, x, idx, k, ignore, g, saved, dx, st);
+struct SelBwdByGrad {
+  static cudaError_t run(const View& x, const Sel& q, const float* g, const float* saved, const Grad& dx,
+                         cudaStream_t st) {
+    return by_grad<T, SelBwdL>(dx.dtype, x, q, g, saved, dx, st);
   }
 };
 
@@ -1144,16 +1231,18 @@ cudaError_t launch_entropy_bwd(const View& x, const float* grad, const float* sa
   return by_input<EntBwdByGrad>(x.dtype, x, grad, saved, dx, stream);
 }
 
-cudaError_t launch_logprobs_fwd(const View& x, const Segs& seg, const int64_t* index, int k,
-                                int64_t ignore_index, float* out, float* saved, int32_t* err_flag,
-                                cudaStream_t stream) {
-  return by_input<LpL>(x.dtype, x, seg, index, k, ignore_index, out, saved, err_flag, stream);
+cudaError_t launch_select_fwd(const View& x, const Segs& seg, const int64_t* index, int k, int64_t ignore_index,
+                              float inv_temperature, int mode, const float* teacher_logp, float* out,
+                              float* row_out, float* saved, int32_t* err_flag, cudaStream_t stream) {
+  const Sel q{index, k, ignore_index, inv_temperature, mode, teacher_logp};
+  return by_input<SelL>(x.dtype, x, seg, q, out, row_out, saved, err_flag, stream);
 }
 
-cudaError_t launch_logprobs_bwd(const View& x, const int64_t* index, int k, int64_t ignore_index,
-                                const float* grad, const float* saved, const Grad& dx,
-                                cudaStream_t stream) {
-  return by_input<LpBwdByGrad>(x.dtype, x, index, k, ignore_index, grad, saved, dx, stream);
+cudaError_t launch_select_bwd(const View& x, const int64_t* index, int k, int64_t ignore_index,
+                              float inv_temperature, int mode, const float* teacher_logp, const float* grad,
+                              const float* saved, const Grad& dx, cudaStream_t stream) {
+  const Sel q{index, k, ignore_index, inv_temperature, mode, teacher_logp};
+  return by_input<SelBwdByGrad>(x.dtype, x, q, grad, saved, dx, stream);
 }
 
 }  // namespace vpd

@@ -118,6 +118,58 @@ class _LogProbs(torch.autograd.Function):
         return dx, None, None, None, None
 
 
+class _CrossEntropy(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, labels, ignore_index, temperature, segments):
+        n = _rows(x)
+        lab = labels.reshape(n).to(torch.int64).contiguous()
+        loss = torch.empty(n, dtype=torch.float32, device=x.device)
+        saved = torch.empty(n, B.SAVED_LOGPROBS, dtype=torch.float32, device=x.device)
+        err = torch.empty(1, dtype=torch.int32, device=x.device)
+        B.vpd_cross_entropy_fwd(x, segments, lab, ignore_index, temperature, loss, saved, err)
+        if int(err.item()):
+            raise IndexError("cross_entropy: a label is outside [0, V) and is not ignore_index")
+        ctx.save_for_backward(x, lab, saved)
+        ctx.ignore_index, ctx.temperature, ctx.segments = ignore_index, temperature, segments
+        return loss.view(_out_shape(x))
+
+    @staticmethod
+    @once_differentiable
+    def backward(ctx, g):
+        x, lab, saved = ctx.saved_tensors
+        dx = _grad_like(x)
+        B.vpd_cross_entropy_bwd(x, ctx.segments, lab, ctx.ignore_index, ctx.temperature,
+                                g.reshape(-1).to(torch.float32).contiguous(), saved, dx)
+        return dx, None, None, None, None
+
+
+class _TopkKL(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, s, index, teacher_logp, ignore_index, temperature, segments):
+        n = _rows(s)
+        idx = index.reshape(n, -1).to(torch.int64).contiguous()
+        k = idx.shape[1]
+        tl = teacher_logp.reshape(n, k).to(torch.float32).contiguous()
+        kl = torch.empty(n, dtype=torch.float32, device=s.device)
+        saved = torch.empty(n, B.SAVED_LOGPROBS, dtype=torch.float32, device=s.device)
+        err = torch.empty(1, dtype=torch.int32, device=s.device)
+        B.vpd_topk_kl_fwd(s, segments, idx, k, ignore_index, tl, temperature, kl, saved, err)
+        if int(err.item()):
+            raise IndexError("topk_forward_kl: an index is outside [0, V) and is not ignore_index")
+        ctx.save_for_backward(s, idx, tl, saved)
+        ctx.k, ctx.ignore_index, ctx.temperature, ctx.segments = k, ignore_index, temperature, segments
+        return kl.view(_out_shape(s))
+
+    @staticmethod
+    @once_differentiable
+    def backward(ctx, g):
+        s, idx, tl, saved = ctx.saved_tensors
+        ds = _grad_like(s)
+        B.vpd_topk_kl_bwd(s, ctx.segments, idx, ctx.k, ctx.ignore_index, tl, ctx.temperature,
+                          g.reshape(-1).to(torch.float32).contiguous(), saved, ds)
+        return ds, None, None, None, None, None
+
+
 def _seg(segments):
     return None if segments is None else tuple(int(w) for w in segments)
 
@@ -158,3 +210,18 @@ def jsd_fwdbwd(student, teacher, beta, grad_loss=None, segments=None, grad_dtype
     dt = torch.empty(teacher.shape, dtype=gd, device=dev) if teacher_grad else None
     B.vpd_jsd_fwdbwd(student, teacher, float(beta), _seg(segments), grad_loss, loss, saved, ds, dt)
     return loss.view(_out_shape(student)), saved, ds, dt
+
+
+def cross_entropy(logits: torch.Tensor, labels: torch.Tensor, ignore_index: int = -100, temperature: float = 1.0,
+                  segments=None) -> torch.Tensor:
+    """Per-token -log softmax(logits / temperature)[label]; ignore_index gives 0."""
+    return _CrossEntropy.apply(logits, labels, int(ignore_index), float(temperature), _seg(segments))
+
+
+def topk_forward_kl(student: torch.Tensor, teacher_topk_ids: torch.Tensor, teacher_topk_logp: torch.Tensor,
+                    ignore_index: int = -100, temperature: float = 1.0, segments=None) -> torch.Tensor:
+    """Teacher top-k forward KL per token ('Add vocabulary-parallel logprobs,
+    entropy and KL ops', section What): sum_k exp(tl_k) (tl_k - log p_s[id_k]),
+    the teacher's top-k log-probs tl given (detached)."""
+    return _TopkKL.apply(student, teacher_topk_ids, teacher_topk_logp, int(ignore_index), float(temperature),
+                         _seg(segments))
