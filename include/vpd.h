@@ -229,6 +229,36 @@ vpd_status vpd_logprobs_bwd(const vpd_view *x, const vpd_segments *seg, const in
                             const float *saved, const vpd_grad *dx, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * Vocabulary-parallel JSD / KL ([ops page], "How"; [JSD page], "Changes"): each
+ * process holds one ordered vocabulary shard [N, V_k] of both inputs (V_k may
+ * be 0) and the forward exchanges only [N]-sized statistics, through three
+ * all-reduces that the caller runs on the [N, 2] float buffer xbuf (NCCL or
+ * any collective library; the library itself communicates with nobody):
+ *   vpd_jsd_shard_stats       local statistics into saved; xbuf = (m_s, m_t)
+ *   -> all-reduce MAX (xbuf)
+ *   vpd_jsd_shard_rescale     saved keeps the global maxima; xbuf = the
+ *                             shard's sums rescaled to them
+ *   -> all-reduce SUM (xbuf)
+ *   vpd_jsd_shard_divergence  saved gets the global log-sum-exps; loss and
+ *                             xbuf get the shard's partial (A, B)
+ *   -> all-reduce SUM (xbuf)
+ *   vpd_jsd_shard_finish      loss = the per-token value, saved = [N, 6] as
+ *                             vpd_jsd_fwd writes it, identical on every shard
+ * The backward needs no exchange: vpd_jsd_bwd on the shard with that saved
+ * gives the shard's columns of dS and dT. beta = 0 / 1 are the forward /
+ * reverse KL branches (a support violation on any shard makes the row +inf).
+ * A row outside the contract on any shard travels as +inf through the MAX and
+ * NaN through the SUMs, so every process ends with the same NaN row.
+ * saved: device float[N, 6]; xbuf: device float[N, 2]; all on `stream`.
+ * ------------------------------------------------------------------------- */
+vpd_status vpd_jsd_shard_stats(const vpd_view *s, const vpd_view *t, float *saved, float *xbuf, void *stream);
+vpd_status vpd_jsd_shard_rescale(int64_t rows, float *saved, float *xbuf, void *stream);
+vpd_status vpd_jsd_shard_divergence(const vpd_view *s, const vpd_view *t, double beta, float *loss,
+                                    float *saved, float *xbuf, void *stream);
+vpd_status vpd_jsd_shard_finish(int64_t rows, double beta, float *saved, const float *xbuf, float *loss,
+                                void *stream);
+
+/* ---------------------------------------------------------------------------
  * Two thin ops on the selected log-probabilities ([ops page], "What": the
  * teacher top-k forward KL written with the log-prob op; "How": the
  * cross-entropy op that validates its shard layout the same way), each with an

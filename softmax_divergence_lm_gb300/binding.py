@@ -34,7 +34,8 @@ SYMBOLS = ("vpd_jsd_fwd", "vpd_jsd_bwd", "vpd_jsd_fwdbwd", "vpd_kl_fwd", "vpd_kl
            "vpd_status_string", "vpd_last_error", "vpd_abi_version", "vpd_device_status",
            "vpd_launch_count", "vpd_test_withhold_copy", "vpd_jsd_linear_workspace", "vpd_jsd_linear_fwd",
            "vpd_jsd_linear_bwd", "vpd_jsd_linear_fwd_noalloc", "vpd_cross_entropy_fwd", "vpd_cross_entropy_bwd",
-           "vpd_topk_kl_fwd", "vpd_topk_kl_bwd")
+           "vpd_topk_kl_fwd", "vpd_topk_kl_bwd", "vpd_jsd_shard_stats", "vpd_jsd_shard_rescale",
+           "vpd_jsd_shard_divergence", "vpd_jsd_shard_finish")
 
 
 class VpdError(RuntimeError):
@@ -108,6 +109,10 @@ def _declare(lib):
         "vpd_cross_entropy_bwd": [V, S, f, i64, dbl, f, f, G, vp],
         "vpd_topk_kl_fwd": [V, S, f, i32, i64, f, dbl, f, f, f, vp],
         "vpd_topk_kl_bwd": [V, S, f, i32, i64, f, dbl, f, f, G, vp],
+        "vpd_jsd_shard_stats": [V, V, f, f, vp],
+        "vpd_jsd_shard_rescale": [i64, f, f, vp],
+        "vpd_jsd_shard_divergence": [V, V, dbl, f, f, f, vp],
+        "vpd_jsd_shard_finish": [i64, dbl, f, f, f, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -444,6 +449,31 @@ def vpd_topk_kl_bwd(s, segments, index, k, ignore_index, teacher_logp, temperatu
                                   int(ignore_index), _fptr(teacher_logp, n * int(k), "teacher_logp"),
                                   float(temperature), _fptr(grad_kl, n, "grad_kl"),
                                   _fptr(saved, n * SAVED_LOGPROBS, "saved"), _ref(gs), _stream(stream)))
+
+
+def vpd_jsd_shard_stats(s, t, saved, xbuf, stream=None):
+    vs, vt, n, _ = _pair(s, t)
+    _check(load().vpd_jsd_shard_stats(ctypes.byref(vs), ctypes.byref(vt), _fptr(saved, n * SAVED_PAIR, "saved"),
+                                      _fptr(xbuf, n * 2, "xbuf"), _stream(stream)))
+
+
+def vpd_jsd_shard_rescale(rows, saved, xbuf, stream=None):
+    n = int(rows)
+    _check(load().vpd_jsd_shard_rescale(n, _fptr(saved, n * SAVED_PAIR, "saved"), _fptr(xbuf, n * 2, "xbuf"),
+                                        _stream(stream)))
+
+
+def vpd_jsd_shard_divergence(s, t, beta, loss, saved, xbuf, stream=None):
+    vs, vt, n, _ = _pair(s, t)
+    _check(load().vpd_jsd_shard_divergence(ctypes.byref(vs), ctypes.byref(vt), float(beta), _fptr(loss, n, "loss"),
+                                           _fptr(saved, n * SAVED_PAIR, "saved"), _fptr(xbuf, n * 2, "xbuf"),
+                                           _stream(stream)))
+
+
+def vpd_jsd_shard_finish(rows, beta, saved, xbuf, loss, stream=None):
+    n = int(rows)
+    _check(load().vpd_jsd_shard_finish(n, float(beta), _fptr(saved, n * SAVED_PAIR, "saved"),
+                                       _fptr(xbuf, n * 2, "xbuf"), _fptr(loss, n, "loss"), _stream(stream)))
 
 
 def vpd_device_status(stream=None):

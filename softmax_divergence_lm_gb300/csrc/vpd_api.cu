@@ -445,6 +445,45 @@ vpd_status check_heads(const vpd_linear_heads* p, vpd::LinearProblem* out) {
 
 extern "C" {
 
+vpd_status vpd_jsd_shard_stats(const vpd_view* s, const vpd_view* t, float* saved, float* xbuf, void* stream) {
+  vpd::View vs, vt;
+  VPD_TRY(check_pair(s, t, &vs, &vt));
+  if (vs.rows == 0) return ok();
+  if (!saved || !xbuf) return fail(VPD_ERR_ARG, "vpd_jsd_shard_stats: saved and xbuf are required");
+  VPD_CUDA(vpd::shard_stats(vs, vt, saved, xbuf, static_cast<cudaStream_t>(stream)), "shard statistics");
+  return ok();
+}
+
+vpd_status vpd_jsd_shard_rescale(int64_t rows, float* saved, float* xbuf, void* stream) {
+  if (rows < 0) return fail(VPD_ERR_SHAPE, "rows must be >= 0");
+  if (rows == 0) return ok();
+  if (!saved || !xbuf) return fail(VPD_ERR_ARG, "vpd_jsd_shard_rescale: saved and xbuf are required");
+  VPD_CUDA(vpd::shard_rescale(rows, saved, xbuf, static_cast<cudaStream_t>(stream)), "shard rescale");
+  return ok();
+}
+
+vpd_status vpd_jsd_shard_divergence(const vpd_view* s, const vpd_view* t, double beta, float* loss, float* saved,
+                                    float* xbuf, void* stream) {
+  vpd::View vs, vt;
+  VPD_TRY(check_pair(s, t, &vs, &vt));
+  VPD_TRY(check_beta(beta));
+  if (vs.rows == 0) return ok();
+  if (!loss || !saved || !xbuf) return fail(VPD_ERR_ARG, "vpd_jsd_shard_divergence: loss, saved and xbuf are required");
+  VPD_CUDA(vpd::shard_divergence(vs, vt, beta, loss, saved, xbuf, static_cast<cudaStream_t>(stream)),
+           "shard divergence");
+  return ok();
+}
+
+vpd_status vpd_jsd_shard_finish(int64_t rows, double beta, float* saved, const float* xbuf, float* loss,
+                                void* stream) {
+  VPD_TRY(check_beta(beta));
+  if (rows < 0) return fail(VPD_ERR_SHAPE, "rows must be >= 0");
+  if (rows == 0) return ok();
+  if (!saved || !xbuf || !loss) return fail(VPD_ERR_ARG, "vpd_jsd_shard_finish: saved, xbuf and loss are required");
+  VPD_CUDA(vpd::shard_finish(rows, beta, saved, xbuf, loss, static_cast<cudaStream_t>(stream)), "shard finish");
+  return ok();
+}
+
 vpd_status vpd_jsd_linear_workspace(const vpd_linear_heads* heads, int32_t student_grads, int32_t teacher_grads,
                                     size_t* fwd_bytes, size_t* bwd_bytes) {
   vpd::LinearProblem p;

@@ -57,6 +57,14 @@ cudaError_t launch_select_bwd(const View& x, const int64_t* index, int k, int64_
                               float inv_temperature, int mode, const float* teacher_logp, const float* grad,
                               const float* saved, const Grad& dx, cudaStream_t stream);
 
+// Vocabulary-parallel JSD / KL, per shard (vpd_shard.cu); x is the [rows, 2]
+// buffer the caller all-reduces between the steps.
+cudaError_t shard_stats(const View& s, const View& t, float* saved, float* x, cudaStream_t st);
+cudaError_t shard_rescale(int64_t rows, float* saved, float* x, cudaStream_t st);
+cudaError_t shard_divergence(const View& s, const View& t, double beta, float* loss, float* saved, float* x,
+                             cudaStream_t st);
+cudaError_t shard_finish(int64_t rows, double beta, float* saved, const float* x, float* loss, cudaStream_t st);
+
 // Single-read fused JSD forward+backward on thread-block clusters. Returns
 // cudaErrorNotSupported (without launching) when the row pair does not fit on
 // chip in clusters of at most max_cluster CTAs or the layout does not allow it;
