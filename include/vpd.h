@@ -178,6 +178,29 @@ vpd_status vpd_jsd_fwdbwd(const vpd_view *s, const vpd_view *t, double beta,
                           const vpd_segments *seg, const float *grad_loss, float *loss,
                           float *saved, const vpd_grad *ds, const vpd_grad *dt, void *stream);
 
+/* JSD forward+backward with the teacher logits in a pinned host cache
+ * ([OPSD page], "Update: copy teacher-cache chunks from pinned memory"). The
+ * teacher rows go to the device in chunks of `chunk_rows` rows, one
+ * cudaMemcpy2DAsync each, on `copy_stream` into a ring of up to four staging
+ * chunks carved from `staging`, and each chunk's vpd_jsd_fwdbwd runs on
+ * `stream` as soon as its rows have arrived, while the next chunks copy.
+ * s: device student view, plain 2-D [N, V]. t_host: pinned (page-locked or
+ * registered) host memory, [N, V] rows `t_row_stride` elements apart, dtype
+ * t_dtype equal to the student's. staging: device memory of at least two
+ * chunks (chunk_rows * V elements each), 16-byte aligned, owned by the caller
+ * and not touched by other work until `stream` has passed this call. Outputs as
+ * vpd_jsd_fwdbwd; dt, when given, is a device [N, V] gradient. Both streams
+ * must belong to the current device and be distinct; the copy stream first
+ * waits for the work already on `stream`, and `stream` ends after the last
+ * chunk. The library keeps nine reusable events per device and calling thread
+ * for this ordering (created on the first call). A pageable cache returns
+ * VPD_ERR_ARG. */
+vpd_status vpd_jsd_fwdbwd_teacher_stream(const vpd_view *s, const void *t_host, int32_t t_dtype,
+                                         int64_t t_row_stride, double beta, const float *grad_loss,
+                                         float *loss, float *saved, const vpd_grad *ds, const vpd_grad *dt,
+                                         void *staging, size_t staging_bytes, int64_t chunk_rows,
+                                         void *stream, void *copy_stream);
+
 /* ---------------------------------------------------------------------------
  * Forward / reverse KL ([ops page], "What"): reverse = 0 gives KL(P_t || P_s)
  * (the teacher is the target), reverse = 1 gives KL(P_s || P_t). The forward

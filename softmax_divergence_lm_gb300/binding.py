@@ -35,7 +35,7 @@ SYMBOLS = ("vpd_jsd_fwd", "vpd_jsd_bwd", "vpd_jsd_fwdbwd", "vpd_kl_fwd", "vpd_kl
            "vpd_launch_count", "vpd_test_withhold_copy", "vpd_jsd_linear_workspace", "vpd_jsd_linear_fwd",
            "vpd_jsd_linear_bwd", "vpd_jsd_linear_fwd_noalloc", "vpd_cross_entropy_fwd", "vpd_cross_entropy_bwd",
            "vpd_topk_kl_fwd", "vpd_topk_kl_bwd", "vpd_jsd_shard_stats", "vpd_jsd_shard_rescale",
-           "vpd_jsd_shard_divergence", "vpd_jsd_shard_finish")
+           "vpd_jsd_shard_divergence", "vpd_jsd_shard_finish", "vpd_jsd_fwdbwd_teacher_stream")
 
 
 class VpdError(RuntimeError):
@@ -110,6 +110,7 @@ def _declare(lib):
         "vpd_topk_kl_fwd": [V, S, f, i32, i64, f, dbl, f, f, f, vp],
         "vpd_topk_kl_bwd": [V, S, f, i32, i64, f, dbl, f, f, G, vp],
         "vpd_jsd_shard_stats": [V, V, f, f, vp],
+        "vpd_jsd_fwdbwd_teacher_stream": [V, vp, i32, i64, dbl, f, f, f, G, G, vp, ctypes.c_size_t, i64, vp, vp],
         "vpd_jsd_shard_rescale": [i64, f, f, vp],
         "vpd_jsd_shard_divergence": [V, V, dbl, f, f, f, vp],
         "vpd_jsd_shard_finish": [i64, dbl, f, f, f, vp],
@@ -474,6 +475,31 @@ def vpd_jsd_shard_finish(rows, beta, saved, xbuf, loss, stream=None):
     n = int(rows)
     _check(load().vpd_jsd_shard_finish(n, float(beta), _fptr(saved, n * SAVED_PAIR, "saved"),
                                        _fptr(xbuf, n * 2, "xbuf"), _fptr(loss, n, "loss"), _stream(stream)))
+
+
+def vpd_jsd_fwdbwd_teacher_stream(s, t_host, beta, grad_loss, loss, saved, ds, dt, staging, chunk_rows,
+                                  stream=None, copy_stream=None):
+    """t_host: a pinned CPU tensor [N, V] (unit stride along V) of the
+    student's dtype; staging: a device tensor of at least two chunks."""
+    vs = make_view(s)
+    n, v = _rows_vocab(vs)
+    if vs.rows_per_batch:
+        raise ValueError("the student must be a plain 2-D [N, V] view")
+    if t_host.is_cuda or t_host.dtype != s.dtype or t_host.dim() != 2 or tuple(t_host.shape) != (n, v):
+        raise ValueError("t_host must be a CPU tensor of the student's dtype and shape")
+    if v > 1 and t_host.stride(1) != 1:
+        raise ValueError("t_host must have unit stride along the vocabulary")
+    if not t_host.is_pinned():
+        raise ValueError("t_host must be pinned host memory")
+    gs, gt = make_grad(ds, n, v), make_grad(dt, n, v)
+    if copy_stream is None:
+        raise ValueError("a copy stream distinct from the compute stream is required")
+    _on_current_device(staging, "staging")
+    _check(load().vpd_jsd_fwdbwd_teacher_stream(
+        ctypes.byref(vs), t_host.data_ptr(), _DTYPES[t_host.dtype], t_host.stride(0) if n > 1 else v, float(beta),
+        _fptr(grad_loss, n, "grad_loss"), _fptr(loss, n, "loss"), _fptr(saved, n * SAVED_PAIR, "saved"),
+        _ref(gs), _ref(gt), staging.data_ptr(), staging.numel() * staging.element_size(), int(chunk_rows),
+        _stream(stream), _stream(copy_stream)))
 
 
 def vpd_device_status(stream=None):

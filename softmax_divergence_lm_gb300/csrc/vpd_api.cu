@@ -17,6 +17,11 @@
 namespace vpd {
 // Reads and clears the device error word (defined with the fused kernel).
 cudaError_t take_device_error(cudaStream_t stream, int* code);
+// The teacher-cache pipeline (vpd_teacher_stream.cu).
+cudaError_t teacher_stream(const vpd_view& s, const void* t_host, int32_t t_dtype, int64_t t_row_stride, double beta,
+                           const float* grad_loss, float* loss, float* saved, const vpd_grad* ds, const vpd_grad* dt,
+                           void* staging, int nstage, int64_t chunk_rows, cudaStream_t stream,
+                           cudaStream_t copy_stream, vpd_status* st_out);
 }  // namespace vpd
 
 namespace {
@@ -444,6 +449,46 @@ vpd_status check_heads(const vpd_linear_heads* p, vpd::LinearProblem* out) {
 }  // namespace
 
 extern "C" {
+
+vpd_status vpd_jsd_fwdbwd_teacher_stream(const vpd_view* s, const void* t_host, int32_t t_dtype,
+                                         int64_t t_row_stride, double beta, const float* grad_loss, float* loss,
+                                         float* saved, const vpd_grad* ds, const vpd_grad* dt, void* staging,
+                                         size_t staging_bytes, int64_t chunk_rows, void* stream,
+                                         void* copy_stream) {
+  vpd::View vs;
+  VPD_TRY(check_view(s, "student", &vs));
+  VPD_TRY(check_beta(beta));
+  if (!dtype_ok(t_dtype) || t_dtype != vs.dtype) return fail(VPD_ERR_DTYPE, "teacher dtype must equal the student's");
+  if (vs.map.rows_per_batch > 0) return fail(VPD_ERR_SHAPE, "the student view must be plain 2-D [N, V]");
+  if (t_row_stride < vs.vocab) return fail(VPD_ERR_SHAPE, "teacher row stride < vocab");
+  if (chunk_rows < 1) return fail(VPD_ERR_ARG, "chunk_rows must be >= 1");
+  if (vs.rows == 0) return ok();
+  if (!t_host || !loss || !saved || !staging)
+    return fail(VPD_ERR_ARG, "vpd_jsd_fwdbwd_teacher_stream: t_host, loss, saved and staging are required");
+  if (vs.vocab == 0) return vpd_jsd_fwdbwd(s, s, beta, nullptr, grad_loss, loss, saved, ds, dt, stream);
+  // the cache must be pinned (page-locked or registered) host memory: a
+  // pageable buffer would be copied through a synchronous temporary
+  cudaPointerAttributes attr;
+  VPD_CUDA(cudaPointerGetAttributes(&attr, t_host), "inspecting the teacher cache");
+  if (attr.type != cudaMemoryTypeHost) return fail(VPD_ERR_ARG, "the teacher cache must be pinned host memory");
+  const int64_t es = elem_size(t_dtype);
+  const size_t chunk_bytes = static_cast<size_t>(chunk_rows) * static_cast<size_t>(vs.vocab * es);
+  int64_t nstage = static_cast<int64_t>(staging_bytes / chunk_bytes);
+  if (nstage < 2) return fail(VPD_ERR_ARG, "staging must hold at least two chunks (%zu bytes)", 2 * chunk_bytes);
+  if (nstage > 4) nstage = 4;
+  if ((vs.vocab * es) % 16 || reinterpret_cast<uintptr_t>(staging) % 16)
+    return fail(VPD_ERR_ARG, "staging must be 16-byte aligned and the row size a multiple of 16 bytes");
+  vpd::Grad gs, gt;
+  VPD_TRY(check_grads_pair(ds, dt, vs, &gs, &gt));
+  vpd_status inner = VPD_OK;
+  cudaError_t e = vpd::teacher_stream(*s, t_host, t_dtype, t_row_stride, beta, grad_loss, loss, saved, ds, dt,
+                                      staging, static_cast<int>(nstage), chunk_rows,
+                                      static_cast<cudaStream_t>(stream), static_cast<cudaStream_t>(copy_stream),
+                                      &inner);
+  if (inner != VPD_OK) return inner;
+  VPD_CUDA(e, "teacher-cache pipeline");
+  return ok();
+}
 
 vpd_status vpd_jsd_shard_stats(const vpd_view* s, const vpd_view* t, float* saved, float* xbuf, void* stream) {
   vpd::View vs, vt;
