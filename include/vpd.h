@@ -22,9 +22,13 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  * Ownership: the caller owns every buffer. The library allocates no device or
- *   host memory and keeps no state between calls (besides one device error
- *   word per GPU, see vpd_device_status). Pointers documented as "device" must
- *   be device-accessible addresses on the current CUDA device.
+ *   host memory for its calls and keeps no state between them besides one
+ *   device error word per GPU (see vpd_device_status), a 4 MiB scratch array
+ *   per GPU for vpd_jsd_linear_fwd_noalloc, and, per device and calling
+ *   thread, a side stream with its events (vpd_jsd_fwd / vpd_jsd_fwdbwd) and
+ *   the events of vpd_jsd_fwdbwd_teacher_stream, created on first use.
+ *   Pointers documented as "device" must be device-accessible addresses on the
+ *   current CUDA device.
  * Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
  *   default stream) and the call returns without waiting, except where stated.
  * Errors: argument, dtype and shape problems are detected on the host before
@@ -169,8 +173,13 @@ vpd_status vpd_jsd_bwd(const vpd_view *s, const vpd_view *t, double beta, const 
  * row fits on a thread-block cluster (V <= 311296). There a cluster of up to
  * 16 CTAs holds each row pair on chip and statistics, divergence and
  * gradients come from one HBM read; a bf16 row whose finite max exceeds 2^126
- * is treated as out of contract (NaN, zero gradient). Otherwise the call runs
- * the two forward kernels and the backward kernel in turn. With both
+ * is treated as out of contract (NaN, zero gradient). The clusters cannot
+ * always cover every SM (at V = 151936, 15 clusters of 9 CTAs use 135 of 152);
+ * when the call has many rows per cluster and a plain 2-D layout, its last
+ * rows go to the streaming kernels on the SMs left idle, on a side stream that
+ * forks from `stream` and joins it again before the call's work ends (the
+ * share follows the measured per-SM rates of the two paths). Otherwise the
+ * call runs the two forward kernels and the backward kernel in turn. With both
  * gradients absent the single-read path is the forward-only kernel. Outputs
  * as vpd_jsd_fwd (loss, and saved, which is required) plus the gradients as
  * vpd_jsd_bwd. */

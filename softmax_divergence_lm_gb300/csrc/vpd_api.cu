@@ -140,6 +140,29 @@ vpd_status check_grads_pair(const vpd_grad* ds, const vpd_grad* dt, const vpd::V
   return VPD_OK;
 }
 
+// A non-blocking side stream and its fork / join events, per device and
+// calling thread, created on first use and kept for the life of the thread.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+cudaError_t side_stream(SideStream** out) {
+  thread_local SideStream ss[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  SideStream& x = ss[dev];
+  if (!x.stream) {
+    if ((e = cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithFlags(&x.stream, cudaStreamNonBlocking)) != cudaSuccess) return e;
+  }
+  *out = &x;
+  return cudaSuccess;
+}
+
 #define VPD_TRY(x)                     \
   do {                                 \
     vpd_status _st = (x);              \
@@ -182,6 +205,39 @@ vpd_status vpd_jsd_fwd(const vpd_view* s, const vpd_view* t, double beta, const 
   // clusters that cover most SMs; else the two streaming passes on every SM.
   if (sg.count == 1) {
     const vpd::Grad none{nullptr, 0, 0};
+    // as in vpd_jsd_fwdbwd: the last rows go to the SMs the clusters leave idle
+    int64_t side = 0;
+    int idle = 0;
+    vpd::fused_idle_split(vs, none, none, kForwardMaxCluster, &side, &idle);
+    if (side > 0) {
+      SideStream* ss = nullptr;
+      VPD_CUDA(side_stream(&ss), "creating the side stream");
+      const int64_t nf = vs.rows - side;
+      vpd::View fs = vs, ft = vt, ss_v = vs, st_v = vt;
+      fs.rows = ft.rows = nf;
+      ss_v.rows = st_v.rows = side;
+      const int64_t es = vs.dtype == VPD_F32 ? 4 : 2;
+      ss_v.data = vs.data + vs.map.offset(nf) * es;
+      st_v.data = vt.data + vt.map.offset(nf) * es;
+      VPD_CUDA(cudaEventRecord(ss->fork, st), "forking the side stream");
+      VPD_CUDA(cudaStreamWaitEvent(ss->stream, ss->fork, 0), "forking the side stream");
+      cudaError_t e = vpd::launch_jsd_fused(fs, ft, beta, nullptr, loss, saved, none, none, st, -1,
+                                            kForwardMaxCluster);
+      if (e == cudaSuccess) {
+        {
+          vpd::GridCap cap(idle);
+          float* sv = saved + nf * VPD_SAVED_PAIR;
+          VPD_CUDA(vpd::launch_pair_stats(ss_v, st_v, sg, sv, ss->stream), "paired statistics kernel");
+          VPD_CUDA(vpd::launch_jsd_div(ss_v, st_v, beta, loss + nf, sv, ss->stream), "divergence kernel");
+        }
+        VPD_CUDA(cudaEventRecord(ss->join, ss->stream), "joining the side stream");
+        VPD_CUDA(cudaStreamWaitEvent(st, ss->join, 0), "joining the side stream");
+        return ok();
+      }
+      VPD_CUDA(cudaEventRecord(ss->join, ss->stream), "joining the side stream");
+      VPD_CUDA(cudaStreamWaitEvent(st, ss->join, 0), "joining the side stream");
+      if (e != cudaErrorNotSupported) return cuda_fail(e, "fused single-read kernel");
+    }
     cudaError_t e = vpd::launch_jsd_fused(vs, vt, beta, nullptr, loss, saved, none, none, st, -1,
                                           kForwardMaxCluster);
     if (e == cudaSuccess) return ok();
@@ -227,6 +283,51 @@ vpd_status vpd_jsd_fwdbwd(const vpd_view* s, const vpd_view* t, double beta,
   // several vocabulary segments takes the streaming kernels, which merge them
   // segment by segment.
   if (sg.count == 1) {
+    // The clusters of the single-read kernel leave some SMs idle (at V =
+    // 151936, 15 clusters of 9 CTAs use 135 of 152 SMs). The last rows of the
+    // call go to the streaming kernels on a side stream, capped to as many
+    // CTAs as fit those SMs; the fused grid is submitted first, so its
+    // clusters take their SMs before the side CTAs arrive (which cannot share
+    // an SM with a fused CTA: its registers are taken).
+    int64_t side = 0;
+    int idle = 0;
+    if (g_withhold_row < 0) vpd::fused_idle_split(vs, gs, gt, 16, &side, &idle);
+    if (side > 0) {
+      SideStream* ss = nullptr;
+      VPD_CUDA(side_stream(&ss), "creating the side stream");
+      const int64_t nf = vs.rows - side;
+      vpd::View fs = vs, ft = vt, ss_v = vs, st_v = vt;
+      fs.rows = ft.rows = nf;
+      ss_v.rows = st_v.rows = side;
+      const int64_t es = vs.dtype == VPD_F32 ? 4 : 2;
+      ss_v.data = vs.data + vs.map.offset(nf) * es;
+      st_v.data = vt.data + vt.map.offset(nf) * es;
+      vpd::Grad sgs = gs, sgt = gt;
+      if (gs.data) sgs.data = gs.data + nf * gs.row_stride * (gs.dtype == VPD_F32 ? 4 : 2);
+      if (gt.data) sgt.data = gt.data + nf * gt.row_stride * (gt.dtype == VPD_F32 ? 4 : 2);
+      VPD_CUDA(cudaEventRecord(ss->fork, st), "forking the side stream");
+      VPD_CUDA(cudaStreamWaitEvent(ss->stream, ss->fork, 0), "forking the side stream");
+      cudaError_t e = vpd::launch_jsd_fused(fs, ft, beta, grad_loss, loss, saved, gs, gt, st, -1);
+      if (e == cudaSuccess) {
+        {
+          // measured: the three streaming passes, two CTAs per idle SM each,
+          // run about as fast per SM as one kernel doing all three per row
+          vpd::GridCap cap(idle);
+          float* sv = saved + nf * VPD_SAVED_PAIR;
+          const float* sg_l = grad_loss ? grad_loss + nf : nullptr;
+          VPD_CUDA(vpd::launch_pair_stats(ss_v, st_v, sg, sv, ss->stream), "paired statistics kernel");
+          VPD_CUDA(vpd::launch_jsd_div(ss_v, st_v, beta, loss + nf, sv, ss->stream), "divergence kernel");
+          VPD_CUDA(vpd::launch_pair_bwd(ss_v, st_v, beta, sg_l, sv, sgs, sgt, ss->stream), "backward kernel");
+        }
+        VPD_CUDA(cudaEventRecord(ss->join, ss->stream), "joining the side stream");
+        VPD_CUDA(cudaStreamWaitEvent(st, ss->join, 0), "joining the side stream");
+        return ok();
+      }
+      // no fused launch: join the (empty) side stream and take the plain path below
+      VPD_CUDA(cudaEventRecord(ss->join, ss->stream), "joining the side stream");
+      VPD_CUDA(cudaStreamWaitEvent(st, ss->join, 0), "joining the side stream");
+      if (e != cudaErrorNotSupported) return cuda_fail(e, "fused single-read kernel");
+    }
     cudaError_t e = vpd::launch_jsd_fused(vs, vt, beta, grad_loss, loss, saved, gs, gt, st, g_withhold_row);
     if (e == cudaSuccess) g_withhold_row = -1;
     if (e == cudaSuccess) return ok();

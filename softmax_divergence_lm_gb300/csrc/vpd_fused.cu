@@ -136,6 +136,47 @@ bool choose(int64_t vocab, int64_t rows, int max_cluster, bool fwd, Config* cfg)
 
 }  // namespace
 
+// Rate of the streaming path on one otherwise idle SM relative to one SM of a
+// fused cluster, in rows per second per SM, measured at V = 151936: 0.45 for
+// forward+backward (three streaming passes against one read), 0.75 for the
+// forward (two passes). VPD_IDLE_RATE / VPD_IDLE_RATE_FWD override them (0
+// disables the split).
+static double idle_rate(bool fwd) {
+  static const double r[2] = {[] {
+                                const char* e = getenv("VPD_IDLE_RATE");
+                                return e && e[0] ? atof(e) : 0.45;
+                              }(),
+                              [] {
+                                const char* e = getenv("VPD_IDLE_RATE_FWD");
+                                return e && e[0] ? atof(e) : 0.75;
+                              }()};
+  return r[fwd ? 1 : 0];
+}
+
+void fused_idle_split(const View& s, const Grad& ds, const Grad& dt, int max_cluster, int64_t* side_rows,
+                      int* idle_sms) {
+  *side_rows = 0;
+  *idle_sms = 0;
+  const bool fwd = !ds.data && !dt.data;
+  const double rate = idle_rate(fwd);
+  if (rate <= 0.0 || s.map.rows_per_batch > 0 || s.dtype == kF32) return;
+  if (!fwd) {
+    const int gdtype = ds.data ? ds.dtype : dt.dtype;
+    if (gdtype != kF32 && gdtype != s.dtype) return;
+  }
+  Config cfg;
+  if (!choose(s.vocab, s.rows, max_cluster, fwd, &cfg)) return;
+  const int clusters = clusters_for(cfg.C);
+  const int used = clusters * cfg.C, idle = sm_count() - used;
+  // worth it only with every cluster busy for many rows
+  if (idle < 4 || s.rows < 8 * static_cast<int64_t>(clusters)) return;
+  const double share = idle * rate / (used + idle * rate);
+  const int64_t side = static_cast<int64_t>(s.rows * share);
+  if (side < idle) return;
+  *side_rows = side;
+  *idle_sms = idle;
+}
+
 cudaError_t launch_jsd_fused(const View& s, const View& t, double beta, const float* grad_loss,
                              float* loss, float* saved, const Grad& ds, const Grad& dt,
                              cudaStream_t stream, int64_t withhold_row, int max_cluster) {

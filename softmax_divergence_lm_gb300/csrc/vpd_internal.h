@@ -74,6 +74,25 @@ cudaError_t launch_jsd_fused(const View& s, const View& t, double beta, const fl
                              float* loss, float* saved, const Grad& ds, const Grad& dt,
                              cudaStream_t stream, int64_t withhold_row, int max_cluster = 16);
 
+// While alive, sizes every streaming-kernel launch made on this thread for
+// `sms` SMs (as many CTAs as fit that many SMs; 0: every SM).
+class GridCap {
+ public:
+  explicit GridCap(int sms);
+  ~GridCap();
+  GridCap(const GridCap&) = delete;
+  GridCap& operator=(const GridCap&) = delete;
+
+ private:
+  int prev_;
+};
+
+// Rows of a single-read JSD call (forward+backward, or forward only when
+// neither gradient is wanted) to hand to the SMs its clusters leave idle, and
+// how many SMs those are (0, 0 when the split does not pay).
+void fused_idle_split(const View& s, const Grad& ds, const Grad& dt, int max_cluster, int64_t* side_rows,
+                      int* idle_sms);
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 

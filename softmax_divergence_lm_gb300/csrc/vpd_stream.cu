@@ -1040,12 +1040,18 @@ int threads_for(int64_t vocab, int esize) {
   return t < 64 ? 64 : (t > kThreads ? kThreads : static_cast<int>(t));
 }
 
+// SMs a launch may fill on this thread, when set (0: all of them): the rows a
+// fused launch hands to the SMs its clusters leave idle run on as many CTAs as
+// fit that many SMs.
+thread_local int g_grid_cap = 0;
+
 template <class Kern>
 int grid_for(Kern kernel, int64_t rows, int threads) {
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess || per_sm < 1)
     per_sm = 1;
-  const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
+  const int sms = g_grid_cap > 0 && g_grid_cap < sm_count() ? g_grid_cap : sm_count();
+  const int64_t cap = static_cast<int64_t>(sms) * per_sm;
   return static_cast<int>(rows < cap ? rows : cap);
 }
 
@@ -1184,6 +1190,9 @@ std::atomic<uint64_t> g_launches{0};
 }  // namespace
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+GridCap::GridCap(int ctas) : prev_(g_grid_cap) { g_grid_cap = ctas; }
+GridCap::~GridCap() { g_grid_cap = prev_; }
 uint64_t launch_count() { return g_launches.load(std::memory_order_relaxed); }
 
 int sm_count() {
