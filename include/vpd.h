@@ -210,6 +210,16 @@ vpd_status vpd_jsd_fwdbwd_teacher_stream(const vpd_view *s, const void *t_host, 
                                          void *staging, size_t staging_bytes, int64_t chunk_rows,
                                          void *stream, void *copy_stream);
 
+/* The path a JSD call with these arguments takes, decided on the host with
+ * nothing launched: how many rows go to the single-read cluster kernel, how
+ * many to the streaming kernels on the SMs its clusters leave idle, and the
+ * number of kernel launches. With ds and dt both absent (NULL or NULL data)
+ * the answer is for vpd_jsd_fwd (the forward-only kernel), otherwise for
+ * vpd_jsd_fwdbwd. The data pointers of the views and gradients are not read.
+ * fused_rows = 0 means the streaming kernels only. Any output may be NULL. */
+vpd_status vpd_jsd_plan(const vpd_view *s, const vpd_view *t, const vpd_segments *seg, const vpd_grad *ds,
+                        const vpd_grad *dt, int64_t *fused_rows, int64_t *idle_sm_rows, int32_t *launches);
+
 /* ---------------------------------------------------------------------------
  * Forward / reverse KL ([ops page], "What"): reverse = 0 gives KL(P_t || P_s)
  * (the teacher is the target), reverse = 1 gives KL(P_s || P_t). The forward

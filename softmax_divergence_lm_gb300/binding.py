@@ -35,7 +35,7 @@ SYMBOLS = ("vpd_jsd_fwd", "vpd_jsd_bwd", "vpd_jsd_fwdbwd", "vpd_kl_fwd", "vpd_kl
            "vpd_launch_count", "vpd_test_withhold_copy", "vpd_jsd_linear_workspace", "vpd_jsd_linear_fwd",
            "vpd_jsd_linear_bwd", "vpd_jsd_linear_fwd_noalloc", "vpd_cross_entropy_fwd", "vpd_cross_entropy_bwd",
            "vpd_topk_kl_fwd", "vpd_topk_kl_bwd", "vpd_jsd_shard_stats", "vpd_jsd_shard_rescale",
-           "vpd_jsd_shard_divergence", "vpd_jsd_shard_finish", "vpd_jsd_fwdbwd_teacher_stream")
+           "vpd_jsd_shard_divergence", "vpd_jsd_shard_finish", "vpd_jsd_fwdbwd_teacher_stream", "vpd_jsd_plan")
 
 
 class VpdError(RuntimeError):
@@ -110,6 +110,7 @@ def _declare(lib):
         "vpd_topk_kl_fwd": [V, S, f, i32, i64, f, dbl, f, f, f, vp],
         "vpd_topk_kl_bwd": [V, S, f, i32, i64, f, dbl, f, f, G, vp],
         "vpd_jsd_shard_stats": [V, V, f, f, vp],
+        "vpd_jsd_plan": [V, V, S, G, G, P(i64), P(i64), P(i32)],
         "vpd_jsd_fwdbwd_teacher_stream": [V, vp, i32, i64, dbl, f, f, f, G, G, vp, ctypes.c_size_t, i64, vp, vp],
         "vpd_jsd_shard_rescale": [i64, f, f, vp],
         "vpd_jsd_shard_divergence": [V, V, dbl, f, f, f, vp],
@@ -500,6 +501,19 @@ def vpd_jsd_fwdbwd_teacher_stream(s, t_host, beta, grad_loss, loss, saved, ds, d
         _fptr(grad_loss, n, "grad_loss"), _fptr(loss, n, "loss"), _fptr(saved, n * SAVED_PAIR, "saved"),
         _ref(gs), _ref(gt), staging.data_ptr(), staging.numel() * staging.element_size(), int(chunk_rows),
         _stream(stream), _stream(copy_stream)))
+
+
+def vpd_jsd_plan(s, t, segments=None, ds=None, dt=None) -> tuple[int, int, int]:
+    """(rows on the single-read kernel, rows on the idle SMs, launches) of a
+    vpd_jsd_fwd (no gradients given) or vpd_jsd_fwdbwd call with these
+    arguments; nothing is launched."""
+    vs, vt, n, v = _pair(s, t)
+    seg, _keep = make_segments(segments)
+    gs, gt = make_grad(ds, n, v), make_grad(dt, n, v)
+    fr, side, k = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int32()
+    _check(load().vpd_jsd_plan(ctypes.byref(vs), ctypes.byref(vt), _ref(seg), _ref(gs), _ref(gt), ctypes.byref(fr),
+                               ctypes.byref(side), ctypes.byref(k)))
+    return int(fr.value), int(side.value), int(k.value)
 
 
 def vpd_device_status(stream=None):

@@ -339,6 +339,40 @@ vpd_status vpd_jsd_fwdbwd(const vpd_view* s, const vpd_view* t, double beta,
   return ok();
 }
 
+vpd_status vpd_jsd_plan(const vpd_view* s, const vpd_view* t, const vpd_segments* seg, const vpd_grad* ds,
+                        const vpd_grad* dt, int64_t* fused_rows, int64_t* idle_sm_rows, int32_t* launches) {
+  vpd::View vs, vt;
+  vpd::Segs sg;
+  vpd::Grad gs, gt;
+  VPD_TRY(check_pair(s, t, &vs, &vt));
+  VPD_TRY(check_segments(seg, vs.vocab, &sg));
+  VPD_TRY(check_grads_pair(ds, dt, vs, &gs, &gt));
+  const bool fwd = !gs.data && !gt.data;
+  const int max_cluster = fwd ? kForwardMaxCluster : 16;
+  int64_t fr = 0, side = 0;
+  int32_t n = 0;
+  if (vs.rows > 0) {
+    int idle = 0;
+    if (sg.count == 1) vpd::fused_idle_split(vs, gs, gt, max_cluster, &side, &idle);
+    vpd::View fs = vs, ft = vt;
+    fs.rows = ft.rows = vs.rows - side;
+    const cudaError_t e = sg.count == 1 ? vpd::launch_jsd_fused(fs, ft, 0.5, nullptr, nullptr, nullptr, gs, gt,
+                                                                nullptr, -1, max_cluster, true)
+                                        : cudaErrorNotSupported;
+    if (e == cudaSuccess) {
+      fr = fs.rows;
+      n = 1 + (side > 0 ? (fwd ? 2 : 3) : 0);
+    } else {
+      side = 0;
+      n = fwd ? 2 : 3;
+    }
+  }
+  if (fused_rows) *fused_rows = fr;
+  if (idle_sm_rows) *idle_sm_rows = side;
+  if (launches) *launches = n;
+  return ok();
+}
+
 vpd_status vpd_kl_fwd(const vpd_view* s, const vpd_view* t, int32_t reverse,
                       const vpd_segments* seg, float* loss, float* saved, void* stream) {
   vpd::View vs, vt;

@@ -179,7 +179,7 @@ void fused_idle_split(const View& s, const Grad& ds, const Grad& dt, int max_clu
 
 cudaError_t launch_jsd_fused(const View& s, const View& t, double beta, const float* grad_loss,
                              float* loss, float* saved, const Grad& ds, const Grad& dt,
-                             cudaStream_t stream, int64_t withhold_row, int max_cluster) {
+                             cudaStream_t stream, int64_t withhold_row, int max_cluster, bool dry_run) {
   // 16-bit inputs only; every row of both inputs and of both gradients must
   // start on a 16-byte boundary, and V must fill whole 16-byte vectors.
   if (s.dtype == kF32 || s.vocab <= 0 || s.vocab % 8 != 0) return cudaErrorNotSupported;
@@ -203,6 +203,7 @@ cudaError_t launch_jsd_fused(const View& s, const View& t, double beta, const fl
   const bool f32g = gdtype == kF32;
   // 16-bit gradients go out through a shared-memory buffer and bulk stores
   // when it fits beside the stages.
+  if (dry_run) return cudaSuccess;
   const bool gstage = gdtype >= 0 && !f32g && fused::smem_bytes(cfg.W, true) <= max_smem_optin();
   if (gstage) cfg.smem = fused::smem_bytes(cfg.W, true);
   fused::FusedArgs args{s.data, t.data, s.map, t.map, s.rows, s.vocab, cfg.W, cfg.nw, gstage ? 1 : 0,

@@ -69,10 +69,12 @@ cudaError_t shard_finish(int64_t rows, double beta, float* saved, const float* x
 // cudaErrorNotSupported (without launching) when the row pair does not fit on
 // chip in clusters of at most max_cluster CTAs or the layout does not allow it;
 // the caller then uses the streaming path. withhold_row >= 0 is the
-// failure-path test hook (vpd_test_withhold_copy).
+// failure-path test hook (vpd_test_withhold_copy). dry_run: only decide
+// (cudaSuccess when the kernel would run), launch nothing.
 cudaError_t launch_jsd_fused(const View& s, const View& t, double beta, const float* grad_loss,
                              float* loss, float* saved, const Grad& ds, const Grad& dt,
-                             cudaStream_t stream, int64_t withhold_row, int max_cluster = 16);
+                             cudaStream_t stream, int64_t withhold_row, int max_cluster = 16,
+                             bool dry_run = false);
 
 // While alive, sizes every streaming-kernel launch made on this thread for
 // `sms` SMs (as many CTAs as fit that many SMs; 0: every SM).
