@@ -180,7 +180,10 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-FUSED_SOURCES = ("vpd_fused.cuh", "vpd_fused_bf16.cu", "vpd_fused_f16.cu", "vpd_fused.cu", "vpd_device.cuh", "vpd_packed.cuh")
+# the sources of the measured step: the single-read kernels, the streaming
+# kernels that take the idle SMs' rows, and the call that splits the rows
+FUSED_SOURCES = ("vpd_fused.cuh", "vpd_fused_bf16.cu", "vpd_fused_f16.cu", "vpd_fused.cu", "vpd_device.cuh",
+                 "vpd_packed.cuh", "vpd_stream.cu", "vpd_api.cu", "vpd_internal.h")
 
 
 def _code_only(text: str) -> str:
