@@ -138,7 +138,7 @@ bool choose(int64_t vocab, int64_t rows, int max_cluster, bool fwd, Config* cfg)
 
 // Rate of the streaming path on one otherwise idle SM relative to one SM of a
 // fused cluster, in rows per second per SM, measured at V = 151936: 0.45 for
-// forward+backward (three streaming passes against one read), 0.75 for the
+// forward+backward (three streaming passes against one read), 0.9 for the
 // forward (two passes). VPD_IDLE_RATE / VPD_IDLE_RATE_FWD override them (0
 // disables the split).
 static double idle_rate(bool fwd) {
@@ -148,7 +148,7 @@ static double idle_rate(bool fwd) {
                               }(),
                               [] {
                                 const char* e = getenv("VPD_IDLE_RATE_FWD");
-                                return e && e[0] ? atof(e) : 0.75;
+                                return e && e[0] ? atof(e) : 0.9;
                               }()};
   return r[fwd ? 1 : 0];
 }
@@ -159,7 +159,9 @@ void fused_idle_split(const View& s, const Grad& ds, const Grad& dt, int max_clu
   *idle_sms = 0;
   const bool fwd = !ds.data && !dt.data;
   const double rate = idle_rate(fwd);
-  if (rate <= 0.0 || s.map.rows_per_batch > 0 || s.dtype == kF32) return;
+  // long rows only: their streaming CTAs are wide enough (at least three warps
+  // of 40 or more registers) that none fits beside a fused CTA on its SM
+  if (rate <= 0.0 || s.map.rows_per_batch > 0 || s.dtype == kF32 || s.vocab < 100000) return;
   if (!fwd) {
     const int gdtype = ds.data ? ds.dtype : dt.dtype;
     if (gdtype != kF32 && gdtype != s.dtype) return;

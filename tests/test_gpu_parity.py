@@ -14,7 +14,7 @@ import pytest
 import torch
 
 from oracle import oracle as O
-from parity_util import assert_grad, assert_loss, assert_zero_rows, to64
+from parity_util import assert_grad, assert_loss, assert_zero_rows, kl_branch_floor, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -93,10 +93,12 @@ def check_pair(B, s, t, beta, *, op="jsd", segments=None, rows=None, gdtype=torc
     tag = f"{label} {op} beta={beta} {s.dtype}->{gdtype}"
     assert_loss(loss[rows], rl, tag + " loss")
     gd = None if gdtype == torch.float32 else gdtype
+    branch = {"kl-fwd": 0.0, "kl-rev": 1.0}.get(op, beta)
+    fs, ft = kl_branch_floor(s64, t64, branch, to64(g)[rows])
     if want_s:
-        assert_grad(ds, rds, tag + " dS", gd)
+        assert_grad(ds, rds, tag + " dS", gd, floor=fs)
     if want_t:
-        assert_grad(dt, rdt, tag + " dT", gd)
+        assert_grad(dt, rdt, tag + " dT", gd, floor=ft)
     bad = np.nonzero(~np.isfinite(rl))[0]
     if want_s:
         assert_zero_rows(ds, bad, tag + " dS")
