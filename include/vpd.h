@@ -362,7 +362,7 @@ typedef struct {
 
 /* Workspace sizes (bytes) of vpd_jsd_linear_fwd and of vpd_jsd_linear_bwd
  * with the given gradients wanted (nonzero flags). The backward works through
- * the rows in chunks of 1024 and keeps, per head, that chunk's gradient of the
+ * the rows in chunks of 8192 and keeps, per head, that chunk's gradient of the
  * logits split in two bf16 parts (row-major and transposed), the head weight
  * transposed and the chunk's hidden states transposed. Either output pointer
  * may be NULL. */

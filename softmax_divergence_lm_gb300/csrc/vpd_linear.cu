@@ -58,7 +58,8 @@ constexpr int BK = 64;                      // k per stage: one 128-byte swizzle
 constexpr int kStages = 6;
 constexpr int kTileBytes = BM * BK * 2;     // 16 KB per operand tile
 constexpr int kStageBytes = 2 * kTileBytes;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+constexpr int kTransWords = 32 * 33;          // per epilogue warp: 32 rows x 32 bf16 pairs (+1 word pad)
+constexpr int kSmemBytes = kStages * kStageBytes + 4 * kTransWords * 4 + 1024;  // + alignment slack
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;
 constexpr float kTinyL = 1e-37f;
@@ -93,6 +94,7 @@ struct Args {
   // kGemm output
   float* C;
   int64_t ldc;
+  int gemm_store;  // 1: C = the product (one k part, nothing to add to); 0: C += by atomics
 };
 
 // ---------------------------------------------------------------------------
@@ -256,6 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ Bars bars;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint32_t* trans = reinterpret_cast<uint32_t*>(smem + kStages * kStageBytes);  // kGrad transposes
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &bars.abort;
 
@@ -417,10 +420,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int i = 0; i < 32; i += 4) {
                 const int64_t j = col0 + c + i;
                 if (j + 3 < a.cols) {
-                  atomicAdd(reinterpret_cast<float4*>(crow + j), make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]));
+                  const float4 v4 = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+                  if (a.gemm_store) *reinterpret_cast<float4*>(crow + j) = v4;
+                  else atomicAdd(reinterpret_cast<float4*>(crow + j), v4);
                 } else {
                   for (int e = 0; e < 4; ++e)
-                    if (j + e < a.cols) atomicAdd(crow + j + e, x[i + e]);
+                    if (j + e < a.cols) {
+                      if (a.gemm_store) crow[j + e] = x[i + e];
+                      else atomicAdd(crow + j + e, x[i + e]);
+                    }
                 }
               }
             }
@@ -472,32 +480,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           } else {  // kGrad
-            // rows past the chunk's end (inside its last row tile) are zero in
-            // the transposed arrays, whose columns the dW product sums over
-            const int64_t rl = row;  // the operand maps start at the chunk's first row
-            if (!rv) {
-              const __nv_bfloat16 z = __float2bfloat16_rn(0.f);
-#pragma unroll 4
-              for (int i = 0; i < 32; ++i) {
-                const int64_t j = col0 + c + i;
-                if (i >= nvalid) continue;
-                if (a.gst_hi) {
-                  a.gst_hi[j * a.ld_t + rl] = z;
-                  a.gst_lo[j * a.ld_t + rl] = z;
-                }
-                if (a.gtt_hi) {
-                  a.gtt_hi[j * a.ld_t + rl] = z;
-                  a.gtt_lo[j * a.ld_t + rl] = z;
-                }
-              }
-              continue;
-            }
+            // dS and dT of this thread's row for 32 columns (0 past the
+            // chunk's rows: the transposed arrays are summed over rows)
+            float gsv[32], gtv[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const int64_t j = col0 + c + i;
-              if (i >= nvalid) continue;
               float gs = 0.f, gt = 0.f;
-              if (live) {
+              if (live && i < nvalid) {
                 const float lp = fmaf(x[i] + nms, kLog2eL, nKs), lq = fmaf(y[i] + nmt, kLog2eL, nKt);
                 const float p = ex2f(lp), qv = ex2f(lq);
                 if (a.jmode == 0) {
@@ -512,21 +501,67 @@ __global__ void __launch_bounds__(kThreads, 1)
                   gt = ct * (qv - p);
                 }
               }
-              if (a.gst_hi) {
-                const __nv_bfloat16 hi = __float2bfloat16_rn(gs);
-                const __nv_bfloat16 lo = __float2bfloat16_rn(gs - __bfloat162float(hi));
-                a.gs_hi[rl * a.cols + j] = hi;
-                a.gs_lo[rl * a.cols + j] = lo;
-                a.gst_hi[j * a.ld_t + rl] = hi;
-                a.gst_lo[j * a.ld_t + rl] = lo;
+              gsv[i] = gs;
+              gtv[i] = gt;
+            }
+            const int64_t rbase = static_cast<int64_t>(w.mt) * BM + 32 * q;  // this warp's first row
+#pragma unroll
+            for (int head = 0; head < 2; ++head) {
+              const float* gv = head == 0 ? gsv : gtv;
+              __nv_bfloat16* rm[2] = {head == 0 ? a.gs_hi : a.gt_hi, head == 0 ? a.gs_lo : a.gt_lo};
+              __nv_bfloat16* tr[2] = {head == 0 ? a.gst_hi : a.gtt_hi, head == 0 ? a.gst_lo : a.gtt_lo};
+              if (!tr[0]) continue;  // warp-uniform: this head's gradient is not wanted
+              uint32_t part[2][16];  // high and low bf16 parts, packed in pairs
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(gv[2 * i], gv[2 * i + 1]);
+                const float2 hf = __bfloat1622float2(h);
+                const __nv_bfloat162 l = __floats2bfloat162_rn(gv[2 * i] - hf.x, gv[2 * i + 1] - hf.y);
+                part[0][i] = *reinterpret_cast<const uint32_t*>(&h);
+                part[1][i] = *reinterpret_cast<const uint32_t*>(&l);
               }
-              if (a.gtt_hi) {
-                const __nv_bfloat16 hi = __float2bfloat16_rn(gt);
-                const __nv_bfloat16 lo = __float2bfloat16_rn(gt - __bfloat162float(hi));
-                a.gt_hi[rl * a.cols + j] = hi;
-                a.gt_lo[rl * a.cols + j] = lo;
-                a.gtt_hi[j * a.ld_t + rl] = hi;
-                a.gtt_lo[j * a.ld_t + rl] = lo;
+#pragma unroll
+              for (int hl = 0; hl < 2; ++hl) {
+                // row-major [rows, V]: this thread's 32 columns, four 16-byte stores
+                if (rv) {
+                  __nv_bfloat16* dst = rm[hl] + row * a.cols + col0 + c;
+                  if (nvalid >= 32) {
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4)
+                      *reinterpret_cast<uint4*>(dst + 8 * v4) =
+                          make_uint4(part[hl][4 * v4], part[hl][4 * v4 + 1], part[hl][4 * v4 + 2], part[hl][4 * v4 + 3]);
+                  } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                      if (i >= nvalid) continue;
+                      const uint32_t w2 = part[hl][i >> 1];
+                      const unsigned short b = static_cast<unsigned short>((i & 1) ? (w2 >> 16) : (w2 & 0xffffu));
+                      reinterpret_cast<unsigned short*>(dst)[i] = b;
+                    }
+                  }
+                }
+                // transposed [V, ld_t]: the warp's 32 x 32 block through shared
+                // memory, then each lane stores one column's 32 rows (64 bytes)
+                uint32_t* tb = trans + (warp - 2) * kTransWords;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) tb[lane * 33 + i] = part[hl][i];
+                __syncwarp();
+                uint32_t colw[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                  const uint32_t w0 = tb[(2 * k) * 33 + (lane >> 1)], w1 = tb[(2 * k + 1) * 33 + (lane >> 1)];
+                  const uint32_t b0 = (lane & 1) ? (w0 >> 16) : (w0 & 0xffffu);
+                  const uint32_t b1 = (lane & 1) ? (w1 >> 16) : (w1 & 0xffffu);
+                  colw[k] = b0 | (b1 << 16);
+                }
+                __syncwarp();
+                if (lane < nvalid) {
+                  __nv_bfloat16* dst = tr[hl] + (col0 + c + lane) * a.ld_t + rbase;
+#pragma unroll
+                  for (int v4 = 0; v4 < 4; ++v4)
+                    *reinterpret_cast<uint4*>(dst + 8 * v4) =
+                        make_uint4(colw[4 * v4], colw[4 * v4 + 1], colw[4 * v4 + 2], colw[4 * v4 + 3]);
+                }
               }
             }
           }
@@ -774,9 +809,10 @@ cudaError_t transpose_bf16(const void* in, int64_t rows, int64_t cols, int64_t l
 }
 
 // C[rows, n] += A0 B0^T + A1 B1^T with K-major bf16 operands (A [rows, k],
-// B [n, k]), split along k so that about four units run per SM.
+// B [n, k]), split along k so that about four units run per SM; with
+// may_store (C holds nothing yet) and a single k part, C = the product.
 cudaError_t gemm_acc(const void* a0p, const void* a1p, int64_t lda, const void* bp, int64_t ldb, int64_t rows,
-                     int64_t n, int64_t k, float* C, int64_t ldc, cudaStream_t stream) {
+                     int64_t n, int64_t k, float* C, int64_t ldc, bool may_store, cudaStream_t stream) {
   CUtensorMap a0, a1, b0;
   cudaError_t e;
   if ((e = make_map(&a0, a0p, rows, k, lda)) != cudaSuccess) return e;
@@ -798,6 +834,8 @@ cudaError_t gemm_acc(const void* a0p, const void* a1p, int64_t lda, const void* 
   a.units = tiles * ks;
   a.C = C;
   a.ldc = ldc;
+  // one k part per tile and nothing in C to add to: plain stores
+  a.gemm_store = may_store && ks == 1 ? 1 : 0;
   return launch(a0, b0, a1, b0, a, stream);
 }
 
@@ -885,7 +923,7 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
       // dh[r0:r0+n] += G_hi W + G_lo W  (K = V; B = W^T [H, V])
       if (dh[x] &&
           (e = gemm_acc(G[x][0], G[x][1], p.vocab, wT[x], p.vocab, n, H[x], p.vocab, dh[x] + r0 * H[x], H[x],
-                        stream)) != cudaSuccess)
+                        true, stream)) != cudaSuccess)
         return e;
       // dW += G_hi^T h + G_lo^T h  (K = chunk rows; A = G^T [V, nc], B = h^T [H, nc])
       if (dw[x]) {
@@ -895,7 +933,8 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
             (e = cudaMemset2DAsync(static_cast<char*>(hT[x]) + n * 2, nc * 2, 0, (nc - n) * 2, H[x], stream)) !=
                 cudaSuccess)
           return e;
-        if ((e = gemm_acc(G[x][2], G[x][3], nc, hT[x], nc, p.vocab, H[x], nc, dw[x], H[x], stream)) != cudaSuccess)
+        if ((e = gemm_acc(G[x][2], G[x][3], nc, hT[x], nc, p.vocab, H[x], nc, dw[x], H[x], r0 == 0, stream)) !=
+            cudaSuccess)
           return e;
       }
     }

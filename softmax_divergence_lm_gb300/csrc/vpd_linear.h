@@ -19,8 +19,9 @@ struct LinearProblem {
   double beta;
 };
 
-// Rows of one backward chunk (a multiple of the 128-row tile).
-constexpr int64_t kLinearChunkRows = 1024;
+// Rows of one backward chunk (a multiple of the 128-row tile): up to this
+// many rows, dW is one contraction over all of them.
+constexpr int64_t kLinearChunkRows = 8192;
 
 size_t linear_fwd_workspace(int64_t rows, int64_t vocab);
 size_t linear_bwd_workspace(int64_t rows, int64_t vocab, int64_t hs, int64_t ht, bool student, bool teacher,
