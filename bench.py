@@ -254,7 +254,12 @@ def cpu_model() -> str:
     impl = re.search(r"^CPU implementer\s*:\s*(\S+)", text, flags=re.M)
     part = re.search(r"^CPU part\s*:\s*(\S+)", text, flags=re.M)
     if impl and part:
-        return f"Arm CPU implementer {impl.group(1)} part {part.group(1)}"
+        # Arm Ltd. (implementer 0x41) core part numbers
+        names = {"0xd0c": "Neoverse N1", "0xd40": "Neoverse V1", "0xd49": "Neoverse N2", "0xd4f": "Neoverse V2",
+                 "0xd84": "Neoverse V3", "0xd8e": "Neoverse N3"}
+        name = names.get(part.group(1).lower()) if impl.group(1).lower() == "0x41" else None
+        return f"{name} (Arm part {part.group(1)})" if name else \
+            f"Arm CPU implementer {impl.group(1)} part {part.group(1)}"
     return "unknown"
 
 
