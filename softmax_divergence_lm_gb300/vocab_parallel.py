@@ -44,6 +44,17 @@ class ShardKernels:
         B.vpd_jsd_bwd(s, t, beta, None, grad, saved, ds, dt)
 
 
+def _all_reduce(x: torch.Tensor, op, group):
+    """All-reduce of the [N, 2] exchange buffer. NCCL reduces it in device
+    memory; a gloo group gets a host copy (the buffer is 8 bytes per row)."""
+    if x.is_cuda and dist.get_backend(group) == "gloo":
+        h = x.cpu()
+        dist.all_reduce(h, op=op, group=group)
+        x.copy_(h)
+    else:
+        dist.all_reduce(x, op=op, group=group)
+
+
 def _rows(x: torch.Tensor) -> int:
     return x.shape[0] if x.dim() == 2 else x.shape[0] * x.shape[1]
 
@@ -59,11 +70,11 @@ def jsd_forward(s_local: torch.Tensor, t_local: torch.Tensor, beta: float, group
     saved = torch.empty(n, B.SAVED_PAIR, dtype=torch.float32, device=dev)
     xbuf = torch.empty(n, 2, dtype=torch.float32, device=dev)
     k.stats(s_local, t_local, saved, xbuf)
-    dist.all_reduce(xbuf, op=dist.ReduceOp.MAX, group=group)   # global maxima
+    _all_reduce(xbuf, dist.ReduceOp.MAX, group)   # global maxima
     k.rescale(n, saved, xbuf)
-    dist.all_reduce(xbuf, op=dist.ReduceOp.SUM, group=group)   # global sum-exps
+    _all_reduce(xbuf, dist.ReduceOp.SUM, group)   # global sum-exps
     k.divergence(s_local, t_local, float(beta), loss, saved, xbuf)
-    dist.all_reduce(xbuf, op=dist.ReduceOp.SUM, group=group)   # global KL-to-mixture sums
+    _all_reduce(xbuf, dist.ReduceOp.SUM, group)   # global KL-to-mixture sums
     k.finish(n, float(beta), saved, xbuf, loss)
     return loss, saved
 
