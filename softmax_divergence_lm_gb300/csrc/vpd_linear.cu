@@ -26,10 +26,11 @@
 //           two pairs), split along K, accumulated into fp32 C by atomics.
 // Small kernels merge the per-chunk partials and transpose bf16 matrices.
 //
-// Warp roles of k_linear (192 threads): warp 0 issues the TMA loads into a
+// Warp roles of k_linear (320 threads): warp 0 issues the TMA loads into a
 // ring of shared-memory stages; warp 1 issues the MMAs (one elected lane) into
-// one of two tensor-memory accumulator buffers; warps 2-5 are the epilogue,
-// thread i of the epilogue owning TMEM lane (and tile row) 32 (warp % 4) + lane.
+// one of two tensor-memory accumulator buffers; warps 2-9 are the epilogue,
+// two per TMEM lane quarter: thread i owns TMEM lane (and tile row)
+// 32 (warp % 4) + lane and one half of each tile's columns.
 // Stages hand over through mbarriers (TMA completion -> MMA; tcgen05.commit ->
 // producer), and so do the accumulator buffers (commit -> epilogue; epilogue
 // arrivals -> MMA), so the epilogue of one tile overlaps the MMAs of the next.
@@ -53,14 +54,16 @@ namespace vpd {
 namespace linear {
 
 constexpr int BM = 128;                     // tile rows (tensor-memory lanes)
-constexpr int BN = 128;                     // tile columns
+constexpr int BN = 256;                     // tile columns (one 128 x 256 MMA per 16 of k)
 constexpr int BK = 64;                      // k per stage: one 128-byte swizzle row of bf16
-constexpr int kStages = 6;
-constexpr int kTileBytes = BM * BK * 2;     // 16 KB per operand tile
-constexpr int kStageBytes = 2 * kTileBytes;
+constexpr int kStages = 4;
+constexpr int kTileBytes = BM * BK * 2;     // 16 KB: the A tile of a stage
+constexpr int kBTileBytes = BN * BK * 2;    // 32 KB: the B tile of a stage
+constexpr int kStageBytes = kTileBytes + kBTileBytes;
+constexpr int kEpiWarps = 8;              // two per tensor-memory lane quarter, one per half of the columns
 constexpr int kTransWords = 32 * 33;          // per epilogue warp: 32 rows x 32 bf16 pairs (+1 word pad)
-constexpr int kSmemBytes = kStages * kStageBytes + 4 * kTransWords * 4 + 1024;  // + alignment slack
-constexpr int kThreads = 192;
+constexpr int kSmemBytes = kStages * kStageBytes + kEpiWarps * kTransWords * 4 + 1024;  // + alignment slack
+constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kTmemCols = 512;
 constexpr float kTinyL = 1e-37f;
 constexpr float kLog2eL = 1.4426950408889634f;
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mb_init(&bars.acc_full[b], 1);
-      mb_init(&bars.acc_empty[b], 4);
+      mb_init(&bars.acc_empty[b], kEpiWarps);
     }
     bars.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -328,7 +331,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           acc_phase[buf] ^= 1u;
           tc_fence_after();
-          const uint32_t acc0 = tmem + 256u * buf;  // kGemm: the one accumulator; JSD modes: S
+          // kGemm: one of two 256-column accumulators; JSD modes: S at
+          // columns 0-255 and T at 256-511 (one buffer)
+          const uint32_t acc0 = tmem + 256u * buf;
           for (int kb = w.kb0; kb < w.kb1; ++kb) {
             if (!mb_wait(&bars.full[stage], phase, abort)) {
               ok = false;
@@ -352,14 +357,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!ok) break;
           mma_commit(&bars.acc_full[buf]);
-          buf ^= 1;
+          if (gemm) buf ^= 1;
         }
       }
       if (!ok) bars.abort = 1;
     }
   } else {
-    // ---------------- epilogue (warps 2-5) ----------------
+    // ---------------- epilogue (warps 2-9) ----------------
     const int q = warp & 3;                     // lane quarter of tensor memory
+    const int half = (warp - 2) >> 2;           // which 64 columns of each tile
     const int rloc = 32 * q + lane;             // row within the tile
     const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
     int buf = 0;
@@ -408,9 +414,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         acc_phase[buf] ^= 1u;
         tc_fence_after();
-        const uint32_t accS = tmem + lane_addr + 256u * buf;
+        const uint32_t accS = tmem + lane_addr + 256u * buf;  // buf is 0 in the JSD modes
         const int64_t col0 = static_cast<int64_t>(nt) * BN;
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
           float x[32];
           tmem_ld32(accS + c, x);
           if (gemm) {
@@ -569,13 +575,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mb_arrive(&bars.acc_empty[buf]);
-        buf ^= 1;
+        if (gemm) buf ^= 1;
       }
       if (!ok) break;
       if (rv && a.mode == kStats) {
-        reinterpret_cast<float4*>(a.part)[static_cast<int64_t>(w.chunk) * a.rows + row] = make_float4(ms, zs, mt, zt);
+        // one partial per (chunk, column half, row)
+        reinterpret_cast<float4*>(a.part)[(2 * static_cast<int64_t>(w.chunk) + half) * a.rows + row] =
+            make_float4(ms, zs, mt, zt);
       } else if (rv && a.mode == kDiv) {
-        reinterpret_cast<float2*>(a.part)[static_cast<int64_t>(w.chunk) * a.rows + row] = make_float2(accA, accB);
+        reinterpret_cast<float2*>(a.part)[(2 * static_cast<int64_t>(w.chunk) + half) * a.rows + row] =
+            make_float2(accA, accB);
       }
     }
     if (!ok) bars.abort = 1;
@@ -693,14 +702,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // A K-major bf16 operand [rows, k] with row stride `ld` elements, tiled in
-// {64, 128} boxes with the 128-byte swizzle; rows and k past the ends read 0.
-cudaError_t make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t k, int64_t ld) {
+// {64, box_rows} boxes with the 128-byte swizzle (A tiles 128 rows, B tiles
+// 256); rows and k past the ends read 0.
+cudaError_t make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t k, int64_t ld, int box_rows = BM) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   if ((reinterpret_cast<uintptr_t>(base) & 15u) || (ld * 2) % 16) return cudaErrorInvalidValue;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
-  const cuuint32_t box[2] = {BK, BM};
+  const cuuint32_t box[2] = {BK, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -743,7 +753,7 @@ using namespace linear;
 size_t linear_fwd_workspace(int64_t rows, int64_t vocab) {
   const int64_t mtiles = cdiv(rows, BM), ntiles = cdiv(vocab, BN);
   const int64_t chunks = cdiv(ntiles, tiles_per_unit(mtiles, ntiles));
-  return static_cast<size_t>(chunks) * static_cast<size_t>(rows) * 16u;
+  return static_cast<size_t>(2 * chunks) * static_cast<size_t>(rows) * 16u;  // two column halves per chunk
 }
 
 size_t linear_bwd_workspace(int64_t rows, int64_t vocab, int64_t hs, int64_t ht, bool student, bool teacher,
@@ -767,9 +777,9 @@ cudaError_t linear_jsd_forward(const LinearProblem& p, float* loss, float* saved
   CUtensorMap hs, wsm, ht, wt;
   cudaError_t e;
   if ((e = make_map(&hs, p.h_s, p.rows, p.hs, p.ld_hs)) != cudaSuccess) return e;
-  if ((e = make_map(&wsm, p.w_s, p.vocab, p.hs, p.ld_ws)) != cudaSuccess) return e;
+  if ((e = make_map(&wsm, p.w_s, p.vocab, p.hs, p.ld_ws, BN)) != cudaSuccess) return e;
   if ((e = make_map(&ht, p.h_t, p.rows, p.ht, p.ld_ht)) != cudaSuccess) return e;
-  if ((e = make_map(&wt, p.w_t, p.vocab, p.ht, p.ld_wt)) != cudaSuccess) return e;
+  if ((e = make_map(&wt, p.w_t, p.vocab, p.ht, p.ld_wt, BN)) != cudaSuccess) return e;
   Args a{};
   a.jmode = p.beta == 0.0 ? 1 : p.beta == 1.0 ? 2 : 0;
   a.rows = p.rows;
@@ -786,13 +796,13 @@ cudaError_t linear_jsd_forward(const LinearProblem& p, float* loss, float* saved
   a.mode = kStats;
   if ((e = launch(hs, wsm, ht, wt, a, stream)) != cudaSuccess) return e;
   const unsigned mg = static_cast<unsigned>(cdiv(p.rows, 256));
-  k_linear_merge_stats<<<mg, 256, 0, stream>>>(reinterpret_cast<const float4*>(ws), static_cast<int>(chunks), p.rows,
+  k_linear_merge_stats<<<mg, 256, 0, stream>>>(reinterpret_cast<const float4*>(ws), static_cast<int>(2 * chunks), p.rows,
                                                saved);
   note_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   a.mode = kDiv;
   if ((e = launch(hs, wsm, ht, wt, a, stream)) != cudaSuccess) return e;
-  k_linear_merge_div<<<mg, 256, 0, stream>>>(reinterpret_cast<const float2*>(ws), static_cast<int>(chunks), p.rows,
+  k_linear_merge_div<<<mg, 256, 0, stream>>>(reinterpret_cast<const float2*>(ws), static_cast<int>(2 * chunks), p.rows,
                                              a.jmode, a.beta, saved, loss);
   note_launch();
   return cudaGetLastError();
@@ -817,7 +827,7 @@ cudaError_t gemm_acc(const void* a0p, const void* a1p, int64_t lda, const void* 
   cudaError_t e;
   if ((e = make_map(&a0, a0p, rows, k, lda)) != cudaSuccess) return e;
   if ((e = make_map(&a1, a1p, rows, k, lda)) != cudaSuccess) return e;
-  if ((e = make_map(&b0, bp, n, k, ldb)) != cudaSuccess) return e;
+  if ((e = make_map(&b0, bp, n, k, ldb, BN)) != cudaSuccess) return e;
   Args a{};
   a.mode = kGemm;
   a.rows = rows;
@@ -886,9 +896,9 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
     const void* hs0 = static_cast<const char*>(p.h_s) + r0 * p.ld_hs * 2;
     const void* ht0 = static_cast<const char*>(p.h_t) + r0 * p.ld_ht * 2;
     if ((e = make_map(&hsm, hs0, n, p.hs, p.ld_hs)) != cudaSuccess) return e;
-    if ((e = make_map(&wsm, p.w_s, p.vocab, p.hs, p.ld_ws)) != cudaSuccess) return e;
+    if ((e = make_map(&wsm, p.w_s, p.vocab, p.hs, p.ld_ws, BN)) != cudaSuccess) return e;
     if ((e = make_map(&htm, ht0, n, p.ht, p.ld_ht)) != cudaSuccess) return e;
-    if ((e = make_map(&wtm, p.w_t, p.vocab, p.ht, p.ld_wt)) != cudaSuccess) return e;
+    if ((e = make_map(&wtm, p.w_t, p.vocab, p.ht, p.ld_wt, BN)) != cudaSuccess) return e;
     Args a{};
     a.mode = kGrad;
     a.jmode = p.beta == 0.0 ? 1 : p.beta == 1.0 ? 2 : 0;
