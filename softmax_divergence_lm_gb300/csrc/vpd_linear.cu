@@ -528,46 +528,50 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
 #pragma unroll
               for (int hl = 0; hl < 2; ++hl) {
-                // row-major [rows, V]: this thread's 32 columns, four 16-byte stores
-                if (rv) {
-                  __nv_bfloat16* dst = rm[hl] + row * a.cols + col0 + c;
-                  if (nvalid >= 32) {
-#pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                      *reinterpret_cast<uint4*>(dst + 8 * v4) =
-                          make_uint4(part[hl][4 * v4], part[hl][4 * v4 + 1], part[hl][4 * v4 + 2], part[hl][4 * v4 + 3]);
-                  } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                      if (i >= nvalid) continue;
-                      const uint32_t w2 = part[hl][i >> 1];
-                      const unsigned short b = static_cast<unsigned short>((i & 1) ? (w2 >> 16) : (w2 & 0xffffu));
-                      reinterpret_cast<unsigned short*>(dst)[i] = b;
-                    }
-                  }
-                }
-                // transposed [V, ld_t]: the warp's 32 x 32 block through shared
-                // memory, then each lane stores one column's 32 rows (64 bytes)
+                // The warp's 32 x 32 block (rows = lanes) goes through shared
+                // memory once; both layouts are then stored with four lanes per
+                // 64-byte run, eight runs per instruction.
                 uint32_t* tb = trans + (warp - 2) * kTransWords;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) tb[lane * 33 + i] = part[hl][i];
                 __syncwarp();
-                uint32_t colw[16];
+                const int piece = lane & 3;  // which 16 bytes of a 64-byte run
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                  const uint32_t w0 = tb[(2 * k) * 33 + (lane >> 1)], w1 = tb[(2 * k + 1) * 33 + (lane >> 1)];
-                  const uint32_t b0 = (lane & 1) ? (w0 >> 16) : (w0 & 0xffffu);
-                  const uint32_t b1 = (lane & 1) ? (w1 >> 16) : (w1 & 0xffffu);
-                  colw[k] = b0 | (b1 << 16);
+                for (int k = 0; k < 4; ++k) {
+                  const int r8 = 8 * k + (lane >> 2);  // block row (row-major) or block column (transposed)
+                  // row-major [rows, V]: row r8 of the block, columns 8 piece .. 8 piece + 7
+                  const int64_t grow = rbase + r8;
+                  if (grow < a.rows) {
+                    const uint32_t* src = tb + r8 * 33 + 4 * piece;
+                    __nv_bfloat16* dst = rm[hl] + grow * a.cols + col0 + c + 8 * piece;
+                    if (8 * piece + 8 <= nvalid) {
+                      *reinterpret_cast<uint4*>(dst) = make_uint4(src[0], src[1], src[2], src[3]);
+                    } else {
+#pragma unroll
+                      for (int e = 0; e < 8; ++e) {
+                        if (8 * piece + e >= nvalid) continue;
+                        const uint32_t w2 = src[e >> 1];
+                        reinterpret_cast<unsigned short*>(dst)[e] =
+                            static_cast<unsigned short>((e & 1) ? (w2 >> 16) : (w2 & 0xffffu));
+                      }
+                    }
+                  }
+                  // transposed [V, ld_t]: column r8 of the block, rows 8 piece .. 8 piece + 7
+                  if (r8 < nvalid) {
+                    uint32_t v[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                      const uint32_t w0 = tb[(8 * piece + 2 * e) * 33 + (r8 >> 1)];
+                      const uint32_t w1 = tb[(8 * piece + 2 * e + 1) * 33 + (r8 >> 1)];
+                      const uint32_t b0 = (r8 & 1) ? (w0 >> 16) : (w0 & 0xffffu);
+                      const uint32_t b1 = (r8 & 1) ? (w1 >> 16) : (w1 & 0xffffu);
+                      v[e] = b0 | (b1 << 16);
+                    }
+                    __nv_bfloat16* dst = tr[hl] + (col0 + c + r8) * a.ld_t + rbase + 8 * piece;
+                    *reinterpret_cast<uint4*>(dst) = make_uint4(v[0], v[1], v[2], v[3]);
+                  }
                 }
                 __syncwarp();
-                if (lane < nvalid) {
-                  __nv_bfloat16* dst = tr[hl] + (col0 + c + lane) * a.ld_t + rbase;
-#pragma unroll
-                  for (int v4 = 0; v4 < 4; ++v4)
-                    *reinterpret_cast<uint4*>(dst + 8 * v4) =
-                        make_uint4(colw[4 * v4], colw[4 * v4 + 1], colw[4 * v4 + 2], colw[4 * v4 + 3]);
-                }
               }
             }
           }
