@@ -406,11 +406,10 @@ vpd_status vpd_jsd_linear_bwd(const vpd_linear_heads *heads, double beta, const 
  * VPD_LINEAR_NOALLOC_MAX_BYTES bytes that the library keeps in device memory
  * for the life of the process (each GPU that loads the library holds one). A
  * problem whose forward workspace (vpd_jsd_linear_workspace) is larger returns
- * VPD_ERR_SHAPE before anything is launched. That workspace is 16 bytes per row
- * and vocabulary chunk, and the chunk count falls as rows grow (to one chunk
- * once the row tiles alone fill the GPU four times), so on a 152-SM GPU the
- * array serves up to about 260000 rows. Nothing is allocated: no cudaMalloc,
- * no cudaFree. The first call on a
+ * VPD_ERR_SHAPE before anything is launched. That workspace is 16 bytes per row,
+ * vocabulary chunk and column half of a tile, and the chunk count falls as
+ * rows grow, so on a 152-SM GPU at V = 151936 the array serves every row count
+ * up to 65536. Nothing is allocated: no cudaMalloc, no cudaFree. The first call on a
  * device looks up the array's device address on that device (make that device
  * current first); make this first call before any stream capture. Every call
  * shares the one array: calls whose work overlaps on the GPU (other streams,
