@@ -447,7 +447,9 @@ def run_e2e(args, B, s, t, g, dev, stream, world, chunks=8):
     # the link alone: plain pinned copies of 1 GiB, each direction by itself
     # and both at once, so the e2e number can be read against them
     peaks = copy_peaks(dev, s_h.view(-1)[: 1 << 29], ds_h.view(-1)[: 1 << 29])
-    bound_ms = max(h2d / peaks["h2d_GBps"], d2h / peaks["d2h_GBps"]) / 1e6
+    # the link's bound for a step: each direction at its own rate, and both
+    # together at the rate they reach when they run at once
+    bound_ms = max(h2d / peaks["h2d_GBps"], d2h / peaks["d2h_GBps"], (h2d + d2h) / peaks["both_GBps"]) / 1e6
     return {"value": round(n * world / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
             "copy_peaks": peaks, "copy_bound_ms_per_step": round(bound_ms, 3),
