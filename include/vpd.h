@@ -135,10 +135,12 @@ typedef struct {
 
 /* Forward. The statistics must be global before the divergence ([JSD page],
  * "Scope and limitations"): under the single-read conditions of vpd_jsd_fwdbwd
- * (one segment, 16-bit inputs, aligned rows), when the row fits in clusters of
- * at most 10 CTAs (V <= 191040 with 227 KB of shared memory per CTA), a
- * forward-only cluster kernel reads each row pair once and keeps it on chip
- * for both steps; otherwise the pages' design in two input passes: a
+ * (one segment, 16-bit inputs, aligned rows), a forward-only cluster kernel
+ * reads each row pair once and keeps it on chip for both steps, when the row
+ * fits in clusters of at most 10 CTAs (V <= 191040 with 227 KB of shared memory
+ * per CTA), or of at most 16 when the call has enough rows for the SMs those
+ * clusters leave idle to take a share (as in vpd_jsd_fwdbwd); otherwise the
+ * pages' design in two input passes: a
  * paired-statistics kernel merges per-segment (max,
  * sum-exp) of both inputs, then a divergence kernel reduces the two
  * KL-to-mixture expectations together ([JSD page], "Changes").

@@ -417,3 +417,27 @@ def test_bf16_row_max_above_2_126(B):
         assert_grad(to64(ds2), rds, f"beta={beta} streaming dS")
         keep = slice(None) if beta > 0.0 else slice(2, None)
         assert_grad(to64(dt2)[keep], rdt[keep], f"beta={beta} streaming dT")
+
+
+def test_forward_16_cta_clusters_with_idle_split(B):
+    """At V = 262144 the forward-only kernel needs clusters of 16 CTAs (112
+    SMs); with enough rows the 40 idle SMs take a share on the streaming passes
+    and the call takes that path (one fused launch plus two streaming ones):
+    every row against the oracle, and the plan query agrees."""
+    v = 262144
+    g = torch.Generator(device="cpu").manual_seed(41)
+    s0 = torch.randn(400, v, generator=g) * 4
+    s = s0.to(torch.bfloat16).cuda()
+    t = (s0 + torch.randn(400, v, generator=g) * 1.5).to(torch.bfloat16).cuda()
+    n = s.shape[0]
+    fused_rows, side_rows, planned = B.vpd_jsd_plan(s, t)
+    loss = torch.empty(n, device="cuda")
+    saved = torch.empty(n, 6, device="cuda")
+    k = launches_of(B, lambda: B.vpd_jsd_fwd(s, t, 0.5, None, loss, saved))
+    assert k == planned
+    if side_rows:
+        assert k == 3 and fused_rows + side_rows == n
+    rl, ra, rb, _, _ = O.jsd(to64(s), to64(t), 0.5, grad=False, threads=8)
+    assert_loss(to64(loss), rl, "V=262144 forward loss")
+    assert_loss(to64(saved)[:, 4], ra, "V=262144 forward saved A")
+    assert_loss(to64(saved)[:, 5], rb, "V=262144 forward saved B")
