@@ -284,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   const bool gemm = a.mode == kGemm;
+  const bool split = a.mode == kStats;  // the two heads' tiles one after the other
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -325,25 +326,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t u = blockIdx.x; u < a.units && ok; u += gridDim.x) {
         const Unit w = unit_of(a, u);
         for (int nt = w.nt0; nt < w.nt1 && ok; ++nt) {
+         // the statistics mode treats the two heads' tiles as two tiles in
+         // alternating buffers (its epilogue needs them one at a time), so one
+         // head's epilogue overlaps the other head's MMAs
+         int kbs = w.kb0;
+         for (int sub = 0; sub < (split ? 2 : 1) && ok; ++sub) {
+          const int kbe = split ? (sub == 0 ? a.nk0 : a.nk0 + a.nk1) : w.kb1;
           if (!mb_wait(&bars.acc_empty[buf], acc_phase[buf] ^ 1u, abort)) {
             ok = false;
             break;
           }
           acc_phase[buf] ^= 1u;
           tc_fence_after();
-          // kGemm: one of two 256-column accumulators; JSD modes: S at
-          // columns 0-255 and T at 256-511 (one buffer)
+          // kGemm and kStats: one of two 256-column accumulators; the other
+          // JSD modes: S at columns 0-255 and T at 256-511 (one buffer)
           const uint32_t acc0 = tmem + 256u * buf;
-          for (int kb = w.kb0; kb < w.kb1; ++kb) {
+          for (int kb = kbs; kb < kbe; ++kb) {
             if (!mb_wait(&bars.full[stage], phase, abort)) {
               ok = false;
               break;
             }
             tc_fence_after();
             const bool second = kb >= a.nk0;
-            const uint32_t dst = (!gemm && second) ? acc0 + BN : acc0;
+            const uint32_t dst = (!gemm && !split && second) ? acc0 + BN : acc0;
             // accumulate unless this is the first k-block into this accumulator
-            const bool first = gemm ? kb == w.kb0 : (second ? kb == a.nk0 : kb == 0);
+            const bool first = (gemm || split) ? kb == kbs : (second ? kb == a.nk0 : kb == 0);
             const uint32_t sa = saddr(smem + stage * kStageBytes);
             const uint64_t da = sw128_desc(sa), db = sw128_desc(sa + kTileBytes);
 #pragma unroll
@@ -357,7 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!ok) break;
           mma_commit(&bars.acc_full[buf]);
-          if (gemm) buf ^= 1;
+          if (gemm || split) buf ^= 1;
+          kbs = kbe;
+         }
         }
       }
       if (!ok) bars.abort = 1;
@@ -405,7 +414,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      for (int nt = w.nt0; nt < w.nt1; ++nt) {
+      for (int nt = w.nt0; nt < w.nt1 && ok; ++nt) {
+       for (int sub = 0; sub < (split ? 2 : 1); ++sub) {
         // every lane waits; the warp goes on only together (the tensor-memory
         // loads below are warp-collective)
         if (!__all_sync(0xffffffffu, mb_wait(&bars.acc_full[buf], acc_phase[buf], abort))) {
@@ -440,35 +450,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             continue;
           }
+          const int nvalid = static_cast<int>(a.cols - (col0 + c) < 32 ? a.cols - (col0 + c) : 32);
+          if (split) {  // kStats: one head's tile, online (max, sum-exp)
+            float m = sub == 0 ? ms : mt;
+            float z = sub == 0 ? zs : zt;
+            float cm = ninf();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < nvalid) cm = fmaxf(cm, x[i]);
+            if (cm > m) {
+              z = m == ninf() ? 0.f : z * expf(m - cm);
+              m = cm;
+            }
+            float e = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < nvalid) e += ex2f((x[i] - m) * kLog2eL);
+            z += e;
+            if (sub == 0) {
+              ms = m;
+              zs = z;
+            } else {
+              mt = m;
+              zt = z;
+            }
+            continue;
+          }
           float y[32];
           tmem_ld32(accS + BN + c, y);
-          const int nvalid = static_cast<int>(a.cols - (col0 + c) < 32 ? a.cols - (col0 + c) : 32);
-          if (a.mode == kStats) {
-            float cm = ninf(), cmt = ninf();
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i < nvalid) {
-                cm = fmaxf(cm, x[i]);
-                cmt = fmaxf(cmt, y[i]);
-              }
-            if (cm > ms) {
-              zs = ms == ninf() ? 0.f : zs * expf(ms - cm);
-              ms = cm;
-            }
-            if (cmt > mt) {
-              zt = mt == ninf() ? 0.f : zt * expf(mt - cmt);
-              mt = cmt;
-            }
-            float es = 0.f, et = 0.f;
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i < nvalid) {
-                es += ex2f((x[i] - ms) * kLog2eL);
-                et += ex2f((y[i] - mt) * kLog2eL);
-              }
-            zs += es;
-            zt += et;
-          } else if (a.mode == kDiv) {
+          if (a.mode == kDiv) {
             if (!live) continue;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -579,7 +589,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mb_arrive(&bars.acc_empty[buf]);
-        if (gemm) buf ^= 1;
+        if (gemm || split) buf ^= 1;
+       }
       }
       if (!ok) break;
       if (rv && a.mode == kStats) {
