@@ -226,11 +226,14 @@ struct Unit {
 __device__ __forceinline__ Unit unit_of(const Args& a, int64_t u) {
   Unit w;
   if (a.mode == kGemm) {
-    w.mt = static_cast<int>(u % a.mtiles);
-    const int64_t rest = u / a.mtiles;
-    w.nt0 = static_cast<int>(rest % a.ntiles);
+    // the column tiles of one row tile are neighbours in the unit order, so
+    // the CTAs that run them at the same time share the A tile through L2
+    // (A is read from DRAM once, not once per column tile)
+    w.nt0 = static_cast<int>(u % a.ntiles);
     w.nt1 = w.nt0 + 1;
-    const int ks = static_cast<int>(rest / a.ntiles);
+    const int64_t rest = u / a.ntiles;
+    w.mt = static_cast<int>(rest % a.mtiles);
+    const int ks = static_cast<int>(rest / a.mtiles);
     const int nk = a.nk0 + a.nk1;
     w.kb0 = static_cast<int>(static_cast<int64_t>(nk) * ks / a.ksplit);
     w.kb1 = static_cast<int>(static_cast<int64_t>(nk) * (ks + 1) / a.ksplit);
