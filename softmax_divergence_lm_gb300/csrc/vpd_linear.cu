@@ -33,7 +33,9 @@
 // 32 (warp % 4) + lane and one half of each tile's columns.
 // Stages hand over through mbarriers (TMA completion -> MMA; tcgen05.commit ->
 // producer), and so do the accumulator buffers (commit -> epilogue; epilogue
-// arrivals -> MMA), so the epilogue of one tile overlaps the MMAs of the next.
+// arrivals -> MMA), so the epilogue of one tile overlaps the MMAs of the next
+// wherever two tiles fit in tensor memory (all passes but kDiv, whose s and t
+// tiles of 256 columns fill it; kGrad takes 128-column tiles for that reason).
 // Every mbarrier wait gives up after two seconds, sets the device error word
 // and leaves the loops; the CTA waits for copies and MMAs in flight before it
 // frees its tensor memory.
@@ -54,15 +56,33 @@ namespace vpd {
 namespace linear {
 
 constexpr int BM = 128;                     // tile rows (tensor-memory lanes)
-constexpr int BN = 256;                     // tile columns (one 128 x 256 MMA per 16 of k)
+constexpr int BN = 256;                     // widest tile: one 128 x 256 MMA per 16 of k
 constexpr int BK = 64;                      // k per stage: one 128-byte swizzle row of bf16
-constexpr int kStages = 4;
 constexpr int kTileBytes = BM * BK * 2;     // 16 KB: the A tile of a stage
-constexpr int kBTileBytes = BN * BK * 2;    // 32 KB: the B tile of a stage
-constexpr int kStageBytes = kTileBytes + kBTileBytes;
+constexpr int kRingBytes = 4 * (kTileBytes + BN * BK * 2);  // shared-memory stages: 4 of 48 KB or 6 of 32 KB
+constexpr int kMaxStages = 6;
+// Tile columns of the gradient pass: it needs both heads' logits at once, and
+// two 128-column tiles of s and t fill the tensor memory, so its long epilogue
+// overlaps the MMAs of the next tile. The other passes use 256 columns: the
+// statistics pass (one head's tile at a time, in two buffers), the GEMMs
+// (two buffers), and the divergence pass, whose short epilogue costs less
+// than the narrower MMAs would (s and t of one 256-column tile fill the
+// tensor memory, so that epilogue does not overlap).
+constexpr int kGradTN = 128;
+template <int TN>
+struct TileShape {
+  static constexpr int kBBytes = TN * BK * 2;             // the B tile of a stage
+  static constexpr int kStageBytes = kTileBytes + kBBytes;
+  static constexpr int kStages = kRingBytes / kStageBytes;
+  static_assert(kStages <= kMaxStages && kStages * kStageBytes <= kRingBytes, "stage ring");
+  // instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1),
+  // bf16 A and B (bits 7-9, 10-12 = 1), both K-major, N >> 3 at bits 17-22,
+  // M >> 4 at bits 24-28
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((TN >> 3) << 17) | ((BM >> 4) << 24);
+};
 constexpr int kEpiWarps = 8;              // two per tensor-memory lane quarter, one per half of the columns
 constexpr int kTransWords = 32 * 33;          // per epilogue warp: 32 rows x 32 bf16 pairs (+1 word pad)
-constexpr int kSmemBytes = kStages * kStageBytes + kEpiWarps * kTransWords * 4 + 1024;  // + alignment slack
+constexpr int kSmemBytes = kRingBytes + kEpiWarps * kTransWords * 4 + 1024;  // + alignment slack
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kTmemCols = 512;
 constexpr float kTinyL = 1e-37f;
@@ -168,11 +188,7 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
   d |= static_cast<uint64_t>(2) << 61;
   return d;
 }
-// Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A
-// and B (bits 7-9, 10-12 = 1), both K-major, N >> 3 at bits 17-22, M >> 4 at
-// bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((BN >> 3) << 17) | ((BM >> 4) << 24);
-
+template <uint32_t kIdesc>
 __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
@@ -250,21 +266,24 @@ __device__ __forceinline__ Unit unit_of(const Args& a, int64_t u) {
 }
 
 struct __align__(8) Bars {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint32_t tmem_base;
   int abort;
 };
 
+template <int TN>
 __global__ void __launch_bounds__(kThreads, 1)
     k_linear(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap b0,
              const __grid_constant__ CUtensorMap a1, const __grid_constant__ CUtensorMap b1, Args a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Bars bars;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint32_t* trans = reinterpret_cast<uint32_t*>(smem + kStages * kStageBytes);  // kGrad transposes
+  using S = TileShape<TN>;
+  constexpr int kStages = S::kStages, kStageBytes = S::kStageBytes;
+  uint32_t* trans = reinterpret_cast<uint32_t*>(smem + kRingBytes);  // kGrad transposes
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &bars.abort;
 
@@ -288,6 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars.tmem_base;
   const bool gemm = a.mode == kGemm;
   const bool split = a.mode == kStats;  // the two heads' tiles one after the other
+  // two accumulator buffers in turn (else one buffer holds s and t of a tile)
+  const bool dbuf = gemm || split || TN < BN;
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -308,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* sa = smem + stage * kStageBytes;
             mb_expect_tx(&bars.full[stage], kStageBytes);
             tma_load_2d(sa, second ? &a1 : &a0, kk * BK, w.mt * BM, &bars.full[stage]);
-            tma_load_2d(sa + kTileBytes, second ? &b1 : &b0, kk * BK, nt * BN, &bars.full[stage]);
+            tma_load_2d(sa + kTileBytes, second ? &b1 : &b0, kk * BK, nt * TN, &bars.full[stage]);
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
@@ -342,7 +363,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc_phase[buf] ^= 1u;
           tc_fence_after();
           // kGemm and kStats: one of two 256-column accumulators; the other
-          // JSD modes: S at columns 0-255 and T at 256-511 (one buffer)
+          // JSD modes: S at columns 0 .. TN-1 and T at TN .. 2 TN - 1 of one of
+          // two buffers (TN = 128) or of the one buffer (TN = 256)
           const uint32_t acc0 = tmem + 256u * buf;
           for (int kb = kbs; kb < kbe; ++kb) {
             if (!mb_wait(&bars.full[stage], phase, abort)) {
@@ -351,14 +373,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const bool second = kb >= a.nk0;
-            const uint32_t dst = (!gemm && !split && second) ? acc0 + BN : acc0;
+            const uint32_t dst = (!gemm && !split && second) ? acc0 + TN : acc0;
             // accumulate unless this is the first k-block into this accumulator
             const bool first = (gemm || split) ? kb == kbs : (second ? kb == a.nk0 : kb == 0);
             const uint32_t sa = saddr(smem + stage * kStageBytes);
             const uint64_t da = sw128_desc(sa), db = sw128_desc(sa + kTileBytes);
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k)  // 16 bf16 = 32 bytes per MMA: +2 in the address field
-              mma_bf16(dst, da + 2u * k, db + 2u * k, (first && k == 0) ? 0u : 1u);
+              mma_bf16<S::kIdesc>(dst, da + 2u * k, db + 2u * k, (first && k == 0) ? 0u : 1u);
             mma_commit(&bars.empty[stage]);
             if (++stage == kStages) {
               stage = 0;
@@ -367,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!ok) break;
           mma_commit(&bars.acc_full[buf]);
-          if (gemm || split) buf ^= 1;
+          if (dbuf) buf ^= 1;
           kbs = kbe;
          }
         }
@@ -427,9 +449,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         acc_phase[buf] ^= 1u;
         tc_fence_after();
-        const uint32_t accS = tmem + lane_addr + 256u * buf;  // buf is 0 in the JSD modes
-        const int64_t col0 = static_cast<int64_t>(nt) * BN;
-        for (int c = half * (BN / 2); c < (half + 1) * (BN / 2); c += 32) {
+        const uint32_t accS = tmem + lane_addr + 256u * buf;  // buf stays 0 with one buffer
+        const int64_t col0 = static_cast<int64_t>(nt) * TN;
+        for (int c = half * (TN / 2); c < (half + 1) * (TN / 2); c += 32) {
           float x[32];
           tmem_ld32(accS + c, x);
           if (gemm) {
@@ -480,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             continue;
           }
           float y[32];
-          tmem_ld32(accS + BN + c, y);
+          tmem_ld32(accS + TN + c, y);
           if (a.mode == kDiv) {
             if (!live) continue;
 #pragma unroll
@@ -592,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mb_arrive(&bars.acc_empty[buf]);
-        if (gemm || split) buf ^= 1;
+        if (dbuf) buf ^= 1;
        }
       }
       if (!ok) break;
@@ -721,7 +743,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // A K-major bf16 operand [rows, k] with row stride `ld` elements, tiled in
 // {64, box_rows} boxes with the 128-byte swizzle (A tiles 128 rows, B tiles
-// 256); rows and k past the ends read 0.
+// as many as the tile has columns); rows and k past the ends read 0.
 cudaError_t make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t k, int64_t ld, int box_rows = BM) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
@@ -736,17 +758,19 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t k, 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// k_linear with TN-column tiles (the B maps' boxes must be TN rows high).
+template <int TN>
 cudaError_t launch(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1, const CUtensorMap& b1,
                    const Args& args, cudaStream_t stream) {
   if (args.units <= 0) return cudaSuccess;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(k_linear, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    attr_err = cudaFuncSetAttribute(k_linear<TN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t grid = args.units < sm_count() ? args.units : sm_count();
-  k_linear<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(a0, b0, a1, b1, args);
+  k_linear<TN><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(a0, b0, a1, b1, args);
   note_launch();
   return cudaGetLastError();
 }
@@ -812,14 +836,14 @@ cudaError_t linear_jsd_forward(const LinearProblem& p, float* loss, float* saved
   a.part = static_cast<float*>(ws);
   a.saved = saved;
   a.mode = kStats;
-  if ((e = launch(hs, wsm, ht, wt, a, stream)) != cudaSuccess) return e;
+  if ((e = launch<BN>(hs, wsm, ht, wt, a, stream)) != cudaSuccess) return e;
   const unsigned mg = static_cast<unsigned>(cdiv(p.rows, 256));
   k_linear_merge_stats<<<mg, 256, 0, stream>>>(reinterpret_cast<const float4*>(ws), static_cast<int>(2 * chunks), p.rows,
                                                saved);
   note_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   a.mode = kDiv;
-  if ((e = launch(hs, wsm, ht, wt, a, stream)) != cudaSuccess) return e;
+  if ((e = launch<BN>(hs, wsm, ht, wt, a, stream)) != cudaSuccess) return e;
   k_linear_merge_div<<<mg, 256, 0, stream>>>(reinterpret_cast<const float2*>(ws), static_cast<int>(2 * chunks), p.rows,
                                              a.jmode, a.beta, saved, loss);
   note_launch();
@@ -864,7 +888,7 @@ cudaError_t gemm_acc(const void* a0p, const void* a1p, int64_t lda, const void* 
   a.ldc = ldc;
   // one k part per tile and nothing in C to add to: plain stores
   a.gemm_store = may_store && ks == 1 ? 1 : 0;
-  return launch(a0, b0, a1, b0, a, stream);
+  return launch<BN>(a0, b0, a1, b0, a, stream);
 }
 
 cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, const float* loss,
@@ -914,9 +938,9 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
     const void* hs0 = static_cast<const char*>(p.h_s) + r0 * p.ld_hs * 2;
     const void* ht0 = static_cast<const char*>(p.h_t) + r0 * p.ld_ht * 2;
     if ((e = make_map(&hsm, hs0, n, p.hs, p.ld_hs)) != cudaSuccess) return e;
-    if ((e = make_map(&wsm, p.w_s, p.vocab, p.hs, p.ld_ws, BN)) != cudaSuccess) return e;
+    if ((e = make_map(&wsm, p.w_s, p.vocab, p.hs, p.ld_ws, kGradTN)) != cudaSuccess) return e;
     if ((e = make_map(&htm, ht0, n, p.ht, p.ld_ht)) != cudaSuccess) return e;
-    if ((e = make_map(&wtm, p.w_t, p.vocab, p.ht, p.ld_wt, BN)) != cudaSuccess) return e;
+    if ((e = make_map(&wtm, p.w_t, p.vocab, p.ht, p.ld_wt, kGradTN)) != cudaSuccess) return e;
     Args a{};
     a.mode = kGrad;
     a.jmode = p.beta == 0.0 ? 1 : p.beta == 1.0 ? 2 : 0;
@@ -925,7 +949,7 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
     a.nk0 = static_cast<int>(p.hs / BK);
     a.nk1 = static_cast<int>(p.ht / BK);
     a.mtiles = static_cast<int>(cdiv(n, BM));
-    a.ntiles = static_cast<int>(cdiv(p.vocab, BN));
+    a.ntiles = static_cast<int>(cdiv(p.vocab, kGradTN));
     a.tiles_per_unit = tiles_per_unit(a.mtiles, a.ntiles);
     a.units = static_cast<int64_t>(a.mtiles) * cdiv(a.ntiles, a.tiles_per_unit);
     a.beta = static_cast<float>(p.beta);
@@ -945,7 +969,7 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
       a.gtt_hi = G[1][2];
       a.gtt_lo = G[1][3];
     }
-    if ((e = launch(hsm, wsm, htm, wtm, a, stream)) != cudaSuccess) return e;
+    if ((e = launch<kGradTN>(hsm, wsm, htm, wtm, a, stream)) != cudaSuccess) return e;
     for (int x = 0; x < 2; ++x) {
       if (!want[x]) continue;
       // dh[r0:r0+n] += G_hi W + G_lo W  (K = V; B = W^T [H, V])
