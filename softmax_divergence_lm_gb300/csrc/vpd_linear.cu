@@ -228,6 +228,13 @@ __device__ __forceinline__ float lg2f(float x) {
   return y;
 }
 __device__ __forceinline__ float ninf() { return __int_as_float(0xff800000); }
+// fp32x2: one packed instruction for two values
+__device__ __forceinline__ float2 pk(float a, float b) { return make_float2(a, b); }
+__device__ __forceinline__ float2 pk_add(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 pk_sub(float2 a, float2 b) { return __fadd2_rn(a, make_float2(-b.x, -b.y)); }
+__device__ __forceinline__ float2 pk_fma(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 pk_ex2(float2 a) { return make_float2(ex2f(a.x), ex2f(a.y)); }
+__device__ __forceinline__ float2 pk_lg2(float2 a) { return make_float2(lg2f(a.x), lg2f(a.y)); }
 
 // ---------------------------------------------------------------------------
 // The sequence of work every role walks through in the same order.
@@ -505,45 +512,70 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(accS + TN + c, y);
           if (a.mode == kDiv) {
             if (!live) continue;
+            // two columns per packed instruction; columns past the vocabulary
+            // (logits 0 from the zero-filled head rows) get p = q = 0
+            const float2 nms2 = pk(nms, nms), nmt2 = pk(nmt, nmt), nKs2 = pk(nKs, nKs), nKt2 = pk(nKt, nKt);
+            const float2 l2e2 = pk(kLog2eL, kLog2eL), ws2 = pk(1.f - beta, 1.f - beta), wt2 = pk(beta, beta);
+            const float2 tiny2 = pk(kTinyL, kTinyL);
+            float2 accA2 = pk(0.f, 0.f), accB2 = pk(0.f, 0.f);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (i >= nvalid) continue;
-              const float lp = fmaf(x[i] + nms, kLog2eL, nKs), lq = fmaf(y[i] + nmt, kLog2eL, nKt);
-              const float p = ex2f(lp), qv = ex2f(lq);
+            for (int i = 0; i < 32; i += 2) {
+              const float2 lp = pk_fma(pk_add(pk(x[i], x[i + 1]), nms2), l2e2, nKs2);
+              const float2 lq = pk_fma(pk_add(pk(y[i], y[i + 1]), nmt2), l2e2, nKt2);
+              float2 p = pk_ex2(lp), qv = pk_ex2(lq);
+              if (nvalid < 32) {  // warp-uniform: the ragged last tile only
+                if (i >= nvalid) p.x = qv.x = 0.f;
+                if (i + 1 >= nvalid) p.y = qv.y = 0.f;
+              }
               if (a.jmode == 0) {
-                const float lm = lg2f(fmaf(1.f - beta, p, fmaf(beta, qv, kTinyL)));
-                accA = fmaf(qv, lq - lm, accA);
-                accB = fmaf(p, lp - lm, accB);
+                const float2 lm = pk_lg2(pk_fma(ws2, p, pk_fma(wt2, qv, tiny2)));
+                accA2 = pk_fma(qv, pk_sub(lq, lm), accA2);
+                accB2 = pk_fma(p, pk_sub(lp, lm), accB2);
               } else if (a.jmode == 1) {
-                accA = fmaf(qv, lq - lp, accA);
+                accA2 = pk_fma(qv, pk_sub(lq, lp), accA2);
               } else {
-                accB = fmaf(p, lp - lq, accB);
+                accB2 = pk_fma(p, pk_sub(lp, lq), accB2);
               }
             }
+            accA += accA2.x + accA2.y;
+            accB += accB2.x + accB2.y;
           } else {  // kGrad
             // dS and dT of this thread's row for 32 columns (0 past the
             // chunk's rows: the transposed arrays are summed over rows)
             float gsv[32], gtv[32];
+            const bool want_t = a.gtt_hi != nullptr;  // warp-uniform: dT wanted
+            const float2 nms2 = pk(nms, nms), nmt2 = pk(nmt, nmt), nKs2 = pk(nKs, nKs), nKt2 = pk(nKt, nKt);
+            const float2 l2e2 = pk(kLog2eL, kLog2eL), ws2 = pk(1.f - beta, 1.f - beta), wt2 = pk(beta, beta);
+            const float2 tiny2 = pk(kTinyL, kTinyL), cs2 = pk(cs, cs), ct2 = pk(ct, ct);
+            const float2 csl2 = pk(cs * kLn2L, cs * kLn2L), ctl2 = pk(ct * kLn2L, ct * kLn2L);
+            const float2 ks2 = pk(ks_, ks_), kt2 = pk(kt_, kt_);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              float gs = 0.f, gt = 0.f;
-              if (live && i < nvalid) {
-                const float lp = fmaf(x[i] + nms, kLog2eL, nKs), lq = fmaf(y[i] + nmt, kLog2eL, nKt);
-                const float p = ex2f(lp), qv = ex2f(lq);
+            for (int i = 0; i < 32; i += 2) {
+              float2 gs = pk(0.f, 0.f), gt = pk(0.f, 0.f);
+              if (live) {
+                const float2 lp = pk_fma(pk_add(pk(x[i], x[i + 1]), nms2), l2e2, nKs2);
+                const float2 lq = pk_fma(pk_add(pk(y[i], y[i + 1]), nmt2), l2e2, nKt2);
+                const float2 p = pk_ex2(lp), qv = pk_ex2(lq);
                 if (a.jmode == 0) {
-                  const float lm = lg2f(fmaf(1.f - beta, p, fmaf(beta, qv, kTinyL)));
-                  gs = p * fmaf(cs * kLn2L, lp - lm, ks_);
-                  gt = qv * fmaf(ct * kLn2L, lq - lm, kt_);
+                  const float2 lm = pk_lg2(pk_fma(ws2, p, pk_fma(wt2, qv, tiny2)));
+                  gs = __fmul2_rn(p, pk_fma(csl2, pk_sub(lp, lm), ks2));
+                  if (want_t) gt = __fmul2_rn(qv, pk_fma(ctl2, pk_sub(lq, lm), kt2));
                 } else if (a.jmode == 1) {  // dS = g (p - q), dT = g q (ln q - ln p - KL)
-                  gs = cs * (p - qv);
-                  gt = qv * fmaf(ct * kLn2L, lq - lp, kt_);
+                  gs = __fmul2_rn(cs2, pk_sub(p, qv));
+                  if (want_t) gt = __fmul2_rn(qv, pk_fma(ctl2, pk_sub(lq, lp), kt2));
                 } else {  // dS = g p (ln p - ln q - KL), dT = g (q - p)
-                  gs = p * fmaf(cs * kLn2L, lp - lq, ks_);
-                  gt = ct * (qv - p);
+                  gs = __fmul2_rn(p, pk_fma(csl2, pk_sub(lp, lq), ks2));
+                  if (want_t) gt = __fmul2_rn(ct2, pk_sub(qv, p));
+                }
+                if (nvalid < 32) {  // warp-uniform: the ragged last tile only
+                  if (i >= nvalid) gs.x = gt.x = 0.f;
+                  if (i + 1 >= nvalid) gs.y = gt.y = 0.f;
                 }
               }
-              gsv[i] = gs;
-              gtv[i] = gt;
+              gsv[i] = gs.x;
+              gsv[i + 1] = gs.y;
+              gtv[i] = gt.x;
+              gtv[i + 1] = gt.y;
             }
             const int64_t rbase = static_cast<int64_t>(w.mt) * BM + 32 * q;  // this warp's first row
 #pragma unroll
@@ -556,8 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
                 const __nv_bfloat162 h = __floats2bfloat162_rn(gv[2 * i], gv[2 * i + 1]);
-                const float2 hf = __bfloat1622float2(h);
-                const __nv_bfloat162 l = __floats2bfloat162_rn(gv[2 * i] - hf.x, gv[2 * i + 1] - hf.y);
+                const float2 lf = pk_sub(pk(gv[2 * i], gv[2 * i + 1]), __bfloat1622float2(h));
+                const __nv_bfloat162 l = __floats2bfloat162_rn(lf.x, lf.y);
                 part[0][i] = *reinterpret_cast<const uint32_t*>(&h);
                 part[1][i] = *reinterpret_cast<const uint32_t*>(&l);
               }
