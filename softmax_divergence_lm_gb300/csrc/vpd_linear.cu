@@ -495,9 +495,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               m = cm;
             }
             float e = 0.f;
+            if (nvalid >= 32) {  // two columns per packed instruction
+              const float2 nm2 = pk(-m, -m), l2e2 = pk(kLog2eL, kLog2eL);
+              float2 e2 = pk(0.f, 0.f);
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i < nvalid) e += ex2f((x[i] - m) * kLog2eL);
+              for (int i = 0; i < 32; i += 2) e2 = pk_add(e2, pk_ex2(__fmul2_rn(pk_add(pk(x[i], x[i + 1]), nm2), l2e2)));
+              e = e2.x + e2.y;
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < nvalid) e += ex2f((x[i] - m) * kLog2eL);
+            }
             z += e;
             if (sub == 0) {
               ms = m;
