@@ -406,12 +406,14 @@ vpd_status vpd_jsd_linear_bwd(const vpd_linear_heads *heads, double beta, const 
  * Same arguments, results and errors as vpd_jsd_linear_fwd, without the
  * workspace: the statistics partials go to one array of
  * VPD_LINEAR_NOALLOC_MAX_BYTES bytes that the library keeps in device memory
- * for the life of the process (each GPU that loads the library holds one). A
- * problem whose forward workspace (vpd_jsd_linear_workspace) is larger returns
- * VPD_ERR_SHAPE before anything is launched. That workspace is 16 bytes per row,
- * vocabulary chunk and column half of a tile, and the chunk count falls as
- * rows grow, so on a 152-SM GPU at V = 151936 the array serves every row count
- * up to 65536. Nothing is allocated: no cudaMalloc, no cudaFree. The first call on a
+ * for the life of the process (each GPU that loads the library holds one).
+ * The partials take 16 bytes per row, vocabulary chunk and column half of a
+ * tile; where the array is smaller than the forward workspace
+ * vpd_jsd_linear_workspace reports (the fastest plan's), the forward splits the
+ * vocabulary into fewer, longer chunks so that they fit, down to one chunk (32
+ * bytes per row). So every problem of up to 131072 rows runs, at any
+ * vocabulary; more rows return VPD_ERR_SHAPE before anything is launched.
+ * Nothing is allocated: no cudaMalloc, no cudaFree. The first call on a
  * device looks up the array's device address on that device (make that device
  * current first); make this first call before any stream capture. Every call
  * shares the one array: calls whose work overlaps on the GPU (other streams,

@@ -703,7 +703,7 @@ vpd_status vpd_jsd_linear_fwd_noalloc(const vpd_linear_heads* heads, double beta
   VPD_TRY(check_beta(beta));
   if (p.rows == 0) return ok();
   if (!loss || !saved) return fail(VPD_ERR_ARG, "vpd_jsd_linear_fwd_noalloc: loss and saved are required");
-  const size_t need = vpd::linear_fwd_workspace(p.rows, p.vocab);
+  const size_t need = vpd::linear_fwd_min_workspace(p.rows);
   if (need > vpd::kLinearNoAllocMaxBytes)
     return fail(VPD_ERR_SHAPE,
                 "vpd_jsd_linear_fwd_noalloc: this problem needs %zu bytes of scratch, the built-in array holds %zu; "

@@ -817,26 +817,64 @@ cudaError_t launch(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorM
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Vocabulary tiles per work unit of the JSD modes: enough units to fill the
-// GPU a few times over, each long enough that its fixed cost is small.
-int tiles_per_unit(int64_t mtiles, int64_t ntiles) {
-  const int64_t want_units = 4 * static_cast<int64_t>(sm_count());
-  int64_t per_m = cdiv(want_units, mtiles);  // chunks per row tile
-  if (per_m < 1) per_m = 1;
-  int64_t t = cdiv(ntiles, per_m);
-  if (t < 4) t = ntiles < 4 ? ntiles : 4;
-  return static_cast<int>(t);
+// Vocabulary tiles per work unit of the JSD modes. CTA b of the G resident
+// ones takes units b, b + G, ...; a pass lasts as long as its busiest CTA, so
+// the unit size t minimises ceil(units / G) x (t + 1/2) (units = row tiles x
+// vocabulary chunks, chunks = ceil(ntiles / t); half a tile stands for the
+// per-unit cost), with at least 4 tiles per unit, at most `max_chunks` chunks
+// (0: no limit; the chunks' partials must fit the workspace) and, on ties, the
+// larger t (fewer partials to merge).
+int tiles_per_unit(int64_t mtiles, int64_t ntiles, int64_t max_chunks = 0) {
+  const int64_t g = sm_count();
+  const int64_t t0 = ntiles < 4 ? ntiles : 4;
+  int64_t best_t = ntiles, best = -1;
+  for (int64_t t = t0; t <= ntiles; ++t) {
+    const int64_t chunks = cdiv(ntiles, t);
+    if (max_chunks > 0 && chunks > max_chunks) continue;
+    const int64_t span = cdiv(mtiles * chunks, g) * (2 * t + 1);
+    if (best < 0 || span <= best) {
+      best = span;
+      best_t = t;
+    }
+  }
+  return static_cast<int>(best_t);
+}
+
+// Parts of the k range of a GEMM with `tiles` output tiles and nk k-blocks:
+// the k that minimises ceil(tiles k / G) x (ceil(nk / k) + 8) (8 k-blocks
+// stand for the per-unit cost of the epilogue's atomics), at most 16 parts
+// and at least 8 k-blocks per part; on ties the smaller k.
+int64_t gemm_ksplit(int64_t tiles, int64_t nk) {
+  const int64_t g = sm_count();
+  int64_t kmax = nk / 8;
+  if (kmax > 16) kmax = 16;
+  if (kmax < 1) kmax = 1;
+  int64_t best_k = 1, best = -1;
+  for (int64_t k = 1; k <= kmax; ++k) {
+    const int64_t span = cdiv(tiles * k, g) * (cdiv(nk, k) + 8);
+    if (best < 0 || span < best) {
+      best = span;
+      best_k = k;
+    }
+  }
+  return best_k;
 }
 
 }  // namespace linear
 
 using namespace linear;
 
+// Partials of the forward: 16 bytes per row, vocabulary chunk and column half.
+static size_t fwd_partial_bytes(int64_t rows, int64_t chunks) {
+  return static_cast<size_t>(2 * chunks) * static_cast<size_t>(rows) * 16u;
+}
+
 size_t linear_fwd_workspace(int64_t rows, int64_t vocab) {
   const int64_t mtiles = cdiv(rows, BM), ntiles = cdiv(vocab, BN);
-  const int64_t chunks = cdiv(ntiles, tiles_per_unit(mtiles, ntiles));
-  return static_cast<size_t>(2 * chunks) * static_cast<size_t>(rows) * 16u;  // two column halves per chunk
+  return fwd_partial_bytes(rows, cdiv(ntiles, tiles_per_unit(mtiles, ntiles)));
 }
+
+size_t linear_fwd_min_workspace(int64_t rows) { return fwd_partial_bytes(rows, 1); }
 
 size_t linear_bwd_workspace(int64_t rows, int64_t vocab, int64_t hs, int64_t ht, bool student, bool teacher,
                             int64_t chunk_rows) {
@@ -852,10 +890,14 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 cudaError_t linear_jsd_forward(const LinearProblem& p, float* loss, float* saved, void* ws, size_t ws_bytes,
                                cudaStream_t stream) {
+  if (p.rows <= 0) return cudaSuccess;
   const int64_t mtiles = cdiv(p.rows, BM), ntiles = cdiv(p.vocab, BN);
-  const int tpu = tiles_per_unit(mtiles, ntiles);
+  if (ws_bytes < linear_fwd_min_workspace(p.rows)) return cudaErrorInvalidValue;
+  // the fastest plan whose partials fit the workspace (the plan of
+  // linear_fwd_workspace when the workspace is at least that large)
+  const int64_t max_chunks = static_cast<int64_t>(ws_bytes / fwd_partial_bytes(p.rows, 1));
+  const int tpu = tiles_per_unit(mtiles, ntiles, max_chunks);
   const int64_t chunks = cdiv(ntiles, tpu);
-  if (ws_bytes < linear_fwd_workspace(p.rows, p.vocab)) return cudaErrorInvalidValue;
   CUtensorMap hs, wsm, ht, wt;
   cudaError_t e;
   if ((e = make_map(&hs, p.h_s, p.rows, p.hs, p.ld_hs)) != cudaSuccess) return e;
@@ -901,7 +943,7 @@ cudaError_t transpose_bf16(const void* in, int64_t rows, int64_t cols, int64_t l
 }
 
 // C[rows, n] += A0 B0^T + A1 B1^T with K-major bf16 operands (A [rows, k],
-// B [n, k]), split along k so that about four units run per SM; with
+// B [n, k]), split along k so that the units spread evenly over the SMs; with
 // may_store (C holds nothing yet) and a single k part, C = the product.
 cudaError_t gemm_acc(const void* a0p, const void* a1p, int64_t lda, const void* bp, int64_t ldb, int64_t rows,
                      int64_t n, int64_t k, float* C, int64_t ldc, bool may_store, cudaStream_t stream) {
@@ -918,10 +960,7 @@ cudaError_t gemm_acc(const void* a0p, const void* a1p, int64_t lda, const void* 
   a.mtiles = static_cast<int>(cdiv(rows, BM));
   a.ntiles = static_cast<int>(cdiv(n, BN));
   const int64_t tiles = static_cast<int64_t>(a.mtiles) * a.ntiles;
-  int64_t ks = cdiv(4 * static_cast<int64_t>(sm_count()), tiles);
-  const int64_t nk = a.nk0 + a.nk1;
-  if (ks > nk / 8) ks = nk / 8;  // at least 8 k-blocks per unit
-  if (ks < 1) ks = 1;
+  const int64_t ks = gemm_ksplit(tiles, a.nk0 + a.nk1);
   a.ksplit = static_cast<int>(ks);
   a.units = tiles * ks;
   a.C = C;

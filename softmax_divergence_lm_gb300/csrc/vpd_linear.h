@@ -24,6 +24,9 @@ struct LinearProblem {
 constexpr int64_t kLinearChunkRows = 8192;
 
 size_t linear_fwd_workspace(int64_t rows, int64_t vocab);
+// The least workspace the forward runs with (its vocabulary in one chunk); a
+// workspace between this and linear_fwd_workspace gets fewer, longer chunks.
+size_t linear_fwd_min_workspace(int64_t rows);
 size_t linear_bwd_workspace(int64_t rows, int64_t vocab, int64_t hs, int64_t ht, bool student, bool teacher,
                             int64_t chunk_rows);
 cudaError_t linear_jsd_forward(const LinearProblem& p, float* loss, float* saved, void* ws, size_t ws_bytes,

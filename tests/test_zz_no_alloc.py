@@ -61,9 +61,32 @@ def test_no_alloc_forward_matches_workspace_forward_twice(B):
         assert np.all(np.isfinite(sv[:, :4]))
 
 
+def test_no_alloc_forward_fewer_chunks_at_qwen_heads(B):
+    """16384 rows of the Qwen heads: the fastest plan's partials exceed the
+    built-in array, so the no-alloc forward runs with fewer, longer vocabulary
+    chunks; same results as the workspace forward within the loss tolerance."""
+    from softmax_divergence_lm_gb300 import synth
+    n = 16384
+    h_s, w_s, h_t, w_t = synth.linear_heads(device="cuda", n=n, seed=23)
+    heads = B.make_heads(h_s, w_s, h_t, w_t)
+    fwd_b, _ = B.vpd_jsd_linear_workspace(heads, False, False)
+    assert fwd_b > 4 << 20 >= 32 * n
+    ref_loss, ref_saved = _forward_with_workspace(B, heads, n, 0.5)
+    loss = torch.full((n,), 7.0, device="cuda")
+    saved = torch.full((n, 6), 7.0, device="cuda")
+    B.vpd_jsd_linear_fwd_noalloc(heads, 0.5, loss, saved)
+    torch.cuda.synchronize()
+    B.vpd_device_status()
+    assert_loss(to64(loss), to64(ref_loss), "no-alloc forward, 16384 rows, loss")
+    sv, rsv = to64(saved), to64(ref_saved)
+    for col in range(6):
+        assert_loss(sv[:, col], rsv[:, col], f"no-alloc forward, 16384 rows, saved[:, {col}]")
+
+
 def test_no_alloc_forward_rejects_oversized_problem(B):
-    """A problem whose scratch would not fit the built-in array is refused on
-    the host with VPD_ERR_SHAPE (nothing is launched, nothing is read)."""
+    """A problem whose scratch would not fit the built-in array even with the
+    vocabulary in one chunk (more than 131072 rows) is refused on the host with
+    VPD_ERR_SHAPE (nothing is launched, nothing is read)."""
     heads = B.vpd_linear_heads(0x10000, 0x10000, 0x10000, 0x10000, 1 << 20, 151936, 896, 1536, 896, 896, 1536, 1536)
     fwd_b, _ = B.vpd_jsd_linear_workspace(heads, False, False)
     assert fwd_b > 4 << 20
