@@ -633,7 +633,7 @@ __device__ __forceinline__ KlAcc block_kl(KlAcc x, float* sc) {
 }
 
 template <class T>
-__global__ void __launch_bounds__(kThreads) k_kl_fwd(View a, View b, Segs seg, int a_is_teacher,
+__global__ void __launch_bounds__(kThreads, 2) k_kl_fwd(View a, View b, Segs seg, int a_is_teacher,
                                                      float* loss, float* saved) {
   __shared__ float scratch[6 * 32];
   for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
