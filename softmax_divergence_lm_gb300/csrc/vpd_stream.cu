@@ -765,7 +765,7 @@ __device__ __forceinline__ EntAcc block_ent(EntAcc x, float* sc) {
 }
 
 template <class T>
-__global__ void __launch_bounds__(kThreads) k_entropy_fwd(View x, Segs seg, float* out, float* saved) {
+__global__ void __launch_bounds__(kThreads, 3) k_entropy_fwd(View x, Segs seg, float* out, float* saved) {
   __shared__ float scratch[3 * 32];
   for (int64_t r = blockIdx.x; r < x.rows; r += gridDim.x) {
     const char* px = row_ptr<T>(x, r);
