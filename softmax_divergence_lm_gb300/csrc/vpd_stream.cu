@@ -246,7 +246,7 @@ struct PairStatBody {
 };
 
 template <class T>
-__global__ void __launch_bounds__(kThreads) k_pair_stats(View s, View t, Segs seg, float* saved) {
+__global__ void __maxnreg__(56) k_pair_stats(View s, View t, Segs seg, float* saved) {
   __shared__ float scratch[2 * 64];
   for (int64_t r = blockIdx.x; r < s.rows; r += gridDim.x) {
     const char* ps = row_ptr<T>(s, r);
@@ -379,7 +379,7 @@ struct DivBody {
 };
 
 template <class T, int MODE>
-__global__ void __launch_bounds__(kThreads) k_jsd_div(View s, View t, float beta, float* loss,
+__global__ void __maxnreg__(40) k_jsd_div(View s, View t, float beta, float* loss,
                                                       float* saved) {
   __shared__ float scratch[2 * 32];
   __shared__ int iscratch[32];
