@@ -282,7 +282,10 @@ def run_ours(args, world, rank, local):
         cuda_build.build()
     barrier(world)
     B.load()
-    s3, t3 = synth.qwen_vocab(device=dev)
+    # rank r holds the r-th contiguous share of a batch of `world` such
+    # workloads: its own rows, drawn with the recipe's seed offset by r (rank 0
+    # is the single-GPU workload)
+    s3, t3 = synth.qwen_vocab(device=dev, seed=synth.SEEDS["qwen_vocab"] + rank)
     s = s3.view(BATCH * SEQ, VOCAB)[:-1]
     t = t3.view(BATCH * SEQ, VOCAB)[:-1]
     g = torch.full((ROWS,), 1.0 / ROWS, device=dev)
@@ -371,7 +374,8 @@ def run_ours(args, world, rank, local):
                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                "config": {"workload": WORKLOAD, "tokens_per_step_per_gpu": ROWS, "vocab": VOCAB, "beta": BETA,
                           "grads": "dS and dT, bf16", "l2": "inputs (4.98 GB per step) larger than the 129 MB L2",
-                          "parallelism": f"rows sharded: {world} independent replica(s), no collective"},
+                          "parallelism": (f"rows sharded contiguously: rank r holds rows [r x {ROWS}, (r + 1) x {ROWS})"
+                                          f" of a {world} x {ROWS}-row batch, no collective")},
                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clock_info,
                "gpu_launches": launches, "impl": "ours"}
         print(json.dumps(out), flush=True)
