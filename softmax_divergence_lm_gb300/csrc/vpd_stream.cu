@@ -109,13 +109,15 @@ __device__ __forceinline__ void visit2(const char* a, const char* b, int64_t n, 
   for (int64_t j = head + nv * V + tid; j < n; j += nt) body.one(j, T::load(a, j), T::load(b, j));
 }
 
+// (tid, nt): this thread's place among the nt threads that share the row (the
+// CTA, or one warp in the warp-per-row kernels).
 template <class T, class Body>
-__device__ __forceinline__ void visit1(const char* a, int64_t n, Body& body) {
+__device__ __forceinline__ void visit1(const char* a, int64_t n, Body& body, int64_t tid = threadIdx.x,
+                                       int64_t nt = blockDim.x) {
   constexpr int V = T::kVec;
   const uintptr_t pa = reinterpret_cast<uintptr_t>(a);
   int64_t head = static_cast<int64_t>((16u - (pa & 15u)) & 15u) / T::kSize;
   if (head > n) head = n;
-  const int64_t tid = threadIdx.x, nt = blockDim.x;
   for (int64_t j = tid; j < head; j += nt) body.one(j, T::load(a, j));
   const int64_t nv = (n - head) / V;
   const char* va = a + head * T::kSize;
@@ -790,6 +792,47 @@ __global__ void __launch_bounds__(kThreads, 3) k_entropy_fwd(View x, Segs seg, f
   }
 }
 
+// The same merge over the 32 lanes of a warp only (every lane gets the result).
+__device__ __forceinline__ EntAcc warp_ent(EntAcc x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    EntAcc y{{__shfl_xor_sync(0xffffffffu, x.s.m, o), __shfl_xor_sync(0xffffffffu, x.s.z, o)},
+             __shfl_xor_sync(0xffffffffu, x.y, o)};
+    x = ent_merge(x, y);
+  }
+  return x;
+}
+
+// Short rows: one warp per row (each CTA of kWarpRowThreads threads holds as
+// many rows as warps), so that more rows are in flight per SM than the limit of
+// resident CTAs allows one CTA per row; the reductions are warp shuffles only.
+template <class T>
+__global__ void __maxnreg__(48) k_entropy_fwd_warp(View x, Segs seg, float* out, float* saved) {
+  const int lane = threadIdx.x & 31, wpb = blockDim.x >> 5;
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * wpb + (threadIdx.x >> 5); r < x.rows;
+       r += static_cast<int64_t>(gridDim.x) * wpb) {
+    const char* px = row_ptr<T>(x, r);
+    EntAcc run{stat_init(), 0.f};
+    for (int k = 0; k < seg.count; ++k) {
+      const int64_t off = seg.off[k], w = seg.off[k + 1] - off;
+      EntBody body{{stat_init(), 0.f}};
+      visit1<T>(px + off * T::kSize, w, body, lane, 32);
+      run = ent_merge(run, warp_ent(body.acc));
+    }
+    if (lane == 0) {
+      const RowStat st = finish_stat(run.s);
+      const float h = stat_ok(st) ? st.L - run.y / run.s.z : qnan();
+      out[r] = h;
+      if (saved) {
+        float* o = saved + r * VPD_SAVED_ENTROPY;
+        o[0] = st.m;
+        o[1] = st.L;
+        o[2] = h;
+      }
+    }
+  }
+}
+
 template <class G>
 struct EntBwdBody {
   float m, L, H, g;
@@ -1075,6 +1118,18 @@ cudaError_t launch_rows(Kern kernel, int64_t rows, int threads, cudaStream_t str
   return cudaGetLastError();
 }
 
+// One warp per row at a time (grid-stride over groups of rows), CTAs of
+// kWarpRowThreads threads.
+constexpr int kWarpRowThreads = 128;
+template <class Kern, class... Args>
+cudaError_t launch_warp_rows(Kern kernel, int64_t rows, cudaStream_t stream, Args... args) {
+  if (rows <= 0) return cudaSuccess;
+  constexpr int wpb = kWarpRowThreads / 32;
+  kernel<<<grid_for(kernel, (rows + wpb - 1) / wpb, kWarpRowThreads), kWarpRowThreads, 0, stream>>>(args...);
+  note_launch();
+  return cudaGetLastError();
+}
+
 template <template <class> class F, class... Args>
 cudaError_t by_input(int dtype, Args&&... args) {
   switch (dtype) {
@@ -1146,7 +1201,10 @@ struct KlL {
 template <class T>
 struct EntL {
   static cudaError_t run(const View& x, const Segs& seg, float* out, float* saved, cudaStream_t st) {
-    return launch_rows(k_entropy_fwd<T>, x.rows, threads_for(x.vocab, T::kSize, true), st, x, seg, out, saved);
+    const int threads = threads_for(x.vocab, T::kSize, true);
+    if (threads == 32)  // short rows: one warp per row
+      return launch_warp_rows(k_entropy_fwd_warp<T>, x.rows, st, x, seg, out, saved);
+    return launch_rows(k_entropy_fwd<T>, x.rows, threads, st, x, seg, out, saved);
   }
 };
 
