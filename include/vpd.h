@@ -177,8 +177,9 @@ vpd_status vpd_jsd_bwd(const vpd_view *s, const vpd_view *t, double beta, const 
  * gradients come from one HBM read; a bf16 row whose finite max exceeds 2^126
  * is treated as out of contract (NaN, zero gradient). The clusters cannot
  * always cover every SM (at V = 151936, 15 clusters of 9 CTAs use 135 of 152);
- * when the call has many rows per cluster and a plain 2-D layout, its last
- * rows go to the streaming kernels on the SMs left idle, on a side stream that
+ * when the call has many rows per cluster, its last rows (from any row of
+ * the view, mid-batch included) go to the streaming kernels on the SMs left
+ * idle, on a side stream that
  * forks from `stream` and joins it again before the call's work ends (the
  * share follows the measured per-SM rates of the two paths). Otherwise the
  * call runs the two forward kernels and the backward kernel in turn. With both

@@ -219,9 +219,9 @@ vpd_status vpd_jsd_fwd(const vpd_view* s, const vpd_view* t, double beta, const 
       vpd::View fs = vs, ft = vt, ss_v = vs, st_v = vt;
       fs.rows = ft.rows = nf;
       ss_v.rows = st_v.rows = side;
-      const int64_t es = vs.dtype == VPD_F32 ? 4 : 2;
-      ss_v.data = vs.data + vs.map.offset(nf) * es;
-      st_v.data = vt.data + vt.map.offset(nf) * es;
+      // the side views start at row nf of the caller's views (mid-batch too)
+      ss_v.map.first += nf;
+      st_v.map.first += nf;
       VPD_CUDA(cudaEventRecord(ss->fork, st), "forking the side stream");
       VPD_CUDA(cudaStreamWaitEvent(ss->stream, ss->fork, 0), "forking the side stream");
       cudaError_t e = vpd::launch_jsd_fused(fs, ft, beta, nullptr, loss, saved, none, none, st, -1, 16);
@@ -301,9 +301,9 @@ vpd_status vpd_jsd_fwdbwd(const vpd_view* s, const vpd_view* t, double beta,
       vpd::View fs = vs, ft = vt, ss_v = vs, st_v = vt;
       fs.rows = ft.rows = nf;
       ss_v.rows = st_v.rows = side;
-      const int64_t es = vs.dtype == VPD_F32 ? 4 : 2;
-      ss_v.data = vs.data + vs.map.offset(nf) * es;
-      st_v.data = vt.data + vt.map.offset(nf) * es;
+      // the side views start at row nf of the caller's views (mid-batch too)
+      ss_v.map.first += nf;
+      st_v.map.first += nf;
       vpd::Grad sgs = gs, sgt = gt;
       if (gs.data) sgs.data = gs.data + nf * gs.row_stride * (gs.dtype == VPD_F32 ? 4 : 2);
       if (gt.data) sgt.data = gt.data + nf * gt.row_stride * (gt.dtype == VPD_F32 ? 4 : 2);

@@ -180,7 +180,9 @@ struct RowMap {
   int64_t row_stride;
   int64_t rows_per_batch;
   int64_t batch_stride;
+  int64_t first = 0;  // row r of this map is row first + r of the caller's view
   __host__ __device__ __forceinline__ int64_t offset(int64_t r) const {
+    r += first;
     if (rows_per_batch > 0)
       return (r / rows_per_batch) * batch_stride + (r % rows_per_batch) * row_stride;
     return r * row_stride;

@@ -161,7 +161,7 @@ void fused_idle_split(const View& s, const Grad& ds, const Grad& dt, int max_clu
   const double rate = idle_rate(fwd);
   // long rows only: their streaming CTAs are wide enough (at least three warps
   // of 40 or more registers) that none fits beside a fused CTA on its SM
-  if (rate <= 0.0 || s.map.rows_per_batch > 0 || s.dtype == kF32 || s.vocab < 100000) return;
+  if (rate <= 0.0 || s.dtype == kF32 || s.vocab < 100000) return;
   if (!fwd) {
     const int gdtype = ds.data ? ds.dtype : dt.dtype;
     if (gdtype != kF32 && gdtype != s.dtype) return;

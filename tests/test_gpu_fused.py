@@ -196,6 +196,26 @@ def test_idle_sm_split_every_row(B, gdtype):
     assert_loss(to64(saved)[live, 5], rb[live], "idle-SM split forward saved B")
 
 
+def test_idle_sm_split_causal_view(B):
+    """A [3, 401, V] causal-shift view at the Qwen vocabulary (1200 rows): the
+    idle-SM split starts its side rows in the middle of a batch; every row of
+    both parts against the oracle, forward+backward and forward only."""
+    g = torch.Generator(device="cpu").manual_seed(29)
+    base_s = (torch.randn(3, 401, 151936, generator=g) * 4).to(torch.bfloat16).cuda()
+    base_t = (base_s.float().cpu() + torch.randn(3, 401, 151936, generator=g) * 2).to(torch.bfloat16).cuda()
+    s, t = base_s[:, :-1], base_t[:, :-1]
+    fused_rows, side_rows, _ = B.vpd_jsd_plan(s, t, None, torch.empty(1200, 151936, dtype=torch.bfloat16,
+                                                                       device="cuda"), None)
+    assert side_rows > 0 and fused_rows % 400 != 0, (fused_rows, side_rows)
+    check(B, s, t, 0.5, torch.bfloat16, label="idle-SM split, causal view", launches=(4,))
+    loss = torch.empty(1200, device="cuda")
+    saved = torch.empty(1200, 6, device="cuda")
+    k = launches_of(B, lambda: B.vpd_jsd_fwd(s, t, 0.5, None, loss, saved))
+    assert k == 3, f"causal forward with the idle-SM split: {k} launches"
+    rl = O.jsd(to64(s.reshape(-1, 151936)), to64(t.reshape(-1, 151936)), 0.5, grad=False, threads=8)[0]
+    assert_loss(to64(loss), rl, "idle-SM split causal forward loss")
+
+
 def test_forward_kernel_many_rows_at_cluster_width(B):
     """The forward-only kernel on 240 rows at the Qwen vocabulary (clusters of
     9 CTAs, 23 workers x R = 3): its stages and slot rings wrap many times."""
