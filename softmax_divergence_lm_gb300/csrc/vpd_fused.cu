@@ -137,20 +137,24 @@ bool choose(int64_t vocab, int64_t rows, int max_cluster, bool fwd, Config* cfg)
 }  // namespace
 
 // Rate of the streaming path on one otherwise idle SM relative to one SM of a
-// fused cluster, in rows per second per SM, measured at V = 151936: 0.45 for
-// forward+backward (three streaming passes against one read), 0.9 for the
-// forward (two passes). VPD_IDLE_RATE / VPD_IDLE_RATE_FWD override them (0
-// disables the split).
-static double idle_rate(bool fwd) {
+// fused cluster, in rows per second per SM: for forward+backward (three
+// streaming passes against one read) 0.5 with clusters of up to 15 CTAs and
+// 0.55 with 16 (a cluster of 16 spends more of each row on its exchanges), for
+// the forward (two passes) 0.9; measured at V = 151936 (clusters of 9) and
+// V = 262144 (clusters of 16). VPD_IDLE_RATE / VPD_IDLE_RATE_FWD override them
+// (0 disables the split).
+static double idle_rate(bool fwd, int cluster) {
   static const double r[2] = {[] {
                                 const char* e = getenv("VPD_IDLE_RATE");
-                                return e && e[0] ? atof(e) : 0.45;
+                                return e && e[0] ? atof(e) : -1.0;
                               }(),
                               [] {
                                 const char* e = getenv("VPD_IDLE_RATE_FWD");
                                 return e && e[0] ? atof(e) : 0.9;
                               }()};
-  return r[fwd ? 1 : 0];
+  if (fwd) return r[1];
+  if (r[0] >= 0.0) return r[0];
+  return cluster >= 16 ? 0.55 : 0.5;
 }
 
 void fused_idle_split(const View& s, const Grad& ds, const Grad& dt, int max_cluster, int64_t* side_rows,
@@ -158,16 +162,17 @@ void fused_idle_split(const View& s, const Grad& ds, const Grad& dt, int max_clu
   *side_rows = 0;
   *idle_sms = 0;
   const bool fwd = !ds.data && !dt.data;
-  const double rate = idle_rate(fwd);
   // long rows only: their streaming CTAs are wide enough (at least three warps
   // of 40 or more registers) that none fits beside a fused CTA on its SM
-  if (rate <= 0.0 || s.dtype == kF32 || s.vocab < 100000) return;
+  if (s.dtype == kF32 || s.vocab < 100000) return;
   if (!fwd) {
     const int gdtype = ds.data ? ds.dtype : dt.dtype;
     if (gdtype != kF32 && gdtype != s.dtype) return;
   }
   Config cfg;
   if (!choose(s.vocab, s.rows, max_cluster, fwd, &cfg)) return;
+  const double rate = idle_rate(fwd, cfg.C);
+  if (rate <= 0.0) return;
   const int clusters = clusters_for(cfg.C);
   const int used = clusters * cfg.C, idle = sm_count() - used;
   // worth it only with every cluster busy for many rows
