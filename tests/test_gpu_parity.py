@@ -354,7 +354,10 @@ def test_qwen_vocab_workload(B):
     n = bsz * seq
     flat_s, flat_t = s3.view(n, v), t3.view(n, v)
     # (i) rows 0..N-2 of the [N, V] buffer
-    rows = _sample(n - 1, count=16)
+    nf, _, _ = B.vpd_jsd_plan(flat_s[:-1], flat_t[:-1], None, torch.empty(n - 1, v, dtype=torch.bfloat16,
+                                                                          device="cuda"), None)
+    nf_fwd, _, _ = B.vpd_jsd_plan(flat_s[:-1], flat_t[:-1])
+    rows = _sample(n - 1, extra=[r for r in (nf - 1, nf, nf_fwd - 1, nf_fwd) if 0 <= r < n - 1], count=16)
     check_pair(B, flat_s[:-1], flat_t[:-1], 0.5, rows=rows, gdtype=torch.bfloat16, fused=True,
                label="qwen rows")
     check_pair(B, flat_s[:-1], flat_t[:-1], 0.5, rows=rows, want_t=False, fused=True, label="qwen detached")
@@ -395,7 +398,11 @@ def test_large_sweep_workload(B, dtype):
     from softmax_divergence_lm_gb300 import synth
     s, t = synth.large_sweep(device="cuda", dtype=dtype)
     n, v = s.shape
-    rows = _sample(n, count=8)
+    # the first and last rows of the idle-SM share of the fwd+bwd and of the
+    # forward-only calls, besides a random sample
+    nf, _, _ = B.vpd_jsd_plan(s, t, None, torch.empty(n, v, dtype=dtype, device="cuda"), None)
+    nf_fwd, _, _ = B.vpd_jsd_plan(s, t)
+    rows = _sample(n, extra=[r for r in (nf - 1, nf, nf_fwd - 1, nf_fwd) if 0 <= r < n], count=12)
     check_pair(B, s, t, 0.5, rows=rows, gdtype=dtype, fused=True, label="sweep fused")
     check_pair(B, s, t, 0.5, rows=rows, fused=True, label="sweep fused fp32 grads")
     check_pair(B, s, t, 0.5, rows=rows, gdtype=dtype, label="sweep two-pass")
