@@ -458,6 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t accS = tmem + lane_addr + 256u * buf;  // buf stays 0 with one buffer
         const int64_t col0 = static_cast<int64_t>(nt) * TN;
+        bool released = false;  // this warp's accumulator columns handed back already
         for (int c = half * (TN / 2); c < (half + 1) * (TN / 2); c += 32) {
           float x[32];
           tmem_ld32(accS + c, x);
@@ -518,6 +519,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           float y[32];
           tmem_ld32(accS + TN + c, y);
+          if (!dbuf && c + 32 >= (half + 1) * (TN / 2)) {
+            // one buffer (s and t fill the tensor memory): once the last
+            // columns are in registers, the MMAs of the next tile may start
+            // while this chunk is computed
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mb_arrive(&bars.acc_empty[buf]);
+            released = true;
+          }
           if (a.mode == kDiv) {
             if (!live) continue;
             // two columns per packed instruction; columns past the vocabulary
@@ -651,9 +661,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mb_arrive(&bars.acc_empty[buf]);
+        if (!released) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mb_arrive(&bars.acc_empty[buf]);
+        }
         if (dbuf) buf ^= 1;
        }
       }
