@@ -26,11 +26,12 @@
 //           two pairs), split along K, accumulated into fp32 C by atomics.
 // Small kernels merge the per-chunk partials and transpose bf16 matrices.
 //
-// Warp roles of k_linear (320 threads): warp 0 issues the TMA loads into a
-// ring of shared-memory stages; warp 1 issues the MMAs (one elected lane) into
-// one of two tensor-memory accumulator buffers; warps 2-9 are the epilogue,
-// two per TMEM lane quarter: thread i owns TMEM lane (and tile row)
-// 32 (warp % 4) + lane and one half of each tile's columns.
+// Warp roles of k_linear (one instantiation per mode): warp 0 issues the TMA
+// loads into a ring of shared-memory stages; warp 1 issues the MMAs (one
+// elected lane) into one of two tensor-memory accumulator buffers; the other
+// warps are the epilogue, eight (320 threads) or, in kDiv, sixteen (576), that
+// is two or four per TMEM lane quarter: thread i owns TMEM lane (and tile
+// row) 32 (warp % 4) + lane and one half (one quarter) of each tile's columns.
 // Stages hand over through mbarriers (TMA completion -> MMA; tcgen05.commit ->
 // producer), and so do the accumulator buffers (commit -> epilogue; epilogue
 // arrivals -> MMA), so the epilogue of one tile overlaps the MMAs of the next
@@ -80,10 +81,7 @@ struct TileShape {
   // M >> 4 at bits 24-28
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((TN >> 3) << 17) | ((BM >> 4) << 24);
 };
-constexpr int kEpiWarps = 8;              // two per tensor-memory lane quarter, one per half of the columns
 constexpr int kTransWords = 32 * 33;          // per epilogue warp: 32 rows x 32 bf16 pairs (+1 word pad)
-constexpr int kSmemBytes = kRingBytes + kEpiWarps * kTransWords * 4 + 1024;  // + alignment slack
-constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kTmemCols = 512;
 constexpr float kTinyL = 1e-37f;
 constexpr float kLog2eL = 1.4426950408889634f;
@@ -91,6 +89,20 @@ constexpr float kLn2L = 0.6931471805599453f;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 enum Mode : int { kStats = 0, kDiv = 1, kGrad = 2, kGemm = 3 };
+
+// Epilogue warps per mode: kParts per tensor-memory lane quarter, each taking
+// 1 / kParts of a tile's columns. The divergence pass, whose epilogue does not
+// overlap the MMAs (its s and t tiles fill the tensor memory), runs sixteen
+// (at most 112 registers a thread); the others run eight.
+template <int MODE>
+struct EpiShape {
+  static constexpr int kWarps = MODE == kDiv ? 16 : 8;
+  static constexpr int kParts = kWarps / 4;
+  static constexpr int kThreads = 32 * (2 + kWarps);
+  // the stage ring, the per-warp transpose blocks of the gradient pass, and
+  // slack for the 1024-byte alignment
+  static constexpr int kSmem = kRingBytes + (MODE == kGrad ? kWarps * kTransWords * 4 : 0) + 1024;
+};
 
 static __device__ int g_linear_error = 0;
 
@@ -281,14 +293,15 @@ struct __align__(8) Bars {
   int abort;
 };
 
-template <int TN>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int TN, int MODE>
+__global__ void __launch_bounds__(EpiShape<MODE>::kThreads, 1)
     k_linear(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap b0,
              const __grid_constant__ CUtensorMap a1, const __grid_constant__ CUtensorMap b1, Args a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Bars bars;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using S = TileShape<TN>;
+  using E = EpiShape<MODE>;
   constexpr int kStages = S::kStages, kStageBytes = S::kStageBytes;
   uint32_t* trans = reinterpret_cast<uint32_t*>(smem + kRingBytes);  // kGrad transposes
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -301,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mb_init(&bars.acc_full[b], 1);
-      mb_init(&bars.acc_empty[b], kEpiWarps);
+      mb_init(&bars.acc_empty[b], E::kWarps);
     }
     bars.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -312,10 +325,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
-  const bool gemm = a.mode == kGemm;
-  const bool split = a.mode == kStats;  // the two heads' tiles one after the other
+  constexpr bool gemm = MODE == kGemm;
+  constexpr bool split = MODE == kStats;  // the two heads' tiles one after the other
   // two accumulator buffers in turn (else one buffer holds s and t of a tile)
-  const bool dbuf = gemm || split || TN < BN;
+  constexpr bool dbuf = gemm || split || TN < BN;
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -406,7 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------- epilogue (warps 2-9) ----------------
     const int q = warp & 3;                     // lane quarter of tensor memory
-    const int half = (warp - 2) >> 2;           // which 64 columns of each tile
+    const int part = (warp - 2) >> 2;           // which 1 / kParts of each tile's columns
+    constexpr int kPartCols = TN / E::kParts;
     const int rloc = 32 * q + lane;             // row within the tile
     const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
     int buf = 0;
@@ -423,14 +437,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       float nms = 0.f, nmt = 0.f, nKs = 0.f, nKt = 0.f;   // -m, -L log2 e
       float cs = 0.f, ct = 0.f, ks_ = 0.f, kt_ = 0.f;     // kGrad coefficients
       bool live = false;
-      if (!gemm && a.mode != kStats && rv) {
+      if (!gemm && MODE != kStats && rv) {
         const float* sv = a.saved + row * 6;
         nms = -sv[0];
         nKs = -sv[1] * kLog2eL;
         nmt = -sv[2];
         nKt = -sv[3] * kLog2eL;
         live = isfinite(sv[0]) && isfinite(sv[1]) && isfinite(sv[2]) && isfinite(sv[3]);
-        if (a.mode == kGrad) {
+        if (MODE == kGrad) {
           const float g = a.grad_loss ? a.grad_loss[row] : 1.f;
           const float A = sv[4], B = sv[5], value = a.loss[row];
           live = live && isfinite(value);
@@ -459,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t accS = tmem + lane_addr + 256u * buf;  // buf stays 0 with one buffer
         const int64_t col0 = static_cast<int64_t>(nt) * TN;
         bool released = false;  // this warp's accumulator columns handed back already
-        for (int c = half * (TN / 2); c < (half + 1) * (TN / 2); c += 32) {
+        for (int c = part * kPartCols; c < (part + 1) * kPartCols; c += 32) {
           float x[32];
           tmem_ld32(accS + c, x);
           if (gemm) {
@@ -519,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           float y[32];
           tmem_ld32(accS + TN + c, y);
-          if (!dbuf && c + 32 >= (half + 1) * (TN / 2)) {
+          if (!dbuf && c + 32 >= (part + 1) * kPartCols) {
             // one buffer (s and t fill the tensor memory): once the last
             // columns are in registers, the MMAs of the next tile may start
             // while this chunk is computed
@@ -528,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mb_arrive(&bars.acc_empty[buf]);
             released = true;
           }
-          if (a.mode == kDiv) {
+          if (MODE == kDiv) {
             if (!live) continue;
             // two columns per packed instruction; columns past the vocabulary
             // (logits 0 from the zero-filled head rows) get p = q = 0
@@ -670,12 +684,12 @@ __global__ void __launch_bounds__(kThreads, 1)
        }
       }
       if (!ok) break;
-      if (rv && a.mode == kStats) {
-        // one partial per (chunk, column half, row)
-        reinterpret_cast<float4*>(a.part)[(2 * static_cast<int64_t>(w.chunk) + half) * a.rows + row] =
+      if (rv && MODE == kStats) {
+        // one partial per (chunk, column part, row)
+        reinterpret_cast<float4*>(a.part)[(E::kParts * static_cast<int64_t>(w.chunk) + part) * a.rows + row] =
             make_float4(ms, zs, mt, zt);
-      } else if (rv && a.mode == kDiv) {
-        reinterpret_cast<float2*>(a.part)[(2 * static_cast<int64_t>(w.chunk) + half) * a.rows + row] =
+      } else if (rv && MODE == kDiv) {
+        reinterpret_cast<float2*>(a.part)[(E::kParts * static_cast<int64_t>(w.chunk) + part) * a.rows + row] =
             make_float2(accA, accB);
       }
     }
@@ -810,19 +824,22 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t k, 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// k_linear with TN-column tiles (the B maps' boxes must be TN rows high).
-template <int TN>
+// k_linear with TN-column tiles (the B maps' boxes must be TN rows high) in
+// mode MODE (args.mode must be MODE).
+template <int TN, int MODE>
 cudaError_t launch(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1, const CUtensorMap& b1,
                    const Args& args, cudaStream_t stream) {
+  using E = EpiShape<MODE>;
   if (args.units <= 0) return cudaSuccess;
+  if (args.mode != MODE) return cudaErrorInvalidValue;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(k_linear<TN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    attr_err = cudaFuncSetAttribute(k_linear<TN, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, E::kSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t grid = args.units < sm_count() ? args.units : sm_count();
-  k_linear<TN><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(a0, b0, a1, b1, args);
+  k_linear<TN, MODE><<<static_cast<unsigned>(grid), E::kThreads, E::kSmem, stream>>>(a0, b0, a1, b1, args);
   note_launch();
   return cudaGetLastError();
 }
@@ -876,9 +893,12 @@ int64_t gemm_ksplit(int64_t tiles, int64_t nk) {
 
 using namespace linear;
 
-// Partials of the forward: 16 bytes per row, vocabulary chunk and column half.
+// Partials of the forward, 32 bytes per row and vocabulary chunk: the
+// statistics pass writes (m_s, z_s, m_t, z_t) per column part (two parts), the
+// divergence pass, into the same bytes, (A, B) per column part (four parts).
+static_assert(EpiShape<kStats>::kParts * 16 == 32 && EpiShape<kDiv>::kParts * 8 == 32, "partial sizes");
 static size_t fwd_partial_bytes(int64_t rows, int64_t chunks) {
-  return static_cast<size_t>(2 * chunks) * static_cast<size_t>(rows) * 16u;
+  return static_cast<size_t>(chunks) * static_cast<size_t>(rows) * 32u;
 }
 
 size_t linear_fwd_workspace(int64_t rows, int64_t vocab) {
@@ -930,16 +950,17 @@ cudaError_t linear_jsd_forward(const LinearProblem& p, float* loss, float* saved
   a.part = static_cast<float*>(ws);
   a.saved = saved;
   a.mode = kStats;
-  if ((e = launch<BN>(hs, wsm, ht, wt, a, stream)) != cudaSuccess) return e;
+  if ((e = launch<BN, kStats>(hs, wsm, ht, wt, a, stream)) != cudaSuccess) return e;
   const unsigned mg = static_cast<unsigned>(cdiv(p.rows, 256));
-  k_linear_merge_stats<<<mg, 256, 0, stream>>>(reinterpret_cast<const float4*>(ws), static_cast<int>(2 * chunks), p.rows,
-                                               saved);
+  k_linear_merge_stats<<<mg, 256, 0, stream>>>(reinterpret_cast<const float4*>(ws),
+                                               static_cast<int>(EpiShape<kStats>::kParts * chunks), p.rows, saved);
   note_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   a.mode = kDiv;
-  if ((e = launch<BN>(hs, wsm, ht, wt, a, stream)) != cudaSuccess) return e;
-  k_linear_merge_div<<<mg, 256, 0, stream>>>(reinterpret_cast<const float2*>(ws), static_cast<int>(2 * chunks), p.rows,
-                                             a.jmode, a.beta, saved, loss);
+  if ((e = launch<BN, kDiv>(hs, wsm, ht, wt, a, stream)) != cudaSuccess) return e;
+  k_linear_merge_div<<<mg, 256, 0, stream>>>(reinterpret_cast<const float2*>(ws),
+                                             static_cast<int>(EpiShape<kDiv>::kParts * chunks), p.rows, a.jmode,
+                                             a.beta, saved, loss);
   note_launch();
   return cudaGetLastError();
 }
@@ -979,7 +1000,7 @@ cudaError_t gemm_acc(const void* a0p, const void* a1p, int64_t lda, const void* 
   a.ldc = ldc;
   // one k part per tile and nothing in C to add to: plain stores
   a.gemm_store = may_store && ks == 1 ? 1 : 0;
-  return launch<BN>(a0, b0, a1, b0, a, stream);
+  return launch<BN, kGemm>(a0, b0, a1, b0, a, stream);
 }
 
 cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, const float* loss,
@@ -1060,7 +1081,7 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
       a.gtt_hi = G[1][2];
       a.gtt_lo = G[1][3];
     }
-    if ((e = launch<kGradTN>(hsm, wsm, htm, wtm, a, stream)) != cudaSuccess) return e;
+    if ((e = launch<kGradTN, kGrad>(hsm, wsm, htm, wtm, a, stream)) != cudaSuccess) return e;
     for (int x = 0; x < 2; ++x) {
       if (!want[x]) continue;
       // dh[r0:r0+n] += G_hi W + G_lo W  (K = V; B = W^T [H, V])
