@@ -99,10 +99,14 @@ struct EpiShape {
   static constexpr int kWarps = MODE == kDiv ? 16 : 8;
   static constexpr int kParts = kWarps / 4;
   static constexpr int kThreads = 32 * (2 + kWarps);
-  // the stage ring, the per-warp transpose blocks of the gradient pass, and
-  // slack for the 1024-byte alignment
-  static constexpr int kSmem = kRingBytes + (MODE == kGrad ? kWarps * kTransWords * 4 : 0) + 1024;
 };
+// Dynamic shared memory: the stage ring, the per-warp transpose blocks of the
+// gradient pass, and slack for the 1024-byte alignment.
+template <int TN, int MODE>
+constexpr int smem_bytes() {
+  return TileShape<TN>::kStages * TileShape<TN>::kStageBytes +
+         (MODE == kGrad ? EpiShape<MODE>::kWarps * kTransWords * 4 : 0) + 1024;
+}
 
 static __device__ int g_linear_error = 0;
 
@@ -303,7 +307,7 @@ __global__ void __launch_bounds__(EpiShape<MODE>::kThreads, 1)
   using S = TileShape<TN>;
   using E = EpiShape<MODE>;
   constexpr int kStages = S::kStages, kStageBytes = S::kStageBytes;
-  uint32_t* trans = reinterpret_cast<uint32_t*>(smem + kRingBytes);  // kGrad transposes
+  uint32_t* trans = reinterpret_cast<uint32_t*>(smem + kStages * kStageBytes);  // kGrad transposes
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &bars.abort;
 
@@ -830,16 +834,18 @@ template <int TN, int MODE>
 cudaError_t launch(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1, const CUtensorMap& b1,
                    const Args& args, cudaStream_t stream) {
   using E = EpiShape<MODE>;
+  static_assert(smem_bytes<TN, MODE>() <= 232448, "dynamic shared memory above the 227 KB a CTA may take");
   if (args.units <= 0) return cudaSuccess;
   if (args.mode != MODE) return cudaErrorInvalidValue;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(k_linear<TN, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, E::kSmem);
+    attr_err =
+        cudaFuncSetAttribute(k_linear<TN, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<TN, MODE>());
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t grid = args.units < sm_count() ? args.units : sm_count();
-  k_linear<TN, MODE><<<static_cast<unsigned>(grid), E::kThreads, E::kSmem, stream>>>(a0, b0, a1, b1, args);
+  k_linear<TN, MODE><<<static_cast<unsigned>(grid), E::kThreads, smem_bytes<TN, MODE>(), stream>>>(a0, b0, a1, b1, args);
   note_launch();
   return cudaGetLastError();
 }
