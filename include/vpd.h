@@ -226,10 +226,8 @@ vpd_status vpd_jsd_plan(const vpd_view *s, const vpd_view *t, const vpd_segments
 /* ---------------------------------------------------------------------------
  * Forward / reverse KL ([ops page], "What"): reverse = 0 gives KL(P_t || P_s)
  * (the teacher is the target), reverse = 1 gives KL(P_s || P_t). The forward
- * reads the inputs once: one online pass (running maxima with rescaled sums),
- * or for short rows (V <= 32768) under the conditions of vpd_jsd_fwdbwd the
- * forward-only cluster kernel's KL branch (where, as in vpd_jsd_fwd, a bf16 row
- * whose largest finite logit exceeds 2^126 comes back NaN). saved may be NULL.
+ * reads the inputs once in one online pass (running maxima with rescaled
+ * sums) on every SM, one CTA per row at a time. saved may be NULL.
  * Saved layout and backward are those of the JSD beta = 0 / 1 branches.
  * ------------------------------------------------------------------------- */
 vpd_status vpd_kl_fwd(const vpd_view *s, const vpd_view *t, int32_t reverse,

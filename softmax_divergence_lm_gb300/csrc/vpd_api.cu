@@ -185,11 +185,10 @@ extern "C" {
 // which use every SM (JSD: 10.7 ms two-pass against 12.1 single-read for
 // 32768 rows). At V = 151936 the JSD forward takes 1.43 ms single-read against
 // 1.69 two-pass for 8191 rows. The KL forward has a one-read streaming kernel
-// of its own, as fast on long rows (V = 151936: 1.355 against 1.361 ms) and
-// slower on short ones (V = 16032: 0.18 against 0.149 single-read), hence
-// kKlFusedMaxVocab.
+// of its own, faster than the single-read kernel's KL branch on long rows
+// (V = 151936: 1.10 against 1.36 ms) and on short ones (V = 16032: 0.141
+// against 0.147 ms), so it takes that kernel at every width.
 constexpr int kForwardMaxCluster = 10;
-constexpr int64_t kKlFusedMaxVocab = 32768;
 
 vpd_status vpd_jsd_fwd(const vpd_view* s, const vpd_view* t, double beta, const vpd_segments* seg,
                        float* loss, float* saved, void* stream) {
@@ -384,15 +383,6 @@ vpd_status vpd_kl_fwd(const vpd_view* s, const vpd_view* t, int32_t reverse,
   VPD_TRY(check_segments(seg, vs.vocab, &sg));
   if (vs.rows == 0) return ok();
   if (!loss) return fail(VPD_ERR_ARG, "vpd_kl_fwd: loss is required");
-  // Short rows: the KL branch of the single-read kernel (beta = 0 / 1); longer
-  // rows: the online single-pass kernel on every SM, which is faster there.
-  if (sg.count == 1 && vs.vocab <= kKlFusedMaxVocab) {
-    const vpd::Grad none{nullptr, 0, 0};
-    cudaError_t e = vpd::launch_jsd_fused(vs, vt, reverse ? 1.0 : 0.0, nullptr, loss, saved, none, none,
-                                          static_cast<cudaStream_t>(stream), -1, kForwardMaxCluster);
-    if (e == cudaSuccess) return ok();
-    if (e != cudaErrorNotSupported) return cuda_fail(e, "fused single-read kernel");
-  }
   VPD_CUDA(vpd::launch_kl_fwd(vs, vt, reverse ? 1 : 0, sg, loss, saved,
                               static_cast<cudaStream_t>(stream)),
            "single-pass KL kernel");
