@@ -139,7 +139,7 @@ bool choose(int64_t vocab, int64_t rows, int max_cluster, bool fwd, Config* cfg)
 // Rate of the streaming path on one otherwise idle SM relative to one SM of a
 // fused cluster, in rows per second per SM: for forward+backward (three
 // streaming passes against one read) 0.5 with clusters of up to 15 CTAs and
-// 0.55 with 16 (a cluster of 16 spends more of each row on its exchanges), for
+// 0.57 with 16 (a cluster of 16 spends more of each row on its exchanges), for
 // the forward (two passes) 0.9; measured at V = 151936 (clusters of 9) and
 // V = 262144 (clusters of 16). VPD_IDLE_RATE / VPD_IDLE_RATE_FWD override them
 // (0 disables the split).
@@ -154,7 +154,7 @@ static double idle_rate(bool fwd, int cluster) {
                               }()};
   if (fwd) return r[1];
   if (r[0] >= 0.0) return r[0];
-  return cluster >= 16 ? 0.55 : 0.5;
+  return cluster >= 16 ? 0.57 : 0.5;
 }
 
 void fused_idle_split(const View& s, const Grad& ds, const Grad& dt, int max_cluster, int64_t* side_rows,
