@@ -15,7 +15,8 @@
 //
 // One persistent kernel, k_linear, in four epilogue modes:
 //   kStats  logits tiles of both heads -> online (max, sum-exp) per row over
-//           the unit's vocabulary tiles -> partials per (vocabulary chunk, row);
+//           the unit's vocabulary tiles -> partials per (vocabulary chunk,
+//           column part, row);
 //   kDiv    logits tiles again -> the two KL-to-mixture partial sums with the
 //           merged statistics (the second of the two passes JSD needs);
 //   kGrad   logits tiles again -> dS and dT of a chunk of rows, each split into
@@ -36,7 +37,9 @@
 // producer), and so do the accumulator buffers (commit -> epilogue; epilogue
 // arrivals -> MMA), so the epilogue of one tile overlaps the MMAs of the next
 // wherever two tiles fit in tensor memory (all passes but kDiv, whose s and t
-// tiles of 256 columns fill it; kGrad takes 128-column tiles for that reason).
+// tiles of 256 columns fill it, and whose epilogue warps hand the accumulator
+// back once their last columns are in registers; kGrad takes 128-column tiles
+// so that two fit).
 // Every mbarrier wait gives up after two seconds, sets the device error word
 // and leaves the loops; the CTA waits for copies and MMAs in flight before it
 // frees its tensor memory.
@@ -60,7 +63,7 @@ constexpr int BM = 128;                     // tile rows (tensor-memory lanes)
 constexpr int BN = 256;                     // widest tile: one 128 x 256 MMA per 16 of k
 constexpr int BK = 64;                      // k per stage: one 128-byte swizzle row of bf16
 constexpr int kTileBytes = BM * BK * 2;     // 16 KB: the A tile of a stage
-constexpr int kRingBytes = 4 * (kTileBytes + BN * BK * 2);  // shared-memory stages: 4 of 48 KB or 6 of 32 KB
+constexpr int kRingBytes = 4 * (kTileBytes + BN * BK * 2);  // stage ring: 4 of 48 KB (256 columns) or 6 of 32 KB (128)
 constexpr int kMaxStages = 6;
 // Tile columns of the gradient pass: it needs both heads' logits at once, and
 // two 128-column tiles of s and t fill the tensor memory, so its long epilogue
@@ -68,7 +71,7 @@ constexpr int kMaxStages = 6;
 // statistics pass (one head's tile at a time, in two buffers), the GEMMs
 // (two buffers), and the divergence pass, whose short epilogue costs less
 // than the narrower MMAs would (s and t of one 256-column tile fill the
-// tensor memory, so that epilogue does not overlap).
+// tensor memory, so that epilogue overlaps only its last columns).
 constexpr int kGradTN = 128;
 template <int TN>
 struct TileShape {
@@ -91,9 +94,10 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 enum Mode : int { kStats = 0, kDiv = 1, kGrad = 2, kGemm = 3 };
 
 // Epilogue warps per mode: kParts per tensor-memory lane quarter, each taking
-// 1 / kParts of a tile's columns. The divergence pass, whose epilogue does not
-// overlap the MMAs (its s and t tiles fill the tensor memory), runs sixteen
-// (at most 112 registers a thread); the others run eight.
+// 1 / kParts of a tile's columns. The divergence pass, whose epilogue overlaps
+// the next tile's MMAs only at its end (its s and t tiles fill the tensor
+// memory), runs sixteen (at most 96 registers a thread: five warps per SM
+// sub-partition); the others run eight.
 template <int MODE>
 struct EpiShape {
   static constexpr int kWarps = MODE == kDiv ? 16 : 8;
