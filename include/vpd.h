@@ -135,7 +135,7 @@ typedef struct {
 
 /* Forward. The statistics must be global before the divergence ([JSD page],
  * "Scope and limitations"): under the single-read conditions of vpd_jsd_fwdbwd
- * (one segment, 16-bit inputs, aligned rows), a forward-only cluster kernel
+ * (aligned rows, V a multiple of 8), a forward-only cluster kernel
  * reads each row pair once and keeps it on chip for both steps, when the row
  * fits in clusters of at most 10 CTAs (V <= 191040 with 227 KB of shared memory
  * per CTA), or of at most 16 when the call has enough rows for the SMs those
@@ -144,9 +144,12 @@ typedef struct {
  * paired-statistics kernel merges per-segment (max,
  * sum-exp) of both inputs, then a divergence kernel reduces the two
  * KL-to-mixture expectations together ([JSD page], "Changes").
- * On the single-read path a bf16 row whose largest finite logit exceeds 2^126
- * is out of contract and comes back NaN (the streaming path and the oracle give
- * a finite value there); the limit keeps every clamped log-difference finite.
+ * On the single-read path a row whose largest finite logit exceeds 2^126 is
+ * out of contract and comes back NaN (the streaming path and the oracle give a
+ * finite value there); the limit keeps every clamped log-difference finite.
+ * Segments: the single-read kernel merges its CTA slices with the same MAX /
+ * SUM merge the segments define, so a segmented call takes it too (results
+ * equal up to the order of the additions).
  * loss:  device float[N], the per-token divergence.
  * saved: device float[N, 6] (see above), required: it carries the statistics
  *        to the backward (and between the two streaming kernels). */
@@ -169,13 +172,14 @@ vpd_status vpd_jsd_bwd(const vpd_view *s, const vpd_view *t, double beta, const 
                        const vpd_grad *dt, void *stream);
 
 /* Forward and backward in one call, with the upstream gradient given up front.
- * The single-read path runs when the inputs are bf16 or fp16, V is a multiple
- * of 8, every row of the inputs and gradients starts on a 16-byte boundary,
- * the gradients are float32 or the input dtype, there is one segment, and the
- * row fits on a thread-block cluster (V <= 311296). There a cluster of up to
- * 16 CTAs holds each row pair on chip and statistics, divergence and
- * gradients come from one HBM read; a bf16 row whose finite max exceeds 2^126
- * is treated as out of contract (NaN, zero gradient). The clusters cannot
+ * The single-read path runs when V is a multiple of 8, every row of the
+ * inputs and gradients starts on a 16-byte boundary, the gradients are
+ * float32 or the input dtype, and the row fits on a thread-block cluster
+ * (V <= 311296 for bf16 / fp16, V <= 229248 for fp32, whose gradients are
+ * stored from registers); any segment table (see vpd_jsd_fwd). There a
+ * cluster of up to 16 CTAs holds each row pair on chip and statistics,
+ * divergence and gradients come from one HBM read; a row whose finite max
+ * exceeds 2^126 is treated as out of contract (NaN, zero gradient). The clusters cannot
  * always cover every SM (at V = 151936, 15 clusters of 9 CTAs use 135 of 152);
  * when the call has many rows per cluster, its last rows (from any row of
  * the view, mid-batch included) go to the streaming kernels on the SMs left

@@ -202,7 +202,10 @@ vpd_status vpd_jsd_fwd(const vpd_view* s, const vpd_view* t, double beta, const 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // One read of the inputs by the single-read forward kernel when it fits in
   // clusters that cover most SMs; else the two streaming passes on every SM.
-  if (sg.count == 1) {
+  // Vocabulary segments change only the grouping of the statistics merge
+  // (the kernel merges its CTA slices with the same MAX / SUM merge), so a
+  // segmented call takes the single-read kernel too.
+  {
     const vpd::Grad none{nullptr, 0, 0};
     // as in vpd_jsd_fwdbwd: the last rows go to the SMs the clusters leave
     // idle; with them the forward kernel may take clusters of up to 16 CTAs
@@ -280,10 +283,10 @@ vpd_status vpd_jsd_fwdbwd(const vpd_view* s, const vpd_view* t, double beta,
   if (vs.rows == 0) return ok();
   if (!loss || !saved) return fail(VPD_ERR_ARG, "vpd_jsd_fwdbwd: loss and saved are required");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // The single-read kernel merges statistics over its CTA slices; a call with
-  // several vocabulary segments takes the streaming kernels, which merge them
-  // segment by segment.
-  if (sg.count == 1) {
+  // The single-read kernel merges statistics over its CTA slices with the
+  // same MAX / SUM merge the segments define, so a segmented call takes it
+  // too (the side rows' streaming kernels merge segment by segment).
+  {
     // The clusters of the single-read kernel leave some SMs idle (at V =
     // 151936, 15 clusters of 9 CTAs use 135 of 152 SMs). The last rows of the
     // call go to the streaming kernels on a side stream, capped to as many
@@ -354,13 +357,12 @@ vpd_status vpd_jsd_plan(const vpd_view* s, const vpd_view* t, const vpd_segments
   int32_t n = 0;
   if (vs.rows > 0) {
     int idle = 0;
-    if (sg.count == 1) vpd::fused_idle_split(vs, gs, gt, 16, &side, &idle);
+    vpd::fused_idle_split(vs, gs, gt, 16, &side, &idle);
     if (side > 0) max_cluster = 16;
     vpd::View fs = vs, ft = vt;
     fs.rows = ft.rows = vs.rows - side;
-    const cudaError_t e = sg.count == 1 ? vpd::launch_jsd_fused(fs, ft, 0.5, nullptr, nullptr, nullptr, gs, gt,
-                                                                nullptr, -1, max_cluster, true)
-                                        : cudaErrorNotSupported;
+    const cudaError_t e =
+        vpd::launch_jsd_fused(fs, ft, 0.5, nullptr, nullptr, nullptr, gs, gt, nullptr, -1, max_cluster, true);
     if (e == cudaSuccess) {
       fr = fs.rows;
       n = 1 + (side > 0 ? (fwd ? 2 : 3) : 0);

@@ -15,22 +15,26 @@
 
 namespace vpd {
 namespace fused {
-// Instantiated in vpd_fused_bf16.cu and vpd_fused_f16.cu.
+// Instantiated in vpd_fused_bf16.cu, vpd_fused_f16.cu and vpd_fused_f32.cu.
 extern template cudaError_t launch_typed<InBF16>(const FusedArgs&, const Config&, int, bool, bool, cudaStream_t, int*);
 extern template cudaError_t launch_typed<InF16>(const FusedArgs&, const Config&, int, bool, bool, cudaStream_t, int*);
+extern template cudaError_t launch_typed<InF32>(const FusedArgs&, const Config&, int, bool, bool, cudaStream_t, int*);
 extern template int resident_clusters<InBF16>(int, int, size_t);
 cudaError_t take_error_bf16(cudaStream_t stream, int* code);
 cudaError_t take_error_f16(cudaStream_t stream, int* code);
+cudaError_t take_error_f32(cudaStream_t stream, int* code);
 }  // namespace fused
 
 cudaError_t take_device_error(cudaStream_t stream, int* code) {
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return e;
-  int a = 0, b = 0;
+  int a = 0, b = 0, c = 0;
   e = fused::take_error_bf16(stream, &a);
   if (e != cudaSuccess) return e;
   e = fused::take_error_f16(stream, &b);
-  *code = a | b;
+  if (e != cudaSuccess) return e;
+  e = fused::take_error_f32(stream, &c);
+  *code = a | b | c;
   return e;
 }
 
@@ -102,14 +106,16 @@ int64_t sched_vectors(int64_t nvec, int R, int nw) {
 // thread within the register and TMEM budgets); then the smallest R that
 // covers the slice and as many workers as the budgets allow without idle
 // warps (more warps hide more latency). Ties go to the smaller cluster.
-// `fwd`: the forward-only kernel (three stages, no tensor memory).
-bool choose(int64_t vocab, int64_t rows, int max_cluster, bool fwd, Config* cfg) {
+// `fwd`: the forward-only kernel (three stages, no tensor memory); `esize`:
+// bytes per input element (2, or 4 for fp32 logits).
+bool choose(int64_t vocab, int64_t rows, int max_cluster, bool fwd, Config* cfg, int esize) {
   const size_t smem_cap = max_smem_optin();
   int64_t best = 0;
   for (int C = 1; C <= fused::kMaxCluster && C <= max_cluster; ++C) {
     const int64_t W = ((vocab + C - 1) / C + 7) / 8 * 8;
     const int64_t nvec = W / 8;
-    const size_t smem = fwd ? fused::smem_bytes_fwd(static_cast<int>(W)) : fused::smem_bytes(static_cast<int>(W));
+    const size_t smem = fwd ? fused::smem_bytes_fwd(static_cast<int>(W), esize)
+                            : fused::smem_bytes(static_cast<int>(W), false, esize);
     if (smem > smem_cap) continue;
     int bR = 0, bnw = 0;
     for (int R = 1; R <= fused::kMaxR && !bR; ++R) {
@@ -164,13 +170,13 @@ void fused_idle_split(const View& s, const Grad& ds, const Grad& dt, int max_clu
   const bool fwd = !ds.data && !dt.data;
   // long rows only: their streaming CTAs are wide enough (at least three warps
   // of 40 or more registers) that none fits beside a fused CTA on its SM
-  if (s.dtype == kF32 || s.vocab < 100000) return;
+  if (s.vocab < 100000) return;
   if (!fwd) {
     const int gdtype = ds.data ? ds.dtype : dt.dtype;
     if (gdtype != kF32 && gdtype != s.dtype) return;
   }
   Config cfg;
-  if (!choose(s.vocab, s.rows, max_cluster, fwd, &cfg)) return;
+  if (!choose(s.vocab, s.rows, max_cluster, fwd, &cfg, s.dtype == kF32 ? 4 : 2)) return;
   const double rate = idle_rate(fwd, cfg.C);
   if (rate <= 0.0) return;
   const int clusters = clusters_for(cfg.C);
@@ -187,12 +193,13 @@ void fused_idle_split(const View& s, const Grad& ds, const Grad& dt, int max_clu
 cudaError_t launch_jsd_fused(const View& s, const View& t, double beta, const float* grad_loss,
                              float* loss, float* saved, const Grad& ds, const Grad& dt,
                              cudaStream_t stream, int64_t withhold_row, int max_cluster, bool dry_run) {
-  // 16-bit inputs only; every row of both inputs and of both gradients must
-  // start on a 16-byte boundary, and V must fill whole 16-byte vectors.
-  if (s.dtype == kF32 || s.vocab <= 0 || s.vocab % 8 != 0) return cudaErrorNotSupported;
+  // Every row of both inputs and of both gradients must start on a 16-byte
+  // boundary, and V must fill whole 8-element vectors.
+  const int es = s.dtype == kF32 ? 4 : 2;
+  if (s.vocab <= 0 || s.vocab % 8 != 0) return cudaErrorNotSupported;
   if (!aligned16(s.data) || !aligned16(t.data)) return cudaErrorNotSupported;
   for (const RowMap* m : {&s.map, &t.map})
-    if ((m->row_stride * 2) % 16 || (m->rows_per_batch > 0 && (m->batch_stride * 2) % 16))
+    if ((m->row_stride * es) % 16 || (m->rows_per_batch > 0 && (m->batch_stride * es) % 16))
       return cudaErrorNotSupported;
   const Grad* gs[2] = {&ds, &dt};
   int gdtype = -1;
@@ -205,21 +212,21 @@ cudaError_t launch_jsd_fused(const View& s, const View& t, double beta, const fl
   }
   const bool fwd = gdtype < 0;  // no gradient wanted: the forward-only kernel
   Config cfg;
-  if (!choose(s.vocab, s.rows, max_cluster, fwd, &cfg)) return cudaErrorNotSupported;
+  if (!choose(s.vocab, s.rows, max_cluster, fwd, &cfg, es)) return cudaErrorNotSupported;
   const int mode = beta == 0.0 ? fused::kForwardKL : beta == 1.0 ? fused::kReverseKL : fused::kInterior;
   const bool f32g = gdtype == kF32;
   // 16-bit gradients go out through a shared-memory buffer and bulk stores
   // when it fits beside the stages.
   if (dry_run) return cudaSuccess;
-  const bool gstage = gdtype >= 0 && !f32g && fused::smem_bytes(cfg.W, true) <= max_smem_optin();
-  if (gstage) cfg.smem = fused::smem_bytes(cfg.W, true);
+  const bool gstage = gdtype >= 0 && !f32g && fused::smem_bytes(cfg.W, true, es) <= max_smem_optin();
+  if (gstage) cfg.smem = fused::smem_bytes(cfg.W, true, es);
   fused::FusedArgs args{s.data, t.data, s.map, t.map, s.rows, s.vocab, cfg.W, cfg.nw, gstage ? 1 : 0,
                         static_cast<float>(beta),
                         grad_loss, loss, saved, ds, dt, withhold_row};
   int clusters = 0;
-  const cudaError_t e = s.dtype == kBF16
-                            ? fused::launch_typed<fused::InBF16>(args, cfg, mode, f32g, fwd, stream, &clusters)
-                            : fused::launch_typed<fused::InF16>(args, cfg, mode, f32g, fwd, stream, &clusters);
+  const cudaError_t e = s.dtype == kBF16  ? fused::launch_typed<fused::InBF16>(args, cfg, mode, f32g, fwd, stream, &clusters)
+                        : s.dtype == kF16 ? fused::launch_typed<fused::InF16>(args, cfg, mode, f32g, fwd, stream, &clusters)
+                                          : fused::launch_typed<fused::InF32>(args, cfg, mode, f32g, fwd, stream, &clusters);
   if (e == cudaSuccess) {
     note_launch();
     if (verbose())

@@ -56,6 +56,7 @@ namespace fused {
 
 using vpd::InBF16;
 using vpd::InF16;
+using vpd::InF32;
 
 constexpr int kStages = 2;                  // shared-memory stages per CTA (forward + backward)
 constexpr int kFwdStages = 3;               // stages of the forward-only kernel
@@ -495,21 +496,27 @@ __host__ __device__ __forceinline__ int vector_order(int warp, int nw, int R) {
 template <class In, int R, bool KEEP = false>
 __device__ __forceinline__ void worker_stats(const unsigned char* sb, int W, const Span& sp, int Tw, int vt,
                                              float* part) {
+  using Word = typename In::Word;
+  using Vec = typename In::Vec;
+  constexpr int kVB = 8 * In::kSize;  // bytes of one 8-element vector
   const int lane = threadIdx.x & 31;
-  const unsigned char* ps = sb + vt * 16;
-  const size_t tofs = static_cast<size_t>(W) * 2;
-  uint32_t mxs = In::kNegInf2, mxt = In::kNegInf2;
-  uint4 ku[R], kv[R];
+  const unsigned char* ps = sb + vt * kVB;
+  const size_t tofs = static_cast<size_t>(W) * In::kSize;
+  Word mxs = In::neg_inf_w(), mxt = In::neg_inf_w();
+  Vec ku[R], kv[R];
 #pragma unroll
   for (int k = 0; k < R; ++k) {
     if (k < sp.kv) {
-      const uint4 u = lds16(ps + k * Tw * 16), v = lds16(ps + tofs + k * Tw * 16);
+      const Vec u = In::ld(ps + k * Tw * kVB), v = In::ld(ps + tofs + k * Tw * kVB);
       if (KEEP) {
         ku[k] = u;
         kv[k] = v;
       }
-      mxs = In::max_nan(mxs, In::max_nan(In::max_nan(u.x, u.y), In::max_nan(u.z, u.w)));
-      mxt = In::max_nan(mxt, In::max_nan(In::max_nan(v.x, v.y), In::max_nan(v.z, v.w)));
+      Word uw[4], vw[4];
+      In::words(u, uw);
+      In::words(v, vw);
+      mxs = In::max_nan(mxs, In::max_nan(In::max_nan(uw[0], uw[1]), In::max_nan(uw[2], uw[3])));
+      mxt = In::max_nan(mxt, In::max_nan(In::max_nan(vw[0], vw[1]), In::max_nan(vw[2], vw[3])));
     }
   }
   const float2 a = In::unpack(mxs), b = In::unpack(mxt);
@@ -519,8 +526,10 @@ __device__ __forceinline__ void worker_stats(const unsigned char* sb, int W, con
 #pragma unroll
   for (int k = 0; k < R; ++k) {
     if (k < sp.kv) {
-      const uint4 u = KEEP ? ku[k] : lds16(ps + k * Tw * 16), v = KEEP ? kv[k] : lds16(ps + tofs + k * Tw * 16);
-      const uint32_t us[4] = {u.x, u.y, u.z, u.w}, vs[4] = {v.x, v.y, v.z, v.w};
+      const Vec u = KEEP ? ku[k] : In::ld(ps + k * Tw * kVB), v = KEEP ? kv[k] : In::ld(ps + tofs + k * Tw * kVB);
+      Word us[4], vs[4];
+      In::words(u, us);
+      In::words(v, vs);
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         // x - m is exact; a -inf entry gives 2^-inf = 0, a NaN gives NaN
@@ -555,7 +564,7 @@ struct FusedArgs {
 
 // log2 of the probabilities of one packed pair: (x - m) log2 e - K.
 template <class In>
-__device__ __forceinline__ float2 lam(uint32_t w, float2 nm, float2 l2e2, float2 nK) {
+__device__ __forceinline__ float2 lam(typename In::Word w, float2 nm, float2 l2e2, float2 nK) {
   return fma2(In::sub(w, nm), l2e2, nK);
 }
 
@@ -568,10 +577,13 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
   const int W = a.W, nw = NW > 0 ? NW : a.nw, Tw = 32 * nw, nthreads = Tw + 32;
   // Shared memory: kStages x [s, t] slices, then (staged gradients) the dS and
   // dT slices of one row, then the tail.
-  unsigned char* gbuf = smem + static_cast<size_t>(kStages) * 4 * W;
+  constexpr int kVB = 8 * In::kSize;  // bytes of one 8-element input vector
+  using Word = typename In::Word;
+  using Vec = typename In::Vec;
+  unsigned char* gbuf = smem + static_cast<size_t>(kStages) * 2 * In::kSize * W;
   const bool staged = a.gstage != 0 && (a.ds.data || a.dt.data);
   Tail* tail = reinterpret_cast<Tail*>(gbuf + (a.gstage ? static_cast<size_t>(4) * W : 0));
-  auto stage_ptr = [&](int st) { return smem + static_cast<size_t>(st) * 4 * W; };
+  auto stage_ptr = [&](int st) { return smem + static_cast<size_t>(st) * 2 * In::kSize * W; };
 
   const uint32_t crank = cluster_rank(), csize = cluster_size();
   const int64_t q = cluster_index(), Q = cluster_count();
@@ -580,7 +592,8 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
   const int64_t col0 = static_cast<int64_t>(crank) * W;
   const int64_t rest = a.vocab - col0;
   const int len = rest <= 0 ? 0 : (rest < W ? static_cast<int>(rest) : W);
-  const uint32_t bytes = static_cast<uint32_t>(len) * 2u;
+  const uint32_t bytes = static_cast<uint32_t>(len) * In::kSize;  // of each input's slice
+  const uint32_t gbytes = static_cast<uint32_t>(len) * 2u;        // of each staged 16-bit gradient slice
 
   // The failure-path test hook: this CTA withholds the copy of one row, so
   // its workers' bounded wait on that stage expires.
@@ -592,18 +605,20 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
     if (lane == 0) {
       unsigned char* dst = stage_ptr(st);
       mbar_expect_tx(&tail->tma_bar[st], 2 * bytes);
-      bulk_load(dst, a.s + (a.ms.offset(r) + col0) * 2, bytes, &tail->tma_bar[st]);
-      bulk_load(dst + static_cast<size_t>(W) * 2, a.t + (a.mt.offset(r) + col0) * 2, bytes, &tail->tma_bar[st]);
+      bulk_load(dst, a.s + (a.ms.offset(r) + col0) * In::kSize, bytes, &tail->tma_bar[st]);
+      bulk_load(dst + static_cast<size_t>(W) * In::kSize, a.t + (a.mt.offset(r) + col0) * In::kSize, bytes,
+                &tail->tma_bar[st]);
     }
     issued_any |= 1u << st;
     issued_odd ^= 1u << st;
   };
 
-  // Control warp: bulk stores of the staged gradients of row r.
+  // Control warp: bulk stores of the staged (16-bit) gradients of row r.
   auto store_grads = [&](int64_t r) {
-    if (lane == 0 && bytes) {
-      if (a.ds.data) bulk_store(a.ds.data + (r * a.ds.row_stride + col0) * 2, gbuf, bytes);
-      if (a.dt.data) bulk_store(a.dt.data + (r * a.dt.row_stride + col0) * 2, gbuf + static_cast<size_t>(W) * 2, bytes);
+    if (lane == 0 && gbytes) {
+      if (a.ds.data) bulk_store(a.ds.data + (r * a.ds.row_stride + col0) * 2, gbuf, gbytes);
+      if (a.dt.data)
+        bulk_store(a.dt.data + (r * a.dt.row_stride + col0) * 2, gbuf + static_cast<size_t>(W) * 2, gbytes);
       bulk_commit();
     }
   };
@@ -790,30 +805,32 @@ __global__ void __launch_bounds__(32 * (max_workers(R) + 1), 1) k_jsd_fused(Fuse
       float2 acc_a = f2(0.f), acc_b = f2(0.f);
       uint32_t viol = 0;
       if (row_ok) {
-        const unsigned char* ps = stage_ptr(cst) + vt * 16;
-        const size_t tofs = static_cast<size_t>(W) * 2;
+        const unsigned char* ps = stage_ptr(cst) + vt * kVB;
+        const size_t tofs = static_cast<size_t>(W) * In::kSize;
         // One vector: PARTIAL marks the warp that straddles the slice end,
         // whose lanes past it compute on the floor value.
         auto vec_c = [&](int k, auto partial) {
           constexpr bool PARTIAL = decltype(partial)::value;
-          uint4 u, v;
+          Vec u, v;
           if (!PARTIAL || k < sp.kv) {
-            u = lds16(ps + k * Tw * 16);
-            v = lds16(ps + tofs + k * Tw * 16);
+            u = In::ld(ps + k * Tw * kVB);
+            v = In::ld(ps + tofs + k * Tw * kVB);
           } else {
-            u = v = make_uint4(In::kNegBig2, In::kNegBig2, In::kNegBig2, In::kNegBig2);
+            u = v = In::fill_neg_big();
           }
-          const uint32_t us[4] = {u.x, u.y, u.z, u.w}, vs[4] = {v.x, v.y, v.z, v.w};
+          Word us[4], vs[4];
+          In::words(u, us);
+          In::words(v, vs);
           float2 t0[4], t1[4], t2[4];
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
             if (MODE != kInterior) {
-              const uint32_t tgt = MODE == kForwardKL ? vs[w] : us[w];
-              const uint32_t oth = MODE == kForwardKL ? us[w] : vs[w];
-              viol |= __vcmpeq2(oth, In::kNegInf2) & ~__vcmpeq2(tgt, In::kNegInf2);
+              const Word tgt = MODE == kForwardKL ? vs[w] : us[w];
+              const Word oth = MODE == kForwardKL ? us[w] : vs[w];
+              viol |= In::viol(tgt, oth);
             }
-            const float2 lp = lam<In>(In::max2(us[w], In::kNegBig2), nms2, l2e2, nKs2);
-            const float2 lq = lam<In>(In::max2(vs[w], In::kNegBig2), nmt2, l2e2, nKt2);
+            const float2 lp = lam<In>(In::max2(us[w], In::neg_big_w()), nms2, l2e2, nKs2);
+            const float2 lq = lam<In>(In::max2(vs[w], In::neg_big_w()), nmt2, l2e2, nKt2);
             const float2 p = ex2_2(lp), qv = ex2_2(lq);
             kq[k][w] = qv;
             t0[w] = p;
@@ -981,8 +998,10 @@ template <class In, int R, int MODE, int NW = 0>  // NW: as for k_jsd_fused
 __global__ void __launch_bounds__(32 * (kMaxWorkersFwd + 1), 1) k_jsd_fused_fwd(FusedArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int W = a.W, nw = NW > 0 ? NW : a.nw, Tw = 32 * nw, nthreads = Tw + 32;
-  Tail* tail = reinterpret_cast<Tail*>(smem + static_cast<size_t>(kFwdStages) * 4 * W);
-  auto stage_ptr = [&](int st) { return smem + static_cast<size_t>(st) * 4 * W; };
+  constexpr int kVB = 8 * In::kSize;  // bytes of one 8-element input vector
+  using Word = typename In::Word;
+  Tail* tail = reinterpret_cast<Tail*>(smem + static_cast<size_t>(kFwdStages) * 2 * In::kSize * W);
+  auto stage_ptr = [&](int st) { return smem + static_cast<size_t>(st) * 2 * In::kSize * W; };
 
   const uint32_t crank = cluster_rank(), csize = cluster_size();
   const int64_t q = cluster_index(), Q = cluster_count();
@@ -991,7 +1010,7 @@ __global__ void __launch_bounds__(32 * (kMaxWorkersFwd + 1), 1) k_jsd_fused_fwd(
   const int64_t col0 = static_cast<int64_t>(crank) * W;
   const int64_t rest = a.vocab - col0;
   const int len = rest <= 0 ? 0 : (rest < W ? static_cast<int>(rest) : W);
-  const uint32_t bytes = static_cast<uint32_t>(len) * 2u;
+  const uint32_t bytes = static_cast<uint32_t>(len) * In::kSize;
   // statistics partials of row i hand over on a named barrier of its parity:
   // the workers may arrive for row i + 1 before the control warp took row i
   auto stat_part_bar = [](int64_t i) { return (i & 1) ? kBarStatPartOdd : kBarStatPart; };
@@ -1004,8 +1023,9 @@ __global__ void __launch_bounds__(32 * (kMaxWorkersFwd + 1), 1) k_jsd_fused_fwd(
     if (lane == 0) {
       unsigned char* dst = stage_ptr(st);
       mbar_expect_tx(&tail->tma_bar[st], 2 * bytes);
-      bulk_load(dst, a.s + (a.ms.offset(r) + col0) * 2, bytes, &tail->tma_bar[st]);
-      bulk_load(dst + static_cast<size_t>(W) * 2, a.t + (a.mt.offset(r) + col0) * 2, bytes, &tail->tma_bar[st]);
+      bulk_load(dst, a.s + (a.ms.offset(r) + col0) * In::kSize, bytes, &tail->tma_bar[st]);
+      bulk_load(dst + static_cast<size_t>(W) * In::kSize, a.t + (a.mt.offset(r) + col0) * In::kSize, bytes,
+                &tail->tma_bar[st]);
     }
     issued_any |= 1u << st;
     issued_odd ^= 1u << st;
@@ -1160,7 +1180,9 @@ __global__ void __launch_bounds__(32 * (kMaxWorkersFwd + 1), 1) k_jsd_fused_fwd(
         if (!mbar_wait(&tail->tma_bar[st], (tma_parity >> st) & 1u)) tail->fail = 1;
         tma_parity ^= 1u << st;
       }
-      worker_stats<In, R, true>(stage_ptr(st), W, sp, Tw, vt, tail->stat_part[i & 1][warp]);
+      // the vectors stay in registers between the two sweeps for 16-bit
+      // inputs (fp32 vectors are twice the registers)
+      worker_stats<In, R, In::kSize == 2>(stage_ptr(st), W, sp, Tw, vt, tail->stat_part[i & 1][warp]);
       bar_arrive(stat_part_bar(i), nthreads);
     };
     if (q < a.rows) stats_of(0);
@@ -1182,22 +1204,23 @@ __global__ void __launch_bounds__(32 * (kMaxWorkersFwd + 1), 1) k_jsd_fused_fwd(
       float2 acc_a = f2(0.f), acc_b = f2(0.f);
       uint32_t viol = 0;
       if (flags.x != 0.f) {
-        const unsigned char* ps = stage_ptr(static_cast<int>(i % kFwdStages)) + vt * 16;
-        const size_t tofs = static_cast<size_t>(W) * 2;
+        const unsigned char* ps = stage_ptr(static_cast<int>(i % kFwdStages)) + vt * kVB;
+        const size_t tofs = static_cast<size_t>(W) * In::kSize;
 #pragma unroll
         for (int k = 0; k < R; ++k) {
           if (k < sp.kv) {
-            const uint4 u = lds16(ps + k * Tw * 16), v = lds16(ps + tofs + k * Tw * 16);
-            const uint32_t us[4] = {u.x, u.y, u.z, u.w}, vs[4] = {v.x, v.y, v.z, v.w};
+            Word us[4], vs[4];
+            In::words(In::ld(ps + k * Tw * kVB), us);
+            In::words(In::ld(ps + tofs + k * Tw * kVB), vs);
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
               if (MODE != kInterior) {
-                const uint32_t tgt = MODE == kForwardKL ? vs[w] : us[w];
-                const uint32_t oth = MODE == kForwardKL ? us[w] : vs[w];
-                viol |= __vcmpeq2(oth, In::kNegInf2) & ~__vcmpeq2(tgt, In::kNegInf2);
+                const Word tgt = MODE == kForwardKL ? vs[w] : us[w];
+                const Word oth = MODE == kForwardKL ? us[w] : vs[w];
+                viol |= In::viol(tgt, oth);
               }
-              const float2 lp = lam<In>(In::max2(us[w], In::kNegBig2), nms2, l2e2, nKs2);
-              const float2 lq = lam<In>(In::max2(vs[w], In::kNegBig2), nmt2, l2e2, nKt2);
+              const float2 lp = lam<In>(In::max2(us[w], In::neg_big_w()), nms2, l2e2, nKs2);
+              const float2 lq = lam<In>(In::max2(vs[w], In::neg_big_w()), nmt2, l2e2, nKt2);
               const float2 p = ex2_2(lp), qv = ex2_2(lq);
               if (MODE == kInterior) {
                 const float2 lm = lg2_2(fma2(ws2, p, fma2(wt2, qv, tiny2)));
@@ -1239,13 +1262,14 @@ struct Config {
 
 // Shared memory of a slice width: both stages of both inputs, then the tail,
 // and at least kMinSmem so that no two CTAs share an SM's tensor memory.
-inline size_t smem_bytes(int W, bool gstage = false) {
-  const size_t s = static_cast<size_t>(kStages) * 4 * W + (gstage ? static_cast<size_t>(4) * W : 0) + sizeof(Tail);
+inline size_t smem_bytes(int W, bool gstage = false, int esize = 2) {
+  const size_t s =
+      static_cast<size_t>(kStages) * 2 * esize * W + (gstage ? static_cast<size_t>(4) * W : 0) + sizeof(Tail);
   return s < kMinSmem ? kMinSmem : s;
 }
 // The forward-only kernel: three stages, then the tail (one CTA per SM too).
-inline size_t smem_bytes_fwd(int W) {
-  const size_t s = static_cast<size_t>(kFwdStages) * 4 * W + sizeof(Tail);
+inline size_t smem_bytes_fwd(int W, int esize = 2) {
+  const size_t s = static_cast<size_t>(kFwdStages) * 2 * esize * W + sizeof(Tail);
   return s < kMinSmem ? kMinSmem : s;
 }
 

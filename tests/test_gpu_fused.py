@@ -44,6 +44,15 @@ def make_rows(n, v, dtype, seed=1):
     return s.to(dtype).cuda(), t.to(dtype).cuda()
 
 
+def off_grid(x):
+    """The same rows with a row stride of V + 1 elements: rows that do not all
+    start on a 16-byte boundary, which the single-read kernels do not take."""
+    n, v = x.shape
+    y = torch.empty(n, v + 1, dtype=x.dtype, device=x.device)
+    y[:, :v].copy_(x)
+    return y[:, :v]
+
+
 def fused_call(B, s, t, beta, g, gdtype, want_s=True, want_t=True):
     n = s.shape[0] if s.dim() == 2 else s.shape[0] * s.shape[1]
     v = s.shape[-1]
@@ -230,6 +239,60 @@ def test_forward_kernel_many_rows_at_cluster_width(B):
             assert_loss(to64(saved)[live, 4], ra[live], "forward 240 rows saved KL(P_t||M)")
 
 
+@pytest.mark.parametrize("beta", [0.5, 0.0, 1.0, 0.3])
+def test_fp32_single_read(B, beta):
+    """fp32 logits on the single-read kernels (32-byte vectors of 8 floats):
+    every special row class, fwd+bwd in one launch, the forward-only kernel,
+    and a segmented call (the same MAX / SUM merge over the CTA slices)."""
+    s, t = make_rows(40, 8192, torch.float32, seed=31)
+    check(B, s, t, beta, torch.float32, label="fp32 single-read", launches=(1,))
+    n, v = s.shape
+    rl, ra, rb, _, _ = O.jsd(to64(s), to64(t), beta, grad=False, threads=8)
+    for seg in (None, [3000, 0, 5192]):
+        loss = torch.full((n,), 7.0, device="cuda")
+        saved = torch.full((n, 6), 7.0, device="cuda")
+        k = launches_of(B, lambda: B.vpd_jsd_fwd(s, t, beta, seg, loss, saved))
+        assert k == 1, f"fp32 forward, segments {seg}: {k} launches"
+        assert_loss(to64(loss), rl, f"fp32 forward beta={beta} segments {seg}")
+        live = np.isfinite(rl)
+        sv = to64(saved)
+        if beta not in (0.0, 1.0):
+            assert_loss(sv[live, 4], ra[live], f"fp32 forward saved A, segments {seg}")
+            assert_loss(sv[live, 5], rb[live], f"fp32 forward saved B, segments {seg}")
+
+
+def test_fp32_single_read_wide_rows_and_split(B):
+    """fp32 rows at V = 128256 in 8 uneven segments (the edge-case workload's
+    shape) with a common offset of 1e4: clusters of 10 or more CTAs, the last
+    rows on the idle SMs; every row against the oracle."""
+    from softmax_divergence_lm_gb300 import synth
+    v = 128256
+    g = torch.Generator(device="cpu").manual_seed(37)
+    s = torch.randn(600, v, generator=g) * 3 + 1.0e4
+    t = torch.randn(600, v, generator=g) * 3 + 1.0e4
+    s[torch.rand(600, v, generator=g) < 0.1] = -math.inf
+    s, t = s.cuda(), t.cuda()
+    seg = synth.segment_widths(37, v)
+    n = s.shape[0]
+    gr = torch.randn(n, generator=g).cuda()
+    loss = torch.empty(n, device="cuda")
+    saved = torch.empty(n, 6, device="cuda")
+    ds = torch.empty(n, v, device="cuda")
+    dt = torch.empty(n, v, device="cuda")
+    fused_rows, side_rows, planned = B.vpd_jsd_plan(s, t, seg, ds, dt)
+    assert fused_rows > 0 and planned in (1, 4)
+    k = launches_of(B, lambda: B.vpd_jsd_fwdbwd(s, t, 0.5, seg, gr, loss, saved, ds, dt))
+    assert k == planned, f"{k} launches, planned {planned}"
+    B.vpd_device_status()
+    rows = np.arange(0, n, 9)
+    rows = np.unique(np.concatenate([rows, [n - 1, fused_rows - 1, min(fused_rows, n - 1)]]))
+    r = torch.as_tensor(rows, device="cuda")
+    rl, _, _, rds, rdt = O.jsd(to64(s[r]), to64(t[r]), 0.5, to64(gr)[rows], threads=8)
+    assert_loss(to64(loss)[rows], rl, "fp32 wide rows loss")
+    assert_grad(to64(ds[r]), rds, "fp32 wide rows dS")
+    assert_grad(to64(dt[r]), rdt, "fp32 wide rows dT")
+
+
 def test_fused_equals_streaming_path(B):
     """The fused single-read call and the two-pass forward + backward agree."""
     s, t = make_rows(32, 151936, torch.bfloat16, seed=7)
@@ -254,8 +317,9 @@ def test_one_hot_against_broad_fp32_floor_every_path(B):
     nats, so fp32 (the saved KL itself is an fp32 number) cannot resolve it to
     the stated absolute tolerance. Every path gets the same allowance, the
     rounding floor of `parity_util.kl_branch_floor`, on top of the stated
-    tolerance: the single-read kernel, the streaming kernels (two segments),
-    and the KL forward + backward in both directions; the loss and every other
+    tolerance: the single-read kernel (one and two segments), the streaming
+    kernels (rows off the 16-byte grid), and the KL forward + backward in both
+    directions; the loss and every other
     gradient meet the stated tolerance."""
     v = 1024
     g0 = torch.Generator(device="cpu").manual_seed(11)
@@ -273,12 +337,16 @@ def test_one_hot_against_broad_fp32_floor_every_path(B):
         loss, _, ds, dt, launches = fused_call(B, s, t, beta, g, torch.float32)
         assert launches == 1
         runs["single-read"] = (loss, ds, dt)
-        for label, seg in (("streaming", [v // 2, v - v // 2]),):
+        # rows off the 16-byte grid (a row stride of V + 1) take the streaming
+        # kernels; a two-segment table keeps the single-read kernel
+        for label, (xs, xt, seg, k_want) in (("streaming", (off_grid(s), off_grid(t), None, 3)),
+                                             ("single-read, two segments", (s, t, [v // 2, v - v // 2], 1))):
             l2 = torch.empty(n, device="cuda")
             sv = torch.empty(n, 6, device="cuda")
             d1 = torch.empty(n, v, device="cuda")
             d2 = torch.empty(n, v, device="cuda")
-            B.vpd_jsd_fwdbwd(s, t, beta, seg, g, l2, sv, d1, d2)
+            k = launches_of(B, lambda: B.vpd_jsd_fwdbwd(xs, xt, beta, seg, g, l2, sv, d1, d2))
+            assert k == k_want, f"{label}: {k} launches"
             runs[label] = (l2, d1, d2)
         l3 = torch.empty(n, device="cuda")
         sv = torch.empty(n, 6, device="cuda")
@@ -401,7 +469,7 @@ def test_bf16_row_max_above_2_126(B):
     """A bf16 row whose largest finite logit exceeds 2^126 is out of contract
     on the single-read kernels: NaN with zero gradients (the limit keeps every
     clamped log-difference finite). The streaming kernels, reached here through
-    a two-segment call, and the oracle give the finite value. At beta = 0 the
+    rows off the 16-byte grid, and the oracle give the finite value. At beta = 0 the
     teacher gradient of such a row is a difference of two log-ratios near
     2^127 that fp32 cannot resolve (the same floor as for near one-hot rows),
     so there only the loss and the student gradient of those rows are
@@ -426,13 +494,13 @@ def test_bf16_row_max_above_2_126(B):
         fwd = torch.empty(4, device="cuda")
         k = launches_of(B, lambda: B.vpd_jsd_fwd(s, t, beta, None, fwd, torch.empty(4, 6, device="cuda")))
         assert k == 1 and np.all(np.isnan(to64(fwd)[:2]))
-        # two segments: the streaming kernels, finite and equal to the oracle
+        # rows off the 16-byte grid: the streaming kernels, finite and equal to the oracle
         ls = torch.empty(4, device="cuda")
         sv = torch.empty(4, 6, device="cuda")
         ds2 = torch.empty(4, v, device="cuda")
         dt2 = torch.empty(4, v, device="cuda")
-        B.vpd_jsd_fwdbwd(s, t, beta, [v // 2, v - v // 2], g, ls, sv, ds2, dt2)
-        torch.cuda.synchronize()
+        k = launches_of(B, lambda: B.vpd_jsd_fwdbwd(off_grid(s), off_grid(t), beta, None, g, ls, sv, ds2, dt2))
+        assert k == 3, f"off-grid rows: {k} launches"
         assert_loss(to64(ls), rl, f"beta={beta} streaming loss")
         assert_grad(to64(ds2), rds, f"beta={beta} streaming dS")
         keep = slice(None) if beta > 0.0 else slice(2, None)
