@@ -1,8 +1,9 @@
 // vpd_fused.cuh -- device code of the single-read fused JSD on thread-block
 // clusters: the forward+backward kernel (k_jsd_fused) and, for calls that
 // want no gradient, the forward-only kernel (k_jsd_fused_fwd, further below);
-// instantiated per input dtype in vpd_fused_bf16.cu / vpd_fused_f16.cu, host
-// dispatch in vpd_fused.cu.
+// instantiated per input dtype in vpd_fused_bf16.cu / vpd_fused_f16.cu /
+// vpd_fused_f32.cu (fp32 vectors: 8 floats in 32 bytes), host dispatch in
+// vpd_fused.cu.
 //
 // Source: DeepSpeed pull request #8958, "[VocabTP] Add vocabulary-parallel
 // generalized JSD with Triton kernels": the op (section Changes: paired softmax
@@ -64,7 +65,7 @@ constexpr int kRing = 3;                    // cluster slots and their mbarriers
 constexpr float kTiny = 1e-37f;             // keeps M > 0 so log2 M stays finite
 constexpr float kMaxLogit = 8.5070592e37f;  // 2^126: a larger finite row max is out of contract
 constexpr int kMaxCluster = 16;
-constexpr int kMaxR = 5;                    // 16-byte vectors of each input per worker thread
+constexpr int kMaxR = 5;                    // 8-element vectors of each input per worker thread
 constexpr int kTmemCols = 512;              // the whole tensor memory of the SM
 constexpr int kMinSmem = 120 * 1024;        // keeps one CTA per SM (each takes all TMEM)
 constexpr int kMaxWorkers = 19;             // worker warps per CTA (plus one control warp)
@@ -361,9 +362,8 @@ struct Out<GF32> {
   __device__ static __forceinline__ void store8_shared(unsigned char*, const float2 (&)[4]) {}
 };
 
-// One 16-byte vector of the stage (plain shared-memory load: ordered after
+// Stage vectors are read with In::ld (plain shared-memory loads: ordered after
 // the mbarrier waits and barriers, free to schedule otherwise).
-__device__ __forceinline__ uint4 lds16(const unsigned char* p) { return *reinterpret_cast<const uint4*>(p); }
 
 // ---------------------------------------------------------------------------
 // Work split inside a CTA. nw worker warps (chosen on the host so that the
