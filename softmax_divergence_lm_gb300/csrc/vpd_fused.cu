@@ -144,12 +144,14 @@ bool choose(int64_t vocab, int64_t rows, int max_cluster, bool fwd, Config* cfg,
 
 // Rate of the streaming path on one otherwise idle SM relative to one SM of a
 // fused cluster, in rows per second per SM: for forward+backward (three
-// streaming passes against one read) 0.5 with clusters of up to 15 CTAs and
-// 0.57 with 16 (a cluster of 16 spends more of each row on its exchanges), for
-// the forward (two passes) 0.9; measured at V = 151936 (clusters of 9) and
-// V = 262144 (clusters of 16). VPD_IDLE_RATE / VPD_IDLE_RATE_FWD override them
-// (0 disables the split).
-static double idle_rate(bool fwd, int cluster) {
+// streaming passes against one read) of 16-bit rows 0.5 with clusters of up
+// to 15 CTAs and 0.57 with 16 (a cluster of 16 spends more of each row on its
+// exchanges), of fp32 rows 0.9 (the fused kernel moves twice the bytes per
+// element through its stages); for the forward (two passes) 0.9; measured at
+// V = 151936 (clusters of 9), V = 262144 (clusters of 16) and V = 128256 fp32
+// (clusters of 9). VPD_IDLE_RATE / VPD_IDLE_RATE_FWD override them (0
+// disables the split).
+static double idle_rate(bool fwd, int cluster, int esize) {
   static const double r[2] = {[] {
                                 const char* e = getenv("VPD_IDLE_RATE");
                                 return e && e[0] ? atof(e) : -1.0;
@@ -160,6 +162,7 @@ static double idle_rate(bool fwd, int cluster) {
                               }()};
   if (fwd) return r[1];
   if (r[0] >= 0.0) return r[0];
+  if (esize == 4) return 0.9;
   return cluster >= 16 ? 0.57 : 0.5;
 }
 
@@ -176,8 +179,9 @@ void fused_idle_split(const View& s, const Grad& ds, const Grad& dt, int max_clu
     if (gdtype != kF32 && gdtype != s.dtype) return;
   }
   Config cfg;
-  if (!choose(s.vocab, s.rows, max_cluster, fwd, &cfg, s.dtype == kF32 ? 4 : 2)) return;
-  const double rate = idle_rate(fwd, cfg.C);
+  const int es = s.dtype == kF32 ? 4 : 2;
+  if (!choose(s.vocab, s.rows, max_cluster, fwd, &cfg, es)) return;
+  const double rate = idle_rate(fwd, cfg.C, es);
   if (rate <= 0.0) return;
   const int clusters = clusters_for(cfg.C);
   const int used = clusters * cfg.C, idle = sm_count() - used;
