@@ -134,7 +134,9 @@ typedef struct {
  * ------------------------------------------------------------------------- */
 
 /* Forward. The statistics must be global before the divergence ([JSD page],
- * "Scope and limitations"): under the single-read conditions of vpd_jsd_fwdbwd
+ * "Scope and limitations"). At beta = 0 / 1 (the KL branches) the call runs
+ * the online single-pass KL kernel of vpd_kl_fwd (same loss and saved
+ * layout). Otherwise, under the single-read conditions of vpd_jsd_fwdbwd
  * (aligned rows, V a multiple of 8), a forward-only cluster kernel
  * reads each row pair once and keeps it on chip for both steps, when the row
  * fits in clusters of at most 10 CTAs (V <= 191040 with 227 KB of shared memory
@@ -221,7 +223,8 @@ vpd_status vpd_jsd_fwdbwd_teacher_stream(const vpd_view *s, const void *t_host, 
  * nothing launched: how many rows go to the single-read cluster kernel, how
  * many to the streaming kernels on the SMs its clusters leave idle, and the
  * number of kernel launches. With ds and dt both absent (NULL or NULL data)
- * the answer is for vpd_jsd_fwd (the forward-only kernel), otherwise for
+ * the answer is for vpd_jsd_fwd with 0 < beta < 1 (the forward-only kernel; at
+ * beta = 0 / 1 that call runs the online KL kernel, one launch), otherwise for
  * vpd_jsd_fwdbwd. The data pointers of the views and gradients are not read.
  * fused_rows = 0 means the streaming kernels only. Any output may be NULL. */
 vpd_status vpd_jsd_plan(const vpd_view *s, const vpd_view *t, const vpd_segments *seg, const vpd_grad *ds,
@@ -231,7 +234,10 @@ vpd_status vpd_jsd_plan(const vpd_view *s, const vpd_view *t, const vpd_segments
  * Forward / reverse KL ([ops page], "What"): reverse = 0 gives KL(P_t || P_s)
  * (the teacher is the target), reverse = 1 gives KL(P_s || P_t). The forward
  * reads the inputs once in one online pass (running maxima with rescaled
- * sums) on every SM, one CTA per row at a time. saved may be NULL.
+ * sums) on every SM, one CTA per row at a time; as on the single-read kernels
+ * a row whose largest finite logit exceeds 2^126 is out of contract and comes
+ * back NaN (the rescaling of the running sums would overflow). saved may be
+ * NULL.
  * Saved layout and backward are those of the JSD beta = 0 / 1 branches.
  * ------------------------------------------------------------------------- */
 vpd_status vpd_kl_fwd(const vpd_view *s, const vpd_view *t, int32_t reverse,

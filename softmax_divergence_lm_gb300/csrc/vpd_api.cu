@@ -200,6 +200,14 @@ vpd_status vpd_jsd_fwd(const vpd_view* s, const vpd_view* t, double beta, const 
   if (vs.rows == 0) return ok();
   if (!loss || !saved) return fail(VPD_ERR_ARG, "vpd_jsd_fwd: loss and saved are required");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // beta = 0 / 1 are the KL branches: the online single-pass KL kernel reads
+  // the inputs once too and writes the same loss and saved layout (the KL ops
+  // take it at every width for that reason: it is faster than the cluster
+  // kernel's KL branch)
+  if (beta == 0.0 || beta == 1.0) {
+    VPD_CUDA(vpd::launch_kl_fwd(vs, vt, beta == 1.0 ? 1 : 0, sg, loss, saved, st), "single-pass KL kernel");
+    return ok();
+  }
   // One read of the inputs by the single-read forward kernel when it fits in
   // clusters that cover most SMs; else the two streaming passes on every SM.
   // Vocabulary segments change only the grouping of the statistics merge

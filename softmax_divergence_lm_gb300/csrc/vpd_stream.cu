@@ -634,6 +634,8 @@ __device__ __forceinline__ KlAcc block_kl(KlAcc x, float* sc) {
   return y;
 }
 
+constexpr float kOnlineMaxLogit = 8.5070592e37f;  // 2^126
+
 template <class T>
 __global__ void __launch_bounds__(kThreads, 2) k_kl_fwd(View a, View b, Segs seg, int a_is_teacher,
                                                      float* loss, float* saved) {
@@ -651,7 +653,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_kl_fwd(View a, View b, Segs seg
     if (threadIdx.x == 0) {
       const RowStat sa = finish_stat(run.a), sb = finish_stat(run.b);
       float kl;
-      if (!stat_ok(sa) || !stat_ok(sb))
+      // a finite row max above 2^126 is out of contract here as on the
+      // single-read kernels (the rescaling of the running sums overflows)
+      if (!stat_ok(sa) || !stat_ok(sb) || sa.m > kOnlineMaxLogit || sb.m > kOnlineMaxLogit)
         kl = qnan();
       else if (run.viol)
         kl = pos_inf();

@@ -467,8 +467,8 @@ def test_forward_calls_through_single_read(B, v):
 
 def test_bf16_row_max_above_2_126(B):
     """A bf16 row whose largest finite logit exceeds 2^126 is out of contract
-    on the single-read kernels: NaN with zero gradients (the limit keeps every
-    clamped log-difference finite). The streaming kernels, reached here through
+    on the single-read kernels and the online KL kernel: NaN with zero
+    gradients (the limit keeps every clamped log-difference finite). The streaming kernels, reached here through
     rows off the 16-byte grid, and the oracle give the finite value. At beta = 0 the
     teacher gradient of such a row is a difference of two log-ratios near
     2^127 that fp32 cannot resolve (the same floor as for near one-hot rows),
@@ -493,7 +493,10 @@ def test_bf16_row_max_above_2_126(B):
         assert_loss(lo[2:], rl[2:], f"beta={beta} in-contract rows")
         fwd = torch.empty(4, device="cuda")
         k = launches_of(B, lambda: B.vpd_jsd_fwd(s, t, beta, None, fwd, torch.empty(4, 6, device="cuda")))
+        # beta = 0.5: the forward-only cluster kernel; beta = 0: the online KL
+        # kernel, where such rows are out of contract too
         assert k == 1 and np.all(np.isnan(to64(fwd)[:2]))
+        assert_loss(to64(fwd)[2:], rl[2:], f"beta={beta} forward in-contract rows")
         # rows off the 16-byte grid: the streaming kernels, finite and equal to the oracle
         ls = torch.empty(4, device="cuda")
         sv = torch.empty(4, 6, device="cuda")
