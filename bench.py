@@ -632,7 +632,9 @@ def run_sweep(args):
         for beta in betas:
             if not fused_only:
                 ms = _trials(lambda: B.vpd_jsd_fwd(s, t, beta, segments, loss, saved), trials, 3, stream)
-                emit(name, "jsd", "fwd", dt_name, beta, n, v, rd, ms, plan(False))
+                # at beta = 0 / 1 the forward is the online KL kernel (one launch)
+                fwd_path = {"path": "online KL kernel", "launches": 1} if beta in (0.0, 1.0) else plan(False)
+                emit(name, "jsd", "fwd", dt_name, beta, n, v, rd, ms, fwd_path)
                 ms = _trials(lambda: B.vpd_jsd_bwd(s, t, beta, segments, g, saved, ds, dt), trials, 3, stream)
                 emit(name, "jsd", "bwd", dt_name, beta, n, v, rd + wr, ms)
             ms = _trials(lambda: B.vpd_jsd_fwdbwd(s, t, beta, segments, g, loss, saved, ds, dt), trials, 3, stream)
