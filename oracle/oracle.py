@@ -1,4 +1,5 @@
-"""Python access to the double-precision CPU oracle in ``vpd_oracle.c``.
+"""Python access to the CPU oracle in ``vpd_oracle.c``, in double precision
+or, on request, in the host's long double.
 
 TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's
 CPU-baseline leg are the only callers allowed. The product path never imports
@@ -11,6 +12,13 @@ float64 (fp32/bf16/fp16 values upcast exactly); outputs are float64 numpy
 arrays. Every function runs one token row at a time over the full vocabulary;
 ``threads > 1`` only splits the rows over host threads (the C calls release
 the interpreter lock).
+
+The same source builds twice: ``libvpd_oracle.so`` works in double, and
+``libvpd_oracle_ld.so`` (the source compiled with ``VPD_ORACLE_LONG_DOUBLE``)
+carries every intermediate in long double (x86-64: 64-bit significand; AArch64:
+113-bit), rounding once to float64 at the output. The row functions take
+``precision="double"`` (default) or ``"long double"``; the second is a check on
+the first's rounding, not a different definition.
 """
 from __future__ import annotations
 
@@ -25,36 +33,55 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 SOURCE = os.path.join(_HERE, "vpd_oracle.c")
 LIBRARY = os.path.join(_HERE, "_build", "libvpd_oracle.so")
+LIBRARY_LONG_DOUBLE = os.path.join(_HERE, "_build", "libvpd_oracle_ld.so")
+PRECISIONS = ("double", "long double")
 
 _lock = threading.Lock()
 _lib = None
+_lib_ld = None
 
 _f64p = ctypes.POINTER(ctypes.c_double)
 _i64p = ctypes.POINTER(ctypes.c_int64)
 
 
-def compile_command(source: str = SOURCE, output: str = LIBRARY) -> list[str]:
+def _check_precision(precision: str) -> None:
+    if precision not in PRECISIONS:
+        raise ValueError(f"precision must be one of {PRECISIONS}, not {precision!r}")
+
+
+def compile_command(source: str = SOURCE, output: str = LIBRARY, precision: str = "double") -> list[str]:
     """The host-compiler command that builds the oracle library."""
-    return ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", output, source, "-lm"]
+    _check_precision(precision)
+    defines = ["-DVPD_ORACLE_LONG_DOUBLE"] if precision == "long double" else []
+    return ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", *defines, "-o", output, source, "-lm"]
 
 
-def build(force: bool = False, source: str = SOURCE, output: str = LIBRARY) -> str:
+def build(force: bool = False, source: str = SOURCE, output: str | None = None,
+          precision: str = "double") -> str:
     """Compile the oracle if the library is missing or older than its source."""
+    _check_precision(precision)
+    if output is None:
+        output = LIBRARY_LONG_DOUBLE if precision == "long double" else LIBRARY
     os.makedirs(os.path.dirname(output), exist_ok=True)
     stale = (not os.path.exists(output)) or os.path.getmtime(output) < os.path.getmtime(source)
     if force or stale:
         tmp = output + f".tmp{os.getpid()}"
-        subprocess.run(compile_command(source, tmp), check=True)
+        subprocess.run(compile_command(source, tmp, precision), check=True)
         os.replace(tmp, output)
     return output
 
 
-def load(path: str | None = None):
+def load(path: str | None = None, precision: str = "double"):
     """Load (building first if needed) and return the ctypes handle."""
-    global _lib
+    global _lib, _lib_ld
+    _check_precision(precision)
     if path is not None:
         return _declare(ctypes.CDLL(path))
     with _lock:
+        if precision == "long double":
+            if _lib_ld is None:
+                _lib_ld = _declare(ctypes.CDLL(build(precision=precision)))
+            return _lib_ld
         if _lib is None:
             _lib = _declare(ctypes.CDLL(build()))
     return _lib
@@ -116,10 +143,10 @@ def _run(n: int, threads: int, fn):
         list(ex.map(lambda ab: fn(*ab), parts))
 
 
-def row_stats(x):
+def row_stats(x, precision: str = "double"):
     """(m, lse, code) per row: max over the finite support, log of the sum-exp
     relative to it, and 0 / 1 (NaN or +inf present) / 2 (fully -inf)."""
-    lib = load()
+    lib = load(precision=precision)
     x = _rows2d(x)
     n, v = x.shape
     m = np.empty(n)
@@ -133,9 +160,9 @@ def row_stats(x):
     return m, lse, code
 
 
-def segment_stats(x, widths):
+def segment_stats(x, widths, precision: str = "double"):
     """Statistics (m, Z) of one row merged over ordered segments."""
-    lib = load()
+    lib = load(precision=precision)
     x = _f64(x).reshape(-1)
     w = np.ascontiguousarray(np.asarray(widths, dtype=np.int64))
     m = ctypes.c_double()
@@ -146,11 +173,11 @@ def segment_stats(x, widths):
     return m.value, z.value
 
 
-def jsd(s, t, beta: float, g=None, grad: bool = True, threads: int = 1):
+def jsd(s, t, beta: float, g=None, grad: bool = True, threads: int = 1, precision: str = "double"):
     """Generalized JSD per row. Returns (loss, kl_tm, kl_sm, ds, dt); kl_tm and
     kl_sm are KL(P_t||M) and KL(P_s||M) (NaN on the beta = 0 / 1 branches);
     ds, dt are None when grad is False."""
-    lib = load()
+    lib = load(precision=precision)
     s = _rows2d(s)
     t = _rows2d(t)
     if s.shape != t.shape:
@@ -172,10 +199,10 @@ def jsd(s, t, beta: float, g=None, grad: bool = True, threads: int = 1):
     return loss, a, b, ds, dt
 
 
-def kl(s, t, reverse: bool, g=None, grad: bool = True, threads: int = 1):
+def kl(s, t, reverse: bool, g=None, grad: bool = True, threads: int = 1, precision: str = "double"):
     """KL(P_t||P_s) (reverse False) or KL(P_s||P_t) (reverse True) per row.
     Returns (loss, ds, dt)."""
-    lib = load()
+    lib = load(precision=precision)
     s = _rows2d(s)
     t = _rows2d(t)
     if s.shape != t.shape:
@@ -196,9 +223,9 @@ def kl(s, t, reverse: bool, g=None, grad: bool = True, threads: int = 1):
     return loss, ds, dt
 
 
-def entropy(x, g=None, grad: bool = True, threads: int = 1):
+def entropy(x, g=None, grad: bool = True, threads: int = 1, precision: str = "double"):
     """Entropy per row. Returns (out, dx)."""
-    lib = load()
+    lib = load(precision=precision)
     x = _rows2d(x)
     n, v = x.shape
     g = None if g is None else _f64(g).reshape(n)
@@ -214,9 +241,10 @@ def entropy(x, g=None, grad: bool = True, threads: int = 1):
     return out, dx
 
 
-def logprobs(x, index, ignore_index: int = -100, g=None, grad: bool = True, threads: int = 1):
+def logprobs(x, index, ignore_index: int = -100, g=None, grad: bool = True, threads: int = 1,
+             precision: str = "double"):
     """Selected log-probs. index is [N] or [N, K]; returns (out [N, K], dx, errors)."""
-    lib = load()
+    lib = load(precision=precision)
     x = _rows2d(x)
     n, v = x.shape
     idx = np.ascontiguousarray(np.asarray(index, dtype=np.int64)).reshape(n, -1)

@@ -17,7 +17,10 @@
  *
  * Every function works one token row at a time, over the full vocabulary, in
  * the order of the steps below (no blocking, no fusion):
- *   1. The caller upcasts the logits exactly to double.
+ *   1. The caller upcasts the logits exactly to double. Built with
+ *      VPD_ORACLE_LONG_DOUBLE, every step below works in long double instead
+ *      (the same steps and terms; only the rounding of the intermediates
+ *      changes) and the outputs are rounded once to double.
  *   2. A row holding NaN or +inf is outside the contract; it is given a NaN
  *      output and an all-zero gradient (a reading: the pages are silent).
  *   3. Row statistics in two naive passes: the support S = {j : x_j > -inf},
@@ -32,7 +35,7 @@
  *      (the target has mass on a token the other side masks, decided by logit
  *      finiteness, [ops page], "Tests") also gets a zero gradient.
  *
- * Sums over the vocabulary are plain left-to-right double sums with Neumaier
+ * Sums over the vocabulary are plain left-to-right sums with Neumaier
  * compensation; they change only the rounding, not the order of the terms.
  * Natural logarithms (nats) throughout.
  */
@@ -41,24 +44,44 @@
 #include <stdint.h>
 
 /* ------------------------------------------------------------------------- */
+/* Working precision: double, or with VPD_ORACLE_LONG_DOUBLE defined the       */
+/* host's long double (80-bit extended on x86-64, 128-bit on AArch64). Inputs  */
+/* and outputs stay double arrays; the values are upcast exactly on entry and  */
+/* every intermediate is carried in the working precision.                    */
+/* ------------------------------------------------------------------------- */
+#ifdef VPD_ORACLE_LONG_DOUBLE
+typedef long double real;
+#define REXP expl
+#define RLOG logl
+#define RLOG1P log1pl
+#define RFABS fabsl
+#else
+typedef double real;
+#define REXP exp
+#define RLOG log
+#define RLOG1P log1p
+#define RFABS fabs
+#endif
+
+/* ------------------------------------------------------------------------- */
 /* Compensated running sum (Neumaier).                                        */
 /* ------------------------------------------------------------------------- */
 typedef struct {
-    double sum;
-    double comp;
+    real sum;
+    real comp;
 } csum;
 
-static void csum_add(csum *a, double v)
+static void csum_add(csum *a, real v)
 {
-    double t = a->sum + v;
-    if (fabs(a->sum) >= fabs(v))
+    real t = a->sum + v;
+    if (RFABS(a->sum) >= RFABS(v))
         a->comp += (a->sum - t) + v;
     else
         a->comp += (v - t) + a->sum;
     a->sum = t;
 }
 
-static double csum_value(const csum *a) { return a->sum + a->comp; }
+static real csum_value(const csum *a) { return a->sum + a->comp; }
 
 /* ------------------------------------------------------------------------- */
 /* Step 2 and 3: row statistics.                                              */
@@ -66,9 +89,9 @@ static double csum_value(const csum *a) { return a->sum + a->comp; }
 typedef struct {
     int bad;      /* the row holds NaN or +inf (step 2)              */
     int empty;    /* the support is empty: every entry is -inf        */
-    double m;     /* max over the support                             */
-    double z;     /* sum over the support of exp(x_j - m)             */
-    double lse;   /* ln z                                             */
+    real m;       /* max over the support                             */
+    real z;       /* sum over the support of exp(x_j - m)             */
+    real lse;     /* ln z                                             */
 } row_stats;
 
 static row_stats stats_of(int64_t V, const double *x)
@@ -81,7 +104,7 @@ static row_stats stats_of(int64_t V, const double *x)
     r.lse = -INFINITY;
     /* pass 1: validity and the max over the support */
     for (int64_t j = 0; j < V; ++j) {
-        double v = x[j];
+        real v = x[j];
         if (isnan(v) || v == INFINITY) {
             r.bad = 1;
             continue;
@@ -97,18 +120,18 @@ static row_stats stats_of(int64_t V, const double *x)
     /* pass 2: the sum of exponentials relative to the max */
     csum z = {0.0, 0.0};
     for (int64_t j = 0; j < V; ++j) {
-        double v = x[j];
+        real v = x[j];
         if (v == -INFINITY)
             continue;
-        csum_add(&z, exp(v - r.m));
+        csum_add(&z, REXP(v - r.m));
     }
     r.z = csum_value(&z);
-    r.lse = log(r.z);
+    r.lse = RLOG(r.z);
     return r;
 }
 
 /* ln p_j for an entry on the support */
-static double log_prob(const row_stats *r, double x) { return (x - r->m) - r->lse; }
+static real log_prob(const row_stats *r, real x) { return (x - r->m) - r->lse; }
 
 /* Public: per-row statistics (m, ln Z). Returns 1 for a NaN/+inf row, 2 for a
  * fully -inf row, 0 otherwise. */
@@ -143,7 +166,7 @@ int vpd_oracle_segment_stats(int64_t V, const double *x, int count, const int64_
     if (total != V)
         return 1;
     /* each segment on its own: (m_k, z_k) with z_k relative to m_k */
-    double m = -INFINITY;
+    real m = -INFINITY;
     int64_t off = 0;
     for (int k = 0; k < count; ++k) {
         row_stats r = stats_of(widths[k], x + off);
@@ -156,7 +179,7 @@ int vpd_oracle_segment_stats(int64_t V, const double *x, int count, const int64_
     for (int k = 0; k < count; ++k) {
         row_stats r = stats_of(widths[k], x + off);
         if (!r.empty)
-            csum_add(&z, r.z * exp(r.m - m));
+            csum_add(&z, r.z * REXP(r.m - m));
         off += widths[k];
     }
     *m_out = m;
@@ -177,17 +200,17 @@ static void zero_row(double *d, int64_t V)
 
 /* ln(a_w * e^{la} + b_w * e^{lb}) for log-weights lwa = ln a_w, lwb = ln b_w;
  * either log-argument may be -inf (the other then decides). */
-static double log_mix(double lwa, double la, double lwb, double lb)
+static real log_mix(real lwa, real la, real lwb, real lb)
 {
-    double u = lwa + la;
-    double v = lwb + lb;
+    real u = lwa + la;
+    real v = lwb + lb;
     if (u == -INFINITY)
         return v;
     if (v == -INFINITY)
         return u;
-    double hi = u > v ? u : v;
-    double lo = u > v ? v : u;
-    return hi + log1p(exp(lo - hi));
+    real hi = u > v ? u : v;
+    real lo = u > v ? v : u;
+    return hi + RLOG1P(REXP(lo - hi));
 }
 
 /* ------------------------------------------------------------------------- */
@@ -199,7 +222,7 @@ static double log_mix(double lwa, double la, double lwb, double lb)
 /*   d/d(logit_a)_j = g * a_j (ln a_j - ln b_j - KL)                           */
 /*   d/d(logit_b)_j = g * (b_j - a_j)                                          */
 /* ------------------------------------------------------------------------- */
-static double kl_row(int64_t V, const double *xa, const double *xb, double g, double *da,
+static real kl_row(int64_t V, const double *xa, const double *xb, real g, double *da,
                      double *db)
 {
     row_stats ra = stats_of(V, xa);
@@ -220,14 +243,14 @@ static double kl_row(int64_t V, const double *xa, const double *xb, double g, do
     for (int64_t j = 0; j < V; ++j) {
         if (xa[j] == -INFINITY)
             continue;
-        double la = log_prob(&ra, xa[j]);
-        double lb = log_prob(&rb, xb[j]);
-        csum_add(&kl, exp(la) * (la - lb));
+        real la = log_prob(&ra, xa[j]);
+        real lb = log_prob(&rb, xb[j]);
+        csum_add(&kl, REXP(la) * (la - lb));
     }
-    double value = csum_value(&kl);
+    real value = csum_value(&kl);
     for (int64_t j = 0; j < V; ++j) {
-        double a = xa[j] == -INFINITY ? 0.0 : exp(log_prob(&ra, xa[j]));
-        double b = xb[j] == -INFINITY ? 0.0 : exp(log_prob(&rb, xb[j]));
+        real a = xa[j] == -INFINITY ? 0.0 : REXP(log_prob(&ra, xa[j]));
+        real b = xb[j] == -INFINITY ? 0.0 : REXP(log_prob(&rb, xb[j]));
         if (da) {
             if (xa[j] == -INFINITY)
                 da[j] = 0.0;
@@ -252,8 +275,8 @@ static double kl_row(int64_t V, const double *xa, const double *xb, double g, do
 /*   dS_j = g (1 - beta) p_j (ln p_j - ln M_j - B)                             */
 /*   dT_j = g beta       q_j (ln q_j - ln M_j - A)                             */
 /* ------------------------------------------------------------------------- */
-static double jsd_row(int64_t V, const double *s, const double *t, double beta, double g,
-                      double *ds, double *dt, double *a_out, double *b_out)
+static real jsd_row(int64_t V, const double *s, const double *t, real beta, real g,
+                      double *ds, double *dt, real *a_out, real *b_out)
 {
     *a_out = NAN;
     *b_out = NAN;
@@ -269,8 +292,8 @@ static double jsd_row(int64_t V, const double *s, const double *t, double beta, 
         zero_row(dt, V);
         return NAN;
     }
-    const double lw_s = log(1.0 - beta); /* log-weight of p in M */
-    const double lw_t = log(beta);       /* log-weight of q in M */
+    const real lw_s = RLOG(1.0 - beta); /* log-weight of p in M */
+    const real lw_t = RLOG(beta);       /* log-weight of q in M */
 
     /* the two KL-to-mixture expectations, reduced together */
     csum A = {0.0, 0.0};
@@ -280,19 +303,19 @@ static double jsd_row(int64_t V, const double *s, const double *t, double beta, 
         int in_t = t[j] != -INFINITY;
         if (!in_s && !in_t)
             continue;
-        double lp = in_s ? log_prob(&rs, s[j]) : -INFINITY;
-        double lq = in_t ? log_prob(&rt, t[j]) : -INFINITY;
-        double lm = log_mix(lw_s, lp, lw_t, lq);
+        real lp = in_s ? log_prob(&rs, s[j]) : -INFINITY;
+        real lq = in_t ? log_prob(&rt, t[j]) : -INFINITY;
+        real lm = log_mix(lw_s, lp, lw_t, lq);
         if (in_t)
-            csum_add(&A, exp(lq) * (lq - lm));
+            csum_add(&A, REXP(lq) * (lq - lm));
         if (in_s)
-            csum_add(&B, exp(lp) * (lp - lm));
+            csum_add(&B, REXP(lp) * (lp - lm));
     }
-    double a = csum_value(&A);
-    double b = csum_value(&B);
+    real a = csum_value(&A);
+    real b = csum_value(&B);
     *a_out = a;
     *b_out = b;
-    double value = beta * a + (1.0 - beta) * b;
+    real value = beta * a + (1.0 - beta) * b;
 
     for (int64_t j = 0; j < V; ++j) {
         int in_s = s[j] != -INFINITY;
@@ -304,13 +327,13 @@ static double jsd_row(int64_t V, const double *s, const double *t, double beta, 
                 dt[j] = 0.0;
             continue;
         }
-        double lp = in_s ? log_prob(&rs, s[j]) : -INFINITY;
-        double lq = in_t ? log_prob(&rt, t[j]) : -INFINITY;
-        double lm = log_mix(lw_s, lp, lw_t, lq);
+        real lp = in_s ? log_prob(&rs, s[j]) : -INFINITY;
+        real lq = in_t ? log_prob(&rt, t[j]) : -INFINITY;
+        real lm = log_mix(lw_s, lp, lw_t, lq);
         if (ds)
-            ds[j] = in_s ? g * (1.0 - beta) * exp(lp) * (lp - lm - b) : 0.0;
+            ds[j] = in_s ? g * (1.0 - beta) * REXP(lp) * (lp - lm - b) : 0.0;
         if (dt)
-            dt[j] = in_t ? g * beta * exp(lq) * (lq - lm - a) : 0.0;
+            dt[j] = in_t ? g * beta * REXP(lq) * (lq - lm - a) : 0.0;
     }
     return value;
 }
@@ -319,7 +342,7 @@ static double jsd_row(int64_t V, const double *s, const double *t, double beta, 
 /* Entropy of one row ([ops page], "What"):                                    */
 /*   H = - sum_{j in S} p_j ln p_j,   dX_j = -g p_j (ln p_j + H)               */
 /* ------------------------------------------------------------------------- */
-static double entropy_row(int64_t V, const double *x, double g, double *dx)
+static real entropy_row(int64_t V, const double *x, real g, double *dx)
 {
     row_stats r = stats_of(V, x);
     if (r.bad || r.empty) {
@@ -330,18 +353,18 @@ static double entropy_row(int64_t V, const double *x, double g, double *dx)
     for (int64_t j = 0; j < V; ++j) {
         if (x[j] == -INFINITY)
             continue;
-        double lp = log_prob(&r, x[j]);
-        csum_add(&h, -exp(lp) * lp);
+        real lp = log_prob(&r, x[j]);
+        csum_add(&h, -REXP(lp) * lp);
     }
-    double value = csum_value(&h);
+    real value = csum_value(&h);
     if (dx) {
         for (int64_t j = 0; j < V; ++j) {
             if (x[j] == -INFINITY) {
                 dx[j] = 0.0;
                 continue;
             }
-            double lp = log_prob(&r, x[j]);
-            dx[j] = -g * exp(lp) * (lp + value);
+            real lp = log_prob(&r, x[j]);
+            dx[j] = -g * REXP(lp) * (lp + value);
         }
     }
     return value;
@@ -356,7 +379,7 @@ void vpd_oracle_jsd(int64_t N, int64_t V, const double *s, const double *t, doub
                     double *dt)
 {
     for (int64_t r = 0; r < N; ++r) {
-        double a, b;
+        real a, b;
         loss[r] = jsd_row(V, s + r * V, t + r * V, beta, g ? g[r] : 1.0, ds ? ds + r * V : NULL,
                           dt ? dt + r * V : NULL, &a, &b);
         if (kl_tm)
@@ -372,7 +395,7 @@ void vpd_oracle_kl(int64_t N, int64_t V, const double *s, const double *t, int r
                    const double *g, double *loss, double *ds, double *dt)
 {
     for (int64_t r = 0; r < N; ++r) {
-        double gr = g ? g[r] : 1.0;
+        real gr = g ? g[r] : 1.0;
         double *dsr = ds ? ds + r * V : NULL;
         double *dtr = dt ? dt + r * V : NULL;
         if (reverse)
@@ -409,8 +432,8 @@ int64_t vpd_oracle_logprobs(int64_t N, int64_t V, const double *x, int64_t K, co
         zero_row(dxr, V);
         for (int64_t k = 0; k < K; ++k) {
             int64_t i = idx[r * K + k];
-            double gk = g ? g[r * K + k] : 1.0;
-            double v;
+            real gk = g ? g[r * K + k] : 1.0;
+            real v;
             if (i == ignore_index) {
                 out[r * K + k] = 0.0;
                 continue;
@@ -434,11 +457,11 @@ int64_t vpd_oracle_logprobs(int64_t N, int64_t V, const double *x, int64_t K, co
             csum_add(&gsum, gk);
         }
         if (dxr && !undefined) {
-            double gs = csum_value(&gsum);
+            real gs = csum_value(&gsum);
             for (int64_t j = 0; j < V; ++j) {
                 if (xr[j] == -INFINITY)
                     continue;
-                dxr[j] -= exp(log_prob(&st, xr[j])) * gs;
+                dxr[j] -= REXP(log_prob(&st, xr[j])) * gs;
             }
         }
     }

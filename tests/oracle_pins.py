@@ -4,8 +4,9 @@ Each ``pin_*`` function raises AssertionError when the oracle disagrees with a
 fact fixed by the pages or by mathematics: hand-derived closed forms
 (``tests/golden/two_token.json``), identities (JSD of a row with itself is 0,
 disjoint supports give the binary entropy H(beta), 0 <= JSD_beta <= H(beta),
-JSD_beta(s, t) = JSD_{1-beta}(t, s)), shift invariance under a large offset and
-masked-vocabulary equivalence to the reduced vocabulary ('Add
+JSD_beta(s, t) = JSD_{1-beta}(t, s)), the second-order closed form for nearly
+identical rows, shift invariance under a large offset and masked-vocabulary
+equivalence to the reduced vocabulary ('Add
 vocabulary-parallel logprobs, entropy and KL ops', section Tests), +inf KL when
 the target has mass on a masked token (same section), the beta = 0 / 1 branches
 against a library KL ('[VocabTP] Add vocabulary-parallel generalized JSD with
@@ -277,6 +278,31 @@ def pin_finite_differences():
     _, dx, _ = O.logprobs(s_int, idx, -100, gk)
     _fd_check(lambda x: float(np.sum(np.nan_to_num(O.logprobs(x, idx, -100, grad=False)[0]) * gk)), s_int, dx,
               "logprobs")
+
+
+def jsd_second_order(s, t, beta):
+    """The leading term of JSD_beta between softmax(s) and softmax(t) for
+    t = s + eps * d: beta (1 - beta) / 2 * Var_p(t - s), p = softmax(s). It
+    follows from KL(a || b) = 1/2 sum (a - b)^2 / b + O(|a - b|^3) with
+    M = p (1 + beta eps u), q = p (1 + eps u), u = d - E_p d to first order; the
+    relative remainder is O(eps). Computed by a library softmax."""
+    p = special.softmax(s, axis=1)
+    d = t - s
+    mu = np.sum(p * d, axis=1)
+    return 0.5 * beta * (1.0 - beta) * np.sum(p * (d - mu[:, None]) ** 2, axis=1)
+
+
+def pin_jsd_second_order_near_identical_rows():
+    # nearly identical rows: the divergence is a difference of O(eps) terms
+    # that cancel to O(eps^2); the closed form above is exact to O(eps) relative
+    rng = np.random.default_rng(27)
+    s = rng.normal(0, 2, (4, 2048))
+    d = rng.normal(0, 1, (4, 2048))
+    for eps in (1e-3, 1e-4):
+        t = s + eps * d
+        for beta in (0.2, 0.5, 0.7):
+            _close(O.jsd(s, t, beta, grad=False)[0], jsd_second_order(s, t, beta), eps, 0.0,
+                   f"second order beta={beta} eps={eps}")
 
 
 def pin_gradient_rows_sum_to_zero():

@@ -15,22 +15,22 @@ import oracle_pins
 from oracle import oracle as O
 
 MUTANTS = {
-    "mixture weights transposed": ("const double lw_s = log(1.0 - beta);", "const double lw_s = log(beta);"),
-    "dropped (1-beta) in the loss": ("double value = beta * a + (1.0 - beta) * b;", "double value = beta * a + b;"),
+    "mixture weights transposed": ("const real lw_s = RLOG(1.0 - beta);", "const real lw_s = RLOG(beta);"),
+    "dropped (1-beta) in the loss": ("real value = beta * a + (1.0 - beta) * b;", "real value = beta * a + b;"),
     "wrong sign of B in dS": ("(lp - lm - b)", "(lp - lm + b)"),
     "A used in place of B in dS": ("(lp - lm - b)", "(lp - lm - a)"),
-    "operands swapped in KL": ("csum_add(&kl, exp(la) * (la - lb));", "csum_add(&kl, exp(la) * (lb - la));"),
+    "operands swapped in KL": ("csum_add(&kl, REXP(la) * (la - lb));", "csum_add(&kl, REXP(la) * (lb - la));"),
     "forward/reverse branches swapped": ("return kl_row(V, t, s, g, dt, ds);", "return kl_row(V, s, t, g, ds, dt);"),
     "entropy gradient sign": ("(lp + value)", "(lp - value)"),
-    "log-prob gradient sign": ("dxr[j] -= exp(log_prob(&st, xr[j])) * gs;", "dxr[j] += exp(log_prob(&st, xr[j])) * gs;"),
-    "max not subtracted": ("csum_add(&z, exp(v - r.m));", "csum_add(&z, exp(v));"),
+    "log-prob gradient sign": ("dxr[j] -= REXP(log_prob(&st, xr[j])) * gs;", "dxr[j] += REXP(log_prob(&st, xr[j])) * gs;"),
+    "max not subtracted": ("csum_add(&z, REXP(v - r.m));", "csum_add(&z, REXP(v));"),
     "min instead of max": ("if (v > r.m)", "if (v < r.m && r.m != -INFINITY || r.m == -INFINITY)"),
     "KL gradient target index": ("db[j] = g * (b - a);", "db[j] = g * (a - b);"),
-    "teacher weight in dT": ("g * beta * exp(lq)", "g * (1.0 - beta) * exp(lq)"),
+    "teacher weight in dT": ("g * beta * REXP(lq)", "g * (1.0 - beta) * REXP(lq)"),
     "support violation ignored": ("if (xa[j] != -INFINITY && xb[j] == -INFINITY) {",
                                   "if (0 && xa[j] != -INFINITY && xb[j] == -INFINITY) {"),
-    "empty segment not skipped": ("if (!r.empty)\n            csum_add(&z, r.z * exp(r.m - m));",
-                                  "csum_add(&z, r.z * exp(r.m - m));"),
+    "empty segment not skipped": ("if (!r.empty)\n            csum_add(&z, r.z * REXP(r.m - m));",
+                                  "csum_add(&z, r.z * REXP(r.m - m));"),
 }
 
 
