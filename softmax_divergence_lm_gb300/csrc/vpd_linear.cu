@@ -21,7 +21,9 @@
 //           merged statistics (the second of the two passes JSD needs);
 //   kGrad   logits tiles again -> dS and dT of a chunk of rows, each split into
 //           a bf16 high part and a bf16 low part (x = hi + lo to 16 bits of
-//           mantissa) and stored row-major and transposed;
+//           mantissa) and stored row-major and transposed: each epilogue
+//           warp stages 32 x 32 blocks in shared memory in both layouts and
+//           one lane writes them out with TMA tensor stores;
 //   kGemm   a plain C += A B^T over one or two (A, B) operand pairs (used for
 //           dh = dS W and dW = dS^T h from the split gradients, hi and lo as the
 //           two pairs), split along K, accumulated into fp32 C by atomics.
@@ -84,7 +86,11 @@ struct TileShape {
   // M >> 4 at bits 24-28
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((TN >> 3) << 17) | ((BM >> 4) << 24);
 };
-constexpr int kTransWords = 32 * 33;          // per epilogue warp: 32 rows x 32 bf16 pairs (+1 word pad)
+// Gradient pass output blocks: each epilogue warp stages a 32 x 32 bf16 block
+// row-major (rows of 64 bytes, 64-byte swizzle) and the same block transposed
+// (no swizzle) for two tensor stores.
+constexpr int kStoreBlockBytes = 32 * 64;
+constexpr int kStoreWarpBytes = 2 * kStoreBlockBytes;
 constexpr int kTmemCols = 512;
 constexpr float kTinyL = 1e-37f;
 constexpr float kLog2eL = 1.4426950408889634f;
@@ -104,13 +110,19 @@ struct EpiShape {
   static constexpr int kParts = kWarps / 4;
   static constexpr int kThreads = 32 * (2 + kWarps);
 };
-// Dynamic shared memory: the stage ring, the per-warp transpose blocks of the
+// Dynamic shared memory: the stage ring, the per-warp output blocks of the
 // gradient pass, and slack for the 1024-byte alignment.
 template <int TN, int MODE>
 constexpr int smem_bytes() {
   return TileShape<TN>::kStages * TileShape<TN>::kStageBytes +
-         (MODE == kGrad ? EpiShape<MODE>::kWarps * kTransWords * 4 : 0) + 1024;
+         (MODE == kGrad ? EpiShape<MODE>::kWarps * kStoreWarpBytes : 0) + 1024;
 }
+
+// Tensor maps of the gradient pass's outputs, per head: row-major high and low
+// parts, then the transposed high and low parts (boxes of 32 x 32).
+struct StoreMaps {
+  CUtensorMap m[2][4];
+};
 
 static __device__ int g_linear_error = 0;
 
@@ -186,6 +198,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(saddr(bar))
       : "memory");
 }
+// Tensor store of a staged shared-memory box to (x, y) of the map's tensor
+// (the part inside the tensor's bounds), tracked by the issuing thread's bulk groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(saddr(src))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tmem_alloc_all(uint32_t* slot) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(slot)), "n"(kTmemCols)
                : "memory");
@@ -304,14 +328,15 @@ struct __align__(8) Bars {
 template <int TN, int MODE>
 __global__ void __launch_bounds__(EpiShape<MODE>::kThreads, 1)
     k_linear(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap b0,
-             const __grid_constant__ CUtensorMap a1, const __grid_constant__ CUtensorMap b1, Args a) {
+             const __grid_constant__ CUtensorMap a1, const __grid_constant__ CUtensorMap b1, Args a,
+             const __grid_constant__ StoreMaps gm) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Bars bars;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using S = TileShape<TN>;
   using E = EpiShape<MODE>;
   constexpr int kStages = S::kStages, kStageBytes = S::kStageBytes;
-  uint32_t* trans = reinterpret_cast<uint32_t*>(smem + kStages * kStageBytes);  // kGrad transposes
+  uint8_t* oblk = smem + kStages * kStageBytes;  // kGrad output blocks
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort = &bars.abort;
 
@@ -618,12 +643,17 @@ __global__ void __launch_bounds__(EpiShape<MODE>::kThreads, 1)
               gtv[i + 1] = gt.y;
             }
             const int64_t rbase = static_cast<int64_t>(w.mt) * BM + 32 * q;  // this warp's first row
+            // This warp's blocks: lane = row of the row-major block (16-byte
+            // piece j of its 64-byte row at j ^ ((row >> 1) & 3), the 64-byte
+            // swizzle) and column of the transposed one.
+            uint8_t* blk = oblk + (warp - 2) * kStoreWarpBytes;
+            uint4* rmb = reinterpret_cast<uint4*>(blk + lane * 64);
+            unsigned short* tbl = reinterpret_cast<unsigned short*>(blk + kStoreBlockBytes) + lane;
+            const int swz = (lane >> 1) & 3;
 #pragma unroll
             for (int head = 0; head < 2; ++head) {
               const float* gv = head == 0 ? gsv : gtv;
-              __nv_bfloat16* rm[2] = {head == 0 ? a.gs_hi : a.gt_hi, head == 0 ? a.gs_lo : a.gt_lo};
-              __nv_bfloat16* tr[2] = {head == 0 ? a.gst_hi : a.gtt_hi, head == 0 ? a.gst_lo : a.gtt_lo};
-              if (!tr[0]) continue;  // warp-uniform: this head's gradient is not wanted
+              if (!(head == 0 ? a.gst_hi : a.gtt_hi)) continue;  // warp-uniform: this head's gradient is not wanted
               uint32_t part[2][16];  // high and low bf16 parts, packed in pairs
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
@@ -635,50 +665,28 @@ __global__ void __launch_bounds__(EpiShape<MODE>::kThreads, 1)
               }
 #pragma unroll
               for (int hl = 0; hl < 2; ++hl) {
-                // The warp's 32 x 32 block (rows = lanes) goes through shared
-                // memory once; both layouts are then stored with four lanes per
-                // 64-byte run, eight runs per instruction.
-                uint32_t* tb = trans + (warp - 2) * kTransWords;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) tb[lane * 33 + i] = part[hl][i];
+                // the blocks are free once the previous stores have read them
+                if (lane == 0) bulk_wait_read_all();
                 __syncwarp();
-                const int piece = lane & 3;  // which 16 bytes of a 64-byte run
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  const int r8 = 8 * k + (lane >> 2);  // block row (row-major) or block column (transposed)
-                  // row-major [rows, V]: row r8 of the block, columns 8 piece .. 8 piece + 7
-                  const int64_t grow = rbase + r8;
-                  if (grow < a.rows) {
-                    const uint32_t* src = tb + r8 * 33 + 4 * piece;
-                    __nv_bfloat16* dst = rm[hl] + grow * a.cols + col0 + c + 8 * piece;
-                    if (8 * piece + 8 <= nvalid) {
-                      *reinterpret_cast<uint4*>(dst) = make_uint4(src[0], src[1], src[2], src[3]);
-                    } else {
+                for (int j = 0; j < 4; ++j)
+                  rmb[j ^ swz] = make_uint4(part[hl][4 * j], part[hl][4 * j + 1], part[hl][4 * j + 2], part[hl][4 * j + 3]);
 #pragma unroll
-                      for (int e = 0; e < 8; ++e) {
-                        if (8 * piece + e >= nvalid) continue;
-                        const uint32_t w2 = src[e >> 1];
-                        reinterpret_cast<unsigned short*>(dst)[e] =
-                            static_cast<unsigned short>((e & 1) ? (w2 >> 16) : (w2 & 0xffffu));
-                      }
-                    }
-                  }
-                  // transposed [V, ld_t]: column r8 of the block, rows 8 piece .. 8 piece + 7
-                  if (r8 < nvalid) {
-                    uint32_t v[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                      const uint32_t w0 = tb[(8 * piece + 2 * e) * 33 + (r8 >> 1)];
-                      const uint32_t w1 = tb[(8 * piece + 2 * e + 1) * 33 + (r8 >> 1)];
-                      const uint32_t b0 = (r8 & 1) ? (w0 >> 16) : (w0 & 0xffffu);
-                      const uint32_t b1 = (r8 & 1) ? (w1 >> 16) : (w1 & 0xffffu);
-                      v[e] = b0 | (b1 << 16);
-                    }
-                    __nv_bfloat16* dst = tr[hl] + (col0 + c + r8) * a.ld_t + rbase + 8 * piece;
-                    *reinterpret_cast<uint4*>(dst) = make_uint4(v[0], v[1], v[2], v[3]);
-                  }
+                for (int i = 0; i < 16; ++i) {
+                  tbl[(2 * i) * 32] = static_cast<unsigned short>(part[hl][i] & 0xffffu);
+                  tbl[(2 * i + 1) * 32] = static_cast<unsigned short>(part[hl][i] >> 16);
                 }
+                fence_async_shared();
                 __syncwarp();
+                // row-major [rows, V] at (column col0 + c, row rbase); transposed
+                // [V, rows rounded to the tile] at (row rbase, column col0 + c).
+                // The maps clip the block to the rows and columns that exist.
+                if (lane == 0 && nvalid > 0) {
+                  if (rbase < a.rows) tma_store_2d(&gm.m[head][hl], blk, static_cast<int>(col0 + c), static_cast<int>(rbase));
+                  tma_store_2d(&gm.m[head][2 + hl], blk + kStoreBlockBytes, static_cast<int>(rbase),
+                               static_cast<int>(col0 + c));
+                  bulk_commit();
+                }
               }
             }
           }
@@ -702,6 +710,8 @@ __global__ void __launch_bounds__(EpiShape<MODE>::kThreads, 1)
       }
     }
     if (!ok) bars.abort = 1;
+    // the output blocks' tensor stores finish before the shared memory goes
+    if (MODE == kGrad && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -832,11 +842,27 @@ cudaError_t make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t k, 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Map of a bf16 output [outer, inner] (row pitch `pitch` elements) for tensor
+// stores of 32 x 32 boxes, with the 64-byte swizzle or none.
+cudaError_t make_store_map(CUtensorMap* m, void* base, int64_t inner, int64_t outer, int64_t pitch, bool swizzle64) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) || (pitch * 2) % 16) return cudaErrorInvalidValue;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch * 2)};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // k_linear with TN-column tiles (the B maps' boxes must be TN rows high) in
 // mode MODE (args.mode must be MODE).
 template <int TN, int MODE>
 cudaError_t launch(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1, const CUtensorMap& b1,
-                   const Args& args, cudaStream_t stream) {
+                   const Args& args, cudaStream_t stream, const StoreMaps* gm = nullptr) {
   using E = EpiShape<MODE>;
   static_assert(smem_bytes<TN, MODE>() <= 232448, "dynamic shared memory above the 227 KB a CTA may take");
   if (args.units <= 0) return cudaSuccess;
@@ -849,7 +875,10 @@ cudaError_t launch(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorM
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t grid = args.units < sm_count() ? args.units : sm_count();
-  k_linear<TN, MODE><<<static_cast<unsigned>(grid), E::kThreads, smem_bytes<TN, MODE>(), stream>>>(a0, b0, a1, b1, args);
+  if (MODE == kGrad && !gm) return cudaErrorInvalidValue;
+  static const StoreMaps none{};
+  k_linear<TN, MODE><<<static_cast<unsigned>(grid), E::kThreads, smem_bytes<TN, MODE>(), stream>>>(a0, b0, a1, b1, args,
+                                                                                                   gm ? *gm : none);
   note_launch();
   return cudaGetLastError();
 }
@@ -1091,7 +1120,18 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
       a.gtt_hi = G[1][2];
       a.gtt_lo = G[1][3];
     }
-    if ((e = launch<kGradTN, kGrad>(hsm, wsm, htm, wtm, a, stream)) != cudaSuccess) return e;
+    // the gradient blocks' tensor stores: row-major [n, V]; transposed
+    // [V, row tiles x 128] (the rows past n of the last tile get zeros)
+    StoreMaps gm{};
+    for (int x = 0; x < 2; ++x) {
+      if (!want[x]) continue;
+      for (int hl = 0; hl < 2; ++hl) {
+        if ((e = make_store_map(&gm.m[x][hl], G[x][hl], p.vocab, n, p.vocab, true)) != cudaSuccess) return e;
+        if ((e = make_store_map(&gm.m[x][2 + hl], G[x][2 + hl], cdiv(n, BM) * BM, p.vocab, nc, false)) != cudaSuccess)
+          return e;
+      }
+    }
+    if ((e = launch<kGradTN, kGrad>(hsm, wsm, htm, wtm, a, stream, &gm)) != cudaSuccess) return e;
     for (int x = 0; x < 2; ++x) {
       if (!want[x]) continue;
       // dh[r0:r0+n] += G_hi W + G_lo W  (K = V; B = W^T [H, V])
