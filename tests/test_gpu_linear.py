@@ -137,6 +137,15 @@ def test_linear_detached_teacher_and_chunks(B):
     check(B, h_s, w_s, h_t, w_t, 0.5, "chunks", teacher=False)
 
 
+def test_linear_teacher_gradients_only(B):
+    """Only the teacher head's gradients wanted (the student's skipped in the
+    gradient pass), a row count that leaves a partial warp block and whole
+    warps past the rows in the last row tile, a ragged last vocabulary tile."""
+    from softmax_divergence_lm_gb300 import synth
+    h_s, w_s, h_t, w_t = synth.linear_heads(device="cuda", n=200, v=648, hidden_s=64, hidden_t=128, seed=15)
+    check(B, h_s, w_s, h_t, w_t, 0.3, "teacher only", student=False)
+
+
 def test_linear_identical_heads(B):
     """The same head and hidden states on both sides: JSD 0 up to the logit
     rounding, gradients 0 up to it."""
