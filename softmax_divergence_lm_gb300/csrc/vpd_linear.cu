@@ -21,12 +21,13 @@
 //           merged statistics (the second of the two passes JSD needs);
 //   kGrad   logits tiles again -> dS and dT of a chunk of rows, each split into
 //           a bf16 high part and a bf16 low part (x = hi + lo to 16 bits of
-//           mantissa) and stored row-major and transposed: each epilogue
-//           warp stages 32 x 32 blocks in shared memory in both layouts and
-//           one lane writes them out with TMA tensor stores;
+//           mantissa) and stored row-major: each epilogue warp stages 32 x 32
+//           blocks in shared memory and one lane writes them out with TMA
+//           tensor stores;
 //   kGemm   a plain C += A B^T over one or two (A, B) operand pairs (used for
 //           dh = dS W and dW = dS^T h from the split gradients, hi and lo as the
-//           two pairs), split along K, accumulated into fp32 C by atomics.
+//           two pairs; for dW the A operand is the same row-major dS, read
+//           MN-major), split along K, accumulated into fp32 C by atomics.
 // Small kernels merge the per-chunk partials and transpose bf16 matrices.
 //
 // Warp roles of k_linear (one instantiation per mode): warp 0 issues the TMA
@@ -87,10 +88,9 @@ struct TileShape {
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((TN >> 3) << 17) | ((BM >> 4) << 24);
 };
 // Gradient pass output blocks: each epilogue warp stages a 32 x 32 bf16 block
-// row-major (rows of 64 bytes, 64-byte swizzle) and the same block transposed
-// (no swizzle) for two tensor stores.
+// row-major (rows of 64 bytes, 64-byte swizzle) for one tensor store.
 constexpr int kStoreBlockBytes = 32 * 64;
-constexpr int kStoreWarpBytes = 2 * kStoreBlockBytes;
+constexpr int kStoreWarpBytes = kStoreBlockBytes;
 constexpr int kTmemCols = 512;
 constexpr float kTinyL = 1e-37f;
 constexpr float kLog2eL = 1.4426950408889634f;
@@ -118,10 +118,10 @@ constexpr int smem_bytes() {
          (MODE == kGrad ? EpiShape<MODE>::kWarps * kStoreWarpBytes : 0) + 1024;
 }
 
-// Tensor maps of the gradient pass's outputs, per head: row-major high and low
-// parts, then the transposed high and low parts (boxes of 32 x 32).
+// Tensor maps of the gradient pass's outputs, per head: the row-major high and
+// low parts (boxes of 32 x 32).
 struct StoreMaps {
-  CUtensorMap m[2][4];
+  CUtensorMap m[2][2];
 };
 
 static __device__ int g_linear_error = 0;
@@ -142,14 +142,14 @@ struct Args {
   const float* loss;       // [rows] (kGrad, endpoint branches)
   const float* grad_loss;  // [rows] or NULL (kGrad)
   float* part;             // [chunks, rows, 4] (kStats) / [chunks, rows, 2] (kDiv)
-  // kGrad outputs, chunk-local: row-major [rows, cols] and transposed [cols, ld_t]
-  __nv_bfloat16 *gs_hi, *gs_lo, *gst_hi, *gst_lo;
-  __nv_bfloat16 *gt_hi, *gt_lo, *gtt_hi, *gtt_lo;
-  int64_t ld_t;
+  // kGrad outputs, chunk-local, row-major [rows, cols] (NULL: head not wanted)
+  __nv_bfloat16 *gs_hi, *gs_lo;
+  __nv_bfloat16 *gt_hi, *gt_lo;
   // kGemm output
   float* C;
   int64_t ldc;
   int gemm_store;  // 1: C = the product (one k part, nothing to add to); 0: C += by atomics
+  int a_mn;        // kGemm: the A operands are stored [K, M] (M contiguous) and read MN-major
 };
 
 // ---------------------------------------------------------------------------
@@ -231,6 +231,27 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
   return d;
+}
+// The same for an MN-major bf16 tile written by two TMA boxes of {64, 64}
+// with the 128-byte swizzle: rows of 128 bytes hold 64 consecutive M (or N)
+// elements, one row per k; 8-row k groups 1024 bytes apart (stride byte
+// offset), the second 64 elements of M 8192 bytes on (leading byte offset).
+__device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t addr) {
+  uint64_t d = static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(8192u >> 4) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+__device__ __forceinline__ void mma_bf16_rt(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 template <uint32_t kIdesc>
 __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t accumulate) {
@@ -381,7 +402,12 @@ __global__ void __launch_bounds__(EpiShape<MODE>::kThreads, 1)
             const int kk = second ? kb - a.nk0 : kb;
             uint8_t* sa = smem + stage * kStageBytes;
             mb_expect_tx(&bars.full[stage], kStageBytes);
-            tma_load_2d(sa, second ? &a1 : &a0, kk * BK, w.mt * BM, &bars.full[stage]);
+            if (gemm && a.a_mn) {  // A stored [K, M]: two boxes of 64 M x 64 k
+              tma_load_2d(sa, second ? &a1 : &a0, w.mt * BM, kk * BK, &bars.full[stage]);
+              tma_load_2d(sa + kTileBytes / 2, second ? &a1 : &a0, w.mt * BM + 64, kk * BK, &bars.full[stage]);
+            } else {
+              tma_load_2d(sa, second ? &a1 : &a0, kk * BK, w.mt * BM, &bars.full[stage]);
+            }
             tma_load_2d(sa + kTileBytes, second ? &b1 : &b0, kk * BK, nt * TN, &bars.full[stage]);
             if (++stage == kStages) {
               stage = 0;
@@ -430,10 +456,20 @@ __global__ void __launch_bounds__(EpiShape<MODE>::kThreads, 1)
             // accumulate unless this is the first k-block into this accumulator
             const bool first = (gemm || split) ? kb == kbs : (second ? kb == a.nk0 : kb == 0);
             const uint32_t sa = saddr(smem + stage * kStageBytes);
-            const uint64_t da = sw128_desc(sa), db = sw128_desc(sa + kTileBytes);
+            const uint64_t db = sw128_desc(sa + kTileBytes);
+            if (gemm && a.a_mn) {
+              // A MN-major (transpose-A bit 15): 16 k per MMA = two 8-row groups,
+              // 2048 bytes: +128 in the address field
+              const uint64_t da = sw128_mn_desc(sa);
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k)  // 16 bf16 = 32 bytes per MMA: +2 in the address field
-              mma_bf16<S::kIdesc>(dst, da + 2u * k, db + 2u * k, (first && k == 0) ? 0u : 1u);
+              for (int k = 0; k < BK / 16; ++k)
+                mma_bf16_rt(dst, da + 128u * k, db + 2u * k, S::kIdesc | (1u << 15), (first && k == 0) ? 0u : 1u);
+            } else {
+              const uint64_t da = sw128_desc(sa);
+#pragma unroll
+              for (int k = 0; k < BK / 16; ++k)  // 16 bf16 = 32 bytes per MMA: +2 in the address field
+                mma_bf16<S::kIdesc>(dst, da + 2u * k, db + 2u * k, (first && k == 0) ? 0u : 1u);
+            }
             mma_commit(&bars.empty[stage]);
             if (++stage == kStages) {
               stage = 0;
@@ -608,7 +644,7 @@ __global__ void __launch_bounds__(EpiShape<MODE>::kThreads, 1)
             // dS and dT of this thread's row for 32 columns (0 past the
             // chunk's rows: the transposed arrays are summed over rows)
             float gsv[32], gtv[32];
-            const bool want_t = a.gtt_hi != nullptr;  // warp-uniform: dT wanted
+            const bool want_t = a.gt_hi != nullptr;  // warp-uniform: dT wanted
             const float2 nms2 = pk(nms, nms), nmt2 = pk(nmt, nmt), nKs2 = pk(nKs, nKs), nKt2 = pk(nKt, nKt);
             const float2 l2e2 = pk(kLog2eL, kLog2eL), ws2 = pk(1.f - beta, 1.f - beta), wt2 = pk(beta, beta);
             const float2 tiny2 = pk(kTinyL, kTinyL), cs2 = pk(cs, cs), ct2 = pk(ct, ct);
@@ -643,17 +679,17 @@ __global__ void __launch_bounds__(EpiShape<MODE>::kThreads, 1)
               gtv[i + 1] = gt.y;
             }
             const int64_t rbase = static_cast<int64_t>(w.mt) * BM + 32 * q;  // this warp's first row
-            // This warp's blocks: lane = row of the row-major block (16-byte
-            // piece j of its 64-byte row at j ^ ((row >> 1) & 3), the 64-byte
-            // swizzle) and column of the transposed one.
+            // This warp's block: lane = its row (16-byte piece j of the 64-byte
+            // row at j ^ ((row >> 1) & 3), the 64-byte swizzle).
             uint8_t* blk = oblk + (warp - 2) * kStoreWarpBytes;
             uint4* rmb = reinterpret_cast<uint4*>(blk + lane * 64);
-            unsigned short* tbl = reinterpret_cast<unsigned short*>(blk + kStoreBlockBytes) + lane;
             const int swz = (lane >> 1) & 3;
+            // warp-uniform: nothing to store past the chunk's rows or the vocabulary
+            const bool store = rbase < a.rows && nvalid > 0;
 #pragma unroll
             for (int head = 0; head < 2; ++head) {
               const float* gv = head == 0 ? gsv : gtv;
-              if (!(head == 0 ? a.gst_hi : a.gtt_hi)) continue;  // warp-uniform: this head's gradient is not wanted
+              if (!(head == 0 ? a.gs_hi : a.gt_hi) || !store) continue;  // warp-uniform
               uint32_t part[2][16];  // high and low bf16 parts, packed in pairs
 #pragma unroll
               for (int i = 0; i < 16; ++i) {
@@ -665,26 +701,18 @@ __global__ void __launch_bounds__(EpiShape<MODE>::kThreads, 1)
               }
 #pragma unroll
               for (int hl = 0; hl < 2; ++hl) {
-                // the blocks are free once the previous stores have read them
+                // the block is free once the previous store has read it
                 if (lane == 0) bulk_wait_read_all();
                 __syncwarp();
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                   rmb[j ^ swz] = make_uint4(part[hl][4 * j], part[hl][4 * j + 1], part[hl][4 * j + 2], part[hl][4 * j + 3]);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                  tbl[(2 * i) * 32] = static_cast<unsigned short>(part[hl][i] & 0xffffu);
-                  tbl[(2 * i + 1) * 32] = static_cast<unsigned short>(part[hl][i] >> 16);
-                }
                 fence_async_shared();
                 __syncwarp();
-                // row-major [rows, V] at (column col0 + c, row rbase); transposed
-                // [V, rows rounded to the tile] at (row rbase, column col0 + c).
-                // The maps clip the block to the rows and columns that exist.
-                if (lane == 0 && nvalid > 0) {
-                  if (rbase < a.rows) tma_store_2d(&gm.m[head][hl], blk, static_cast<int>(col0 + c), static_cast<int>(rbase));
-                  tma_store_2d(&gm.m[head][2 + hl], blk + kStoreBlockBytes, static_cast<int>(rbase),
-                               static_cast<int>(col0 + c));
+                // [rows, V] at (column col0 + c, row rbase); the map clips the
+                // block to the rows and columns that exist
+                if (lane == 0) {
+                  tma_store_2d(&gm.m[head][hl], blk, static_cast<int>(col0 + c), static_cast<int>(rbase));
                   bulk_commit();
                 }
               }
@@ -952,8 +980,8 @@ size_t linear_bwd_workspace(int64_t rows, int64_t vocab, int64_t hs, int64_t ht,
   const int64_t nc = rows < chunk_rows ? cdiv(rows, BM) * BM : chunk_rows;
   size_t b = 0;
   const size_t g = static_cast<size_t>(nc) * static_cast<size_t>(vocab) * 2u;  // one bf16 [nc, V]
-  if (student) b += 4 * g + static_cast<size_t>(hs) * vocab * 2u + static_cast<size_t>(hs) * nc * 2u;
-  if (teacher) b += 4 * g + static_cast<size_t>(ht) * vocab * 2u + static_cast<size_t>(ht) * nc * 2u;
+  if (student) b += 2 * g + static_cast<size_t>(hs) * vocab * 2u + static_cast<size_t>(hs) * nc * 2u;
+  if (teacher) b += 2 * g + static_cast<size_t>(ht) * vocab * 2u + static_cast<size_t>(ht) * nc * 2u;
   return b + 1024;
 }
 
@@ -1018,11 +1046,17 @@ cudaError_t transpose_bf16(const void* in, int64_t rows, int64_t cols, int64_t l
 // B [n, k]), split along k so that the units spread evenly over the SMs; with
 // may_store (C holds nothing yet) and a single k part, C = the product.
 cudaError_t gemm_acc(const void* a0p, const void* a1p, int64_t lda, const void* bp, int64_t ldb, int64_t rows,
-                     int64_t n, int64_t k, float* C, int64_t ldc, bool may_store, cudaStream_t stream) {
+                     int64_t n, int64_t k, float* C, int64_t ldc, bool may_store, cudaStream_t stream,
+                     bool a_mn) {
   CUtensorMap a0, a1, b0;
   cudaError_t e;
-  if ((e = make_map(&a0, a0p, rows, k, lda)) != cudaSuccess) return e;
-  if ((e = make_map(&a1, a1p, rows, k, lda)) != cudaSuccess) return e;
+  if (a_mn) {  // A stored [k, rows] with row pitch lda, read in boxes of 64 rows x 64 k
+    if ((e = make_map(&a0, a0p, k, rows, lda, 64)) != cudaSuccess) return e;
+    if ((e = make_map(&a1, a1p, k, rows, lda, 64)) != cudaSuccess) return e;
+  } else {
+    if ((e = make_map(&a0, a0p, rows, k, lda)) != cudaSuccess) return e;
+    if ((e = make_map(&a1, a1p, rows, k, lda)) != cudaSuccess) return e;
+  }
   if ((e = make_map(&b0, bp, n, k, ldb, BN)) != cudaSuccess) return e;
   Args a{};
   a.mode = kGemm;
@@ -1039,6 +1073,7 @@ cudaError_t gemm_acc(const void* a0p, const void* a1p, int64_t lda, const void* 
   a.ldc = ldc;
   // one k part per tile and nothing in C to add to: plain stores
   a.gemm_store = may_store && ks == 1 ? 1 : 0;
+  a.a_mn = a_mn ? 1 : 0;
   return launch<BN, kGemm>(a0, b0, a1, b0, a, stream);
 }
 
@@ -1050,7 +1085,7 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
   const int64_t nc = p.rows < chunk_rows ? cdiv(p.rows, BM) * BM : chunk_rows;
   if (ws_bytes < linear_bwd_workspace(p.rows, p.vocab, p.hs, p.ht, student, teacher, chunk_rows))
     return cudaErrorInvalidValue;
-  // workspace: per head [hi, lo, hi^T, lo^T] gradients of one chunk, the head
+  // workspace: per head the [hi, lo] gradients of one chunk, row-major, the head
   // weight transposed [H, V], the chunk's hidden states transposed [H, nc]
   uint8_t* w = static_cast<uint8_t*>(ws);
   const size_t g = align256(static_cast<size_t>(nc) * p.vocab * 2u);
@@ -1059,7 +1094,7 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
     w += align256(bytes);
     return r;
   };
-  __nv_bfloat16* G[2][4] = {};
+  __nv_bfloat16* G[2][2] = {};
   void* wT[2] = {nullptr, nullptr};
   void* hT[2] = {nullptr, nullptr};
   const int64_t H[2] = {p.hs, p.ht};
@@ -1073,7 +1108,7 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
   cudaError_t e;
   for (int x = 0; x < 2; ++x) {
     if (!want[x]) continue;
-    for (int i = 0; i < 4; ++i) G[x][i] = reinterpret_cast<__nv_bfloat16*>(take(g));
+    for (int i = 0; i < 2; ++i) G[x][i] = reinterpret_cast<__nv_bfloat16*>(take(g));
     wT[x] = take(static_cast<size_t>(H[x]) * p.vocab * 2u);
     hT[x] = take(static_cast<size_t>(H[x]) * nc * 2u);
     // dh and dW accumulate by atomics: start from zero
@@ -1107,29 +1142,21 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
     a.saved = saved + r0 * 6;
     a.loss = loss + r0;
     a.grad_loss = grad_loss ? grad_loss + r0 : nullptr;
-    a.ld_t = nc;
+    // row-major only: dW reads the same arrays MN-major
     if (student) {
       a.gs_hi = G[0][0];
       a.gs_lo = G[0][1];
-      a.gst_hi = G[0][2];
-      a.gst_lo = G[0][3];
     }
     if (teacher) {
       a.gt_hi = G[1][0];
       a.gt_lo = G[1][1];
-      a.gtt_hi = G[1][2];
-      a.gtt_lo = G[1][3];
     }
-    // the gradient blocks' tensor stores: row-major [n, V]; transposed
-    // [V, row tiles x 128] (the rows past n of the last tile get zeros)
+    // the gradient blocks' tensor stores, row-major [n, V]
     StoreMaps gm{};
     for (int x = 0; x < 2; ++x) {
       if (!want[x]) continue;
-      for (int hl = 0; hl < 2; ++hl) {
+      for (int hl = 0; hl < 2; ++hl)
         if ((e = make_store_map(&gm.m[x][hl], G[x][hl], p.vocab, n, p.vocab, true)) != cudaSuccess) return e;
-        if ((e = make_store_map(&gm.m[x][2 + hl], G[x][2 + hl], cdiv(n, BM) * BM, p.vocab, nc, false)) != cudaSuccess)
-          return e;
-      }
     }
     if ((e = launch<kGradTN, kGrad>(hsm, wsm, htm, wtm, a, stream, &gm)) != cudaSuccess) return e;
     for (int x = 0; x < 2; ++x) {
@@ -1137,18 +1164,15 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
       // dh[r0:r0+n] += G_hi W + G_lo W  (K = V; B = W^T [H, V])
       if (dh[x] &&
           (e = gemm_acc(G[x][0], G[x][1], p.vocab, wT[x], p.vocab, n, H[x], p.vocab, dh[x] + r0 * H[x], H[x],
-                        true, stream)) != cudaSuccess)
+                        true, stream, false)) != cudaSuccess)
         return e;
-      // dW += G_hi^T h + G_lo^T h  (K = chunk rows; A = G^T [V, nc], B = h^T [H, nc])
+      // dW += G_hi^T h + G_lo^T h  (K = the chunk's n rows; A = G [n, V] read
+      // MN-major, B = h^T [H, nc]; the maps end K at n, the loads fill zeros past it)
       if (dw[x]) {
         const void* h0 = static_cast<const char*>(hp[x]) + r0 * ldh[x] * 2;
         if ((e = transpose_bf16(h0, n, H[x], ldh[x], hT[x], nc, stream)) != cudaSuccess) return e;
-        if (n < nc &&
-            (e = cudaMemset2DAsync(static_cast<char*>(hT[x]) + n * 2, nc * 2, 0, (nc - n) * 2, H[x], stream)) !=
-                cudaSuccess)
-          return e;
-        if ((e = gemm_acc(G[x][2], G[x][3], nc, hT[x], nc, p.vocab, H[x], nc, dw[x], H[x], r0 == 0, stream)) !=
-            cudaSuccess)
+        if ((e = gemm_acc(G[x][0], G[x][1], p.vocab, hT[x], nc, p.vocab, H[x], n, dw[x], H[x], r0 == 0, stream,
+                          true)) != cudaSuccess)
           return e;
       }
     }
