@@ -130,10 +130,10 @@ def test_linear_small_every_row(B, beta):
 
 
 def test_linear_detached_teacher_and_chunks(B):
-    """More rows than one backward chunk (1024): two chunks, the second ragged;
-    teacher gradients not wanted."""
+    """More rows than one backward chunk (8192): two chunks, the second ragged
+    (300 rows), dW accumulated over both; teacher gradients not wanted."""
     from softmax_divergence_lm_gb300 import synth
-    h_s, w_s, h_t, w_t = synth.linear_heads(device="cuda", n=1300, v=504, hidden_s=64, hidden_t=128, seed=12)
+    h_s, w_s, h_t, w_t = synth.linear_heads(device="cuda", n=8192 + 300, v=504, hidden_s=64, hidden_t=128, seed=12)
     check(B, h_s, w_s, h_t, w_t, 0.5, "chunks", teacher=False)
 
 
