@@ -28,7 +28,7 @@
 //           dh = dS W and dW = dS^T h from the split gradients, hi and lo as the
 //           two pairs; for dW the A operand is the same row-major dS, read
 //           MN-major), split along K, accumulated into fp32 C by atomics.
-// Small kernels merge the per-chunk partials and transpose bf16 matrices.
+// Small kernels merge the per-chunk partials.
 //
 // Warp roles of k_linear (one instantiation per mode): warp 0 issues the TMA
 // loads into a ring of shared-memory stages; warp 1 issues the MMAs (one
@@ -150,6 +150,7 @@ struct Args {
   int64_t ldc;
   int gemm_store;  // 1: C = the product (one k part, nothing to add to); 0: C += by atomics
   int a_mn;        // kGemm: the A operands are stored [K, M] (M contiguous) and read MN-major
+  int b_mn;        // kGemm: the B operand is stored [K, N] (N contiguous) and read MN-major
 };
 
 // ---------------------------------------------------------------------------
@@ -408,7 +409,14 @@ __global__ void __launch_bounds__(EpiShape<MODE>::kThreads, 1)
             } else {
               tma_load_2d(sa, second ? &a1 : &a0, kk * BK, w.mt * BM, &bars.full[stage]);
             }
-            tma_load_2d(sa + kTileBytes, second ? &b1 : &b0, kk * BK, nt * TN, &bars.full[stage]);
+            if (gemm && a.b_mn) {  // B stored [K, N]: TN / 64 boxes of 64 N x 64 k
+#pragma unroll
+              for (int i = 0; i < TN / 64; ++i)
+                tma_load_2d(sa + kTileBytes + i * (kTileBytes / 2), second ? &b1 : &b0, nt * TN + 64 * i, kk * BK,
+                            &bars.full[stage]);
+            } else {
+              tma_load_2d(sa + kTileBytes, second ? &b1 : &b0, kk * BK, nt * TN, &bars.full[stage]);
+            }
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
@@ -456,15 +464,19 @@ __global__ void __launch_bounds__(EpiShape<MODE>::kThreads, 1)
             // accumulate unless this is the first k-block into this accumulator
             const bool first = (gemm || split) ? kb == kbs : (second ? kb == a.nk0 : kb == 0);
             const uint32_t sa = saddr(smem + stage * kStageBytes);
-            const uint64_t db = sw128_desc(sa + kTileBytes);
-            if (gemm && a.a_mn) {
-              // A MN-major (transpose-A bit 15): 16 k per MMA = two 8-row groups,
-              // 2048 bytes: +128 in the address field
-              const uint64_t da = sw128_mn_desc(sa);
+            if (gemm && (a.a_mn || a.b_mn)) {
+              // an MN-major operand (transpose bit 15 for A, 16 for B): 16 k per
+              // MMA = two 8-row groups, 2048 bytes: +128 in the address field
+              // (a K-major one: 32 bytes, +2)
+              const uint64_t da = a.a_mn ? sw128_mn_desc(sa) : sw128_desc(sa);
+              const uint64_t db = a.b_mn ? sw128_mn_desc(sa + kTileBytes) : sw128_desc(sa + kTileBytes);
+              const uint32_t sta = a.a_mn ? 128u : 2u, stb = a.b_mn ? 128u : 2u;
+              const uint32_t idesc = S::kIdesc | (a.a_mn ? 1u << 15 : 0u) | (a.b_mn ? 1u << 16 : 0u);
 #pragma unroll
               for (int k = 0; k < BK / 16; ++k)
-                mma_bf16_rt(dst, da + 128u * k, db + 2u * k, S::kIdesc | (1u << 15), (first && k == 0) ? 0u : 1u);
+                mma_bf16_rt(dst, da + sta * k, db + stb * k, idesc, (first && k == 0) ? 0u : 1u);
             } else {
+              const uint64_t db = sw128_desc(sa + kTileBytes);
               const uint64_t da = sw128_desc(sa);
 #pragma unroll
               for (int k = 0; k < BK / 16; ++k)  // 16 bf16 = 32 bytes per MMA: +2 in the address field
@@ -641,8 +653,8 @@ __global__ void __launch_bounds__(EpiShape<MODE>::kThreads, 1)
             accA += accA2.x + accA2.y;
             accB += accB2.x + accB2.y;
           } else {  // kGrad
-            // dS and dT of this thread's row for 32 columns (0 past the
-            // chunk's rows: the transposed arrays are summed over rows)
+            // dS and dT of this thread's row for 32 columns (0 on rows that
+            // carry no value; rows past the chunk are not stored)
             float gsv[32], gtv[32];
             const bool want_t = a.gt_hi != nullptr;  // warp-uniform: dT wanted
             const float2 nms2 = pk(nms, nms), nmt2 = pk(nmt, nmt), nKs2 = pk(nKs, nKs), nKt2 = pk(nKt, nKt);
@@ -819,22 +831,6 @@ __global__ void k_linear_merge_div(const float2* part, int chunks, int64_t rows,
   loss[r] = value;
 }
 
-// out[c, r] = in[r, c] for a bf16 [rows, cols] matrix (32 x 32 tiles through
-// shared memory; rows and cols of the output are those of the transposed view).
-__global__ void k_transpose_bf16(const __nv_bfloat16* in, int64_t rows, int64_t cols, int64_t ld_in,
-                                 __nv_bfloat16* out, int64_t ld_out) {
-  __shared__ __nv_bfloat16 tile[32][33];
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32, c0 = static_cast<int64_t>(blockIdx.x) * 32;
-  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-    const int64_t r = r0 + i, c = c0 + threadIdx.x;
-    if (r < rows && c < cols) tile[i][threadIdx.x] = in[r * ld_in + c];
-  }
-  __syncthreads();
-  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-    const int64_t c = c0 + i, r = r0 + threadIdx.x;
-    if (r < rows && c < cols) out[c * ld_out + r] = tile[threadIdx.x][i];
-  }
-}
 
 // ---------------------------------------------------------------------------
 // Host side
@@ -980,8 +976,8 @@ size_t linear_bwd_workspace(int64_t rows, int64_t vocab, int64_t hs, int64_t ht,
   const int64_t nc = rows < chunk_rows ? cdiv(rows, BM) * BM : chunk_rows;
   size_t b = 0;
   const size_t g = static_cast<size_t>(nc) * static_cast<size_t>(vocab) * 2u;  // one bf16 [nc, V]
-  if (student) b += 2 * g + static_cast<size_t>(hs) * vocab * 2u + static_cast<size_t>(hs) * nc * 2u;
-  if (teacher) b += 2 * g + static_cast<size_t>(ht) * vocab * 2u + static_cast<size_t>(ht) * nc * 2u;
+  if (student) b += 2 * g;
+  if (teacher) b += 2 * g;
   return b + 1024;
 }
 
@@ -1032,22 +1028,13 @@ cudaError_t linear_jsd_forward(const LinearProblem& p, float* loss, float* saved
   return cudaGetLastError();
 }
 
-cudaError_t transpose_bf16(const void* in, int64_t rows, int64_t cols, int64_t ld_in, void* out, int64_t ld_out,
-                           cudaStream_t stream) {
-  if (rows <= 0 || cols <= 0) return cudaSuccess;
-  dim3 grid(static_cast<unsigned>(cdiv(cols, 32)), static_cast<unsigned>(cdiv(rows, 32)));
-  k_transpose_bf16<<<grid, dim3(32, 8), 0, stream>>>(static_cast<const __nv_bfloat16*>(in), rows, cols, ld_in,
-                                                       static_cast<__nv_bfloat16*>(out), ld_out);
-  note_launch();
-  return cudaGetLastError();
-}
 
 // C[rows, n] += A0 B0^T + A1 B1^T with K-major bf16 operands (A [rows, k],
 // B [n, k]), split along k so that the units spread evenly over the SMs; with
 // may_store (C holds nothing yet) and a single k part, C = the product.
 cudaError_t gemm_acc(const void* a0p, const void* a1p, int64_t lda, const void* bp, int64_t ldb, int64_t rows,
                      int64_t n, int64_t k, float* C, int64_t ldc, bool may_store, cudaStream_t stream,
-                     bool a_mn) {
+                     bool a_mn, bool b_mn) {
   CUtensorMap a0, a1, b0;
   cudaError_t e;
   if (a_mn) {  // A stored [k, rows] with row pitch lda, read in boxes of 64 rows x 64 k
@@ -1057,7 +1044,11 @@ cudaError_t gemm_acc(const void* a0p, const void* a1p, int64_t lda, const void* 
     if ((e = make_map(&a0, a0p, rows, k, lda)) != cudaSuccess) return e;
     if ((e = make_map(&a1, a1p, rows, k, lda)) != cudaSuccess) return e;
   }
-  if ((e = make_map(&b0, bp, n, k, ldb, BN)) != cudaSuccess) return e;
+  if (b_mn) {  // B stored [k, n] with row pitch ldb, read in boxes of 64 n x 64 k
+    if ((e = make_map(&b0, bp, k, n, ldb, 64)) != cudaSuccess) return e;
+  } else {
+    if ((e = make_map(&b0, bp, n, k, ldb, BN)) != cudaSuccess) return e;
+  }
   Args a{};
   a.mode = kGemm;
   a.rows = rows;
@@ -1074,6 +1065,7 @@ cudaError_t gemm_acc(const void* a0p, const void* a1p, int64_t lda, const void* 
   // one k part per tile and nothing in C to add to: plain stores
   a.gemm_store = may_store && ks == 1 ? 1 : 0;
   a.a_mn = a_mn ? 1 : 0;
+  a.b_mn = b_mn ? 1 : 0;
   return launch<BN, kGemm>(a0, b0, a1, b0, a, stream);
 }
 
@@ -1085,8 +1077,8 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
   const int64_t nc = p.rows < chunk_rows ? cdiv(p.rows, BM) * BM : chunk_rows;
   if (ws_bytes < linear_bwd_workspace(p.rows, p.vocab, p.hs, p.ht, student, teacher, chunk_rows))
     return cudaErrorInvalidValue;
-  // workspace: per head the [hi, lo] gradients of one chunk, row-major, the head
-  // weight transposed [H, V], the chunk's hidden states transposed [H, nc]
+  // workspace: per head the [hi, lo] gradients of one chunk, row-major (the
+  // contractions read the head weight and the hidden states in place)
   uint8_t* w = static_cast<uint8_t*>(ws);
   const size_t g = align256(static_cast<size_t>(nc) * p.vocab * 2u);
   auto take = [&](size_t bytes) {
@@ -1095,8 +1087,6 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
     return r;
   };
   __nv_bfloat16* G[2][2] = {};
-  void* wT[2] = {nullptr, nullptr};
-  void* hT[2] = {nullptr, nullptr};
   const int64_t H[2] = {p.hs, p.ht};
   const void* hp[2] = {p.h_s, p.h_t};
   const int64_t ldh[2] = {p.ld_hs, p.ld_ht};
@@ -1109,14 +1099,11 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
   for (int x = 0; x < 2; ++x) {
     if (!want[x]) continue;
     for (int i = 0; i < 2; ++i) G[x][i] = reinterpret_cast<__nv_bfloat16*>(take(g));
-    wT[x] = take(static_cast<size_t>(H[x]) * p.vocab * 2u);
-    hT[x] = take(static_cast<size_t>(H[x]) * nc * 2u);
     // dh and dW accumulate by atomics: start from zero
     if (dh[x] && (e = cudaMemsetAsync(dh[x], 0, static_cast<size_t>(p.rows) * H[x] * 4u, stream)) != cudaSuccess)
       return e;
     if (dw[x] && (e = cudaMemsetAsync(dw[x], 0, static_cast<size_t>(p.vocab) * H[x] * 4u, stream)) != cudaSuccess)
       return e;
-    if (dh[x] && (e = transpose_bf16(wp[x], p.vocab, H[x], ldw[x], wT[x], p.vocab, stream)) != cudaSuccess) return e;
   }
   CUtensorMap hsm, wsm, htm, wtm;
   for (int64_t r0 = 0; r0 < p.rows; r0 += nc) {
@@ -1161,18 +1148,18 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
     if ((e = launch<kGradTN, kGrad>(hsm, wsm, htm, wtm, a, stream, &gm)) != cudaSuccess) return e;
     for (int x = 0; x < 2; ++x) {
       if (!want[x]) continue;
-      // dh[r0:r0+n] += G_hi W + G_lo W  (K = V; B = W^T [H, V])
+      // dh[r0:r0+n] += G_hi W + G_lo W  (K = V; A = G K-major, B = W [V, H] read MN-major)
       if (dh[x] &&
-          (e = gemm_acc(G[x][0], G[x][1], p.vocab, wT[x], p.vocab, n, H[x], p.vocab, dh[x] + r0 * H[x], H[x],
-                        true, stream, false)) != cudaSuccess)
+          (e = gemm_acc(G[x][0], G[x][1], p.vocab, wp[x], ldw[x], n, H[x], p.vocab, dh[x] + r0 * H[x], H[x],
+                        true, stream, false, true)) != cudaSuccess)
         return e;
-      // dW += G_hi^T h + G_lo^T h  (K = the chunk's n rows; A = G [n, V] read
-      // MN-major, B = h^T [H, nc]; the maps end K at n, the loads fill zeros past it)
+      // dW += G_hi^T h + G_lo^T h  (K = the chunk's n rows; A = G [n, V] and
+      // B = h [n, H], both read MN-major; the maps end K at n, the loads fill
+      // zeros past it)
       if (dw[x]) {
         const void* h0 = static_cast<const char*>(hp[x]) + r0 * ldh[x] * 2;
-        if ((e = transpose_bf16(h0, n, H[x], ldh[x], hT[x], nc, stream)) != cudaSuccess) return e;
-        if ((e = gemm_acc(G[x][0], G[x][1], p.vocab, hT[x], nc, p.vocab, H[x], n, dw[x], H[x], r0 == 0, stream,
-                          true)) != cudaSuccess)
+        if ((e = gemm_acc(G[x][0], G[x][1], p.vocab, h0, ldh[x], p.vocab, H[x], n, dw[x], H[x], r0 == 0, stream,
+                          true, true)) != cudaSuccess)
           return e;
       }
     }
