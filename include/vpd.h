@@ -374,9 +374,9 @@ typedef struct {
 /* Workspace sizes (bytes) of vpd_jsd_linear_fwd and of vpd_jsd_linear_bwd
  * with the given gradients wanted (nonzero flags). The backward works through
  * the rows in chunks of 8192 and keeps, per head, that chunk's gradient of the
- * logits split in two bf16 parts (row-major; the contractions read them, the
- * head weight and the hidden states in place, transposed where they need).
- * Either output pointer
+ * logits split in two bf16 parts (row-major; the contractions read them and
+ * the head weight in place, transposed where they need) and the chunk's hidden
+ * states transposed. Either output pointer
  * may be NULL. */
 vpd_status vpd_jsd_linear_workspace(const vpd_linear_heads *heads, int32_t student_grads,
                                     int32_t teacher_grads, size_t *fwd_bytes, size_t *bwd_bytes);

@@ -28,7 +28,8 @@
 //           dh = dS W and dW = dS^T h from the split gradients, hi and lo as the
 //           two pairs; for dW the A operand is the same row-major dS, read
 //           MN-major), split along K, accumulated into fp32 C by atomics.
-// Small kernels merge the per-chunk partials.
+// Small kernels merge the per-chunk partials and transpose the chunk's hidden
+// states for dW.
 //
 // Warp roles of k_linear (one instantiation per mode): warp 0 issues the TMA
 // loads into a ring of shared-memory stages; warp 1 issues the MMAs (one
@@ -831,6 +832,23 @@ __global__ void k_linear_merge_div(const float2* part, int chunks, int64_t rows,
   loss[r] = value;
 }
 
+// out[c, r] = in[r, c] for a bf16 [rows, cols] matrix (32 x 32 tiles through
+// shared memory; rows and cols of the output are those of the transposed view).
+__global__ void k_transpose_bf16(const __nv_bfloat16* in, int64_t rows, int64_t cols, int64_t ld_in,
+                                 __nv_bfloat16* out, int64_t ld_out) {
+  __shared__ __nv_bfloat16 tile[32][33];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32, c0 = static_cast<int64_t>(blockIdx.x) * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int64_t r = r0 + i, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) tile[i][threadIdx.x] = in[r * ld_in + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int64_t c = c0 + i, r = r0 + threadIdx.x;
+    if (r < rows && c < cols) out[c * ld_out + r] = tile[threadIdx.x][i];
+  }
+}
+
 
 // ---------------------------------------------------------------------------
 // Host side
@@ -976,8 +994,8 @@ size_t linear_bwd_workspace(int64_t rows, int64_t vocab, int64_t hs, int64_t ht,
   const int64_t nc = rows < chunk_rows ? cdiv(rows, BM) * BM : chunk_rows;
   size_t b = 0;
   const size_t g = static_cast<size_t>(nc) * static_cast<size_t>(vocab) * 2u;  // one bf16 [nc, V]
-  if (student) b += 2 * g;
-  if (teacher) b += 2 * g;
+  if (student) b += 2 * g + static_cast<size_t>(hs) * nc * 2u;
+  if (teacher) b += 2 * g + static_cast<size_t>(ht) * nc * 2u;
   return b + 1024;
 }
 
@@ -1029,6 +1047,16 @@ cudaError_t linear_jsd_forward(const LinearProblem& p, float* loss, float* saved
 }
 
 
+cudaError_t transpose_bf16(const void* in, int64_t rows, int64_t cols, int64_t ld_in, void* out, int64_t ld_out,
+                           cudaStream_t stream) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  dim3 grid(static_cast<unsigned>(cdiv(cols, 32)), static_cast<unsigned>(cdiv(rows, 32)));
+  k_transpose_bf16<<<grid, dim3(32, 8), 0, stream>>>(static_cast<const __nv_bfloat16*>(in), rows, cols, ld_in,
+                                                       static_cast<__nv_bfloat16*>(out), ld_out);
+  note_launch();
+  return cudaGetLastError();
+}
+
 // C[rows, n] += A0 B0^T + A1 B1^T with K-major bf16 operands (A [rows, k],
 // B [n, k]), split along k so that the units spread evenly over the SMs; with
 // may_store (C holds nothing yet) and a single k part, C = the product.
@@ -1077,8 +1105,8 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
   const int64_t nc = p.rows < chunk_rows ? cdiv(p.rows, BM) * BM : chunk_rows;
   if (ws_bytes < linear_bwd_workspace(p.rows, p.vocab, p.hs, p.ht, student, teacher, chunk_rows))
     return cudaErrorInvalidValue;
-  // workspace: per head the [hi, lo] gradients of one chunk, row-major (the
-  // contractions read the head weight and the hidden states in place)
+  // workspace: per head the [hi, lo] gradients of one chunk, row-major, and the
+  // chunk's hidden states transposed [H, nc] (the head weight is read in place)
   uint8_t* w = static_cast<uint8_t*>(ws);
   const size_t g = align256(static_cast<size_t>(nc) * p.vocab * 2u);
   auto take = [&](size_t bytes) {
@@ -1087,6 +1115,7 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
     return r;
   };
   __nv_bfloat16* G[2][2] = {};
+  void* hT[2] = {nullptr, nullptr};
   const int64_t H[2] = {p.hs, p.ht};
   const void* hp[2] = {p.h_s, p.h_t};
   const int64_t ldh[2] = {p.ld_hs, p.ld_ht};
@@ -1099,6 +1128,7 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
   for (int x = 0; x < 2; ++x) {
     if (!want[x]) continue;
     for (int i = 0; i < 2; ++i) G[x][i] = reinterpret_cast<__nv_bfloat16*>(take(g));
+    hT[x] = take(static_cast<size_t>(H[x]) * nc * 2u);
     // dh and dW accumulate by atomics: start from zero
     if (dh[x] && (e = cudaMemsetAsync(dh[x], 0, static_cast<size_t>(p.rows) * H[x] * 4u, stream)) != cudaSuccess)
       return e;
@@ -1153,13 +1183,14 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
           (e = gemm_acc(G[x][0], G[x][1], p.vocab, wp[x], ldw[x], n, H[x], p.vocab, dh[x] + r0 * H[x], H[x],
                         true, stream, false, true)) != cudaSuccess)
         return e;
-      // dW += G_hi^T h + G_lo^T h  (K = the chunk's n rows; A = G [n, V] and
-      // B = h [n, H], both read MN-major; the maps end K at n, the loads fill
-      // zeros past it)
+      // dW += G_hi^T h + G_lo^T h  (K = the chunk's n rows; A = G [n, V] read
+      // MN-major, B = h^T [H, nc] K-major: h read in place as an MN-major B
+      // drew more from DRAM; the maps end K at n, the loads fill zeros past it)
       if (dw[x]) {
         const void* h0 = static_cast<const char*>(hp[x]) + r0 * ldh[x] * 2;
-        if ((e = gemm_acc(G[x][0], G[x][1], p.vocab, h0, ldh[x], p.vocab, H[x], n, dw[x], H[x], r0 == 0, stream,
-                          true, true)) != cudaSuccess)
+        if ((e = transpose_bf16(h0, n, H[x], ldh[x], hT[x], nc, stream)) != cudaSuccess) return e;
+        if ((e = gemm_acc(G[x][0], G[x][1], p.vocab, hT[x], nc, p.vocab, H[x], n, dw[x], H[x], r0 == 0, stream,
+                          true, false)) != cudaSuccess)
           return e;
       }
     }
