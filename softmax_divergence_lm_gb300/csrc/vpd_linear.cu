@@ -1129,10 +1129,15 @@ cudaError_t linear_jsd_backward(const LinearProblem& p, const float* grad_loss, 
     if (!want[x]) continue;
     for (int i = 0; i < 2; ++i) G[x][i] = reinterpret_cast<__nv_bfloat16*>(take(g));
     hT[x] = take(static_cast<size_t>(H[x]) * nc * 2u);
-    // dh and dW accumulate by atomics: start from zero
+    // dh accumulates by atomics: start from zero
     if (dh[x] && (e = cudaMemsetAsync(dh[x], 0, static_cast<size_t>(p.rows) * H[x] * 4u, stream)) != cudaSuccess)
       return e;
-    if (dw[x] && (e = cudaMemsetAsync(dw[x], 0, static_cast<size_t>(p.vocab) * H[x] * 4u, stream)) != cudaSuccess)
+    // dW: unless the first chunk's contraction runs unsplit and stores its
+    // product (every element once), later chunks add to it
+    const int64_t n0 = p.rows < nc ? p.rows : nc;
+    const bool dw_stored = gemm_ksplit(cdiv(p.vocab, BM) * cdiv(H[x], BN), 2 * cdiv(n0, BK)) == 1;
+    if (dw[x] && !dw_stored &&
+        (e = cudaMemsetAsync(dw[x], 0, static_cast<size_t>(p.vocab) * H[x] * 4u, stream)) != cudaSuccess)
       return e;
   }
   CUtensorMap hsm, wsm, htm, wtm;
