@@ -69,14 +69,14 @@ constexpr int BK = 64;                      // k per stage: one 128-byte swizzle
 constexpr int kTileBytes = BM * BK * 2;     // 16 KB: the A tile of a stage
 constexpr int kRingBytes = 4 * (kTileBytes + BN * BK * 2);  // stage ring: 4 of 48 KB (256 columns) or 6 of 32 KB (128)
 constexpr int kMaxStages = 6;
-// Tile columns of the gradient pass: it needs both heads' logits at once, and
-// two 128-column tiles of s and t fill the tensor memory, so its long epilogue
-// overlaps the MMAs of the next tile. The other passes use 256 columns: the
-// statistics pass (one head's tile at a time, in two buffers), the GEMMs
-// (two buffers), and the divergence pass, whose short epilogue costs less
-// than the narrower MMAs would (s and t of one 256-column tile fill the
-// tensor memory, so that epilogue overlaps only its last columns).
-constexpr int kGradTN = 128;
+// Tile columns of every pass: 256. The statistics pass takes one head's tile
+// at a time, in two buffers, and the GEMMs two buffers. The divergence and
+// gradient passes need both heads' logits of a tile at once: s and t of one
+// 256-column tile fill the tensor memory, so their epilogue overlaps the next
+// tile's MMAs only from each warp's last columns on; 128-column tiles, two of
+// which fit, overlap fully but draw a third more operand bytes from L2 per
+// flop, which costs more than the overlap saves.
+constexpr int kGradTN = 256;
 template <int TN>
 struct TileShape {
   static constexpr int kBBytes = TN * BK * 2;             // the B tile of a stage
