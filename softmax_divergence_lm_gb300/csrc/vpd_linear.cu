@@ -40,10 +40,9 @@
 // Stages hand over through mbarriers (TMA completion -> MMA; tcgen05.commit ->
 // producer), and so do the accumulator buffers (commit -> epilogue; epilogue
 // arrivals -> MMA), so the epilogue of one tile overlaps the MMAs of the next
-// wherever two tiles fit in tensor memory (all passes but kDiv, whose s and t
-// tiles of 256 columns fill it, and whose epilogue warps hand the accumulator
-// back once their last columns are in registers; kGrad takes 128-column tiles
-// so that two fit).
+// wherever two tiles fit in tensor memory (kStats and kGemm); in kDiv and
+// kGrad the s and t tiles of 256 columns fill it, and each epilogue warp hands
+// the accumulator back once its last columns are in registers.
 // Every mbarrier wait gives up after two seconds, sets the device error word
 // and leaves the loops; the CTA waits for copies and MMAs in flight before it
 // frees its tensor memory.
@@ -76,7 +75,7 @@ constexpr int kMaxStages = 6;
 // tile's MMAs only from each warp's last columns on; 128-column tiles, two of
 // which fit, overlap fully but draw a third more operand bytes from L2 per
 // flop, which costs more than the overlap saves.
-constexpr int kGradTN = 256;
+constexpr int kGradTN = 256;  // the gradient pass's tile columns (its W maps' box rows)
 template <int TN>
 struct TileShape {
   static constexpr int kBBytes = TN * BK * 2;             // the B tile of a stage
@@ -104,7 +103,8 @@ enum Mode : int { kStats = 0, kDiv = 1, kGrad = 2, kGemm = 3 };
 // 1 / kParts of a tile's columns. The divergence pass, whose epilogue overlaps
 // the next tile's MMAs only at its end (its s and t tiles fill the tensor
 // memory), runs sixteen (at most 96 registers a thread: five warps per SM
-// sub-partition); the others run eight.
+// sub-partition); the others run eight (the gradient pass, in the same
+// position, needs more registers than sixteen warps leave).
 template <int MODE>
 struct EpiShape {
   static constexpr int kWarps = MODE == kDiv ? 16 : 8;
